@@ -1,0 +1,398 @@
+#!/usr/bin/env python3
+"""Benchmark of the q4_K x q8_1 MMQ hot path on GB300.
+
+One step = the whole hot path over one batch: the q8_1 quantize prepass of
+the activations followed by the q4_K x q8_1 GEMM, on the 7B attention
+q-projection at 2K-token prefill (M=2048 tokens, K=4096, N=4096), seeded
+synthetic inputs.  Metric: TMAC/s = M*N*K / step time / 1e12 (higher is
+better), with us/GMAC and the GEMM-only figures alongside.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl mine|reference]
+
+Under torchrun each rank runs its own independent problem on its own GPU
+(weak scaling, no data-path collective); rank 0 prints one JSON line with
+the max time over ranks.  `--impl reference` times the CPU oracle on a
+bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+WORKLOADS = {"q_proj": (2048, 4096, 4096)}
+METRIC = "q4_K x q8_1 GEMM TMAC/s at 7B@2K (q-proj 2048x4096x4096), prepass included"
+UNIT = "TMAC/s"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="mine", choices=["mine", "reference"])
+    ap.add_argument("--workload", default="q_proj", choices=sorted(WORKLOADS))
+    ap.add_argument("--path", default="auto", choices=["auto", "mma_s8", "tc", "small_m"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="target seconds of oracle work for the CPU baseline sample")
+    return ap.parse_args()
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+# --------------------------------------------------------------------- clocks
+class ClockSampler:
+    """Samples nvidia-smi clocks/throttle reasons every 200 ms while active."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.lines = []
+        self.t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200", "-i", str(self.gpu_index)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except (FileNotFoundError, OSError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.t.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": float(np.median(sm)) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ roofline
+def kernel_source_hash(names):
+    h = hashlib.sha256()
+    for n in names:
+        with open(os.path.join(ROOT, "q4_q8_int8_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+def recorded_traffic(kernel_key, src_hash):
+    """Per-launch DRAM bytes from a committed ncu summary, if it was taken on
+    the current kernel source; else None."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get(kernel_key)
+    if not e or e.get("src_hash") != src_hash:
+        return None
+    return e.get("bytes_per_launch")
+
+
+# ----------------------------------------------------------------- CPU leg
+def cpu_oracle_sample(M, K, N, target_s, x, blk):
+    """Time the oracle (quantize + blockwise GEMM) on the first m rows of the
+    workload, m sized for about target_s seconds; returns (TMAC/s, m, secs, cores)."""
+    import oracle
+    oracle.build()
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    m = 1
+    while True:
+        t0 = time.perf_counter()
+        q, da, sa = oracle.quantize_q8_1(x[:m])
+        oracle.gemm(q, da, sa, blk, N, want_bound=False)
+        dt = time.perf_counter() - t0
+        if dt >= target_s or m >= M:
+            break
+        grow = max(2, int(target_s / max(dt, 1e-3) * 0.9))
+        m = min(M, m * grow)
+    return m * N * K / dt / 1e12, m, dt, cores
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    M, K, N = WORKLOADS[args.workload]
+    from q4_q8_int8_gb300 import synthetic
+    x, blk, _ = synthetic.config_inputs(args.workload)
+    import oracle
+    oracle.build()
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    # each step: quantize + GEMM over a bounded row sample (sized from one probe step)
+    per_step_budget = max(0.5, 150.0 / max(1, args.steps + args.warmup))
+    _, m, _, _ = cpu_oracle_sample(M, K, N, per_step_budget, x, blk)
+    xs = x[:m]
+    for _ in range(args.warmup):
+        q, da, sa = oracle.quantize_q8_1(xs)
+        oracle.gemm(q, da, sa, blk, N, want_bound=False)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        q, da, sa = oracle.quantize_q8_1(xs)
+        oracle.gemm(q, da, sa, blk, N, want_bound=False)
+    dt = time.perf_counter() - t0
+    value = m * N * K * args.steps / dt / 1e12
+    sample = f"first {m} of {M} token rows of {args.workload} (K={K}, N={N}) per step"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": f"{args.workload} M={M} K={K} N={N}"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------- GPU leg
+def run_mine(args, rank, world, local_rank):
+    import torch
+    import q4_q8_int8_gb300 as mmq
+    from q4_q8_int8_gb300 import build as mmq_build, synthetic
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    mmq_build.build()
+    mmq.load_library()
+    path = {"auto": mmq.MMQ_PATH_AUTO, "mma_s8": mmq.MMQ_PATH_MMA_S8, "tc": mmq.MMQ_PATH_TC,
+            "small_m": mmq.MMQ_PATH_SMALL_M}[args.path]
+
+    M, K, N = WORKLOADS[args.workload]
+    # Inputs: R independent sets rotated step by step so that every step reads
+    # its inputs from HBM (R sets together exceed twice the 129 MB L2).
+    set_bytes = M * K * 4 + M * K * 1.25 + N * K * 0.5625 + M * N * 4
+    R = max(2, int(np.ceil(2 * 129e6 / set_bytes)) + 1)
+    xs, ws, aqs, Cs = [], [], [], []
+    for r in range(R):
+        xs.append(synthetic.torch_activations(M, K, 7000 + 97 * rank + r, dev, 0.01))
+        ws.append(synthetic.torch_q4K_weights(N, K, 8000 + 97 * rank + r, dev).view(-1))
+        aqs.append(mmq.empty_q8_1(M, K, dev))
+        Cs.append(torch.empty((M, N), dtype=torch.float32, device=dev))
+    stream = torch.cuda.current_stream(dev)
+    sp = mmq._stream_ptr(stream)
+    import ctypes
+
+    def step(i, evs=None):
+        r = i % R
+        x, w, (qs, da, sa), C = xs[r], ws[r], aqs[r], Cs[r]
+        aq = mmq.q8_1_struct(qs, da, sa)
+        if evs is not None:
+            evs[0].record(stream)
+        rc = mmq.mmq_quantize_q8_1(ctypes.c_void_p(x.data_ptr()), M, K, aq, sp)
+        if evs is not None:
+            evs[1].record(stream)
+        rc |= mmq.mmq_q4K_gemm_path(aq, ctypes.c_void_p(w.data_ptr()), ctypes.c_void_p(C.data_ptr()),
+                                    M, N, K, path, sp)
+        if evs is not None:
+            evs[2].record(stream)
+        if rc:
+            raise RuntimeError(f"MMQ call failed: {rc}")
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize(dev)
+    if mmq.status(stream) != 0:
+        raise RuntimeError("device status error after warm-up")
+
+    clocks = ClockSampler(local_rank) if rank == 0 else None
+    if clocks:
+        clocks.start()
+        time.sleep(0.3)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        step(args.warmup + i, evs[i])
+    torch.cuda.synchronize(dev)
+    wall = time.perf_counter() - t0
+    if world > 1:
+        torch.distributed.barrier()
+    clk = clocks.stop() if clocks else None
+    rc = mmq.status(stream)
+    if rc != 0:
+        raise RuntimeError(f"device status {rc} after timed region")
+
+    step_ms = evs[0][0].elapsed_time(evs[-1][2]) / args.steps
+    q_ms = float(np.mean([e[0].elapsed_time(e[1]) for e in evs]))
+    g_ms = float(np.mean([e[1].elapsed_time(e[2]) for e in evs]))
+    t = torch.tensor([step_ms, q_ms, g_ms], device=dev)
+    if world > 1:
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    step_ms, q_ms, g_ms = t.tolist()
+
+    # ---- end to end through the C ABI with pinned host buffers
+    xh = torch.empty((M, K), dtype=torch.float32, pin_memory=True)
+    xh.copy_(xs[0].cpu())
+    Ch = torch.empty((M, N), dtype=torch.float32, pin_memory=True)
+    xd = torch.empty_like(xs[0])
+
+    def e2e_step(i):
+        r = i % R
+        (qs, da, sa), C, w = aqs[r], Cs[r], ws[r]
+        xd.copy_(xh, non_blocking=True)
+        aq = mmq.q8_1_struct(qs, da, sa)
+        rc = mmq.mmq_quantize_q8_1(ctypes.c_void_p(xd.data_ptr()), M, K, aq, sp)
+        rc |= mmq.mmq_q4K_gemm_path(aq, ctypes.c_void_p(w.data_ptr()), ctypes.c_void_p(C.data_ptr()),
+                                    M, N, K, path, sp)
+        Ch.copy_(C, non_blocking=True)
+        if rc:
+            raise RuntimeError(f"MMQ call failed: {rc}")
+
+    e2e_steps = max(3, min(args.steps, 20))
+    for i in range(2):
+        e2e_step(i)
+    torch.cuda.synchronize(dev)
+    ea, eb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ea.record(stream)
+    for i in range(e2e_steps):
+        e2e_step(i)
+    eb.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = ea.elapsed_time(eb) / e2e_steps
+    te = torch.tensor([e2e_ms], device=dev)
+    if world > 1:
+        torch.distributed.all_reduce(te, op=torch.distributed.ReduceOp.MAX)
+    e2e_ms = te.item()
+
+    if rank != 0:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return
+
+    macs = M * N * K
+    value = macs * world / (step_ms * 1e-3) / 1e12
+    gemm_tmacs = macs / (g_ms * 1e-3) / 1e12
+    peaks = measured_peaks()
+    # dominant kernel = the GEMM; tensor roofline of the pipe it uses
+    used_path = path
+    if used_path == mmq.MMQ_PATH_AUTO:
+        used_path = mmq.MMQ_PATH_SMALL_M if M <= mmq.SMALL_M_MAX else mmq.MMQ_PATH_TC
+    kname = {mmq.MMQ_PATH_MMA_S8: ("gemm_mma_s8", "gemm_mma.cu"),
+             mmq.MMQ_PATH_TC: ("gemm_tc", "gemm_tc.cu"),
+             mmq.MMQ_PATH_SMALL_M: ("gemm_small_m", "gemm_small.cu")}[used_path]
+    src_hash = kernel_source_hash([kname[1]])
+    traffic = recorded_traffic(kname[0], src_hash)
+    alg_bytes = 0.5625 * N * K + 1.25 * M * K + 4 * M * N
+    if used_path == mmq.MMQ_PATH_SMALL_M:
+        achieved = alg_bytes / (g_ms * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / peaks["hbm_gbs"], "traffic": traffic}
+    else:
+        # 2 flops per multiply-add; fp16-operand tensor path measured at the bf16 rate
+        achieved = 2 * macs / (g_ms * 1e-3) / 1e12
+        peak = peaks["bf16_tflops_sustained"] or peaks["bf16_tflops"]
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "traffic": traffic}
+    roof["kernel"] = kname[0]
+    roof["peak_source"] = f"{peaks['source']} (MEASURED_PEAKS.json sustained bf16)" \
+        if roof["unit"] == "TFLOP/s" else f"{peaks['source']} (MEASURED_PEAKS.json hbm copy)"
+    roof["algorithmic_bytes_per_launch"] = alg_bytes
+    roof["algorithmic_flops_per_launch"] = 2 * macs
+
+    cpu = None
+    if not args.no_cpu_baseline:
+        from q4_q8_int8_gb300 import synthetic as syn
+        x0, blk0, _ = syn.config_inputs(args.workload)
+        v, m, secs, cores = cpu_oracle_sample(M, K, N, args.cpu_seconds, x0, blk0)
+        cpu = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
+               "sample": f"first {m} of {M} token rows of {args.workload}, quantize + blockwise "
+                         f"GEMM, {secs:.1f} s"}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "int8xu4->f32 (fp16-exact ints on tensor cores)"
+        if used_path == mmq.MMQ_PATH_TC else "s8xs8->s32, f32 rescale",
+        "data": "synthetic",
+        "config": {"workload": f"{args.workload} M={M} K={K} N={N}", "global_batch_tokens": M * world,
+                   "parallelism": f"independent problem per GPU x{world}",
+                   "l2": f"{R} rotating input sets ({R * set_bytes / 1e6:.0f} MB > 2x L2)",
+                   "path": args.path},
+        "us_per_gmac": step_ms * 1e3 / (macs / 1e9),
+        "gemm_only": {"tmacs": gemm_tmacs, "us_per_gmac": g_ms * 1e3 / (macs / 1e9), "ms": g_ms},
+        "prepass": {"ms": q_ms, "gbs": (M * K * 4 + M * K * 1.25) / (q_ms * 1e-3) / 1e9},
+        "roofline": roof,
+        "cpu_baseline": cpu,
+        "e2e": {"value": macs * world / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
+                "h2d_bytes_per_step": M * K * 4, "d2h_bytes_per_step": M * N * 4,
+                "ms_per_step": e2e_ms},
+        "gpu_launches": 2 * args.steps,
+        "clocks": clk,
+        "wall_s_timed": wall,
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def main():
+    args = parse()
+    rank, world, local_rank = dist_env()
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_mine(args, rank, world, local_rank)
+
+
+if __name__ == "__main__":
+    main()

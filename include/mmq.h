@@ -1,0 +1,152 @@
+/*
+ * mmq.h -- C ABI of the GB300 (sm_103a) q4_K-weight x q8_1-activation
+ * quantized GEMM ("MMQ") used in LLM prefill.
+ *
+ * The operation (web page "20 . r15 -- f32-accumulate mma probe (dead end) +
+ * rank-1 term2 rescale", section 2.1 "Where the two-term rescale comes
+ * from"): activations are quantized per 32 elements to q8_1 (scale da,
+ * int8 quants, integer block sum sa); weights are q4_K (256-element
+ * super-blocks with fp16 d and dmin, eight 32-element sub-blocks with 6-bit
+ * sc and m, 4-bit quants v).  For every 32-k chunk c,
+ *     C_ij += da_ic * dsv_jc * S_ijc + dmv_jc * (da_ic * sa_ic)
+ * where S_ijc = sum_k a_int[i,k] * v[j,k] exactly, dsv = d*sc and
+ * dmv = -dmin*m.  The row factor dma = da*sa is formed once per token row
+ * and chunk (the rank-1 fold: page "21 . r16 -- Narrow kernel gets the
+ * rank-1 fold", section 2.1).
+ *
+ * Conventions for every entry point:
+ *  - Pointers are DEVICE pointers unless the parameter name ends in _host.
+ *    All buffers are owned and allocated by the caller; the library
+ *    allocates no device memory per call.
+ *  - `stream` is a cudaStream_t (NULL = legacy default stream).  Device work
+ *    is enqueued asynchronously on it; argument errors are returned
+ *    synchronously before anything is enqueued.
+ *  - Return value: 0 on success, a negative MMQ_ERR_* code otherwise
+ *    (mmq_strerror gives the text).  Nothing is written on an error return.
+ *  - Inputs must be finite; NaN/Inf activations are outside the contract.
+ *  - All device pointers must be 16-byte aligned (tensor-memory-access
+ *    copies require it).
+ */
+#ifndef MMQ_H
+#define MMQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MMQ_OK 0
+#define MMQ_ERR_ARG (-1)            /* null pointer, bad size or value range  */
+#define MMQ_ERR_ALIGN (-2)          /* pointer not 16-byte aligned            */
+#define MMQ_ERR_DEVICE (-3)         /* current device is not sm_103           */
+#define MMQ_ERR_RESOURCE (-4)       /* shared/tensor memory budget exceeded:  */
+                                    /* launch refused, no fallback            */
+#define MMQ_ERR_CUDA (-5)           /* a CUDA runtime call or launch failed   */
+#define MMQ_ERR_DEVICE_TIMEOUT (-6) /* a bounded device-side wait gave up     */
+
+/* q8_1 activations, three planes (page r15 section 2.1: "each 32-element
+ * block carrying scale da and the in-block integer sum sa"):
+ *   qs  int8    [M][K]     row-major quants, q = round(x / da) in [-127, 127]
+ *   da  float   [M][K/32]  per-block scale amax/127 (f32)
+ *   sa  int32   [M][K/32]  per-block sum of the 32 quants                  */
+typedef struct {
+    int8_t* qs;
+    float* da;
+    int32_t* sa;
+} mmq_q8_1_t;
+
+/* Bytes of one buffer holding all three q8_1 planes for an M x K activation
+ * (planes 256-byte aligned inside it).  K must be a multiple of 32.
+ * Returns 0 for invalid sizes. */
+size_t mmq_q8_1_bytes(int64_t M, int64_t K);
+
+/* Carve the three planes out of a buffer of mmq_q8_1_bytes(M, K) bytes
+ * (buf must be 256-byte aligned).  Host-only pointer arithmetic. */
+int mmq_q8_1_view(void* buf, int64_t M, int64_t K, mmq_q8_1_t* out);
+
+/* q8_1 quantize prepass (page r15 section 2.1; the prepass writes da and sa
+ * together, so sa costs no extra pass).  Per token row i and 32-block b:
+ *   amax = max |x|;  da = amax / 127 (IEEE f32 division);
+ *   if da == 0: all q = 0, sa = 0;
+ *   else q_k = clamp(roundf(x_k / da), -127, 127) with IEEE division and
+ *        round-half-away-from-zero;  sa = sum q_k.
+ * x float [M][K] row-major (device).  M >= 1, K >= 32, K % 32 == 0.
+ * Output planes as in mmq_q8_1_t.  Bit-exact against the CPU reference. */
+int mmq_quantize_q8_1(const float* x, int64_t M, int64_t K, mmq_q8_1_t aq,
+                      void* stream);
+
+/* Bytes of q4_K weights for an N x K matrix: N * (K/256) * 144. */
+size_t mmq_q4K_bytes(int64_t N, int64_t K);
+
+/* Host q4_K packer (page r15 section 2.1 fields; customary 144-byte
+ * super-block: fp16 d, fp16 dmin, 12 bytes of 6-bit sc/m, 128 bytes of
+ * nibbles).  Inputs (host, row-major):
+ *   v_host    uint8  [N][K]      quants 0..15
+ *   sc_host   uint8  [N][K/32]   sub-block scales 0..63
+ *   m_host    uint8  [N][K/32]   sub-block mins 0..63
+ *   d_host    uint16 [N][K/256]  fp16 bit patterns of d
+ *   dmin_host uint16 [N][K/256]  fp16 bit patterns of dmin
+ * out_host: mmq_q4K_bytes(N, K) bytes, row j's super-blocks contiguous.
+ * Errors: MMQ_ERR_ARG for null pointers, N < 1, K % 256 != 0 or a field out
+ * of range (nothing written). */
+int mmq_pack_q4K(const uint8_t* v_host, const uint8_t* sc_host,
+                 const uint8_t* m_host, const uint16_t* d_host,
+                 const uint16_t* dmin_host, int64_t N, int64_t K,
+                 uint8_t* out_host);
+
+/* The GEMM: C[i][j] = sum over 32-k chunks c of
+ *     da_ic * dsv_jc * S_ijc + dmv_jc * (da_ic * sa_ic)
+ * (page r15 section 2.1, two-term rescale; the per-chunk integer dot S is
+ * exact; the rescale is f32 with the rank-1 fold dma = da*sa per token row).
+ * aq: q8_1 planes of the M x K activations; bq4k: q4_K bytes of the N x K
+ * weights (row j = output feature j); C float [M][N] row-major, overwritten.
+ * M >= 1 (any), N >= 1 with N % 4 == 0, K >= 256 with K % 256 == 0.
+ * Picks the kernel for the shape (small-M weight-streaming kernel or the
+ * large-M tensor-core kernel).  Results agree with the CPU reference within
+ * |C - C_ref| <= 1e-4 * sum_k |a_k w_k| + 1e-6 and are bitwise
+ * deterministic run to run. */
+int mmq_q4K_gemm(mmq_q8_1_t aq, const uint8_t* bq4k, float* C, int64_t M,
+                 int64_t N, int64_t K, void* stream);
+
+/* Kernel selection for mmq_q4K_gemm_path (testing and A/B timing). */
+#define MMQ_PATH_AUTO 0
+#define MMQ_PATH_MMA_S8 1   /* warp-level mma.sync s8 x s8 -> s32 kernel    */
+#define MMQ_PATH_TC 2       /* tcgen05 kernel (exact integers in fp16, f32   */
+                            /* accumulation in tensor memory)               */
+#define MMQ_PATH_SMALL_M 3  /* weight-streaming kernel for few tokens       */
+
+/* Same as mmq_q4K_gemm with an explicit kernel.  MMQ_ERR_ARG if `path` is
+ * unknown or the kernel does not accept the shape (the small-M kernel takes
+ * M <= 64). */
+int mmq_q4K_gemm_path(mmq_q8_1_t aq, const uint8_t* bq4k, float* C, int64_t M,
+                      int64_t N, int64_t K, int path, void* stream);
+
+/* Debug/test dump of the exact per-chunk integer dots (page r15 section 2.1:
+ * S_ij = sum_k a_int[i,k] * v[j,k]; section 2.3: |S| <= 32*127*15) computed
+ * by the same unpack and MMA code as the GEMM kernel selected by `path`
+ * (MMQ_PATH_MMA_S8 or MMQ_PATH_TC).  S int32 [M][N][K/32].  Same shape
+ * rules as the GEMM. */
+int mmq_q4K_block_dots(mmq_q8_1_t aq, const uint8_t* bq4k, int32_t* S,
+                       int64_t M, int64_t N, int64_t K, int path, void* stream);
+
+/* Synchronizes `stream`, then returns and clears the current device's status
+ * word: MMQ_OK, or MMQ_ERR_DEVICE_TIMEOUT if a kernel's bounded wait gave up
+ * since the last call (that kernel's output is then invalid), or
+ * MMQ_ERR_CUDA if the synchronization itself failed. */
+int mmq_status(void* stream);
+
+/* Static text for an MMQ_* code. */
+const char* mmq_strerror(int code);
+
+/* Test hook: when nonzero, the next tensor-core GEMM launch on this host
+ * thread withholds one producer arrival so that its consumers' bounded
+ * waits run out; the kernel then records MMQ_ERR_DEVICE_TIMEOUT and returns
+ * without hanging.  Used only to test the failure path. */
+void mmq_debug_inject_timeout(int enable);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MMQ_H */

@@ -59,10 +59,9 @@ static double half_to_double(uint16_t h) {
 }
 
 /* ---------------------------------------------------------------------------
- * O1  q8_1 quantize  ([r15] 2.1: "each 32-element block carrying scale da and
- *     the in-block integer sum sa ... computed for free by the quantize
- *     prepass").  Oracle layout: q [M][K] int8, da [M][K/32] f32,
- *     sa [M][K/32] int32.
+ * O1  q8_1 quantize ([r15] 2.1: every 32 activations get a scale da and the
+ *     sum sa of their integer quants, both written by the quantize pass).
+ *     Oracle layout: q [M][K] int8, da [M][K/32] f32, sa [M][K/32] int32.
  * ------------------------------------------------------------------------- */
 void oracle_quantize_q8_1(const float* x, int64_t M, int64_t K,
                           int8_t* q, float* da, int32_t* sa) {
@@ -97,9 +96,9 @@ void oracle_quantize_q8_1(const float* x, int64_t M, int64_t K,
 }
 
 /* ---------------------------------------------------------------------------
- * O2  q4_K unpack of one super-block ([r15] 2.1: d, dmin fp16 per super-block;
- *     sc, m 6-bit per 32-sub-block "get_scale_min_k4 table semantics";
- *     v in [0,15]).  Customary 144-byte layout:
+ * O2  q4_K unpack of one super-block ([r15] 2.1: fp16 d and dmin per
+ *     super-block; 6-bit sc and m per 32-element sub-block, decoded the way
+ *     get_scale_min_k4 decodes them; v in [0,15]).  Customary 144-byte layout:
  *       bytes 0-1  d (fp16, little endian)     bytes 2-3  dmin (fp16)
  *       bytes 4-15 s[0..11]: for c < 4:  sc = s[c] & 63,  m = s[c+4] & 63
  *                            for c >= 4: sc = (s[c+4] & 15) | (s[c-4] >> 6) << 4
@@ -143,8 +142,8 @@ void oracle_unpack_q4K(const uint8_t* blk, int64_t N, int64_t K,
                               v + j * K + b * QKK);
 }
 
-/* Dequantized weight w_jk = d*sc*v - dmin*m ([r15] 2.1: "the true product is
- * b = d*sc*v - dmin*m"), in double, [N][K]. */
+/* Dequantized weight w_jk = d*sc*v - dmin*m ([r15] 2.1: the weight a q4_K
+ * code stands for), in double, [N][K]. */
 void oracle_dequant_q4K(const uint8_t* blk, int64_t N, int64_t K, double* w) {
     const int64_t nsb = K / QKK;
     int64_t j;
@@ -216,9 +215,11 @@ static void gemm_one(const int8_t* q, const float* da, const int32_t* sa,
             const double a_d = (double)da[i * nb + c];
             const double a_s = (double)sa[i * nb + c];
             acc += a_d * dsv * (double)S + dmv * (a_d * a_s);
-            for (int l = 0; l < QK; l++) {
-                const double w = d * sc[c8] * v[c8 * QK + l] - dmin * m[c8];
-                tol += fabs((a_d * (double)q[i * K + c * QK + l]) * w);
+            if (T) {
+                for (int l = 0; l < QK; l++) {
+                    const double w = d * sc[c8] * v[c8 * QK + l] - dmin * m[c8];
+                    tol += fabs((a_d * (double)q[i * K + c * QK + l]) * w);
+                }
             }
         }
     }

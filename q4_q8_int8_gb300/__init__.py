@@ -1,1 +1,209 @@
-"""q4_K x q8_1 quantized GEMM for GB300 (sm_103a)."""
+"""q4_K x q8_1 quantized GEMM (MMQ) for GB300 (sm_103a).
+
+Thin ctypes binding over the C-ABI library ``lib/libmmq.so`` (declared in
+``include/mmq.h``).  Functions named ``mmq_*`` mirror the C entry points
+one to one and take raw pointers; the snake-case helpers below them only
+allocate outputs with PyTorch and pass ``data_ptr()`` and the current CUDA
+stream.  Every step of the computation runs in the library's CUDA kernels;
+if the library is missing, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "lib", "libmmq.so")
+
+MMQ_OK = 0
+MMQ_ERR_ARG = -1
+MMQ_ERR_ALIGN = -2
+MMQ_ERR_DEVICE = -3
+MMQ_ERR_RESOURCE = -4
+MMQ_ERR_CUDA = -5
+MMQ_ERR_DEVICE_TIMEOUT = -6
+
+MMQ_PATH_AUTO = 0
+MMQ_PATH_MMA_S8 = 1
+MMQ_PATH_TC = 2
+MMQ_PATH_SMALL_M = 3
+SMALL_M_MAX = 64
+
+# Every symbol include/mmq.h declares.
+EXPORTS = (
+    "mmq_q8_1_bytes", "mmq_q8_1_view", "mmq_quantize_q8_1", "mmq_q4K_bytes",
+    "mmq_pack_q4K", "mmq_q4K_gemm", "mmq_q4K_gemm_path", "mmq_q4K_block_dots",
+    "mmq_status", "mmq_strerror", "mmq_debug_inject_timeout",
+)
+
+
+class mmq_q8_1_t(ctypes.Structure):
+    _fields_ = [("qs", ctypes.c_void_p), ("da", ctypes.c_void_p), ("sa", ctypes.c_void_p)]
+
+
+class MMQError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        super().__init__(f"{what}: {strerror(code)} ({code})")
+        self.code = code
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def load_library(path: str = LIB_PATH):
+    """Load libmmq.so (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(path):
+                raise RuntimeError(f"libmmq.so not built ({path}); run q4_q8_int8_gb300.build.build()")
+            lib = ctypes.CDLL(path)
+            P, I, S = ctypes.c_void_p, ctypes.c_int64, ctypes.c_size_t
+            Q = mmq_q8_1_t
+            sigs = {
+                "mmq_q8_1_bytes": ([I, I], S),
+                "mmq_q8_1_view": ([P, I, I, ctypes.POINTER(Q)], ctypes.c_int),
+                "mmq_quantize_q8_1": ([P, I, I, Q, P], ctypes.c_int),
+                "mmq_q4K_bytes": ([I, I], S),
+                "mmq_pack_q4K": ([P, P, P, P, P, I, I, P], ctypes.c_int),
+                "mmq_q4K_gemm": ([Q, P, P, I, I, I, P], ctypes.c_int),
+                "mmq_q4K_gemm_path": ([Q, P, P, I, I, I, ctypes.c_int, P], ctypes.c_int),
+                "mmq_q4K_block_dots": ([Q, P, P, I, I, I, ctypes.c_int, P], ctypes.c_int),
+                "mmq_status": ([P], ctypes.c_int),
+                "mmq_strerror": ([ctypes.c_int], ctypes.c_char_p),
+                "mmq_debug_inject_timeout": ([ctypes.c_int], None),
+            }
+            for name, (args, res) in sigs.items():
+                f = getattr(lib, name)
+                f.argtypes = args
+                f.restype = res
+            _lib = lib
+    return _lib
+
+
+# ---- one-to-one mirrors of the C entry points (raw pointers) ---------------
+def mmq_q8_1_bytes(M, K):
+    return load_library().mmq_q8_1_bytes(M, K)
+
+
+def mmq_q8_1_view(buf, M, K, out):
+    return load_library().mmq_q8_1_view(buf, M, K, ctypes.byref(out))
+
+
+def mmq_quantize_q8_1(x, M, K, aq, stream):
+    return load_library().mmq_quantize_q8_1(x, M, K, aq, stream)
+
+
+def mmq_q4K_bytes(N, K):
+    return load_library().mmq_q4K_bytes(N, K)
+
+
+def mmq_pack_q4K(v, sc, m, d, dmin, N, K, out):
+    return load_library().mmq_pack_q4K(v, sc, m, d, dmin, N, K, out)
+
+
+def mmq_q4K_gemm(aq, bq4k, C, M, N, K, stream):
+    return load_library().mmq_q4K_gemm(aq, bq4k, C, M, N, K, stream)
+
+
+def mmq_q4K_gemm_path(aq, bq4k, C, M, N, K, path, stream):
+    return load_library().mmq_q4K_gemm_path(aq, bq4k, C, M, N, K, path, stream)
+
+
+def mmq_q4K_block_dots(aq, bq4k, S, M, N, K, path, stream):
+    return load_library().mmq_q4K_block_dots(aq, bq4k, S, M, N, K, path, stream)
+
+
+def mmq_status(stream):
+    return load_library().mmq_status(stream)
+
+
+def mmq_strerror(code):
+    return load_library().mmq_strerror(code).decode()
+
+
+def mmq_debug_inject_timeout(enable):
+    load_library().mmq_debug_inject_timeout(1 if enable else 0)
+
+
+def strerror(code: int) -> str:
+    return mmq_strerror(code)
+
+
+def _check(rc: int, what: str):
+    if rc != MMQ_OK:
+        raise MMQError(rc, what)
+
+
+# ---- PyTorch-facing helpers (memory and streams only) ----------------------
+def _stream_ptr(stream=None):
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def q8_1_struct(qs, da, sa) -> mmq_q8_1_t:
+    return mmq_q8_1_t(qs.data_ptr(), da.data_ptr(), sa.data_ptr())
+
+
+def empty_q8_1(M: int, K: int, device="cuda"):
+    """Allocate (qs int8 [M][K], da f32 [M][K/32], sa int32 [M][K/32])."""
+    import torch
+    return (torch.empty((M, K), dtype=torch.int8, device=device),
+            torch.empty((M, K // 32), dtype=torch.float32, device=device),
+            torch.empty((M, K // 32), dtype=torch.int32, device=device))
+
+
+def quantize_q8_1(x, out=None, stream=None):
+    """x float32 [M][K] (CUDA, contiguous) -> (qs, da, sa) CUDA tensors."""
+    M, K = x.shape
+    qs, da, sa = out if out is not None else empty_q8_1(M, K, x.device)
+    _check(mmq_quantize_q8_1(ctypes.c_void_p(x.data_ptr()), M, K, q8_1_struct(qs, da, sa),
+                             _stream_ptr(stream)), "mmq_quantize_q8_1")
+    return qs, da, sa
+
+
+def q4K_gemm(aq, w, N: int, path: int = MMQ_PATH_AUTO, out=None, stream=None):
+    """aq = (qs, da, sa); w uint8 q4_K bytes of an N x K matrix -> C float32 [M][N]."""
+    import torch
+    qs, da, sa = aq
+    M, K = qs.shape
+    C = out if out is not None else torch.empty((M, N), dtype=torch.float32, device=qs.device)
+    _check(mmq_q4K_gemm_path(q8_1_struct(qs, da, sa), ctypes.c_void_p(w.data_ptr()),
+                             ctypes.c_void_p(C.data_ptr()), M, N, K, path, _stream_ptr(stream)),
+           "mmq_q4K_gemm")
+    return C
+
+
+def q4K_block_dots(aq, w, N: int, path: int = MMQ_PATH_MMA_S8, out=None, stream=None):
+    """Exact per-chunk int32 dots S [M][N][K/32] from the selected kernel's MMA path."""
+    import torch
+    qs, da, sa = aq
+    M, K = qs.shape
+    S = out if out is not None else torch.empty((M, N, K // 32), dtype=torch.int32, device=qs.device)
+    _check(mmq_q4K_block_dots(q8_1_struct(qs, da, sa), ctypes.c_void_p(w.data_ptr()),
+                              ctypes.c_void_p(S.data_ptr()), M, N, K, path, _stream_ptr(stream)),
+           "mmq_q4K_block_dots")
+    return S
+
+
+def status(stream=None) -> int:
+    return mmq_status(_stream_ptr(stream))
+
+
+def pack_q4K(v, sc, m, d_bits, dmin_bits):
+    """Host packer (numpy arrays): fields -> q4_K bytes [N][K/256][144]."""
+    import numpy as np
+    v = np.ascontiguousarray(v, np.uint8)
+    N, K = v.shape
+    sc = np.ascontiguousarray(sc, np.uint8)
+    m = np.ascontiguousarray(m, np.uint8)
+    d_bits = np.ascontiguousarray(d_bits, np.uint16)
+    dmin_bits = np.ascontiguousarray(dmin_bits, np.uint16)
+    out = np.empty((N, K // 256, 144), np.uint8)
+    ptr = lambda a: a.ctypes.data_as(ctypes.c_void_p)
+    _check(mmq_pack_q4K(ptr(v), ptr(sc), ptr(m), ptr(d_bits), ptr(dmin_bits), N, K, ptr(out)),
+           "mmq_pack_q4K")
+    return out

@@ -1,0 +1,203 @@
+// C-ABI entry points: argument validation, kernel choice, status word.
+#include <atomic>
+#include <cstring>
+#include <mutex>
+
+#include "mmq_internal.h"
+
+namespace {
+
+__device__ int g_status_word;   // one per device (module globals are per context)
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+int* g_status_addr[kMaxDevices];       // device address of g_status_word
+signed char g_arch_ok[kMaxDevices];    // 0 unknown, 1 sm_103, -1 other
+
+thread_local int t_inject_timeout = 0;
+
+int current_device(int* dev) {
+    if (cudaGetDevice(dev) != cudaSuccess) { cudaGetLastError(); return MMQ_ERR_CUDA; }
+    if (*dev < 0 || *dev >= kMaxDevices) return MMQ_ERR_DEVICE;
+    return MMQ_OK;
+}
+
+int check_device() {
+    int dev;
+    int rc = current_device(&dev);
+    if (rc) return rc;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (g_arch_ok[dev] == 0) {
+        int major = 0, minor = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
+            cudaGetLastError();
+            return MMQ_ERR_CUDA;
+        }
+        g_arch_ok[dev] = (major == 10 && minor == 3) ? 1 : -1;
+    }
+    return g_arch_ok[dev] == 1 ? MMQ_OK : MMQ_ERR_DEVICE;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+int check_q8(const mmq_q8_1_t& aq) {
+    if (!aq.qs || !aq.da || !aq.sa) return MMQ_ERR_ARG;
+    if (!aligned16(aq.qs) || !aligned16(aq.da) || !aligned16(aq.sa)) return MMQ_ERR_ALIGN;
+    return MMQ_OK;
+}
+
+int check_gemm_args(const mmq_q8_1_t& aq, const void* w, const void* out, int64_t M,
+                    int64_t N, int64_t K) {
+    int rc = check_q8(aq);
+    if (rc) return rc;
+    if (!w || !out) return MMQ_ERR_ARG;
+    if (M < 1 || N < 1 || K < 256 || (K % 256) != 0 || (N % 4) != 0) return MMQ_ERR_ARG;
+    // Coordinates fed to the kernels and tensor maps are 32-bit.
+    if (M > (int64_t(1) << 31) - 1 || N > (int64_t(1) << 31) - 1 || K > (int64_t(1) << 31) - 1)
+        return MMQ_ERR_ARG;
+    if (!aligned16(w) || !aligned16(out)) return MMQ_ERR_ALIGN;
+    return check_device();
+}
+
+int from_cuda(cudaError_t e) {
+    if (e == cudaSuccess) return MMQ_OK;
+    cudaGetLastError();
+    return MMQ_ERR_CUDA;
+}
+
+}  // namespace
+
+namespace mmq {
+
+int* status_word_ptr() {
+    int dev;
+    if (current_device(&dev)) return nullptr;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_status_addr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) {
+            cudaGetLastError();
+            return nullptr;
+        }
+        g_status_addr[dev] = static_cast<int*>(p);
+    }
+    return g_status_addr[dev];
+}
+
+}  // namespace mmq
+
+extern "C" {
+
+size_t mmq_q8_1_bytes(int64_t M, int64_t K) {
+    if (M < 1 || K < 32 || (K % 32) != 0) return 0;
+    auto up = [](size_t b) { return (b + 255) & ~size_t(255); };
+    const size_t nb = size_t(M) * size_t(K / 32);
+    return up(size_t(M) * size_t(K)) + up(nb * 4) + up(nb * 4);
+}
+
+int mmq_q8_1_view(void* buf, int64_t M, int64_t K, mmq_q8_1_t* out) {
+    if (!buf || !out || mmq_q8_1_bytes(M, K) == 0) return MMQ_ERR_ARG;
+    if (reinterpret_cast<uintptr_t>(buf) & 255) return MMQ_ERR_ALIGN;
+    auto up = [](size_t b) { return (b + 255) & ~size_t(255); };
+    const size_t nb = size_t(M) * size_t(K / 32);
+    char* p = static_cast<char*>(buf);
+    out->qs = reinterpret_cast<int8_t*>(p);
+    out->da = reinterpret_cast<float*>(p + up(size_t(M) * size_t(K)));
+    out->sa = reinterpret_cast<int32_t*>(p + up(size_t(M) * size_t(K)) + up(nb * 4));
+    return MMQ_OK;
+}
+
+int mmq_quantize_q8_1(const float* x, int64_t M, int64_t K, mmq_q8_1_t aq, void* stream) {
+    if (!x) return MMQ_ERR_ARG;
+    int rc = check_q8(aq);
+    if (rc) return rc;
+    if (M < 1 || K < 32 || (K % 32) != 0) return MMQ_ERR_ARG;
+    if (M > (int64_t(1) << 31) - 1 || K > (int64_t(1) << 31) - 1) return MMQ_ERR_ARG;
+    if (!aligned16(x)) return MMQ_ERR_ALIGN;
+    if ((rc = check_device())) return rc;
+    return from_cuda(mmq::launch_quantize_q8_1(x, M, K, aq, static_cast<cudaStream_t>(stream)));
+}
+
+size_t mmq_q4K_bytes(int64_t N, int64_t K) {
+    if (N < 1 || K < 256 || (K % 256) != 0) return 0;
+    return size_t(N) * size_t(K / 256) * 144;
+}
+
+static int run_gemm(mmq_q8_1_t aq, const uint8_t* w, float* C, int32_t* S, int64_t M,
+                    int64_t N, int64_t K, int path, cudaStream_t s) {
+    int* status = mmq::status_word_ptr();
+    if (!status) return MMQ_ERR_CUDA;
+    if (path == MMQ_PATH_AUTO) path = MMQ_PATH_MMA_S8;
+    switch (path) {
+        case MMQ_PATH_MMA_S8:
+            return from_cuda(mmq::launch_gemm_mma_s8(aq, w, C, S, M, N, K, status, s));
+        case MMQ_PATH_TC: {
+            int rc = mmq::tc_gemm_check_resources();
+            if (rc) return rc;
+            const int inject = t_inject_timeout;
+            t_inject_timeout = 0;
+            return from_cuda(mmq::launch_gemm_tc(aq, w, C, S, M, N, K, status, inject, s));
+        }
+        case MMQ_PATH_SMALL_M:
+            if (S || M > mmq::kSmallMMax) return MMQ_ERR_ARG;
+            return from_cuda(mmq::launch_gemm_small_m(aq, w, C, M, N, K, status, s));
+        default:
+            return MMQ_ERR_ARG;
+    }
+}
+
+int mmq_q4K_gemm(mmq_q8_1_t aq, const uint8_t* bq4k, float* C, int64_t M, int64_t N,
+                 int64_t K, void* stream) {
+    return mmq_q4K_gemm_path(aq, bq4k, C, M, N, K, MMQ_PATH_AUTO, stream);
+}
+
+int mmq_q4K_gemm_path(mmq_q8_1_t aq, const uint8_t* bq4k, float* C, int64_t M, int64_t N,
+                      int64_t K, int path, void* stream) {
+    if (path < MMQ_PATH_AUTO || path > MMQ_PATH_SMALL_M) return MMQ_ERR_ARG;
+    if (path == MMQ_PATH_SMALL_M && M > mmq::kSmallMMax) return MMQ_ERR_ARG;
+    int rc = check_gemm_args(aq, bq4k, C, M, N, K);
+    if (rc) return rc;
+    return run_gemm(aq, bq4k, C, nullptr, M, N, K, path, static_cast<cudaStream_t>(stream));
+}
+
+int mmq_q4K_block_dots(mmq_q8_1_t aq, const uint8_t* bq4k, int32_t* S, int64_t M, int64_t N,
+                       int64_t K, int path, void* stream) {
+    if (path != MMQ_PATH_MMA_S8 && path != MMQ_PATH_TC) return MMQ_ERR_ARG;
+    int rc = check_gemm_args(aq, bq4k, S, M, N, K);
+    if (rc) return rc;
+    return run_gemm(aq, bq4k, nullptr, S, M, N, K, path, static_cast<cudaStream_t>(stream));
+}
+
+int mmq_status(void* stream) {
+    int* p = mmq::status_word_ptr();
+    if (!p) return MMQ_ERR_CUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int v = 0;
+    const int zero = 0;
+    if (cudaStreamSynchronize(s) != cudaSuccess) { cudaGetLastError(); return MMQ_ERR_CUDA; }
+    if (cudaMemcpyAsync(&v, p, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaMemcpyAsync(p, &zero, sizeof(int), cudaMemcpyHostToDevice, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess) {
+        cudaGetLastError();
+        return MMQ_ERR_CUDA;
+    }
+    return v;
+}
+
+const char* mmq_strerror(int code) {
+    switch (code) {
+        case MMQ_OK: return "ok";
+        case MMQ_ERR_ARG: return "invalid argument (null pointer, size or value range)";
+        case MMQ_ERR_ALIGN: return "pointer not 16-byte aligned";
+        case MMQ_ERR_DEVICE: return "current device is not sm_103 (GB300)";
+        case MMQ_ERR_RESOURCE: return "shared/tensor memory budget exceeded; launch refused";
+        case MMQ_ERR_CUDA: return "CUDA runtime error";
+        case MMQ_ERR_DEVICE_TIMEOUT: return "a bounded device-side wait timed out; output invalid";
+        default: return "unknown error code";
+    }
+}
+
+void mmq_debug_inject_timeout(int enable) { t_inject_timeout = enable ? 1 : 0; }
+
+}  // extern "C"

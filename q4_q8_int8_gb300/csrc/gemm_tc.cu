@@ -1,0 +1,549 @@
+// q4_K x q8_1 GEMM on the 5th-generation tensor cores (tcgen05) of sm_103a.
+//
+// Math (web page "20 . r15 -- f32-accumulate mma probe (dead end) + rank-1
+// term2 rescale", section 2.1): for every 32-k chunk c the exact integer dot
+// S_ij = sum_k a_ik * v_jk (|S| <= 32*127*15, section 2.3) is rescaled into
+// f32:  acc_ij += (da_ic * dsv_jc) * S_ij + dma_ic * dmv_jc, dsv = d*sc,
+// dmv = -dmin*m, dma = da*sa once per token row and chunk (the rank-1 fold,
+// page "21 . r16 -- Narrow kernel gets the rank-1 fold", section 2.1).
+//
+// sm_103a has no integer kind for tcgen05.mma, so the integers go through
+// kind::f16: every quant a in [-127, 127] and nibble v in [0, 15] is an exact
+// fp16 value, every product and partial sum is an integer below 2^24, so the
+// f32 accumulator in tensor memory holds S exactly (checked bit for bit by the
+// S dump).  The nibbles are written as fp16 subnormals v * 2^-24 (just the
+// zero-extended nibble bits, no arithmetic); the 2^24 is folded into dsv.
+//
+// One CTA per SM, persistent over 128 (tokens) x 128 (weight rows) tiles,
+// warp-specialised:
+//   warp 0      TMA producer: per 256-k super-block the raw int8 A tile (two
+//               128-byte-swizzled boxes), the raw 144-byte q4_K rows, and the
+//               da / sa slices, all zero-filled past M / N.
+//   warp 1      MMA issuer (one thread): per chunk two K=16 MMAs into one of
+//               four 128-column f32 tensor-memory buffers.
+//   warps 2-3   converters: int8 -> fp16 (exact, via the 1024-offset bit
+//               pattern and one fp16 subtraction) and nibble -> fp16 into the
+//               128-byte-swizzled K-major operand layout, one 64-k chunk pair
+//               at a time; plus dsv/dmv per sub-block and weight row.
+//   warps 4-11  epilogue: thread = token row (tensor-memory lane), 64 columns;
+//               per chunk: tcgen05.ld the S tile, rescale with the fold into
+//               f32 registers; at the end of a tile store C.
+// Within a chunk the k order of both operands is permuted identically
+// (groups of four as 0,2,1,3) so that both unpacks are plain byte/nibble
+// moves; a dot product does not depend on the order of its terms.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_fp16.h>
+
+#include <mutex>
+
+#include "mmq_internal.h"
+#include "sm103_ptx.cuh"
+
+namespace {
+
+using namespace mmq::ptx;
+
+constexpr int BM = 128, BN = 128;
+constexpr int kNumRaw = 2, kNumScl = 3, kNumOp = 2, kNumTm = 4;
+constexpr int kConvWarp0 = 2, kNumConvWarps = 2, kEpiWarp0 = 4, kNumEpiWarps = 8;
+constexpr int kThreads = (kEpiWarp0 + kNumEpiWarps) * 32;   // 384: 3 warps per SM sub-partition
+constexpr uint32_t kTmemCols = 512;                          // kNumTm x BN
+
+// Shared memory map (offsets from a 1024-byte aligned base).
+constexpr int kRawASub = BM * 128;                   // 16 KB: 128 rows x 128 B, swizzled
+constexpr int kRawA = 2 * kRawASub;                  // 256 k of int8
+constexpr int kRawB = BN * 144;                      // raw q4_K rows
+constexpr int kRawStage = kRawA + kRawB;             // 51200 = 50 KB
+constexpr int kSclDa = BM * 8 * 4;                   // da [128][8] f32
+constexpr int kSclSa = BM * 8 * 4;                   // sa [128][8] i32
+constexpr int kSclCol = 8 * BN * 8;                  // (dsv, dmv) [8][128] float2
+constexpr int kSclStage = kSclDa + kSclSa + kSclCol; // 16 KB
+constexpr int kOpTile = 128 * 128;                   // 128 rows x 64 fp16 (128 B), swizzled
+constexpr int kOpStage = 2 * kOpTile;                // A + B
+constexpr int kOffRaw = 0;
+constexpr int kOffScl = kOffRaw + kNumRaw * kRawStage;
+constexpr int kOffOp = kOffScl + kNumScl * kSclStage;
+constexpr int kOffBar = kOffOp + kNumOp * kOpStage;
+// barriers: raw_full, raw_empty, scl_tma, scl_col, scl_empty, op_full, op_empty, tm_full, tm_empty
+constexpr int kNumBars = 2 * kNumRaw + 3 * kNumScl + 2 * kNumOp + 2 * kNumTm;
+constexpr int kOffMisc = kOffBar + kNumBars * 8;     // tmem slot, abort flag
+constexpr int kSmemBytes = kOffMisc + 16 + 1024;     // + alignment slack
+static_assert(kOffOp % 1024 == 0, "operand tiles need 1024-byte alignment");
+static_assert(kRawStage % 1024 == 0 && kSclStage % 1024 == 0, "stage alignment");
+static_assert(kSmemBytes <= 232448, "shared memory budget");
+
+constexpr uint32_t kRawTx = kRawA + kRawB;
+constexpr uint32_t kSclTx = kSclDa + kSclSa;
+constexpr uint32_t kIdesc = idesc_f16_f32(BM, BN);
+constexpr float kDsvScale = 16777216.0f;             // 2^24: nibbles are fp16 subnormals
+
+struct TmaMaps {
+    CUtensorMap a, b, da, sa;
+};
+
+struct Bars {
+    uint32_t base;
+    __device__ uint32_t raw_full(int s) const { return base + 8 * s; }
+    __device__ uint32_t raw_empty(int s) const { return base + 8 * (kNumRaw + s); }
+    __device__ uint32_t scl_tma(int s) const { return base + 8 * (2 * kNumRaw + s); }
+    __device__ uint32_t scl_col(int s) const { return base + 8 * (2 * kNumRaw + kNumScl + s); }
+    __device__ uint32_t scl_empty(int s) const { return base + 8 * (2 * kNumRaw + 2 * kNumScl + s); }
+    __device__ uint32_t op_full(int s) const { return base + 8 * (2 * kNumRaw + 3 * kNumScl + s); }
+    __device__ uint32_t op_empty(int s) const {
+        return base + 8 * (2 * kNumRaw + 3 * kNumScl + kNumOp + s);
+    }
+    __device__ uint32_t tm_full(int s) const {
+        return base + 8 * (2 * kNumRaw + 3 * kNumScl + 2 * kNumOp + s);
+    }
+    __device__ uint32_t tm_empty(int s) const {
+        return base + 8 * (2 * kNumRaw + 3 * kNumScl + 2 * kNumOp + kNumTm + s);
+    }
+};
+
+// Ring position: slot index and the parity of the current pass over the ring.
+template <int N>
+struct Ring {
+    int slot = 0;
+    uint32_t phase = 0;
+    __device__ void next() {
+        if (++slot == N) {
+            slot = 0;
+            phase ^= 1u;
+        }
+    }
+};
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+    uint32_t d;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+    return d;
+}
+
+// Four int8 (a0 a1 a2 a3) -> fp16 pairs {a0, a2} and {a1, a3}, exact:
+// 0x6400 | (a ^ 0x80) is the fp16 1024 + (a + 128); subtracting 1152 leaves a.
+__device__ __forceinline__ void cvt_a4(uint32_t w, uint32_t& h02, uint32_t& h13) {
+    const uint32_t u = w ^ 0x80808080u;
+    const __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));
+    __half2 x = __hsub2(*reinterpret_cast<const __half2*>(&(h02 = prmt(u, 0x64646464u, 0x4240u))), bias);
+    __half2 y = __hsub2(*reinterpret_cast<const __half2*>(&(h13 = prmt(u, 0x64646464u, 0x4341u))), bias);
+    h02 = *reinterpret_cast<uint32_t*>(&x);
+    h13 = *reinterpret_cast<uint32_t*>(&y);
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
+                 "r"(d)
+                 : "memory");
+}
+
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(addr)
+                 : "memory");
+    return v;
+}
+
+template <bool kDump>
+__global__ void __launch_bounds__(kThreads, 1)
+gemm_tc_kernel(const __grid_constant__ TmaMaps maps, float* __restrict__ C,
+               int32_t* __restrict__ S, int M, int N, int K, int* status, int inject_timeout) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~uintptr_t(1023));
+    const uint32_t sbase = smem_u32(smem);
+    const Bars bars{sbase + kOffBar};
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nsb = K / 256;
+    const int tiles_m = (M + BM - 1) / BM, tiles_n = (N + BN - 1) / BN;
+    const int num_tiles = tiles_m * tiles_n;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kNumRaw; ++s) {
+            mbar_init(bars.raw_full(s), 1);
+            mbar_init(bars.raw_empty(s), kNumConvWarps);
+        }
+        for (int s = 0; s < kNumScl; ++s) {
+            mbar_init(bars.scl_tma(s), 1);
+            mbar_init(bars.scl_col(s), kNumConvWarps);
+            mbar_init(bars.scl_empty(s), kNumEpiWarps);
+        }
+        for (int s = 0; s < kNumOp; ++s) {
+            mbar_init(bars.op_full(s), kNumConvWarps);
+            mbar_init(bars.op_empty(s), 1);
+        }
+        for (int s = 0; s < kNumTm; ++s) {
+            mbar_init(bars.tm_full(s), 1);
+            mbar_init(bars.tm_empty(s), kNumEpiWarps);
+        }
+        *abort_flag = 0;
+        fence_barrier_init();
+        fence_proxy_async_smem();
+        prefetch_tmap(&maps.a);
+        prefetch_tmap(&maps.b);
+        prefetch_tmap(&maps.da);
+        prefetch_tmap(&maps.sa);
+    }
+    __syncwarp();
+    if (warp == 0) {
+        tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            Ring<kNumRaw> rr;
+            Ring<kNumScl> sr;
+            int raw_issued[kNumRaw] = {0, 0};
+            uint32_t raw_par[kNumRaw] = {0, 0};
+            int scl_issued[kNumScl] = {0, 0, 0};
+            uint32_t scl_par[kNumScl] = {0, 0, 0};
+            bool first = true;
+            for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+                const int m0 = (tile / tiles_n) * BM, n0 = (tile % tiles_n) * BN;
+                for (int sb = 0; sb < nsb; ++sb) {
+                    if (!wait_bounded(bars.raw_empty(rr.slot), rr.phase ^ 1u, abort_flag, status))
+                        goto producer_done;
+                    const uint32_t raw = sbase + kOffRaw + rr.slot * kRawStage;
+                    if (!(first && inject_timeout)) {   // test hook: withhold this arrival
+                        mbar_arrive_expect_tx(bars.raw_full(rr.slot), kRawTx);
+                        tma_load_2d(raw, &maps.a, bars.raw_full(rr.slot), sb * 256, m0);
+                        tma_load_2d(raw + kRawASub, &maps.a, bars.raw_full(rr.slot), sb * 256 + 128, m0);
+                        tma_load_2d(raw + kRawA, &maps.b, bars.raw_full(rr.slot), sb * 144, n0);
+                        raw_issued[rr.slot] = 1;
+                        raw_par[rr.slot] = rr.phase;
+                    }
+                    first = false;
+                    rr.next();
+                    if (!wait_bounded(bars.scl_empty(sr.slot), sr.phase ^ 1u, abort_flag, status))
+                        goto producer_done;
+                    const uint32_t scl = sbase + kOffScl + sr.slot * kSclStage;
+                    mbar_arrive_expect_tx(bars.scl_tma(sr.slot), kSclTx);
+                    tma_load_2d(scl, &maps.da, bars.scl_tma(sr.slot), sb * 8, m0);
+                    tma_load_2d(scl + kSclDa, &maps.sa, bars.scl_tma(sr.slot), sb * 8, m0);
+                    scl_issued[sr.slot] = 1;
+                    scl_par[sr.slot] = sr.phase;
+                    sr.next();
+                }
+            }
+        producer_done:
+            // Let every copy already issued land before the CTA can exit.
+            for (int s = 0; s < kNumRaw; ++s)
+                if (raw_issued[s]) wait_drain(bars.raw_full(s), raw_par[s], status);
+            for (int s = 0; s < kNumScl; ++s)
+                if (scl_issued[s]) wait_drain(bars.scl_tma(s), scl_par[s], status);
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            Ring<kNumOp> orr;
+            Ring<kNumTm> tr;
+            int issued = 0;
+            int last_slot = 0;
+            uint32_t last_par = 0;
+            for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+                for (int sb = 0; sb < nsb; ++sb) {
+                    for (int q = 0; q < 4; ++q) {
+                        if (!wait_bounded(bars.op_full(orr.slot), orr.phase, abort_flag, status))
+                            goto mma_done;
+                        tc_fence_after();
+                        const uint32_t opA = sbase + kOffOp + orr.slot * kOpStage;
+                        const uint32_t opB = opA + kOpTile;
+                        for (int h = 0; h < 2; ++h) {
+                            if (!wait_bounded(bars.tm_empty(tr.slot), tr.phase ^ 1u, abort_flag, status))
+                                goto mma_done;
+                            tc_fence_after();
+                            const uint32_t d = tmem_base + uint32_t(tr.slot * BN);
+#pragma unroll
+                            for (int kk = 0; kk < 2; ++kk) {
+                                const uint32_t koff = uint32_t(h * 64 + kk * 32);   // bytes within the 128-B row
+                                mma_f16(d, smem_desc_sw128(opA + koff), smem_desc_sw128(opB + koff),
+                                        kIdesc, uint32_t(kk));
+                            }
+                            mma_commit(bars.tm_full(tr.slot));
+                            issued = 1;
+                            last_slot = tr.slot;
+                            last_par = tr.phase;
+                            tr.next();
+                        }
+                        mma_commit(bars.op_empty(orr.slot));
+                        orr.next();
+                    }
+                }
+            }
+        mma_done:
+            if (issued) wait_drain(bars.tm_full(last_slot), last_par, status);
+        }
+    } else if (warp < kEpiWarp0) {
+        // -------------------------------------------------------- converters
+        const int tc = threadIdx.x - kConvWarp0 * 32;   // 0..63: rows tc and tc + 64
+        Ring<kNumRaw> rr;
+        Ring<kNumScl> sr;
+        Ring<kNumOp> orr;
+        for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+            for (int sb = 0; sb < nsb; ++sb) {
+                if (!wait_bounded(bars.raw_full(rr.slot), rr.phase, abort_flag, status)) goto conv_done;
+                const uint32_t raw = sbase + kOffRaw + rr.slot * kRawStage;
+                const uint8_t* rawB = smem + kOffRaw + rr.slot * kRawStage + kRawA;
+                // per-sub-block weight scales (exact in f32)
+                if (!wait_bounded(bars.scl_empty(sr.slot), sr.phase ^ 1u, abort_flag, status)) goto conv_done;
+                for (int rh = 0; rh < 2; ++rh) {
+                    const int t = tc + 64 * rh;
+                    const uint8_t* blk = rawB + t * 144;
+                    const float d = __half2float(__ushort_as_half(uint16_t(blk[0] | (blk[1] << 8))));
+                    const float dmin = __half2float(__ushort_as_half(uint16_t(blk[2] | (blk[3] << 8))));
+                    const uint8_t* s = blk + 4;
+                    float2* col = reinterpret_cast<float2*>(smem + kOffScl + sr.slot * kSclStage + kSclDa + kSclSa);
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        int sc, m;
+                        if (c < 4) {
+                            sc = s[c] & 63;
+                            m = s[c + 4] & 63;
+                        } else {
+                            sc = (s[c + 4] & 15) | ((s[c - 4] >> 6) << 4);
+                            m = (s[c + 4] >> 4) | ((s[c] >> 6) << 4);
+                        }
+                        col[c * BN + t] = make_float2(d * float(sc) * kDsvScale, -(dmin * float(m)));
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bars.scl_col(sr.slot));
+                sr.next();
+
+                for (int q = 0; q < 4; ++q) {   // chunk pair q = chunks 2q, 2q+1
+                    if (!wait_bounded(bars.op_empty(orr.slot), orr.phase ^ 1u, abort_flag, status))
+                        goto conv_done;
+                    const uint32_t opA = sbase + kOffOp + orr.slot * kOpStage;
+                    const uint32_t opB = opA + kOpTile;
+#pragma unroll 1
+                    for (int rh = 0; rh < 2; ++rh) {
+                        const int t = tc + 64 * rh;
+                        const int sw = t & 7;
+                        // A: row t, 64 bytes of the pair = 4 granules of 16 int8
+#pragma unroll
+                        for (int g = 0; g < 4; ++g) {
+                            const int lg = (q & 1) * 4 + g;   // granule within the 128-B swizzled sub-tile
+                            const uint4 w = ld_shared_v4(raw + (q >> 1) * kRawASub + t * 128 + ((lg ^ sw) << 4));
+                            uint32_t p0, p1, p2, p3, p4, p5, p6, p7;
+                            cvt_a4(w.x, p0, p1);
+                            cvt_a4(w.y, p2, p3);
+                            cvt_a4(w.z, p4, p5);
+                            cvt_a4(w.w, p6, p7);
+                            st_shared_v4(opA + t * 128 + (((2 * g) ^ sw) << 4), p0, p1, p2, p3);
+                            st_shared_v4(opA + t * 128 + (((2 * g + 1) ^ sw) << 4), p4, p5, p6, p7);
+                        }
+                        // B: row t, 32 bytes of nibbles = chunk 2q (low) and 2q+1 (high)
+#pragma unroll
+                        for (int G = 0; G < 2; ++G) {
+                            const uint4 w = *reinterpret_cast<const uint4*>(rawB + t * 144 + 16 + 32 * q + 16 * G);
+                            const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+                            uint32_t lo[8], hi[8];
+#pragma unroll
+                            for (int u = 0; u < 4; ++u) {
+                                lo[2 * u] = ww[u] & 0x000F000Fu;            // {e0, e2} low nibbles
+                                lo[2 * u + 1] = (ww[u] >> 8) & 0x000F000Fu; // {e1, e3}
+                                hi[2 * u] = (ww[u] >> 4) & 0x000F000Fu;
+                                hi[2 * u + 1] = (ww[u] >> 12) & 0x000F000Fu;
+                            }
+                            st_shared_v4(opB + t * 128 + (((2 * G) ^ sw) << 4), lo[0], lo[1], lo[2], lo[3]);
+                            st_shared_v4(opB + t * 128 + (((2 * G + 1) ^ sw) << 4), lo[4], lo[5], lo[6], lo[7]);
+                            st_shared_v4(opB + t * 128 + (((4 + 2 * G) ^ sw) << 4), hi[0], hi[1], hi[2], hi[3]);
+                            st_shared_v4(opB + t * 128 + (((5 + 2 * G) ^ sw) << 4), hi[4], hi[5], hi[6], hi[7]);
+                        }
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bars.op_full(orr.slot));
+                    orr.next();
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bars.raw_empty(rr.slot));
+                rr.next();
+            }
+        }
+    conv_done:;
+    } else {
+        // ---------------------------------------------------------- epilogue
+        const int ew = warp - kEpiWarp0;
+        const int quarter = warp & 3;                  // tensor-memory lanes this warp may read
+        const int colhalf = ew >> 2;                   // columns [64*colhalf, +64)
+        const int row = quarter * 32 + lane;
+        Ring<kNumScl> sr;
+        Ring<kNumTm> tr;
+        for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+            const int m0 = (tile / tiles_n) * BM, n0 = (tile % tiles_n) * BN;
+            float acc[64];
+#pragma unroll
+            for (int j = 0; j < 64; ++j) acc[j] = 0.0f;
+            for (int sb = 0; sb < nsb; ++sb) {
+                if (!wait_bounded(bars.scl_tma(sr.slot), sr.phase, abort_flag, status)) goto epi_done;
+                if (!wait_bounded(bars.scl_col(sr.slot), sr.phase, abort_flag, status)) goto epi_done;
+                const uint8_t* scl = smem + kOffScl + sr.slot * kSclStage;
+                const float* sda = reinterpret_cast<const float*>(scl);
+                const int32_t* ssa = reinterpret_cast<const int32_t*>(scl + kSclDa);
+                const float4* col4 = reinterpret_cast<const float4*>(scl + kSclDa + kSclSa);
+                for (int c = 0; c < 8; ++c) {
+                    if (!wait_bounded(bars.tm_full(tr.slot), tr.phase, abort_flag, status)) goto epi_done;
+                    tc_fence_after();
+                    const float da = sda[row * 8 + c];
+                    const float dma = da * float(ssa[row * 8 + c]);   // rank-1 fold: once per row
+                    const uint32_t taddr = tmem_base + (uint32_t(quarter * 32) << 16) +
+                                           uint32_t(tr.slot * BN + colhalf * 64);
+#pragma unroll
+                    for (int part = 0; part < 4; ++part) {
+                        uint32_t s[16];
+                        tmem_ld_32x32b_x16(taddr + part * 16, s);
+                        tmem_wait_ld();
+                        if (part == 3) {   // whole S tile is in registers: hand the buffer back
+                            tc_fence_before();
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive(bars.tm_empty(tr.slot));
+                        }
+                        if (kDump) {
+                            const int64_t gr = int64_t(m0) + row;
+#pragma unroll
+                            for (int j = 0; j < 16; ++j) {
+                                const int64_t gc = int64_t(n0) + colhalf * 64 + part * 16 + j;
+                                if (gr < M && gc < N)
+                                    S[(gr * N + gc) * (K / 32) + sb * 8 + c] =
+                                        int32_t(__uint_as_float(s[j]) * kDsvScale);
+                            }
+                        } else {
+#pragma unroll
+                            for (int j = 0; j < 16; j += 2) {
+                                const float4 cs = col4[(c * BN + colhalf * 64 + part * 16 + j) >> 1];
+                                float a0 = acc[part * 16 + j], a1 = acc[part * 16 + j + 1];
+                                a0 = fmaf(da * cs.x, __uint_as_float(s[j]), a0);
+                                a1 = fmaf(da * cs.z, __uint_as_float(s[j + 1]), a1);
+                                a0 = fmaf(dma, cs.y, a0);
+                                a1 = fmaf(dma, cs.w, a1);
+                                acc[part * 16 + j] = a0;
+                                acc[part * 16 + j + 1] = a1;
+                            }
+                        }
+                    }
+                    tr.next();
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bars.scl_empty(sr.slot));
+                sr.next();
+            }
+            if (!kDump) {
+                const int64_t gr = int64_t(m0) + row;
+                if (gr < M) {
+                    float* crow = C + gr * N;
+#pragma unroll
+                    for (int j = 0; j < 64; j += 4) {
+                        const int gc = n0 + colhalf * 64 + j;
+                        if (gc < N)
+                            *reinterpret_cast<float4*>(crow + gc) =
+                                make_float4(acc[j], acc[j + 1], acc[j + 2], acc[j + 3]);
+                    }
+                }
+            }
+        }
+    epi_done:;
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem_base, kTmemCols);
+    }
+}
+
+// ------------------------------------------------------------------- host
+PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+        else
+            cudaGetLastError();
+    });
+    return fn;
+}
+
+bool encode_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t inner,
+               uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
+               CUtensorMapSwizzle sw) {
+    auto fn = get_encode();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {inner, outer};
+    const cuuint64_t strides[1] = {row_bytes};
+    const cuuint32_t box[2] = {box_inner, box_outer};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+namespace mmq {
+
+int tc_gemm_check_resources() {
+    int dev = 0, optin = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess) {
+        cudaGetLastError();
+        return MMQ_ERR_CUDA;
+    }
+    return optin >= kSmemBytes ? MMQ_OK : MMQ_ERR_RESOURCE;
+}
+
+cudaError_t launch_gemm_tc(mmq_q8_1_t aq, const uint8_t* w, float* C, int32_t* S, int64_t M,
+                           int64_t N, int64_t K, int* status, int inject_timeout, cudaStream_t s) {
+    TmaMaps maps;
+    const uint64_t nb = uint64_t(K / 32), nsb = uint64_t(K / 256);
+    if (!encode_2d(&maps.a, CU_TENSOR_MAP_DATA_TYPE_UINT8, aq.qs, uint64_t(K), uint64_t(M),
+                   uint64_t(K), 128, BM, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_2d(&maps.b, CU_TENSOR_MAP_DATA_TYPE_UINT8, w, nsb * 144, uint64_t(N), nsb * 144,
+                   144, BN, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !encode_2d(&maps.da, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, aq.da, nb, uint64_t(M), nb * 4, 8, BM,
+                   CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !encode_2d(&maps.sa, CU_TENSOR_MAP_DATA_TYPE_INT32, aq.sa, nb, uint64_t(M), nb * 4, 8, BM,
+                   CU_TENSOR_MAP_SWIZZLE_NONE))
+        return cudaErrorInvalidValue;
+    int dev = 0, nsm = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
+    const int64_t tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
+    const int grid = int(tiles < nsm ? tiles : nsm);
+    cudaError_t e;
+    if (S) {
+        auto k = gemm_tc_kernel<true>;
+        if ((e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes)))
+            return e;
+        k<<<grid, kThreads, kSmemBytes, s>>>(maps, C, S, int(M), int(N), int(K), status,
+                                              inject_timeout);
+    } else {
+        auto k = gemm_tc_kernel<false>;
+        if ((e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes)))
+            return e;
+        k<<<grid, kThreads, kSmemBytes, s>>>(maps, C, S, int(M), int(N), int(K), status,
+                                              inject_timeout);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace mmq

@@ -1,0 +1,30 @@
+// Internal declarations shared by the library's translation units (host side).
+#pragma once
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/mmq.h"
+
+namespace mmq {
+
+// Per-device status word (a __device__ int defined in api.cu); kernels get
+// its address as an argument and set it to an MMQ_ERR_* code on failure.
+int* status_word_ptr();   // nullptr on failure (sets no error)
+
+// Launchers (defined in the kernel translation units).  Arguments are
+// already validated; they return cudaGetLastError() of the launch.
+cudaError_t launch_quantize_q8_1(const float* x, int64_t M, int64_t K,
+                                 mmq_q8_1_t aq, cudaStream_t s);
+cudaError_t launch_gemm_mma_s8(mmq_q8_1_t aq, const uint8_t* w, float* C,
+                               int32_t* S, int64_t M, int64_t N, int64_t K,
+                               int* status, cudaStream_t s);
+int tc_gemm_check_resources();   // MMQ_OK or MMQ_ERR_RESOURCE
+cudaError_t launch_gemm_tc(mmq_q8_1_t aq, const uint8_t* w, float* C,
+                           int32_t* S, int64_t M, int64_t N, int64_t K,
+                           int* status, int inject_timeout, cudaStream_t s);
+cudaError_t launch_gemm_small_m(mmq_q8_1_t aq, const uint8_t* w, float* C,
+                                int64_t M, int64_t N, int64_t K, int* status,
+                                cudaStream_t s);
+constexpr int64_t kSmallMMax = 64;
+
+}  // namespace mmq
