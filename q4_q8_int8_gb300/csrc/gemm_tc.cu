@@ -15,19 +15,23 @@
 // zero-extended nibble bits, no arithmetic); the 2^24 is folded into dsv.
 //
 // One CTA per SM, persistent over 128 (tokens) x 128 (weight rows) tiles,
-// warp-specialised:
+// warp-specialised (16 warps; setmaxnreg moves registers to the epilogue):
 //   warp 0      TMA producer: per 256-k super-block the raw int8 A tile (two
 //               128-byte-swizzled boxes), the raw 144-byte q4_K rows, and the
 //               da / sa slices, all zero-filled past M / N.
 //   warp 1      MMA issuer (one thread): per chunk two K=16 MMAs into one of
 //               four 128-column f32 tensor-memory buffers.
-//   warps 2-3   converters: int8 -> fp16 (exact, via the 1024-offset bit
-//               pattern and one fp16 subtraction) and nibble -> fp16 into the
-//               128-byte-swizzled K-major operand layout, one 64-k chunk pair
-//               at a time; plus dsv/dmv per sub-block and weight row.
-//   warps 4-11  epilogue: thread = token row (tensor-memory lane), 64 columns;
-//               per chunk: tcgen05.ld the S tile, rescale with the fold into
-//               f32 registers; at the end of a tile store C.
+//   warps 2-3   scale tables per super-block: dsv/dmv per weight row and
+//               chunk, (da, dma = da*sa) per token row and chunk.
+//   warps 4-7   operand converters: int8 -> fp16 (exact, via the 1024-offset
+//               bit pattern and one fp16 subtraction) and nibble -> fp16 into
+//               the 128-byte-swizzled K-major layout, one 64-k chunk pair at a
+//               time, one row per thread.
+//   warps 8-15  epilogue: per chunk tcgen05.ld of the S tile (16x256b shape:
+//               each thread holds 4 rows x 16 columns, so one column-scale load
+//               serves four rows), the rescale with the fold in packed f32x2
+//               arithmetic, the next tensor-memory load issued before the
+//               current part is computed; C stored at the end of a tile.
 // Within a chunk the k order of both operands is permuted identically
 // (groups of four as 0,2,1,3) so that both unpacks are plain byte/nibble
 // moves; a dot product does not depend on the order of its terms.
@@ -45,9 +49,14 @@ namespace {
 using namespace mmq::ptx;
 
 constexpr int BM = 128, BN = 128;
-constexpr int kNumRaw = 2, kNumScl = 3, kNumOp = 2, kNumTm = 4;
-constexpr int kConvWarp0 = 2, kNumConvWarps = 2, kEpiWarp0 = 4, kNumEpiWarps = 8;
-constexpr int kThreads = (kEpiWarp0 + kNumEpiWarps) * 32;   // 384: 3 warps per SM sub-partition
+constexpr int kNumRaw = 2, kNumScl = 2, kNumOp = 2, kNumTm = 4;
+constexpr int kSclWarp0 = 2, kNumSclWarps = 2, kConvWarp0 = 4, kNumConvWarps = 4;
+constexpr int kEpiWarp0 = 8, kNumEpiWarps = 8;
+constexpr int kThreads = (kEpiWarp0 + kNumEpiWarps) * 32;   // 512
+// Register split: warpgroups 0-1 (producer, MMA, scale tables, converters)
+// give up registers to warpgroups 2-3 (epilogue).  Launch budget: 512 x 128.
+constexpr uint32_t kRegsLow = 72, kRegsHigh = 184, kRegsLaunch = 128;
+static_assert(256 * kRegsLow + 256 * kRegsHigh <= kThreads * kRegsLaunch, "register split");
 constexpr uint32_t kTmemCols = 512;                          // kNumTm x BN
 
 // Shared memory map (offsets from a 1024-byte aligned base).
@@ -57,8 +66,12 @@ constexpr int kRawB = BN * 144;                      // raw q4_K rows
 constexpr int kRawStage = kRawA + kRawB;             // 51200 = 50 KB
 constexpr int kSclDa = BM * 8 * 4;                   // da [128][8] f32
 constexpr int kSclSa = BM * 8 * 4;                   // sa [128][8] i32
-constexpr int kSclCol = 8 * BN * 8;                  // (dsv, dmv) [8][128] float2
-constexpr int kSclStage = kSclDa + kSclSa + kSclCol; // 16 KB
+constexpr int kSclCol = 8 * BN * 8;                  // [8 chunks][64 column pairs] float4
+                                                     //   {dsv_2p, dsv_2p+1, dmv_2p, dmv_2p+1}
+constexpr int kSclRow = 8 * BM * 8;                  // [8 chunks][128 rows] float2 {da, da*sa}
+constexpr int kOffSclCol = kSclDa + kSclSa;
+constexpr int kOffSclRow = kOffSclCol + kSclCol;
+constexpr int kSclStage = kOffSclRow + kSclRow;      // 24 KB
 constexpr int kOpTile = 128 * 128;                   // 128 rows x 64 fp16 (128 B), swizzled
 constexpr int kOpStage = 2 * kOpTile;                // A + B
 constexpr int kOffRaw = 0;
@@ -167,11 +180,11 @@ gemm_tc_kernel(const __grid_constant__ TmaMaps maps, float* __restrict__ C,
     if (threadIdx.x == 0) {
         for (int s = 0; s < kNumRaw; ++s) {
             mbar_init(bars.raw_full(s), 1);
-            mbar_init(bars.raw_empty(s), kNumConvWarps);
+            mbar_init(bars.raw_empty(s), kNumConvWarps + kNumSclWarps);
         }
         for (int s = 0; s < kNumScl; ++s) {
             mbar_init(bars.scl_tma(s), 1);
-            mbar_init(bars.scl_col(s), kNumConvWarps);
+            mbar_init(bars.scl_col(s), kNumSclWarps);
             mbar_init(bars.scl_empty(s), kNumEpiWarps);
         }
         for (int s = 0; s < kNumOp; ++s) {
@@ -200,15 +213,17 @@ gemm_tc_kernel(const __grid_constant__ TmaMaps maps, float* __restrict__ C,
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
+    if (warp < kEpiWarp0) {
+    setmaxnreg_dec<kRegsLow>();
     if (warp == 0) {
         // ------------------------------------------------------ TMA producer
         if (lane == 0) {
             Ring<kNumRaw> rr;
             Ring<kNumScl> sr;
-            int raw_issued[kNumRaw] = {0, 0};
-            uint32_t raw_par[kNumRaw] = {0, 0};
-            int scl_issued[kNumScl] = {0, 0, 0};
-            uint32_t scl_par[kNumScl] = {0, 0, 0};
+            int raw_issued[kNumRaw] = {};
+            uint32_t raw_par[kNumRaw] = {};
+            int scl_issued[kNumScl] = {};
+            uint32_t scl_par[kNumScl] = {};
             bool first = true;
             for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
                 const int m0 = (tile / tiles_n) * BM, n0 = (tile % tiles_n) * BN;
@@ -285,83 +300,116 @@ gemm_tc_kernel(const __grid_constant__ TmaMaps maps, float* __restrict__ C,
         mma_done:
             if (issued) wait_drain(bars.tm_full(last_slot), last_par, status);
         }
-    } else if (warp < kEpiWarp0) {
-        // -------------------------------------------------------- converters
-        const int tc = threadIdx.x - kConvWarp0 * 32;   // 0..63: rows tc and tc + 64
+    } else if (warp < kConvWarp0) {
+        // ------------------------------------------------------ scale tables
+        // Weight rows: dsv = d*sc (times 2^24 for the subnormal nibbles) and
+        // dmv = -dmin*m, exact in f32, as column pairs {dsv0, dsv1, dmv0, dmv1};
+        // token rows: {da, dma = da*sa}, the rank-1 fold once per row and chunk.
+        const int ts = threadIdx.x - kSclWarp0 * 32;   // 0..63: rows ts and ts + 64
         Ring<kNumRaw> rr;
         Ring<kNumScl> sr;
+        for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+            for (int sb = 0; sb < nsb; ++sb) {
+                if (!wait_bounded(bars.raw_full(rr.slot), rr.phase, abort_flag, status)) goto scl_done;
+                if (!wait_bounded(bars.scl_empty(sr.slot), sr.phase ^ 1u, abort_flag, status)) goto scl_done;
+                if (!wait_bounded(bars.scl_tma(sr.slot), sr.phase, abort_flag, status)) goto scl_done;
+                {
+                    const uint32_t rawB = sbase + kOffRaw + rr.slot * kRawStage + kRawA;
+                    const uint32_t scl = sbase + kOffScl + sr.slot * kSclStage;
+                    float* colf = reinterpret_cast<float*>(smem + kOffScl + sr.slot * kSclStage + kOffSclCol);
+                    float2* row2 = reinterpret_cast<float2*>(smem + kOffScl + sr.slot * kSclStage + kOffSclRow);
+#pragma unroll
+                    for (int rh = 0; rh < 2; ++rh) {
+                        const int t = ts + 64 * rh;
+                        const uint4 hdr = ld_shared_v4(rawB + t * 144);   // d, dmin, s[0..11]
+                        const float d = __half2float(__ushort_as_half(uint16_t(hdr.x & 0xFFFFu)));
+                        const float dmin = __half2float(__ushort_as_half(uint16_t(hdr.x >> 16)));
+                        const uint32_t s0 = hdr.y, s1 = hdr.z, s2 = hdr.w;   // s[0..3], s[4..7], s[8..11]
+                        float* cp = colf + (t >> 1) * 4 + (t & 1);
+#pragma unroll
+                        for (int c = 0; c < 8; ++c) {
+                            uint32_t sc, m;
+                            if (c < 4) {
+                                sc = (s0 >> (8 * c)) & 63u;
+                                m = (s1 >> (8 * c)) & 63u;
+                            } else {
+                                const int b = 8 * (c - 4);
+                                sc = ((s2 >> b) & 15u) | (((s0 >> (b + 6)) & 3u) << 4);
+                                m = ((s2 >> (b + 4)) & 15u) | (((s1 >> (b + 6)) & 3u) << 4);
+                            }
+                            cp[c * (BN * 2)] = d * float(sc) * kDsvScale;
+                            cp[c * (BN * 2) + 2] = -(dmin * float(m));
+                        }
+                        const uint4 da0 = ld_shared_v4(scl + t * 32), da1 = ld_shared_v4(scl + t * 32 + 16);
+                        const uint4 sa0 = ld_shared_v4(scl + kSclDa + t * 32);
+                        const uint4 sa1 = ld_shared_v4(scl + kSclDa + t * 32 + 16);
+                        const uint32_t dav[8] = {da0.x, da0.y, da0.z, da0.w, da1.x, da1.y, da1.z, da1.w};
+                        const uint32_t sav[8] = {sa0.x, sa0.y, sa0.z, sa0.w, sa1.x, sa1.y, sa1.z, sa1.w};
+#pragma unroll
+                        for (int c = 0; c < 8; ++c) {
+                            const float da = __uint_as_float(dav[c]);
+                            row2[c * BM + t] = make_float2(da, da * float(int32_t(sav[c])));
+                        }
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(bars.scl_col(sr.slot));
+                    mbar_arrive(bars.raw_empty(rr.slot));
+                }
+                sr.next();
+                rr.next();
+            }
+        }
+    scl_done:;
+    } else if (warp < kEpiWarp0) {
+        // -------------------------------------------------------- converters
+        const int t = threadIdx.x - kConvWarp0 * 32;   // 0..127: this thread's row
+        const int sw = t & 7;
+        Ring<kNumRaw> rr;
         Ring<kNumOp> orr;
         for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
             for (int sb = 0; sb < nsb; ++sb) {
                 if (!wait_bounded(bars.raw_full(rr.slot), rr.phase, abort_flag, status)) goto conv_done;
                 const uint32_t raw = sbase + kOffRaw + rr.slot * kRawStage;
-                const uint8_t* rawB = smem + kOffRaw + rr.slot * kRawStage + kRawA;
-                // per-sub-block weight scales (exact in f32)
-                if (!wait_bounded(bars.scl_empty(sr.slot), sr.phase ^ 1u, abort_flag, status)) goto conv_done;
-                for (int rh = 0; rh < 2; ++rh) {
-                    const int t = tc + 64 * rh;
-                    const uint8_t* blk = rawB + t * 144;
-                    const float d = __half2float(__ushort_as_half(uint16_t(blk[0] | (blk[1] << 8))));
-                    const float dmin = __half2float(__ushort_as_half(uint16_t(blk[2] | (blk[3] << 8))));
-                    const uint8_t* s = blk + 4;
-                    float2* col = reinterpret_cast<float2*>(smem + kOffScl + sr.slot * kSclStage + kSclDa + kSclSa);
-#pragma unroll
-                    for (int c = 0; c < 8; ++c) {
-                        int sc, m;
-                        if (c < 4) {
-                            sc = s[c] & 63;
-                            m = s[c + 4] & 63;
-                        } else {
-                            sc = (s[c + 4] & 15) | ((s[c - 4] >> 6) << 4);
-                            m = (s[c + 4] >> 4) | ((s[c] >> 6) << 4);
-                        }
-                        col[c * BN + t] = make_float2(d * float(sc) * kDsvScale, -(dmin * float(m)));
-                    }
-                }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bars.scl_col(sr.slot));
-                sr.next();
-
+                const uint32_t rawB = raw + kRawA + t * 144 + 16;
                 for (int q = 0; q < 4; ++q) {   // chunk pair q = chunks 2q, 2q+1
                     if (!wait_bounded(bars.op_empty(orr.slot), orr.phase ^ 1u, abort_flag, status))
                         goto conv_done;
-                    const uint32_t opA = sbase + kOffOp + orr.slot * kOpStage;
+                    const uint32_t opA = sbase + kOffOp + orr.slot * kOpStage + t * 128;
                     const uint32_t opB = opA + kOpTile;
-#pragma unroll 1
-                    for (int rh = 0; rh < 2; ++rh) {
-                        const int t = tc + 64 * rh;
-                        const int sw = t & 7;
-                        // A: row t, 64 bytes of the pair = 4 granules of 16 int8
+                    uint4 wa[4], wb[2];
 #pragma unroll
-                        for (int g = 0; g < 4; ++g) {
-                            const int lg = (q & 1) * 4 + g;   // granule within the 128-B swizzled sub-tile
-                            const uint4 w = ld_shared_v4(raw + (q >> 1) * kRawASub + t * 128 + ((lg ^ sw) << 4));
-                            uint32_t p0, p1, p2, p3, p4, p5, p6, p7;
-                            cvt_a4(w.x, p0, p1);
-                            cvt_a4(w.y, p2, p3);
-                            cvt_a4(w.z, p4, p5);
-                            cvt_a4(w.w, p6, p7);
-                            st_shared_v4(opA + t * 128 + (((2 * g) ^ sw) << 4), p0, p1, p2, p3);
-                            st_shared_v4(opA + t * 128 + (((2 * g + 1) ^ sw) << 4), p4, p5, p6, p7);
+                    for (int g = 0; g < 4; ++g)   // A: 64 int8 of the pair, granule (q&1)*4+g of a swizzled sub-tile
+                        wa[g] = ld_shared_v4(raw + (q >> 1) * kRawASub + t * 128 + ((((q & 1) * 4 + g) ^ sw) << 4));
+#pragma unroll
+                    for (int G = 0; G < 2; ++G)   // B: 32 bytes of nibbles, chunk 2q low / 2q+1 high
+                        wb[G] = ld_shared_v4(rawB + 32 * q + 16 * G);
+#pragma unroll
+                    for (int g = 0; g < 4; ++g) {
+                        uint32_t p0, p1, p2, p3, p4, p5, p6, p7;
+                        cvt_a4(wa[g].x, p0, p1);
+                        cvt_a4(wa[g].y, p2, p3);
+                        cvt_a4(wa[g].z, p4, p5);
+                        cvt_a4(wa[g].w, p6, p7);
+                        st_shared_v4(opA + (((2 * g) ^ sw) << 4), p0, p1, p2, p3);
+                        st_shared_v4(opA + (((2 * g + 1) ^ sw) << 4), p4, p5, p6, p7);
+                    }
+#pragma unroll
+                    for (int G = 0; G < 2; ++G) {
+                        const uint32_t ww[4] = {wb[G].x, wb[G].y, wb[G].z, wb[G].w};
+                        uint32_t lo[8], hi[8];
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            lo[2 * u] = ww[u] & 0x000F000Fu;            // {e0, e2} low nibbles
+                            lo[2 * u + 1] = (ww[u] >> 8) & 0x000F000Fu; // {e1, e3}
+                            hi[2 * u] = (ww[u] >> 4) & 0x000F000Fu;
+                            hi[2 * u + 1] = (ww[u] >> 12) & 0x000F000Fu;
                         }
-                        // B: row t, 32 bytes of nibbles = chunk 2q (low) and 2q+1 (high)
-#pragma unroll
-                        for (int G = 0; G < 2; ++G) {
-                            const uint4 w = *reinterpret_cast<const uint4*>(rawB + t * 144 + 16 + 32 * q + 16 * G);
-                            const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
-                            uint32_t lo[8], hi[8];
-#pragma unroll
-                            for (int u = 0; u < 4; ++u) {
-                                lo[2 * u] = ww[u] & 0x000F000Fu;            // {e0, e2} low nibbles
-                                lo[2 * u + 1] = (ww[u] >> 8) & 0x000F000Fu; // {e1, e3}
-                                hi[2 * u] = (ww[u] >> 4) & 0x000F000Fu;
-                                hi[2 * u + 1] = (ww[u] >> 12) & 0x000F000Fu;
-                            }
-                            st_shared_v4(opB + t * 128 + (((2 * G) ^ sw) << 4), lo[0], lo[1], lo[2], lo[3]);
-                            st_shared_v4(opB + t * 128 + (((2 * G + 1) ^ sw) << 4), lo[4], lo[5], lo[6], lo[7]);
-                            st_shared_v4(opB + t * 128 + (((4 + 2 * G) ^ sw) << 4), hi[0], hi[1], hi[2], hi[3]);
-                            st_shared_v4(opB + t * 128 + (((5 + 2 * G) ^ sw) << 4), hi[4], hi[5], hi[6], hi[7]);
-                        }
+                        st_shared_v4(opB + (((2 * G) ^ sw) << 4), lo[0], lo[1], lo[2], lo[3]);
+                        st_shared_v4(opB + (((2 * G + 1) ^ sw) << 4), lo[4], lo[5], lo[6], lo[7]);
+                        st_shared_v4(opB + (((4 + 2 * G) ^ sw) << 4), hi[0], hi[1], hi[2], hi[3]);
+                        st_shared_v4(opB + (((5 + 2 * G) ^ sw) << 4), hi[4], hi[5], hi[6], hi[7]);
                     }
                     fence_proxy_async_smem();
                     __syncwarp();
@@ -374,82 +422,132 @@ gemm_tc_kernel(const __grid_constant__ TmaMaps maps, float* __restrict__ C,
             }
         }
     conv_done:;
+    }
     } else {
+        setmaxnreg_inc<kRegsHigh>();
         // ---------------------------------------------------------- epilogue
+        // Thread t of a warp holds, per chunk, rows quarter*32 + t/4 + 8k
+        // (k = 0..3) x columns colhalf*64 + 8g + 2(t%4) + {0,1} (g = 0..7).
+        // A chunk is read from tensor memory in two parts (lanes +0..15 give
+        // rows k = 0,1; lanes +16..31 give k = 2,3); the load of the next part
+        // is in flight while the current one is computed.
         const int ew = warp - kEpiWarp0;
         const int quarter = warp & 3;                  // tensor-memory lanes this warp may read
         const int colhalf = ew >> 2;                   // columns [64*colhalf, +64)
-        const int row = quarter * 32 + lane;
+        const int tq = lane >> 2, tr4 = lane & 3;
+        const uint32_t tlane0 = uint32_t(quarter * 32) << 16, tlane1 = uint32_t(quarter * 32 + 16) << 16;
         Ring<kNumScl> sr;
         Ring<kNumTm> tr;
         for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
             const int m0 = (tile / tiles_n) * BM, n0 = (tile % tiles_n) * BN;
-            float acc[64];
+            uint64_t acc[4][8];
 #pragma unroll
-            for (int j = 0; j < 64; ++j) acc[j] = 0.0f;
+            for (int k = 0; k < 4; ++k)
+#pragma unroll
+                for (int g = 0; g < 8; ++g) acc[k][g] = 0ull;
+            uint32_t b0[32], b1[32];
+            // prologue: first part of the tile's first chunk
+            if (!wait_bounded(bars.scl_col(sr.slot), sr.phase, abort_flag, status)) goto epi_done;
+            if (!wait_bounded(bars.tm_full(tr.slot), tr.phase, abort_flag, status)) goto epi_done;
+            tc_fence_after();
+            tmem_ld_16x256b_x8(tmem_base + tlane0 + uint32_t(tr.slot * BN + colhalf * 64), b0);
+            tmem_wait_ld();
             for (int sb = 0; sb < nsb; ++sb) {
-                if (!wait_bounded(bars.scl_tma(sr.slot), sr.phase, abort_flag, status)) goto epi_done;
-                if (!wait_bounded(bars.scl_col(sr.slot), sr.phase, abort_flag, status)) goto epi_done;
                 const uint8_t* scl = smem + kOffScl + sr.slot * kSclStage;
-                const float* sda = reinterpret_cast<const float*>(scl);
-                const int32_t* ssa = reinterpret_cast<const int32_t*>(scl + kSclDa);
-                const float4* col4 = reinterpret_cast<const float4*>(scl + kSclDa + kSclSa);
+                const float4* col4 = reinterpret_cast<const float4*>(scl + kOffSclCol);
+                const float2* row2 = reinterpret_cast<const float2*>(scl + kOffSclRow);
                 for (int c = 0; c < 8; ++c) {
-                    if (!wait_bounded(bars.tm_full(tr.slot), tr.phase, abort_flag, status)) goto epi_done;
-                    tc_fence_after();
-                    const float da = sda[row * 8 + c];
-                    const float dma = da * float(ssa[row * 8 + c]);   // rank-1 fold: once per row
-                    const uint32_t taddr = tmem_base + (uint32_t(quarter * 32) << 16) +
-                                           uint32_t(tr.slot * BN + colhalf * 64);
+                    float4 cs[8];
 #pragma unroll
-                    for (int part = 0; part < 4; ++part) {
-                        uint32_t s[16];
-                        tmem_ld_32x32b_x16(taddr + part * 16, s);
-                        tmem_wait_ld();
-                        if (part == 3) {   // whole S tile is in registers: hand the buffer back
-                            tc_fence_before();
-                            __syncwarp();
-                            if (lane == 0) mbar_arrive(bars.tm_empty(tr.slot));
-                        }
+                    for (int g = 0; g < 8; ++g) cs[g] = col4[c * 64 + colhalf * 32 + 4 * g + tr4];
+                    float2 rr[4];
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) rr[k] = row2[c * BM + quarter * 32 + tq + 8 * k];
+                    // second part of this chunk, then compute the first part
+                    tmem_ld_16x256b_x8(tmem_base + tlane1 + uint32_t(tr.slot * BN + colhalf * 64), b1);
+#pragma unroll
+                    for (int kk = 0; kk < 2; ++kk) {
                         if (kDump) {
-                            const int64_t gr = int64_t(m0) + row;
+                            const int64_t gr = int64_t(m0) + quarter * 32 + tq + 8 * kk;
 #pragma unroll
-                            for (int j = 0; j < 16; ++j) {
-                                const int64_t gc = int64_t(n0) + colhalf * 64 + part * 16 + j;
-                                if (gr < M && gc < N)
-                                    S[(gr * N + gc) * (K / 32) + sb * 8 + c] =
-                                        int32_t(__uint_as_float(s[j]) * kDsvScale);
-                            }
+                            for (int g = 0; g < 8; ++g)
+#pragma unroll
+                                for (int e = 0; e < 2; ++e) {
+                                    const int64_t gc = int64_t(n0) + colhalf * 64 + 8 * g + 2 * tr4 + e;
+                                    if (gr < M && gc < N)
+                                        S[(gr * N + gc) * (K / 32) + sb * 8 + c] =
+                                            int32_t(__uint_as_float(b0[4 * g + 2 * kk + e]) * kDsvScale);
+                                }
                         } else {
+                            const uint64_t da2 = pack2(rr[kk].x, rr[kk].x), dma2 = pack2(rr[kk].y, rr[kk].y);
 #pragma unroll
-                            for (int j = 0; j < 16; j += 2) {
-                                const float4 cs = col4[(c * BN + colhalf * 64 + part * 16 + j) >> 1];
-                                float a0 = acc[part * 16 + j], a1 = acc[part * 16 + j + 1];
-                                a0 = fmaf(da * cs.x, __uint_as_float(s[j]), a0);
-                                a1 = fmaf(da * cs.z, __uint_as_float(s[j + 1]), a1);
-                                a0 = fmaf(dma, cs.y, a0);
-                                a1 = fmaf(dma, cs.w, a1);
-                                acc[part * 16 + j] = a0;
-                                acc[part * 16 + j + 1] = a1;
+                            for (int g = 0; g < 8; ++g) {
+                                const uint64_t c1 = fmul2(da2, pack2(cs[g].x, cs[g].y));
+                                const uint64_t a = ffma2(c1, pack2u(b0[4 * g + 2 * kk], b0[4 * g + 2 * kk + 1]), acc[kk][g]);
+                                acc[kk][g] = ffma2(dma2, pack2(cs[g].z, cs[g].w), a);
                             }
                         }
                     }
+                    tmem_wait_ld();
+                    // the whole S tile of this chunk is in registers: hand the buffer back
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bars.tm_empty(tr.slot));
                     tr.next();
+                    const bool last_in_sb = (c == 7);
+                    const bool has_next = !(last_in_sb && sb == nsb - 1);
+                    if (last_in_sb) {   // scale tables of this super-block no longer needed
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(bars.scl_empty(sr.slot));
+                        sr.next();
+                    }
+                    if (has_next) {
+                        if (last_in_sb &&
+                            !wait_bounded(bars.scl_col(sr.slot), sr.phase, abort_flag, status))
+                            goto epi_done;
+                        if (!wait_bounded(bars.tm_full(tr.slot), tr.phase, abort_flag, status)) goto epi_done;
+                        tc_fence_after();
+                        tmem_ld_16x256b_x8(tmem_base + tlane0 + uint32_t(tr.slot * BN + colhalf * 64), b0);
+                    }
+#pragma unroll
+                    for (int kk = 0; kk < 2; ++kk) {
+                        const int k = 2 + kk;
+                        if (kDump) {
+                            const int64_t gr = int64_t(m0) + quarter * 32 + tq + 8 * k;
+#pragma unroll
+                            for (int g = 0; g < 8; ++g)
+#pragma unroll
+                                for (int e = 0; e < 2; ++e) {
+                                    const int64_t gc = int64_t(n0) + colhalf * 64 + 8 * g + 2 * tr4 + e;
+                                    if (gr < M && gc < N)
+                                        S[(gr * N + gc) * (K / 32) + sb * 8 + c] =
+                                            int32_t(__uint_as_float(b1[4 * g + 2 * kk + e]) * kDsvScale);
+                                }
+                        } else {
+                            const uint64_t da2 = pack2(rr[k].x, rr[k].x), dma2 = pack2(rr[k].y, rr[k].y);
+#pragma unroll
+                            for (int g = 0; g < 8; ++g) {
+                                const uint64_t c1 = fmul2(da2, pack2(cs[g].x, cs[g].y));
+                                const uint64_t a = ffma2(c1, pack2u(b1[4 * g + 2 * kk], b1[4 * g + 2 * kk + 1]), acc[k][g]);
+                                acc[k][g] = ffma2(dma2, pack2(cs[g].z, cs[g].w), a);
+                            }
+                        }
+                    }
+                    if (has_next) tmem_wait_ld();
                 }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bars.scl_empty(sr.slot));
-                sr.next();
             }
             if (!kDump) {
-                const int64_t gr = int64_t(m0) + row;
-                if (gr < M) {
-                    float* crow = C + gr * N;
 #pragma unroll
-                    for (int j = 0; j < 64; j += 4) {
-                        const int gc = n0 + colhalf * 64 + j;
-                        if (gc < N)
-                            *reinterpret_cast<float4*>(crow + gc) =
-                                make_float4(acc[j], acc[j + 1], acc[j + 2], acc[j + 3]);
+                for (int k = 0; k < 4; ++k) {
+                    const int64_t gr = int64_t(m0) + quarter * 32 + tq + 8 * k;
+                    if (gr < M) {
+                        float* crow = C + gr * N;
+#pragma unroll
+                        for (int g = 0; g < 8; ++g) {
+                            const int gc = n0 + colhalf * 64 + 8 * g + 2 * tr4;
+                            if (gc < N)
+                                *reinterpret_cast<float2*>(crow + gc) = make_float2(lo_f(acc[k][g]), hi_f(acc[k][g]));
+                        }
                     }
                 }
             }
@@ -527,6 +625,15 @@ cudaError_t launch_gemm_tc(mmq_q8_1_t aq, const uint8_t* w, float* C, int32_t* S
     int dev = 0, nsm = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
+    // The register split (setmaxnreg) needs the block launched with exactly
+    // kRegsLaunch registers per thread; refuse anything else.
+    {
+        cudaFuncAttributes fa;
+        cudaError_t e = S ? cudaFuncGetAttributes(&fa, gemm_tc_kernel<true>)
+                          : cudaFuncGetAttributes(&fa, gemm_tc_kernel<false>);
+        if (e != cudaSuccess) return e;
+        if (fa.numRegs != int(kRegsLaunch)) return cudaErrorInvalidConfiguration;
+    }
     const int64_t tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
     const int grid = int(tiles < nsm ? tiles : nsm);
     cudaError_t e;
