@@ -128,7 +128,7 @@ static int run_gemm(mmq_q8_1_t aq, const uint8_t* w, float* C, int32_t* S, int64
                     int64_t N, int64_t K, int path, cudaStream_t s) {
     int* status = mmq::status_word_ptr();
     if (!status) return MMQ_ERR_CUDA;
-    if (path == MMQ_PATH_AUTO) path = MMQ_PATH_MMA_S8;
+    if (path == MMQ_PATH_AUTO) path = (M <= mmq::kSmallMMax && !S) ? MMQ_PATH_SMALL_M : MMQ_PATH_TC;
     switch (path) {
         case MMQ_PATH_MMA_S8:
             return from_cuda(mmq::launch_gemm_mma_s8(aq, w, C, S, M, N, K, status, s));

@@ -74,6 +74,76 @@ __global__ void ffma2_loop(int iters, float* out) {
     if (s == 1234.5f) out[0] = s;
 }
 
+
+// ---- tensor-memory load bandwidth: each warp reads its lane quarter of a
+// 512-column allocation repeatedly (contents are whatever the allocation
+// holds; only the data movement is timed).
+template <int kShape, int kInflight>
+__global__ void tmem_ld_loop(int iters, unsigned* out) {
+    __shared__ unsigned slot;
+    const int warp = threadIdx.x >> 5;
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(
+            (unsigned)__cvta_generic_to_shared(&slot)));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+    asm volatile("tcgen05.fence::before_thread_sync;");
+    __syncthreads();
+    asm volatile("tcgen05.fence::after_thread_sync;");
+    const unsigned base = slot + ((unsigned)((warp & 3) * 32) << 16);
+    const unsigned col0 = (unsigned)((warp >> 2) * 64);
+    unsigned acc = 0;
+    for (int it = 0; it < iters; ++it) {
+#pragma unroll
+        for (int f = 0; f < kInflight; ++f) {
+            unsigned r[32];
+            // 64-column aligned start in [0, 384]: every load stays inside the 512 columns
+            const unsigned addr = base + ((col0 + (unsigned)(f * 64 + it * 64)) % 448u / 64u * 64u);
+            if (kShape == 0)
+                asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+                    : "=r"(r[0]),"=r"(r[1]),"=r"(r[2]),"=r"(r[3]),"=r"(r[4]),"=r"(r[5]),"=r"(r[6]),"=r"(r[7]),"=r"(r[8]),"=r"(r[9]),"=r"(r[10]),"=r"(r[11]),"=r"(r[12]),"=r"(r[13]),"=r"(r[14]),"=r"(r[15]),"=r"(r[16]),"=r"(r[17]),"=r"(r[18]),"=r"(r[19]),"=r"(r[20]),"=r"(r[21]),"=r"(r[22]),"=r"(r[23]),"=r"(r[24]),"=r"(r[25]),"=r"(r[26]),"=r"(r[27]),"=r"(r[28]),"=r"(r[29]),"=r"(r[30]),"=r"(r[31]) : "r"(addr));
+            else
+                asm volatile("tcgen05.ld.sync.aligned.16x256b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+                    : "=r"(r[0]),"=r"(r[1]),"=r"(r[2]),"=r"(r[3]),"=r"(r[4]),"=r"(r[5]),"=r"(r[6]),"=r"(r[7]),"=r"(r[8]),"=r"(r[9]),"=r"(r[10]),"=r"(r[11]),"=r"(r[12]),"=r"(r[13]),"=r"(r[14]),"=r"(r[15]),"=r"(r[16]),"=r"(r[17]),"=r"(r[18]),"=r"(r[19]),"=r"(r[20]),"=r"(r[21]),"=r"(r[22]),"=r"(r[23]),"=r"(r[24]),"=r"(r[25]),"=r"(r[26]),"=r"(r[27]),"=r"(r[28]),"=r"(r[29]),"=r"(r[30]),"=r"(r[31]) : "r"(addr));
+            asm volatile("tcgen05.wait::ld.sync.aligned;");
+#pragma unroll
+            for (int i = 0; i < 32; ++i) acc ^= r[i];
+        }
+    }
+    if (acc == 0x9e3779b9u) out[0] = acc;
+    asm volatile("tcgen05.fence::before_thread_sync;");
+    __syncthreads();
+    if (warp == 0) {
+        __syncwarp();
+        asm volatile("tcgen05.fence::after_thread_sync;");
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(slot));
+    }
+}
+
+// ---- legacy warp-level f16 MMA rate (mma.sync m16n8k16, f32 accumulate).
+__global__ void hmma_loop(int iters, int* out) {
+    uint32_t a[4] = {threadIdx.x, threadIdx.x * 3u, threadIdx.x ^ 5u, 7u};
+    uint32_t b0 = threadIdx.x * 11u, b1 = 13u;
+    float c[8][4];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int r = 0; r < 4; ++r) c[i][r] = 0.f;
+    for (int it = 0; it < iters; ++it) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            asm volatile(
+                "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+                "{%8,%9}, {%0,%1,%2,%3};\n"
+                : "+f"(c[i][0]), "+f"(c[i][1]), "+f"(c[i][2]), "+f"(c[i][3])
+                : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+    }
+    float s = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) s += c[i][0] + c[i][1] + c[i][2] + c[i][3];
+    if (s == 1234.5f) out[0] = 1;
+}
+
 int main() {
     int dev = 0, nsm = 0, clk = 0;
     CK(cudaGetDevice(&dev));
@@ -121,5 +191,39 @@ int main() {
     printf("{\"sms\": %d, \"clock_khz_attr\": %d, \"mma_sync_s8_tops\": %.2f, "
            "\"ffma_tflops\": %.2f, \"ffma2_tflops\": %.2f}\n",
            nsm, clk, mma_tops, ffma_tflops, ffma2_tflops);
+    // hmma f16
+    hmma_loop<<<blocks, threads>>>(100, dout);
+    CK(cudaDeviceSynchronize());
+    CK(cudaEventRecord(e0));
+    hmma_loop<<<blocks, threads>>>(it_mma, dout);
+    CK(cudaEventRecord(e1));
+    CK(cudaEventSynchronize(e1));
+    CK(cudaEventElapsedTime(&ms, e0, e1));
+    const double hmma_tflops = warps * it_mma * 8 * (16.0 * 8 * 16) * 2 / (ms * 1e-3) / 1e12;
+    printf("{\"hmma_f16_f32_tflops\": %.2f}\n", hmma_tflops);
+
+    // tensor-memory loads: bytes per SM per clock at the attribute clock
+    const int it_t = 4000;
+    auto run_t = [&](void (*k)(int, unsigned*), int nwarps, int inflight, const char* name) -> int {
+        k<<<nsm, nwarps * 32>>>(10, (unsigned*)dout);
+        if (cudaDeviceSynchronize() != cudaSuccess) return 1;
+        cudaEventRecord(e0);
+        k<<<nsm, nwarps * 32>>>(it_t, (unsigned*)dout);
+        cudaEventRecord(e1);
+        cudaEventSynchronize(e1);
+        float t;
+        cudaEventElapsedTime(&t, e0, e1);
+        const double bytes = double(nsm) * nwarps * it_t * inflight * 32 * 32 * 4;
+        const double per_sm_per_ns = bytes / nsm / (t * 1e6);
+        printf("{\"tmem_ld\": \"%s\", \"warps\": %d, \"inflight\": %d, \"GBps_per_sm\": %.1f, \"bytes_per_clk_at_2070MHz\": %.1f, \"TBps_total\": %.2f}\n",
+               name, nwarps, inflight, per_sm_per_ns, per_sm_per_ns / 2.07, bytes / (t * 1e-3) / 1e12);
+        return 0;
+    };
+    if (run_t(tmem_ld_loop<0, 1>, 4, 1, "32x32b.x32") || run_t(tmem_ld_loop<0, 1>, 8, 1, "32x32b.x32") ||
+        run_t(tmem_ld_loop<0, 1>, 16, 1, "32x32b.x32") || run_t(tmem_ld_loop<0, 2>, 8, 2, "32x32b.x32") ||
+        run_t(tmem_ld_loop<1, 1>, 8, 1, "16x256b.x8") || run_t(tmem_ld_loop<1, 1>, 16, 1, "16x256b.x8") ||
+        run_t(tmem_ld_loop<1, 2>, 8, 2, "16x256b.x8"))
+        return 1;
     return 0;
 }
+
