@@ -1,5 +1,6 @@
 // q4_K x q8_1 GEMM for few tokens (M <= 64): bound by streaming the q4_K
-// weights from HBM once.
+// weights from HBM once.  M <= 4 uses a dp4a dot-product kernel (below);
+// 4 < M <= 64 the tensor-core kernel described here.
 //
 // Math as in the large-M kernels (web page "20 . r15 -- f32-accumulate mma
 // probe (dead end) + rank-1 term2 rescale", section 2.1; fold from page
@@ -9,13 +10,18 @@
 //
 // Design (weights are the big operand, so they go on the MMA's 16-row side
 // and the tokens on its 8-column side):
-//  - CTA = 4 warps = 64 weight rows (16 per warp); a cluster of S CTAs splits
-//    the 256-k super-blocks of K; the S partial sums are added in rank order
-//    through distributed shared memory, so the result is deterministic and
-//    no global scratch is used.
+//  - CTA = G groups of 4 warps, 64 weight rows (16 per warp of a group);
+//    the CTA's super-blocks are dealt round-robin to the groups, each group
+//    with its own TMA stage, so the super-blocks in flight are worked on in
+//    parallel; the group partials are added in group order at the end.
+//  - A cluster of S CTAs splits the 256-k super-blocks of K; ranks 1..S-1
+//    push their partial sums into rank 0's shared memory, which adds them in
+//    rank order: deterministic, and no global scratch.
+//  - Once a stage has landed, its group converts the tokens' quants into
+//    ready-made fp16 MMA fragments and a (da, dma = da*sa) table in shared
+//    memory, once for the group's four warps.
 //  - Per super-block one TMA stage brings the 64 raw q4_K rows (144 B each),
-//    the tokens' int8 quants (two 128-byte-swizzled boxes) and their da / sa;
-//    a 4-deep ring keeps up to 4 super-blocks of weights in flight per CTA.
+//    the tokens' int8 quants (two 128-byte-swizzled boxes) and their da / sa.
 //  - Integer dots on mma.sync m16n8k16 with fp16 operands holding exact
 //    integers (nibbles as fp16 subnormals v * 2^-24, quants via the 1024
 //    bit-pattern offset), f32 accumulation: S comes out exact (times 2^-24,
@@ -39,11 +45,9 @@ namespace {
 
 using namespace mmq::ptx;
 
-constexpr int kRows = 64;                 // weight rows per CTA
-constexpr int kWarps = 4;
-constexpr int kThreads = kWarps * 32;
-constexpr int kStages = 4;
+constexpr int kRows = 64;                 // weight rows per CTA (4 row-warps x 16)
 constexpr int kMaxTok = 64;               // tokens per launch (M <= 64)
+constexpr int kMaxSplit = 8;              // CTAs per cluster along K
 constexpr int kW = kRows * 144;           // 9216 B raw q4_K rows
 constexpr float kDsvScale = 16777216.0f;  // 2^24: nibbles are fp16 subnormals
 
@@ -51,19 +55,30 @@ struct SmallMaps {
     CUtensorMap w, a, da, sa;
 };
 
-// Stage layout for a token count padded to mp (multiple of 8):
-//   [0, kW)                     raw q4_K rows
-//   [aoff, aoff + 2*mp*128)      token quants: two swizzled boxes of mp x 128 B
-//   [doff, doff + mp*32)         da [mp][8] f32
-//   [soff, soff + mp*32)         sa [mp][8] i32
-struct StageLayout {
-    int aoff, doff, soff, bytes;
-    __host__ __device__ static StageLayout make(int mp) {
-        StageLayout L;
-        L.aoff = ((kW + 1023) / 1024) * 1024;                 // swizzled boxes want 1024-B alignment
+// Shared-memory layout for NF token fragments (mp = 8*NF tokens) and G warp
+// groups.  Group q owns one TMA stage and one work area:
+//   stage  [0, kW) raw q4_K rows | [aoff, +2*mp*128) token quants as two
+//          128-byte-swizzled boxes | [doff, +mp*32) da [mp][8] | [soff, +mp*32) sa
+//   work   [0, NF*8*32*16) fp16 token fragments [f][c][lane] (4 x u32 each) |
+//          [fbytes, +8*NF*4*16) token scales [c][f][j] {da_t0, da_t1, dma_t0, dma_t1}
+// then the split-K landing area (partials pushed by cluster ranks 1..S-1:
+// [rank-1][128 threads][NF] float4), barriers and the abort flag.
+struct Layout {
+    int aoff, doff, soff, stage, fbytes, work, stages_off, work_off, red_off, bar_off, total;
+    __host__ __device__ static Layout make(int nf, int groups, int split) {
+        Layout L;
+        const int mp = 8 * nf;
+        L.aoff = ((kW + 1023) / 1024) * 1024;
         L.doff = L.aoff + 2 * mp * 128;
         L.soff = L.doff + mp * 32;
-        L.bytes = ((L.soff + mp * 32 + 1023) / 1024) * 1024;
+        L.stage = ((L.soff + mp * 32 + 1023) / 1024) * 1024;
+        L.fbytes = nf * 8 * 32 * 16;
+        L.work = L.fbytes + 8 * nf * 4 * 16;
+        L.stages_off = 0;
+        L.work_off = groups * L.stage;
+        L.red_off = L.work_off + groups * L.work;
+        L.bar_off = L.red_off + (split - 1) * 128 * nf * 16;
+        L.total = L.bar_off + 8 * groups + 16;
         return L;
     }
 };
@@ -94,11 +109,6 @@ __device__ __forceinline__ void hmma(float (&c)[4], uint32_t a0, uint32_t a1, ui
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
 __device__ __forceinline__ void cluster_sync() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
@@ -107,14 +117,17 @@ __device__ __forceinline__ uint32_t map_shared_rank(uint32_t saddr, uint32_t ran
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(d) : "r"(saddr), "r"(rank));
     return d;
 }
-__device__ __forceinline__ float ld_dsmem_f32(uint32_t addr) {
-    float v;
-    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
-    return v;
+__device__ __forceinline__ void st_dsmem_v4(uint32_t addr, float4 v) {
+    asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(v.x), "f"(v.y),
+                 "f"(v.z), "f"(v.w)
+                 : "memory");
+}
+__device__ __forceinline__ void group_sync(int group) {   // the 4 warps (128 threads) of a group
+    asm volatile("bar.sync %0, 128;" ::"r"(group + 1) : "memory");
 }
 
-template <int NF>
-__global__ void __launch_bounds__(kThreads)
+template <int NF, int G>
+__global__ void __launch_bounds__(G * 128)
 gemm_small_kernel(const __grid_constant__ SmallMaps maps, float* __restrict__ C, int M, int N,
                   int K, int split, int* status) {
     extern __shared__ uint8_t smem_raw[];
@@ -122,11 +135,12 @@ gemm_small_kernel(const __grid_constant__ SmallMaps maps, float* __restrict__ C,
                                                ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
     constexpr int mp = NF * 8;
-    const StageLayout L = StageLayout::make(mp);
-    const uint32_t bar0 = sbase + kStages * L.bytes;
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kStages * L.bytes + 8 * kStages);
+    const Layout L = Layout::make(NF, G, split);
+    const uint32_t bar0 = sbase + L.bar_off;
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.bar_off + 8 * G);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int grp = warp >> 2, gt = threadIdx.x & 127;   // group, thread within the group
     const int g = lane >> 2, j = lane & 3;
     const int rank = int(blockIdx.x % unsigned(split));
     const int n0 = int(blockIdx.x / unsigned(split)) * kRows;
@@ -134,44 +148,70 @@ gemm_small_kernel(const __grid_constant__ SmallMaps maps, float* __restrict__ C,
     const int sb_begin = (nsb * rank) / split, sb_end = (nsb * (rank + 1)) / split;
     const int nmine = sb_end - sb_begin;
     const uint32_t stage_tx = uint32_t(kW + 2 * mp * 128 + 2 * mp * 32);
+    const uint32_t bar = bar0 + 8 * grp;
+    uint8_t* st = smem + L.stages_off + grp * L.stage;
+    const uint32_t st_s = sbase + L.stages_off + grp * L.stage;
+    uint8_t* work = smem + L.work_off + grp * L.work;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) mbar_init(bar0 + 8 * s, 1);
+        for (int q = 0; q < G; ++q) mbar_init(bar0 + 8 * q, 1);
         *abort_flag = 0;
         fence_barrier_init();
         fence_proxy_async_smem();
     }
     __syncthreads();
 
-    auto issue = [&](int i) {   // super-block sb_begin + i into stage i % kStages
-        const int s = i % kStages;
-        const uint32_t st = sbase + s * L.bytes;
+    // group leader issues the TMA of super-block sb_begin + i into its stage
+    auto issue = [&](int i) {
         const int sb = sb_begin + i;
-        mbar_arrive_expect_tx(bar0 + 8 * s, stage_tx);
-        tma_load_2d(st, &maps.w, bar0 + 8 * s, sb * 144, n0);
-        tma_load_2d(st + L.aoff, &maps.a, bar0 + 8 * s, sb * 256, 0);
-        tma_load_2d(st + L.aoff + mp * 128, &maps.a, bar0 + 8 * s, sb * 256 + 128, 0);
-        tma_load_2d(st + L.doff, &maps.da, bar0 + 8 * s, sb * 8, 0);
-        tma_load_2d(st + L.soff, &maps.sa, bar0 + 8 * s, sb * 8, 0);
+        mbar_arrive_expect_tx(bar, stage_tx);
+        tma_load_2d(st_s, &maps.w, bar, sb * 144, n0);
+        tma_load_2d(st_s + L.aoff, &maps.a, bar, sb * 256, 0);
+        tma_load_2d(st_s + L.aoff + mp * 128, &maps.a, bar, sb * 256 + 128, 0);
+        tma_load_2d(st_s + L.doff, &maps.da, bar, sb * 8, 0);
+        tma_load_2d(st_s + L.soff, &maps.sa, bar, sb * 8, 0);
     };
-    int issued = 0;   // stages issued (thread 0's count)
-    if (threadIdx.x == 0) {
-        prefetch_tmap(&maps.w);
-        prefetch_tmap(&maps.a);
-        for (; issued < kStages && issued < nmine; ++issued) issue(issued);
+    int last_issued = -1;   // leader only
+    if (gt == 0 && grp < nmine) {
+        issue(grp);
+        last_issued = grp;
     }
 
     uint64_t acc[NF][2];   // per token fragment: rows g (tokens 2j, 2j+1) and g + 8
 #pragma unroll
     for (int f = 0; f < NF; ++f) acc[f][0] = acc[f][1] = 0ull;
 
-    const int r0 = warp * 16 + g;   // this thread's weight rows r0 and r0 + 8 (within the CTA)
-    for (int i = 0; i < nmine; ++i) {
-        const int s = i % kStages;
-        // A timed-out wait raises the CTA abort flag; the loop exit below is
-        // decided after a barrier, so every thread leaves at the same point.
-        if (wait_bounded(bar0 + 8 * s, uint32_t((i / kStages) & 1), abort_flag, status)) {
-            const uint8_t* st = smem + s * L.bytes;
+    const int r0 = (warp & 3) * 16 + g;   // this thread's weight rows r0 and r0 + 8 (within the CTA)
+    int pass = 0;
+    for (int i = grp; i < nmine; i += G, ++pass) {
+        // A timed-out wait raises the CTA abort flag; the exit is decided after
+        // a group barrier, so the group's threads leave together.
+        const bool landed = wait_bounded(bar, uint32_t(pass & 1), abort_flag, status);
+        if (landed) {
+            // ---- tokens: fp16 fragments and (da, dma) once for the group
+            for (int e = gt; e < NF * 8 * 32; e += 128) {
+                const int f = e >> 8, c = (e >> 5) & 7, ln = e & 31;
+                const int tok = 8 * f + (ln >> 2), jj = ln & 3;
+                const uint32_t gran = uint32_t(((c & 3) * 2 + (jj >> 1)) ^ (tok & 7));
+                const uint2 q = *reinterpret_cast<const uint2*>(st + L.aoff + (c >> 2) * mp * 128 +
+                                                                tok * 128 + (gran << 4) + (jj & 1) * 8);
+                uint4 fr;
+                cvt_a4(q.x, fr.x, fr.y);
+                cvt_a4(q.y, fr.z, fr.w);
+                *reinterpret_cast<uint4*>(work + e * 16) = fr;
+            }
+            for (int e = gt; e < 8 * NF * 4; e += 128) {
+                const int c = e / (NF * 4), f = (e >> 2) % NF, jj = e & 3;
+                const int t0 = 8 * f + 2 * jj;
+                const float* sda = reinterpret_cast<const float*>(st + L.doff);
+                const int32_t* ssa = reinterpret_cast<const int32_t*>(st + L.soff);
+                const float da0 = sda[t0 * 8 + c], da1 = sda[(t0 + 1) * 8 + c];
+                *reinterpret_cast<float4*>(work + L.fbytes + e * 16) =
+                    make_float4(da0, da1, da0 * float(ssa[t0 * 8 + c]), da1 * float(ssa[(t0 + 1) * 8 + c]));
+            }
+        }
+        group_sync(grp);   // fragments and token scales are ready
+        if (landed) {
             // weight-row scales for the 8 chunks: dsv (times 2^24) and dmv
             float dsv[2][8], dmv[2][8];
             uint32_t wq[2][4][2];   // [row][pair][step]: nibble words, elements 8j + 4s + 0..3
@@ -196,97 +236,89 @@ gemm_small_kernel(const __grid_constant__ SmallMaps maps, float* __restrict__ C,
                     dmv[h][c] = -(dmin * float(m));
                 }
 #pragma unroll
-                for (int p = 0; p < 4; ++p) {
-                    const uint2 v = *reinterpret_cast<const uint2*>(row + 16 + 32 * p + 8 * j);
-                    wq[h][p][0] = v.x;
-                    wq[h][p][1] = v.y;
+                for (int pp = 0; pp < 4; ++pp) {
+                    const uint2 v = *reinterpret_cast<const uint2*>(row + 16 + 32 * pp + 8 * j);
+                    wq[h][pp][0] = v.x;
+                    wq[h][pp][1] = v.y;
                 }
             }
-            const float* sda = reinterpret_cast<const float*>(st + L.doff);
-            const int32_t* ssa = reinterpret_cast<const int32_t*>(st + L.soff);
-            const uint8_t* sa8 = st + L.aoff;
 #pragma unroll
             for (int c = 0; c < 8; ++c) {
-                const int p = c >> 1, hsh = (c & 1) * 4;   // chunk 2p: low nibbles, 2p+1: high
+                const int pp = c >> 1, hsh = (c & 1) * 4;   // chunk 2p: low nibbles, 2p+1: high
                 uint32_t a[2][4];
 #pragma unroll
                 for (int sstep = 0; sstep < 2; ++sstep) {
-                    a[sstep][0] = (wq[0][p][sstep] >> hsh) & 0x000F000Fu;        // row g, elements +0, +2
-                    a[sstep][1] = (wq[1][p][sstep] >> hsh) & 0x000F000Fu;        // row g + 8
-                    a[sstep][2] = (wq[0][p][sstep] >> (hsh + 8)) & 0x000F000Fu;  // row g, elements +1, +3
-                    a[sstep][3] = (wq[1][p][sstep] >> (hsh + 8)) & 0x000F000Fu;
+                    a[sstep][0] = (wq[0][pp][sstep] >> hsh) & 0x000F000Fu;        // row g, elements +0, +2
+                    a[sstep][1] = (wq[1][pp][sstep] >> hsh) & 0x000F000Fu;        // row g + 8
+                    a[sstep][2] = (wq[0][pp][sstep] >> (hsh + 8)) & 0x000F000Fu;  // row g, elements +1, +3
+                    a[sstep][3] = (wq[1][pp][sstep] >> (hsh + 8)) & 0x000F000Fu;
                 }
                 const uint64_t dsv0 = pack2(dsv[0][c], dsv[0][c]), dsv1 = pack2(dsv[1][c], dsv[1][c]);
                 const uint64_t dmv0 = pack2(dmv[0][c], dmv[0][c]), dmv1 = pack2(dmv[1][c], dmv[1][c]);
 #pragma unroll
                 for (int f = 0; f < NF; ++f) {
-                    // token g of fragment f: 8 bytes at chunk c, offset 8j (128-B swizzled box c / 4)
-                    const int tok = 8 * f + g;
-                    const uint32_t gran = uint32_t(((c & 3) * 2 + (j >> 1)) ^ (tok & 7));
-                    const uint2 q = *reinterpret_cast<const uint2*>(
-                        sa8 + (c >> 2) * mp * 128 + tok * 128 + (gran << 4) + (j & 1) * 8);
-                    uint32_t b00, b01, b10, b11;
-                    cvt_a4(q.x, b00, b01);
-                    cvt_a4(q.y, b10, b11);
+                    const uint4 fr = *reinterpret_cast<const uint4*>(work + ((f * 8 + c) * 32 + lane) * 16);
+                    const float4 ts = *reinterpret_cast<const float4*>(work + L.fbytes + ((c * NF + f) * 4 + j) * 16);
                     float sc4[4] = {0.f, 0.f, 0.f, 0.f};
-                    hmma(sc4, a[0][0], a[0][1], a[0][2], a[0][3], b00, b01);
-                    hmma(sc4, a[1][0], a[1][1], a[1][2], a[1][3], b10, b11);
+                    hmma(sc4, a[0][0], a[0][1], a[0][2], a[0][3], fr.x, fr.y);
+                    hmma(sc4, a[1][0], a[1][1], a[1][2], a[1][3], fr.z, fr.w);
                     // C fragment: (row g, tokens 8f + 2j, +1) and (row g + 8, same tokens)
-                    const int t0 = 8 * f + 2 * j;
-                    const float da0 = sda[t0 * 8 + c], da1 = sda[(t0 + 1) * 8 + c];
-                    const uint64_t da2 = pack2(da0, da1);
-                    const uint64_t dma2 =
-                        pack2(da0 * float(ssa[t0 * 8 + c]), da1 * float(ssa[(t0 + 1) * 8 + c]));
+                    const uint64_t da2 = pack2(ts.x, ts.y), dma2 = pack2(ts.z, ts.w);
                     const uint64_t s01 = pack2(sc4[0], sc4[1]), s23 = pack2(sc4[2], sc4[3]);
                     acc[f][0] = ffma2(dma2, dmv0, ffma2(fmul2(da2, dsv0), s01, acc[f][0]));
                     acc[f][1] = ffma2(dma2, dmv1, ffma2(fmul2(da2, dsv1), s23, acc[f][1]));
                 }
             }
         }
-        __syncthreads();   // every warp is done reading stage s
+        group_sync(grp);   // the group is done reading its stage
         if (*abort_flag) break;
-        if (threadIdx.x == 0 && issued < nmine) {
+        if (gt == 0 && i + G < nmine) {
             fence_proxy_async_smem();
-            issue(issued);
-            ++issued;
+            issue(i + G);
+            last_issued = i + G;
         }
     }
-    if (threadIdx.x == 0) {
-        // let every copy issued land before stage memory is reused or the CTA exits
-        for (int i2 = (issued > kStages ? issued - kStages : 0); i2 < issued; ++i2)
-            wait_drain(bar0 + 8 * (i2 % kStages), uint32_t((i2 / kStages) & 1), status);
+    if (gt == 0 && last_issued >= 0) {
+        // the group's last copy must land before its stage memory is reused or the CTA exits
+        wait_drain(bar, uint32_t(((last_issued - grp) / G) & 1), status);
     }
     __syncthreads();
 
-    // ---- reduce the split-K partials across the cluster in rank order
-    float* part = reinterpret_cast<float*>(smem);   // [NF][2][2] per thread, 16*NF B
-    const uint32_t my_off = uint32_t(threadIdx.x) * (NF * 4) * 4;
-    if (split > 1) {
+    // ---- add the groups' partials (super-blocks were dealt round-robin)
+    float4* part = reinterpret_cast<float4*>(smem + L.stages_off);   // [G][128][NF]
+    if (grp > 0) {
 #pragma unroll
-        for (int f = 0; f < NF; ++f) {
-            part[(threadIdx.x * NF + f) * 4 + 0] = lo_f(acc[f][0]);
-            part[(threadIdx.x * NF + f) * 4 + 1] = hi_f(acc[f][0]);
-            part[(threadIdx.x * NF + f) * 4 + 2] = lo_f(acc[f][1]);
-            part[(threadIdx.x * NF + f) * 4 + 3] = hi_f(acc[f][1]);
-        }
-        cluster_sync();
-        if (rank == 0) {
-            for (int r = 1; r < split; ++r) {
-                const uint32_t remote = map_shared_rank(sbase + my_off, uint32_t(r));
-#pragma unroll
-                for (int f = 0; f < NF; ++f) {
-                    const float x0 = ld_dsmem_f32(remote + (f * 4 + 0) * 4);
-                    const float x1 = ld_dsmem_f32(remote + (f * 4 + 1) * 4);
-                    const float x2 = ld_dsmem_f32(remote + (f * 4 + 2) * 4);
-                    const float x3 = ld_dsmem_f32(remote + (f * 4 + 3) * 4);
-                    acc[f][0] = pack2(lo_f(acc[f][0]) + x0, hi_f(acc[f][0]) + x1);
-                    acc[f][1] = pack2(lo_f(acc[f][1]) + x2, hi_f(acc[f][1]) + x3);
-                }
-            }
-        }
-        cluster_sync();   // remote partials stay alive until rank 0 has read them
+        for (int f = 0; f < NF; ++f)
+            part[(grp * 128 + gt) * NF + f] = make_float4(lo_f(acc[f][0]), hi_f(acc[f][0]), lo_f(acc[f][1]), hi_f(acc[f][1]));
     }
-    if (rank == 0) {
+    __syncthreads();
+    if (grp == 0) {
+        for (int q = 1; q < G; ++q)
+#pragma unroll
+            for (int f = 0; f < NF; ++f) {
+                const float4 o = part[(q * 128 + gt) * NF + f];
+                acc[f][0] = pack2(lo_f(acc[f][0]) + o.x, hi_f(acc[f][0]) + o.y);
+                acc[f][1] = pack2(lo_f(acc[f][1]) + o.z, hi_f(acc[f][1]) + o.w);
+            }
+        // ---- split-K: ranks 1..S-1 push their partials into rank 0's landing area
+        if (split > 1 && rank > 0) {
+            const uint32_t dst = map_shared_rank(sbase + L.red_off, 0u) +
+                                 uint32_t(((rank - 1) * 128 + gt) * NF) * 16u;
+#pragma unroll
+            for (int f = 0; f < NF; ++f)
+                st_dsmem_v4(dst + f * 16, make_float4(lo_f(acc[f][0]), hi_f(acc[f][0]), lo_f(acc[f][1]), hi_f(acc[f][1])));
+        }
+    }
+    if (split > 1) cluster_sync();   // pushed partials are visible in rank 0
+    if (rank == 0 && grp == 0) {
+        const float4* land = reinterpret_cast<const float4*>(smem + L.red_off);
+        for (int r = 1; r < split; ++r)
+#pragma unroll
+            for (int f = 0; f < NF; ++f) {
+                const float4 o = land[((r - 1) * 128 + gt) * NF + f];
+                acc[f][0] = pack2(lo_f(acc[f][0]) + o.x, hi_f(acc[f][0]) + o.y);
+                acc[f][1] = pack2(lo_f(acc[f][1]) + o.z, hi_f(acc[f][1]) + o.w);
+            }
 #pragma unroll
         for (int f = 0; f < NF; ++f) {
             const int t0 = 8 * f + 2 * j;
@@ -299,6 +331,101 @@ gemm_small_kernel(const __grid_constant__ SmallMaps maps, float* __restrict__ C,
                 }
             }
         }
+    }
+}
+
+
+// ---------------------------------------------------------------------------
+// M <= 4 tokens: one warp per weight row, a plain streaming dot product.
+// Lane l takes the row's chunk pairs l, l+32, ...: 32 nibble bytes (chunk 2p
+// in the low nibbles, 2p+1 in the high ones, both in natural k order) plus
+// the super-block header.  S comes from dp4a (unsigned nibble bytes x signed
+// int8 quants, exact int32), then the per-chunk rescale with the fold; the
+// lanes' partial sums are added by a fixed xor-shuffle tree.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ int dp4a_us(uint32_t a_u8, uint32_t b_s8, int c) {
+    int d;
+    asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a_u8), "r"(b_s8), "r"(c));
+    return d;
+}
+
+template <int MT>
+__global__ void __launch_bounds__(128)
+gemv_dp4a_kernel(mmq_q8_1_t aq, const uint8_t* __restrict__ w, float* __restrict__ C, int M,
+                 int N, int K) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int row = blockIdx.x * 4 + warp;
+    if (row >= N) return;
+    const int nsb = K / 256, npairs = K / 64, nb = K / 32;
+    const uint8_t* wrow = w + int64_t(row) * nsb * 144;
+    float acc[MT];
+#pragma unroll
+    for (int t = 0; t < MT; ++t) acc[t] = 0.0f;
+    for (int pr = lane; pr < npairs; pr += 32) {
+        const int sb = pr >> 2, p = pr & 3;
+        const uint8_t* blk = wrow + sb * 144;
+        const uint4 hdr = __ldg(reinterpret_cast<const uint4*>(blk));
+        const uint4 q0 = __ldcs(reinterpret_cast<const uint4*>(blk + 16 + 32 * p));
+        const uint4 q1 = __ldcs(reinterpret_cast<const uint4*>(blk + 32 + 32 * p));
+        const float d = __half2float(__ushort_as_half(uint16_t(hdr.x & 0xFFFFu)));
+        const float dmin = __half2float(__ushort_as_half(uint16_t(hdr.x >> 16)));
+        float dsv[2], dmv[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int c = 2 * p + h;   // sub-block within the super-block
+            uint32_t sc, m;
+            if (c < 4) {
+                sc = (hdr.y >> (8 * c)) & 63u;
+                m = (hdr.z >> (8 * c)) & 63u;
+            } else {
+                const int b = 8 * (c - 4);
+                sc = ((hdr.w >> b) & 15u) | (((hdr.y >> (b + 6)) & 3u) << 4);
+                m = ((hdr.w >> (b + 4)) & 15u) | (((hdr.z >> (b + 6)) & 3u) << 4);
+            }
+            dsv[h] = d * float(sc);
+            dmv[h] = -(dmin * float(m));
+        }
+        const uint32_t wv[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+        uint32_t lo[8], hi[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            lo[u] = wv[u] & 0x0F0F0F0Fu;
+            hi[u] = (wv[u] >> 4) & 0x0F0F0F0Fu;
+        }
+#pragma unroll
+        for (int t = 0; t < MT; ++t) {
+            if (t < M) {
+                const int8_t* qt = aq.qs + int64_t(t) * K + 64 * pr;
+                const uint4 a0 = __ldg(reinterpret_cast<const uint4*>(qt));
+                const uint4 a1 = __ldg(reinterpret_cast<const uint4*>(qt + 16));
+                const uint4 a2 = __ldg(reinterpret_cast<const uint4*>(qt + 32));
+                const uint4 a3 = __ldg(reinterpret_cast<const uint4*>(qt + 48));
+                int s0 = 0, s1 = 0;
+                s0 = dp4a_us(lo[0], a0.x, s0); s0 = dp4a_us(lo[1], a0.y, s0);
+                s0 = dp4a_us(lo[2], a0.z, s0); s0 = dp4a_us(lo[3], a0.w, s0);
+                s0 = dp4a_us(lo[4], a1.x, s0); s0 = dp4a_us(lo[5], a1.y, s0);
+                s0 = dp4a_us(lo[6], a1.z, s0); s0 = dp4a_us(lo[7], a1.w, s0);
+                s1 = dp4a_us(hi[0], a2.x, s1); s1 = dp4a_us(hi[1], a2.y, s1);
+                s1 = dp4a_us(hi[2], a2.z, s1); s1 = dp4a_us(hi[3], a2.w, s1);
+                s1 = dp4a_us(hi[4], a3.x, s1); s1 = dp4a_us(hi[5], a3.y, s1);
+                s1 = dp4a_us(hi[6], a3.z, s1); s1 = dp4a_us(hi[7], a3.w, s1);
+                const float2 da = __ldg(reinterpret_cast<const float2*>(aq.da + int64_t(t) * nb + 2 * pr));
+                const int2 sa = __ldg(reinterpret_cast<const int2*>(aq.sa + int64_t(t) * nb + 2 * pr));
+                float a = acc[t];
+                a = fmaf(da.x * dsv[0], float(s0), a);
+                a = fmaf(da.x * float(sa.x), dmv[0], a);   // rank-1 fold: dma = da*sa
+                a = fmaf(da.y * dsv[1], float(s1), a);
+                a = fmaf(da.y * float(sa.y), dmv[1], a);
+                acc[t] = a;
+            }
+        }
+    }
+#pragma unroll
+    for (int t = 0; t < MT; ++t) {
+        float a = acc[t];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
+        if (lane == 0 && t < M) C[int64_t(t) * N + row] = a;
     }
 }
 
@@ -331,25 +458,29 @@ bool encode(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t i
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int NF>
+template <int NF, int G>
 cudaError_t launch_nf(const SmallMaps& maps, float* C, int64_t M, int64_t N, int64_t K, int* status,
                       cudaStream_t s) {
-    const StageLayout L = StageLayout::make(NF * 8);
-    const int smem = kStages * L.bytes + 8 * kStages + 16 + 1024;
-    int dev = 0, nsm = 0;
+    int dev = 0, nsm = 0, optin = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
+    cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
     const int64_t row_tiles = (N + kRows - 1) / kRows;
     const int nsb = int(K / 256);
-    // split K over a cluster so that about two CTAs land on every SM
+    // Split K over a cluster so that about two CTAs land on every SM, within
+    // the shared-memory budget of the landing area.
     int split = 1;
-    while (split < 8 && row_tiles * split * 2 <= 2 * int64_t(nsm) && split * 2 <= nsb) split *= 2;
-    auto k = gemm_small_kernel<NF>;
+    while (split < kMaxSplit && row_tiles * split * 2 <= 2 * int64_t(nsm) && split * 2 <= nsb &&
+           Layout::make(NF, G, split * 2).total + 1024 <= optin)
+        split *= 2;
+    const int smem = Layout::make(NF, G, split).total + 1024;   // + alignment slack
+    if (smem > optin) return cudaErrorInvalidConfiguration;
+    auto k = gemm_small_kernel<NF, G>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(unsigned(row_tiles * split));
-    cfg.blockDim = dim3(kThreads);
+    cfg.blockDim = dim3(G * 128);
     cfg.dynamicSmemBytes = size_t(smem);
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
@@ -369,6 +500,15 @@ namespace mmq {
 cudaError_t launch_gemm_small_m(mmq_q8_1_t aq, const uint8_t* w, float* C, int64_t M, int64_t N,
                                 int64_t K, int* status, cudaStream_t s) {
     if (M > kMaxTok) return cudaErrorInvalidValue;
+    if (M <= 4) {   // a few tokens: streaming dot products on dp4a
+        const unsigned grid = unsigned((N + 3) / 4);
+        switch (M) {
+            case 1: gemv_dp4a_kernel<1><<<grid, 128, 0, s>>>(aq, w, C, int(M), int(N), int(K)); break;
+            case 2: gemv_dp4a_kernel<2><<<grid, 128, 0, s>>>(aq, w, C, int(M), int(N), int(K)); break;
+            default: gemv_dp4a_kernel<4><<<grid, 128, 0, s>>>(aq, w, C, int(M), int(N), int(K)); break;
+        }
+        return cudaGetLastError();
+    }
     const int nf = int((M + 7) / 8);
     const uint32_t mp = uint32_t(nf * 8);
     const uint64_t nb = uint64_t(K / 32), nsb = uint64_t(K / 256);
@@ -383,14 +523,14 @@ cudaError_t launch_gemm_small_m(mmq_q8_1_t aq, const uint8_t* w, float* C, int64
                 CU_TENSOR_MAP_SWIZZLE_NONE))
         return cudaErrorInvalidValue;
     switch (nf) {
-        case 1: return launch_nf<1>(maps, C, M, N, K, status, s);
-        case 2: return launch_nf<2>(maps, C, M, N, K, status, s);
-        case 3: return launch_nf<3>(maps, C, M, N, K, status, s);
-        case 4: return launch_nf<4>(maps, C, M, N, K, status, s);
-        case 5: return launch_nf<5>(maps, C, M, N, K, status, s);
-        case 6: return launch_nf<6>(maps, C, M, N, K, status, s);
-        case 7: return launch_nf<7>(maps, C, M, N, K, status, s);
-        default: return launch_nf<8>(maps, C, M, N, K, status, s);
+        case 1: return launch_nf<1, 4>(maps, C, M, N, K, status, s);
+        case 2: return launch_nf<2, 4>(maps, C, M, N, K, status, s);
+        case 3: return launch_nf<3, 4>(maps, C, M, N, K, status, s);
+        case 4: return launch_nf<4, 4>(maps, C, M, N, K, status, s);
+        case 5: return launch_nf<5, 2>(maps, C, M, N, K, status, s);
+        case 6: return launch_nf<6, 2>(maps, C, M, N, K, status, s);
+        case 7: return launch_nf<7, 2>(maps, C, M, N, K, status, s);
+        default: return launch_nf<8, 2>(maps, C, M, N, K, status, s);
     }
 }
 

@@ -89,7 +89,7 @@ def test_gemm_full_small(path_name, M, N, K):
 
 def test_gemm_small_m_full():
     mmq = require_gpu()
-    for M in (1, 2, 7, 16, 33, 64):
+    for M in (1, 2, 3, 4, 5, 7, 8, 9, 16, 33, 64):
         x = synthetic.activations(M, 1024, 71 + M, 0.01)
         blk = synthetic.q4K_weights(260, 1024, 81)
         _full_check(x, blk, 260, mmq.MMQ_PATH_SMALL_M)
