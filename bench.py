@@ -38,8 +38,8 @@ UNIT = "TMAC/s"
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="mine", choices=["mine", "reference"])
     ap.add_argument("--workload", default="q_proj", choices=sorted(WORKLOADS))
     ap.add_argument("--path", default="auto", choices=["auto", "mma_s8", "tc", "small_m"])
@@ -128,6 +128,11 @@ def measured_peaks():
                 "bf16_tflops_sustained": d.get("bf16_tflops_sustained"), "source": "measured"}
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
             "source": "fallback"}
+
+
+def microbench_peaks():
+    with open(os.path.join(ROOT, "profiles", "peaks.json")) as f:
+        return json.load(f)
 
 
 def recorded_traffic(kernel_key, src_hash):
@@ -246,16 +251,15 @@ def run_mine(args, rank, world, local_rank):
         if rc:
             raise RuntimeError(f"MMQ call failed: {rc}")
 
+    # clocks are sampled from the start of warm-up to the end of the timed region
+    clocks = ClockSampler(local_rank) if rank == 0 else None
+    if clocks:
+        clocks.start()
     for i in range(args.warmup):
         step(i)
     torch.cuda.synchronize(dev)
     if mmq.status(stream) != 0:
         raise RuntimeError("device status error after warm-up")
-
-    clocks = ClockSampler(local_rank) if rank == 0 else None
-    if clocks:
-        clocks.start()
-        time.sleep(0.3)
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
     if world > 1:
         torch.distributed.barrier()
@@ -323,7 +327,7 @@ def run_mine(args, rank, world, local_rank):
     value = macs * world / (step_ms * 1e-3) / 1e12
     gemm_tmacs = macs / (g_ms * 1e-3) / 1e12
     peaks = measured_peaks()
-    # dominant kernel = the GEMM; tensor roofline of the pipe it uses
+    micro = microbench_peaks()
     used_path = path
     if used_path == mmq.MMQ_PATH_AUTO:
         used_path = mmq.MMQ_PATH_SMALL_M if M <= mmq.SMALL_M_MAX else mmq.MMQ_PATH_TC
@@ -333,21 +337,35 @@ def run_mine(args, rank, world, local_rank):
     src_hash = kernel_source_hash([kname[1]])
     traffic = recorded_traffic(kname[0], src_hash)
     alg_bytes = 0.5625 * N * K + 1.25 * M * K + 4 * M * N
+    sm_mhz = (clk or {}).get("sm_mhz") or micro["sm_max_mhz"]
     if used_path == mmq.MMQ_PATH_SMALL_M:
         achieved = alg_bytes / (g_ms * 1e-3) / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": achieved / peaks["hbm_gbs"], "traffic": traffic}
+                "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
+                "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json hbm copy)"}
+    elif used_path == mmq.MMQ_PATH_TC:
+        # Binding resource: the per-chunk f32 rescale, 1 FMUL + 2 FFMA per
+        # output per 32-k chunk = 5 flops (FMA = 2); FP32 peak from unit counts:
+        # 152 SMs x 128 lanes x 2 flops x clock.
+        flops = 5.0 * macs / 32
+        achieved = flops / (g_ms * 1e-3) / 1e12
+        peak = micro["sms"] * 128 * 2 * sm_mhz * 1e6 / 1e12
+        roof = {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "traffic": traffic,
+                "peak_source": f"derived: {micro['sms']} SMs x 128 FP32 lanes x 2 x {sm_mhz:.0f} MHz "
+                               "(rescale FMULs use full FMA slots: attainable max 5/6 of peak)",
+                "tensor_frac_of_measured_bf16_sustained": 2 * macs / (g_ms * 1e-3) / 1e12
+                / (peaks["bf16_tflops_sustained"] or peaks["bf16_tflops"])}
     else:
-        # 2 flops per multiply-add; fp16-operand tensor path measured at the bf16 rate
         achieved = 2 * macs / (g_ms * 1e-3) / 1e12
-        peak = peaks["bf16_tflops_sustained"] or peaks["bf16_tflops"]
-        roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                "frac": achieved / peak, "traffic": traffic}
+        peak = micro["int8_mma_sync_tops"]
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TOP/s",
+                "frac": achieved / peak, "traffic": traffic,
+                "peak_source": "measured int8 mma.sync peak (profiles/peaks.json)"}
     roof["kernel"] = kname[0]
-    roof["peak_source"] = f"{peaks['source']} (MEASURED_PEAKS.json sustained bf16)" \
-        if roof["unit"] == "TFLOP/s" else f"{peaks['source']} (MEASURED_PEAKS.json hbm copy)"
     roof["algorithmic_bytes_per_launch"] = alg_bytes
-    roof["algorithmic_flops_per_launch"] = 2 * macs
+    roof["algorithmic_macs_per_launch"] = macs
+    int8_frac = 2 * gemm_tmacs / micro["int8_mma_sync_tops"]
 
     cpu = None
     if not args.no_cpu_baseline:
@@ -369,7 +387,9 @@ def run_mine(args, rank, world, local_rank):
                    "l2": f"{R} rotating input sets ({R * set_bytes / 1e6:.0f} MB > 2x L2)",
                    "path": args.path},
         "us_per_gmac": step_ms * 1e3 / (macs / 1e9),
-        "gemm_only": {"tmacs": gemm_tmacs, "us_per_gmac": g_ms * 1e3 / (macs / 1e9), "ms": g_ms},
+        "gemm_only": {"tmacs": gemm_tmacs, "us_per_gmac": g_ms * 1e3 / (macs / 1e9), "ms": g_ms,
+                      "frac_of_int8_peak": int8_frac,
+                      "int8_peak_source": "measured mma.sync s8 peak, profiles/peaks.json"},
         "prepass": {"ms": q_ms, "gbs": (M * K * 4 + M * K * 1.25) / (q_ms * 1e-3) / 1e9},
         "roofline": roof,
         "cpu_baseline": cpu,
@@ -378,6 +398,7 @@ def run_mine(args, rank, world, local_rank):
                 "ms_per_step": e2e_ms},
         "gpu_launches": 2 * args.steps,
         "clocks": clk,
+        "clocks_window": "nvidia-smi every 200 ms from warm-up start to timed-region end",
         "wall_s_timed": wall,
     }
     print(json.dumps(line), flush=True)

@@ -33,7 +33,7 @@ def shapes():
         yield f"sweep_M{M}", M, 4096, 4096
 
 
-def time_gemm(M, K, N, path, reps, dev):
+def time_gemm(M, K, N, path, reps, dev, graph=True):
     set_bytes = N * K * 0.5625 + M * K * 1.25 + M * N * 4 + M * K * 4
     R = max(2, math.ceil(2 * 129e6 / set_bytes) + 1)
     R = min(R, 64)
@@ -69,6 +69,9 @@ def time_gemm(M, K, N, path, reps, dev):
         e1.record()
         torch.cuda.synchronize()
         out[label] = e0.elapsed_time(e1) / reps
+        if not graph:
+            out[label + "_graph"] = out[label]
+            continue
         # device time without host launch cost: the same launches replayed from a CUDA graph
         g = torch.cuda.CUDAGraph()
         s = torch.cuda.Stream()
@@ -104,17 +107,22 @@ def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--reps", type=int, default=50)
     ap.add_argument("--paths", default="auto")
+    ap.add_argument("--workloads", default="", help="comma-separated subset, e.g. q_proj,sweep_M1")
+    ap.add_argument("--no-graph", action="store_true", help="skip the CUDA-graph timing (for profilers)")
     args = ap.parse_args()
     build.build()
     mmq.load_library()
     dev = torch.device("cuda", 0)
     hbm = 6785.2
+    only = set(w for w in args.workloads.split(",") if w)
     for name, M, K, N in shapes():
+        if only and name not in only:
+            continue
         for pname in args.paths.split(","):
             path = PATHS[pname]
             if path == mmq.MMQ_PATH_SMALL_M and M > mmq.SMALL_M_MAX:
                 continue
-            t, R = time_gemm(M, K, N, path, args.reps, dev)
+            t, R = time_gemm(M, K, N, path, args.reps, dev, graph=not args.no_graph)
             ms = t["gemm_graph"]
             macs = M * N * K
             gbytes = (N * K * 0.5625 + M * K * 1.25 + M * N * 4) / 1e9
