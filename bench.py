@@ -56,18 +56,64 @@ def dist_env():
 
 # --------------------------------------------------------------------- clocks
 class ClockSampler:
-    """Samples nvidia-smi clocks/throttle reasons every 200 ms while active."""
+    """Samples the SM clock and clock-event reasons while active: through
+    NVML (read-only queries, every 2 ms) when libnvidia-ml is present, else
+    nvidia-smi every 200 ms."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    # NVML clock-event reason bits
+    BITS = {"sw_power_cap": 0x4, "hw_slowdown": 0x8, "sw_thermal_slowdown": 0x20,
+            "hw_thermal_slowdown": 0x40, "hw_power_brake_slowdown": 0x80}
 
-    def __init__(self, gpu_index: int):
+    def __init__(self, gpu_index: int, pci_bus_id: str | None = None):
         self.gpu_index = gpu_index
+        self.pci_bus_id = pci_bus_id
         self.proc = None
         self.lines = []
         self.t = None
+        self.nvml = None
+        self.samples = []
+        self.running = False
+
+    def _nvml_open(self):
+        import ctypes
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            return None
+        h = ctypes.c_void_p()
+        ok = False
+        if self.pci_bus_id:
+            ok = lib.nvmlDeviceGetHandleByPciBusId_v2(self.pci_bus_id.encode(), ctypes.byref(h)) == 0
+        if not ok:
+            n = ctypes.c_uint()
+            if lib.nvmlDeviceGetCount_v2(ctypes.byref(n)) != 0 or n.value != 1:
+                return None
+            if lib.nvmlDeviceGetHandleByIndex_v2(0, ctypes.byref(h)) != 0:
+                return None
+        return lib, h
+
+    def _nvml_loop(self):
+        import ctypes
+        lib, h = self.nvml
+        clk, mx, rs = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+        while self.running:
+            if (lib.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(clk)) == 0 and
+                    lib.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0 and
+                    lib.nvmlDeviceGetCurrentClocksEventReasons(h, ctypes.byref(rs)) == 0):
+                self.samples.append((clk.value, mx.value, rs.value))
+            time.sleep(0.002)
 
     def start(self):
+        try:
+            self.nvml = self._nvml_open()
+        except OSError:
+            self.nvml = None
+        if self.nvml:
+            self.running = True
+            self.t = threading.Thread(target=self._nvml_loop, daemon=True)
+            self.t.start()
+            return
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
@@ -83,8 +129,20 @@ class ClockSampler:
             self.lines.append(line.strip())
 
     def stop(self):
+        if self.nvml:
+            self.running = False
+            self.t.join(timeout=2)
+            sm = [c for c, _, _ in self.samples]
+            reasons = set()
+            for _, _, r in self.samples:
+                for name, bit in self.BITS.items():
+                    if r & bit:
+                        reasons.add(name)
+            return {"sm_mhz": float(np.median(sm)) if sm else None,
+                    "sm_max_mhz": max(m for _, m, _ in self.samples) if self.samples else None,
+                    "reasons": sorted(reasons), "samples": len(sm), "source": "nvml, 2 ms"}
         if self.proc is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["clock sampling unavailable"]}
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
@@ -107,7 +165,7 @@ class ClockSampler:
                     reasons.add(name)
         return {"sm_mhz": float(np.median(sm)) if sm else None,
                 "sm_max_mhz": max(smax) if smax else None,
-                "reasons": sorted(reasons), "samples": len(sm)}
+                "reasons": sorted(reasons), "samples": len(sm), "source": "nvidia-smi, 200 ms"}
 
 
 # ------------------------------------------------------------------ roofline
@@ -252,7 +310,13 @@ def run_mine(args, rank, world, local_rank):
             raise RuntimeError(f"MMQ call failed: {rc}")
 
     # clocks are sampled from the start of warm-up to the end of the timed region
-    clocks = ClockSampler(local_rank) if rank == 0 else None
+    pci = None
+    try:
+        pr = torch.cuda.get_device_properties(dev)
+        pci = f"{pr.pci_domain_id:08x}:{pr.pci_bus_id:02x}:{pr.pci_device_id:02x}.0"
+    except AttributeError:
+        pass
+    clocks = ClockSampler(local_rank, pci) if rank == 0 else None
     if clocks:
         clocks.start()
     for i in range(args.warmup):
@@ -398,7 +462,7 @@ def run_mine(args, rank, world, local_rank):
                 "ms_per_step": e2e_ms},
         "gpu_launches": 2 * args.steps,
         "clocks": clk,
-        "clocks_window": "nvidia-smi every 200 ms from warm-up start to timed-region end",
+        "clocks_window": "from warm-up start to timed-region end",
         "wall_s_timed": wall,
     }
     print(json.dumps(line), flush=True)

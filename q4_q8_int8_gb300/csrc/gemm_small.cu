@@ -353,6 +353,7 @@ template <int MT>
 __global__ void __launch_bounds__(128)
 gemv_dp4a_kernel(mmq_q8_1_t aq, const uint8_t* __restrict__ w, float* __restrict__ C, int M,
                  int N, int K) {
+    constexpr int kU = 2;   // chunk pairs per lane per batch; all their loads are issued first
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int row = blockIdx.x * 4 + warp;
     if (row >= N) return;
@@ -361,62 +362,74 @@ gemv_dp4a_kernel(mmq_q8_1_t aq, const uint8_t* __restrict__ w, float* __restrict
     float acc[MT];
 #pragma unroll
     for (int t = 0; t < MT; ++t) acc[t] = 0.0f;
-    for (int pr = lane; pr < npairs; pr += 32) {
-        const int sb = pr >> 2, p = pr & 3;
-        const uint8_t* blk = wrow + sb * 144;
-        const uint4 hdr = __ldg(reinterpret_cast<const uint4*>(blk));
-        const uint4 q0 = __ldcs(reinterpret_cast<const uint4*>(blk + 16 + 32 * p));
-        const uint4 q1 = __ldcs(reinterpret_cast<const uint4*>(blk + 32 + 32 * p));
-        const float d = __half2float(__ushort_as_half(uint16_t(hdr.x & 0xFFFFu)));
-        const float dmin = __half2float(__ushort_as_half(uint16_t(hdr.x >> 16)));
-        float dsv[2], dmv[2];
+    for (int base = 0; base < npairs; base += 32 * kU) {
+        uint4 hdr[kU], q0[kU], q1[kU];
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int c = 2 * p + h;   // sub-block within the super-block
-            uint32_t sc, m;
-            if (c < 4) {
-                sc = (hdr.y >> (8 * c)) & 63u;
-                m = (hdr.z >> (8 * c)) & 63u;
-            } else {
-                const int b = 8 * (c - 4);
-                sc = ((hdr.w >> b) & 15u) | (((hdr.y >> (b + 6)) & 3u) << 4);
-                m = ((hdr.w >> (b + 4)) & 15u) | (((hdr.z >> (b + 6)) & 3u) << 4);
+        for (int u = 0; u < kU; ++u) {
+            const int pr = base + lane + 32 * u;
+            if (pr < npairs) {
+                const uint8_t* blk = wrow + (pr >> 2) * 144;
+                hdr[u] = __ldg(reinterpret_cast<const uint4*>(blk));
+                q0[u] = __ldcs(reinterpret_cast<const uint4*>(blk + 16 + 32 * (pr & 3)));
+                q1[u] = __ldcs(reinterpret_cast<const uint4*>(blk + 32 + 32 * (pr & 3)));
             }
-            dsv[h] = d * float(sc);
-            dmv[h] = -(dmin * float(m));
-        }
-        const uint32_t wv[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
-        uint32_t lo[8], hi[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            lo[u] = wv[u] & 0x0F0F0F0Fu;
-            hi[u] = (wv[u] >> 4) & 0x0F0F0F0Fu;
         }
 #pragma unroll
-        for (int t = 0; t < MT; ++t) {
-            if (t < M) {
-                const int8_t* qt = aq.qs + int64_t(t) * K + 64 * pr;
-                const uint4 a0 = __ldg(reinterpret_cast<const uint4*>(qt));
-                const uint4 a1 = __ldg(reinterpret_cast<const uint4*>(qt + 16));
-                const uint4 a2 = __ldg(reinterpret_cast<const uint4*>(qt + 32));
-                const uint4 a3 = __ldg(reinterpret_cast<const uint4*>(qt + 48));
-                int s0 = 0, s1 = 0;
-                s0 = dp4a_us(lo[0], a0.x, s0); s0 = dp4a_us(lo[1], a0.y, s0);
-                s0 = dp4a_us(lo[2], a0.z, s0); s0 = dp4a_us(lo[3], a0.w, s0);
-                s0 = dp4a_us(lo[4], a1.x, s0); s0 = dp4a_us(lo[5], a1.y, s0);
-                s0 = dp4a_us(lo[6], a1.z, s0); s0 = dp4a_us(lo[7], a1.w, s0);
-                s1 = dp4a_us(hi[0], a2.x, s1); s1 = dp4a_us(hi[1], a2.y, s1);
-                s1 = dp4a_us(hi[2], a2.z, s1); s1 = dp4a_us(hi[3], a2.w, s1);
-                s1 = dp4a_us(hi[4], a3.x, s1); s1 = dp4a_us(hi[5], a3.y, s1);
-                s1 = dp4a_us(hi[6], a3.z, s1); s1 = dp4a_us(hi[7], a3.w, s1);
-                const float2 da = __ldg(reinterpret_cast<const float2*>(aq.da + int64_t(t) * nb + 2 * pr));
-                const int2 sa = __ldg(reinterpret_cast<const int2*>(aq.sa + int64_t(t) * nb + 2 * pr));
-                float a = acc[t];
-                a = fmaf(da.x * dsv[0], float(s0), a);
-                a = fmaf(da.x * float(sa.x), dmv[0], a);   // rank-1 fold: dma = da*sa
-                a = fmaf(da.y * dsv[1], float(s1), a);
-                a = fmaf(da.y * float(sa.y), dmv[1], a);
-                acc[t] = a;
+        for (int u = 0; u < kU; ++u) {
+            const int pr = base + lane + 32 * u;
+            if (pr >= npairs) continue;
+            const int p = pr & 3;
+            const float d = __half2float(__ushort_as_half(uint16_t(hdr[u].x & 0xFFFFu)));
+            const float dmin = __half2float(__ushort_as_half(uint16_t(hdr[u].x >> 16)));
+            float dsv[2], dmv[2];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int c = 2 * p + h;   // sub-block within the super-block
+                uint32_t sc, m;
+                if (c < 4) {
+                    sc = (hdr[u].y >> (8 * c)) & 63u;
+                    m = (hdr[u].z >> (8 * c)) & 63u;
+                } else {
+                    const int bsh = 8 * (c - 4);
+                    sc = ((hdr[u].w >> bsh) & 15u) | (((hdr[u].y >> (bsh + 6)) & 3u) << 4);
+                    m = ((hdr[u].w >> (bsh + 4)) & 15u) | (((hdr[u].z >> (bsh + 6)) & 3u) << 4);
+                }
+                dsv[h] = d * float(sc);
+                dmv[h] = -(dmin * float(m));
+            }
+            const uint32_t wv[8] = {q0[u].x, q0[u].y, q0[u].z, q0[u].w, q1[u].x, q1[u].y, q1[u].z, q1[u].w};
+            uint32_t lo[8], hi[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                lo[e] = wv[e] & 0x0F0F0F0Fu;          // chunk 2p, natural k order
+                hi[e] = (wv[e] >> 4) & 0x0F0F0F0Fu;   // chunk 2p + 1
+            }
+#pragma unroll
+            for (int t = 0; t < MT; ++t) {
+                if (t < M) {
+                    const int8_t* qt = aq.qs + int64_t(t) * K + 64 * pr;
+                    const uint4 a0 = __ldg(reinterpret_cast<const uint4*>(qt));
+                    const uint4 a1 = __ldg(reinterpret_cast<const uint4*>(qt + 16));
+                    const uint4 a2 = __ldg(reinterpret_cast<const uint4*>(qt + 32));
+                    const uint4 a3 = __ldg(reinterpret_cast<const uint4*>(qt + 48));
+                    int s0 = 0, s1 = 0;
+                    s0 = dp4a_us(lo[0], a0.x, s0); s0 = dp4a_us(lo[1], a0.y, s0);
+                    s0 = dp4a_us(lo[2], a0.z, s0); s0 = dp4a_us(lo[3], a0.w, s0);
+                    s0 = dp4a_us(lo[4], a1.x, s0); s0 = dp4a_us(lo[5], a1.y, s0);
+                    s0 = dp4a_us(lo[6], a1.z, s0); s0 = dp4a_us(lo[7], a1.w, s0);
+                    s1 = dp4a_us(hi[0], a2.x, s1); s1 = dp4a_us(hi[1], a2.y, s1);
+                    s1 = dp4a_us(hi[2], a2.z, s1); s1 = dp4a_us(hi[3], a2.w, s1);
+                    s1 = dp4a_us(hi[4], a3.x, s1); s1 = dp4a_us(hi[5], a3.y, s1);
+                    s1 = dp4a_us(hi[6], a3.z, s1); s1 = dp4a_us(hi[7], a3.w, s1);
+                    const float2 da = __ldg(reinterpret_cast<const float2*>(aq.da + int64_t(t) * nb + 2 * pr));
+                    const int2 sa = __ldg(reinterpret_cast<const int2*>(aq.sa + int64_t(t) * nb + 2 * pr));
+                    float a = acc[t];
+                    a = fmaf(da.x * dsv[0], float(s0), a);
+                    a = fmaf(da.x * float(sa.x), dmv[0], a);   // rank-1 fold: dma = da*sa
+                    a = fmaf(da.y * dsv[1], float(s1), a);
+                    a = fmaf(da.y * float(sa.y), dmv[1], a);
+                    acc[t] = a;
+                }
             }
         }
     }

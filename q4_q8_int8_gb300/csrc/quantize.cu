@@ -9,7 +9,9 @@
 // of 8 lanes owns one 32-element block (one float4 per lane), so a warp
 // covers four consecutive blocks = 512 contiguous bytes per load; amax and
 // the sum are reduced with three xor-shuffles inside the 8-lane group.
-// Each warp keeps kUnroll groups of four blocks in flight.
+// Each warp keeps kUnroll groups of four blocks in flight.  The quotient
+// x / da is formed from the block's reciprocal with an exactness check (see
+// quant1), so the bits match IEEE division followed by roundf.
 #include "mmq_internal.h"
 
 namespace {
@@ -21,13 +23,27 @@ __device__ __forceinline__ float4 load_stream(const float* p) {
     return __ldcs(reinterpret_cast<const float4*>(p));
 }
 
-__device__ __forceinline__ int quant1(float x, float d) {
-    // IEEE division and round-half-away-from-zero, then the +-127 guard.
-    int q = static_cast<int>(roundf(__fdiv_rn(x, d)));
-    q = q > 127 ? 127 : q;
-    q = q < -127 ? -127 : q;
-    return q;
+// q = clamp(roundf(x / d), -127, 127) with IEEE division, computed without a
+// division in almost every case.  r = 1/d correctly rounded; q0 = x * r then
+// differs from the exact quotient y = x/d by at most 2^-23 |y| < 2^-16 (|y| is
+// at most 127 * (1 + 2^-23)), and fl(y) differs from y by at most 2^-18.  If
+// q0 is more than 2^-15 away from every half-integer, q0, y and fl(y) lie in
+// the same open interval (k - 1/2, k + 1/2), so roundf(fl(y)) is q0 rounded to
+// the nearest integer (no tie is possible there, so the rounding mode of the
+// conversion does not matter).  Otherwise `redo` is set and the caller
+// recomputes that element with IEEE division.
+__device__ __forceinline__ int quant_fast(float x, float r, bool& redo) {
+    const float q0 = x * r;
+    const float fr = fabsf(q0 - truncf(q0));   // exact (Sterbenz)
+    redo = redo || !(fabsf(fr - 0.5f) > 0x1p-15f);
+    return __float2int_rn(q0);
 }
+
+__device__ __forceinline__ int quant_exact(float x, float d) {
+    return static_cast<int>(roundf(__fdiv_rn(x, d)));
+}
+
+__device__ __forceinline__ int clamp127(int q) { return q > 127 ? 127 : (q < -127 ? -127 : q); }
 
 __global__ void __launch_bounds__(kThreads)
 quantize_q8_1_kernel(const float* __restrict__ x, int8_t* __restrict__ qs,
@@ -57,13 +73,30 @@ quantize_q8_1_kernel(const float* __restrict__ x, int8_t* __restrict__ qs,
             amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
             amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
             const float d = __fdiv_rn(amax, 127.0f);
-            int q0 = 0, q1 = 0, q2 = 0, q3 = 0;
+            int q0 = 0, q1 = 0, q2 = 0, q3 = 0;   // a zero scale gives zero quants
+            bool redo = false;
             if (d != 0.0f) {
-                q0 = quant1(v[u].x, d);
-                q1 = quant1(v[u].y, d);
-                q2 = quant1(v[u].z, d);
-                q3 = quant1(v[u].w, d);
+                redo = d < 0x1p-126f;   // d below the smallest normal float: always divide
+                const float r = __frcp_rn(d);
+                q0 = quant_fast(v[u].x, r, redo);
+                q1 = quant_fast(v[u].y, r, redo);
+                q2 = quant_fast(v[u].z, r, redo);
+                q3 = quant_fast(v[u].w, r, redo);
             }
+            // Rare: some lane needs IEEE division.  The vote runs on all 32
+            // lanes (outside the per-block branch above).
+            if (__any_sync(0xffffffffu, redo)) {
+                if (redo) {
+                    q0 = quant_exact(v[u].x, d);
+                    q1 = quant_exact(v[u].y, d);
+                    q2 = quant_exact(v[u].z, d);
+                    q3 = quant_exact(v[u].w, d);
+                }
+            }
+            q0 = clamp127(q0);
+            q1 = clamp127(q1);
+            q2 = clamp127(q2);
+            q3 = clamp127(q3);
             int s = q0 + q1 + q2 + q3;
             s += __shfl_xor_sync(0xffffffffu, s, 1);
             s += __shfl_xor_sync(0xffffffffu, s, 2);

@@ -49,3 +49,23 @@ def test_edge_blocks():
     x = np.concatenate(blocks).astype(np.float32).reshape(1, -1)
     _check(x)
     _check(x.reshape(len(blocks), 32).copy())
+
+
+def test_near_tie_quotients():
+    # Activations whose quotients x/da sit at or within a few ulps of
+    # half-integers, for many scales: exercises both the reciprocal fast path
+    # and the exact-division fallback, which must agree with IEEE division.
+    rng = np.random.default_rng(42)
+    rows = []
+    for _ in range(256):
+        amax = np.float32(rng.uniform(0.5, 2.0) * 2.0 ** int(rng.integers(-60, 60)))
+        d = np.float32(amax) / np.float32(127.0)
+        x = np.empty(31, np.float32)
+        for i in range(31):
+            k = int(rng.integers(-126, 127))
+            v = np.float32((k + 0.5) * float(d))           # nearest float to the tie point
+            for _ in range(abs(int(rng.integers(-3, 4)))):
+                v = np.nextafter(v, np.float32(np.inf if rng.integers(0, 2) else -np.inf))
+            x[i] = v
+        rows.append(np.concatenate([[amax], x]).astype(np.float32))
+    _check(np.stack(rows))
