@@ -160,10 +160,45 @@ __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
     return v;
 }
 
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t map_shared_rank(uint32_t saddr, uint32_t rank) {
+    uint32_t d;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(d) : "r"(saddr), "r"(rank));
+    return d;
+}
+__device__ __forceinline__ float4 ld_dsmem_v4(uint32_t addr) {
+    float4 v;
+    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(addr)
+                 : "memory");
+    return v;
+}
+
+// Epilogue thread's 4 rows x 16 columns of the 128x128 tile (m0, n0) -> C.
+__device__ __forceinline__ void store_tile(float* C, const uint64_t (&acc)[4][8], int M, int N, int m0,
+                                           int n0, int quarter, int colhalf, int tq, int tr4) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const int64_t gr = int64_t(m0) + quarter * 32 + tq + 8 * k;
+        if (gr < M) {
+            float* crow = C + gr * N;
+#pragma unroll
+            for (int g = 0; g < 8; ++g) {
+                const int gc = n0 + colhalf * 64 + 8 * g + 2 * tr4;
+                if (gc < N)
+                    *reinterpret_cast<float2*>(crow + gc) = make_float2(lo_f(acc[k][g]), hi_f(acc[k][g]));
+            }
+        }
+    }
+}
+
 template <bool kDump>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_tc_kernel(const __grid_constant__ TmaMaps maps, float* __restrict__ C,
-               int32_t* __restrict__ S, int M, int N, int K, int* status, int inject_timeout) {
+               int32_t* __restrict__ S, int M, int N, int K, int split, int* status, int inject_timeout) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~uintptr_t(1023));
@@ -176,6 +211,14 @@ gemm_tc_kernel(const __grid_constant__ TmaMaps maps, float* __restrict__ C,
     const int nsb = K / 256;
     const int tiles_m = (M + BM - 1) / BM, tiles_n = (N + BN - 1) / BN;
     const int num_tiles = tiles_m * tiles_n;
+    // Persistent mode (split == 1): CTAs stride over all tiles and K.  Split
+    // mode: a cluster of `split` CTAs shares one tile, rank r takes
+    // super-blocks [nsb*r/split, nsb*(r+1)/split), and rank 0 adds the
+    // partial sums in rank order.
+    const int rank = split > 1 ? int(blockIdx.x % unsigned(split)) : 0;
+    const int tile_first = split > 1 ? int(blockIdx.x / unsigned(split)) : int(blockIdx.x);
+    const int tile_step = split > 1 ? num_tiles : int(gridDim.x);
+    const int sb_lo = (nsb * rank) / split, sb_hi = (nsb * (rank + 1)) / split;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kNumRaw; ++s) {
@@ -225,9 +268,9 @@ gemm_tc_kernel(const __grid_constant__ TmaMaps maps, float* __restrict__ C,
             int scl_issued[kNumScl] = {};
             uint32_t scl_par[kNumScl] = {};
             bool first = true;
-            for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+            for (int tile = tile_first; tile < num_tiles; tile += tile_step) {
                 const int m0 = (tile / tiles_n) * BM, n0 = (tile % tiles_n) * BN;
-                for (int sb = 0; sb < nsb; ++sb) {
+                for (int sb = sb_lo; sb < sb_hi; ++sb) {
                     if (!wait_bounded(bars.raw_empty(rr.slot), rr.phase ^ 1u, abort_flag, status))
                         goto producer_done;
                     const uint32_t raw = sbase + kOffRaw + rr.slot * kRawStage;
@@ -267,8 +310,8 @@ gemm_tc_kernel(const __grid_constant__ TmaMaps maps, float* __restrict__ C,
             int issued = 0;
             int last_slot = 0;
             uint32_t last_par = 0;
-            for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
-                for (int sb = 0; sb < nsb; ++sb) {
+            for (int tile = tile_first; tile < num_tiles; tile += tile_step) {
+                for (int sb = sb_lo; sb < sb_hi; ++sb) {
                     for (int q = 0; q < 4; ++q) {
                         if (!wait_bounded(bars.op_full(orr.slot), orr.phase, abort_flag, status))
                             goto mma_done;
@@ -308,8 +351,8 @@ gemm_tc_kernel(const __grid_constant__ TmaMaps maps, float* __restrict__ C,
         const int ts = threadIdx.x - kSclWarp0 * 32;   // 0..63: rows ts and ts + 64
         Ring<kNumRaw> rr;
         Ring<kNumScl> sr;
-        for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
-            for (int sb = 0; sb < nsb; ++sb) {
+        for (int tile = tile_first; tile < num_tiles; tile += tile_step) {
+            for (int sb = sb_lo; sb < sb_hi; ++sb) {
                 if (!wait_bounded(bars.raw_full(rr.slot), rr.phase, abort_flag, status)) goto scl_done;
                 if (!wait_bounded(bars.scl_empty(sr.slot), sr.phase ^ 1u, abort_flag, status)) goto scl_done;
                 if (!wait_bounded(bars.scl_tma(sr.slot), sr.phase, abort_flag, status)) goto scl_done;
@@ -368,8 +411,8 @@ gemm_tc_kernel(const __grid_constant__ TmaMaps maps, float* __restrict__ C,
         const int sw = t & 7;
         Ring<kNumRaw> rr;
         Ring<kNumOp> orr;
-        for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
-            for (int sb = 0; sb < nsb; ++sb) {
+        for (int tile = tile_first; tile < num_tiles; tile += tile_step) {
+            for (int sb = sb_lo; sb < sb_hi; ++sb) {
                 if (!wait_bounded(bars.raw_full(rr.slot), rr.phase, abort_flag, status)) goto conv_done;
                 const uint32_t raw = sbase + kOffRaw + rr.slot * kRawStage;
                 const uint32_t rawB = raw + kRawA + t * 144 + 16;
@@ -423,6 +466,10 @@ gemm_tc_kernel(const __grid_constant__ TmaMaps maps, float* __restrict__ C,
         }
     conv_done:;
     }
+    if (split > 1) {   // every thread of every CTA in the cluster takes both barriers
+        cluster_sync_all();
+        cluster_sync_all();
+    }
     } else {
         setmaxnreg_inc<kRegsHigh>();
         // ---------------------------------------------------------- epilogue
@@ -438,9 +485,9 @@ gemm_tc_kernel(const __grid_constant__ TmaMaps maps, float* __restrict__ C,
         const uint32_t tlane0 = uint32_t(quarter * 32) << 16, tlane1 = uint32_t(quarter * 32 + 16) << 16;
         Ring<kNumScl> sr;
         Ring<kNumTm> tr;
-        for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+        uint64_t acc[4][8];
+        for (int tile = tile_first; tile < num_tiles; tile += tile_step) {
             const int m0 = (tile / tiles_n) * BM, n0 = (tile % tiles_n) * BN;
-            uint64_t acc[4][8];
 #pragma unroll
             for (int k = 0; k < 4; ++k)
 #pragma unroll
@@ -452,7 +499,7 @@ gemm_tc_kernel(const __grid_constant__ TmaMaps maps, float* __restrict__ C,
             tc_fence_after();
             tmem_ld_16x256b_x8(tmem_base + tlane0 + uint32_t(tr.slot * BN + colhalf * 64), b0);
             tmem_wait_ld();
-            for (int sb = 0; sb < nsb; ++sb) {
+            for (int sb = sb_lo; sb < sb_hi; ++sb) {
                 const uint8_t* scl = smem + kOffScl + sr.slot * kSclStage;
                 const float4* col4 = reinterpret_cast<const float4*>(scl + kOffSclCol);
                 const float2* row2 = reinterpret_cast<const float2*>(scl + kOffSclRow);
@@ -495,7 +542,7 @@ gemm_tc_kernel(const __grid_constant__ TmaMaps maps, float* __restrict__ C,
                     if (lane == 0) mbar_arrive(bars.tm_empty(tr.slot));
                     tr.next();
                     const bool last_in_sb = (c == 7);
-                    const bool has_next = !(last_in_sb && sb == nsb - 1);
+                    const bool has_next = !(last_in_sb && sb == sb_hi - 1);
                     if (last_in_sb) {   // scale tables of this super-block no longer needed
                         __syncwarp();
                         if (lane == 0) mbar_arrive(bars.scl_empty(sr.slot));
@@ -536,23 +583,38 @@ gemm_tc_kernel(const __grid_constant__ TmaMaps maps, float* __restrict__ C,
                     if (has_next) tmem_wait_ld();
                 }
             }
-            if (!kDump) {
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const int64_t gr = int64_t(m0) + quarter * 32 + tq + 8 * k;
-                    if (gr < M) {
-                        float* crow = C + gr * N;
-#pragma unroll
-                        for (int g = 0; g < 8; ++g) {
-                            const int gc = n0 + colhalf * 64 + 8 * g + 2 * tr4;
-                            if (gc < N)
-                                *reinterpret_cast<float2*>(crow + gc) = make_float2(lo_f(acc[k][g]), hi_f(acc[k][g]));
-                        }
-                    }
-                }
-            }
+            if (!kDump && split == 1) store_tile(C, acc, M, N, m0, n0, quarter, colhalf, tq, tr4);
         }
     epi_done:;
+        if (split > 1) {
+            // Each rank leaves its partial tile in its own (now idle) staging
+            // memory; rank 0 pulls ranks 1..split-1 in order and stores C.
+            const int e = threadIdx.x - kEpiWarp0 * 32;   // 0..255
+            float4* mine = reinterpret_cast<float4*>(smem + kOffRaw) + e * 16;
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+#pragma unroll
+                for (int g = 0; g < 8; g += 2)
+                    mine[k * 4 + g / 2] = make_float4(lo_f(acc[k][g]), hi_f(acc[k][g]),
+                                                      lo_f(acc[k][g + 1]), hi_f(acc[k][g + 1]));
+            cluster_sync_all();
+            if (rank == 0 && !kDump) {
+                for (int r = 1; r < split; ++r) {
+                    const uint32_t remote = map_shared_rank(sbase + kOffRaw + uint32_t(e) * 256u, uint32_t(r));
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+#pragma unroll
+                        for (int g = 0; g < 8; g += 2) {
+                            const float4 v = ld_dsmem_v4(remote + uint32_t(k * 4 + g / 2) * 16u);
+                            acc[k][g] = pack2(lo_f(acc[k][g]) + v.x, hi_f(acc[k][g]) + v.y);
+                            acc[k][g + 1] = pack2(lo_f(acc[k][g + 1]) + v.z, hi_f(acc[k][g + 1]) + v.w);
+                        }
+                }
+                const int m0 = (tile_first / tiles_n) * BM, n0 = (tile_first % tiles_n) * BN;
+                store_tile(C, acc, M, N, m0, n0, quarter, colhalf, tq, tr4);
+            }
+            cluster_sync_all();   // remote partials stay alive until rank 0 has read them
+        }
     }
 
     tc_fence_before();
@@ -635,21 +697,28 @@ cudaError_t launch_gemm_tc(mmq_q8_1_t aq, const uint8_t* w, float* C, int32_t* S
         if (fa.numRegs != int(kRegsLaunch)) return cudaErrorInvalidConfiguration;
     }
     const int64_t tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
-    const int grid = int(tiles < nsm ? tiles : nsm);
+    // Few tiles: split K over a cluster so that most SMs get work.
+    int split = 1;
+    if (tiles * 2 <= nsm)
+        while (split < 8 && tiles * split * 2 <= nsm && split * 2 <= int64_t(nsb)) split *= 2;
+    auto k = S ? gemm_tc_kernel<true> : gemm_tc_kernel<false>;
     cudaError_t e;
-    if (S) {
-        auto k = gemm_tc_kernel<true>;
-        if ((e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes)))
-            return e;
-        k<<<grid, kThreads, kSmemBytes, s>>>(maps, C, S, int(M), int(N), int(K), status,
-                                              inject_timeout);
-    } else {
-        auto k = gemm_tc_kernel<false>;
-        if ((e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes)))
-            return e;
-        k<<<grid, kThreads, kSmemBytes, s>>>(maps, C, S, int(M), int(N), int(K), status,
-                                              inject_timeout);
-    }
+    if ((e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes)))
+        return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(unsigned(split > 1 ? tiles * split : (tiles < nsm ? tiles : nsm)));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = size_t(kSmemBytes);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = unsigned(split);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, k, maps, C, S, int(M), int(N), int(K), split, status, inject_timeout);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
