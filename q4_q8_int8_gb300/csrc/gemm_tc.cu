@@ -63,31 +63,31 @@ constexpr uint32_t kTmemCols = 512;                          // kNumTm x BN
 constexpr int kRawASub = BM * 128;                   // 16 KB: 128 rows x 128 B, swizzled
 constexpr int kRawA = 2 * kRawASub;                  // 256 k of int8
 constexpr int kRawB = BN * 144;                      // raw q4_K rows
-constexpr int kRawStage = kRawA + kRawB;             // 51200 = 50 KB
-constexpr int kSclDa = BM * 8 * 4;                   // da [128][8] f32
-constexpr int kSclSa = BM * 8 * 4;                   // sa [128][8] i32
+constexpr int kRawDa = BM * 8 * 4;                   // da [128][8] f32
+constexpr int kRawSa = BM * 8 * 4;                   // sa [128][8] i32
+constexpr int kOffRawB = kRawA, kOffRawDa = kRawA + kRawB, kOffRawSa = kOffRawDa + kRawDa;
+constexpr int kRawStage = kOffRawSa + kRawSa;        // 58 KB: everything one super-block needs from HBM
 constexpr int kSclCol = 8 * BN * 8;                  // [8 chunks][64 column pairs] float4
                                                      //   {dsv_2p, dsv_2p+1, dmv_2p, dmv_2p+1}
 constexpr int kSclRow = 8 * BM * 8;                  // [8 chunks][128 rows] float2 {da, da*sa}
-constexpr int kOffSclCol = kSclDa + kSclSa;
+constexpr int kOffSclCol = 0;
 constexpr int kOffSclRow = kOffSclCol + kSclCol;
-constexpr int kSclStage = kOffSclRow + kSclRow;      // 24 KB
+constexpr int kSclStage = kOffSclRow + kSclRow;      // 16 KB of scale tables (no copies land here)
 constexpr int kOpTile = 128 * 128;                   // 128 rows x 64 fp16 (128 B), swizzled
 constexpr int kOpStage = 2 * kOpTile;                // A + B
 constexpr int kOffRaw = 0;
 constexpr int kOffScl = kOffRaw + kNumRaw * kRawStage;
 constexpr int kOffOp = kOffScl + kNumScl * kSclStage;
 constexpr int kOffBar = kOffOp + kNumOp * kOpStage;
-// barriers: raw_full, raw_empty, scl_tma, scl_col, scl_empty, op_full, op_empty, tm_full, tm_empty
-constexpr int kNumBars = 2 * kNumRaw + 3 * kNumScl + 2 * kNumOp + 2 * kNumTm;
+// barriers: raw_full, raw_empty, scl_col, scl_empty, op_full, op_empty, tm_full, tm_empty
+constexpr int kNumBars = 2 * kNumRaw + 2 * kNumScl + 2 * kNumOp + 2 * kNumTm;
 constexpr int kOffMisc = kOffBar + kNumBars * 8;     // tmem slot, abort flag
 constexpr int kSmemBytes = kOffMisc + 16 + 1024;     // + alignment slack
 static_assert(kOffOp % 1024 == 0, "operand tiles need 1024-byte alignment");
 static_assert(kRawStage % 1024 == 0 && kSclStage % 1024 == 0, "stage alignment");
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 
-constexpr uint32_t kRawTx = kRawA + kRawB;
-constexpr uint32_t kSclTx = kSclDa + kSclSa;
+constexpr uint32_t kRawTx = kRawStage;
 constexpr uint32_t kIdesc = idesc_f16_f32(BM, BN);
 constexpr float kDsvScale = 16777216.0f;             // 2^24: nibbles are fp16 subnormals
 
@@ -99,18 +99,17 @@ struct Bars {
     uint32_t base;
     __device__ uint32_t raw_full(int s) const { return base + 8 * s; }
     __device__ uint32_t raw_empty(int s) const { return base + 8 * (kNumRaw + s); }
-    __device__ uint32_t scl_tma(int s) const { return base + 8 * (2 * kNumRaw + s); }
-    __device__ uint32_t scl_col(int s) const { return base + 8 * (2 * kNumRaw + kNumScl + s); }
-    __device__ uint32_t scl_empty(int s) const { return base + 8 * (2 * kNumRaw + 2 * kNumScl + s); }
-    __device__ uint32_t op_full(int s) const { return base + 8 * (2 * kNumRaw + 3 * kNumScl + s); }
+    __device__ uint32_t scl_col(int s) const { return base + 8 * (2 * kNumRaw + s); }
+    __device__ uint32_t scl_empty(int s) const { return base + 8 * (2 * kNumRaw + kNumScl + s); }
+    __device__ uint32_t op_full(int s) const { return base + 8 * (2 * kNumRaw + 2 * kNumScl + s); }
     __device__ uint32_t op_empty(int s) const {
-        return base + 8 * (2 * kNumRaw + 3 * kNumScl + kNumOp + s);
+        return base + 8 * (2 * kNumRaw + 2 * kNumScl + kNumOp + s);
     }
     __device__ uint32_t tm_full(int s) const {
-        return base + 8 * (2 * kNumRaw + 3 * kNumScl + 2 * kNumOp + s);
+        return base + 8 * (2 * kNumRaw + 2 * kNumScl + 2 * kNumOp + s);
     }
     __device__ uint32_t tm_empty(int s) const {
-        return base + 8 * (2 * kNumRaw + 3 * kNumScl + 2 * kNumOp + kNumTm + s);
+        return base + 8 * (2 * kNumRaw + 2 * kNumScl + 2 * kNumOp + kNumTm + s);
     }
 };
 
@@ -226,7 +225,6 @@ gemm_tc_kernel(const __grid_constant__ TmaMaps maps, float* __restrict__ C,
             mbar_init(bars.raw_empty(s), kNumConvWarps + kNumSclWarps);
         }
         for (int s = 0; s < kNumScl; ++s) {
-            mbar_init(bars.scl_tma(s), 1);
             mbar_init(bars.scl_col(s), kNumSclWarps);
             mbar_init(bars.scl_empty(s), kNumEpiWarps);
         }
@@ -262,11 +260,8 @@ gemm_tc_kernel(const __grid_constant__ TmaMaps maps, float* __restrict__ C,
         // ------------------------------------------------------ TMA producer
         if (lane == 0) {
             Ring<kNumRaw> rr;
-            Ring<kNumScl> sr;
             int raw_issued[kNumRaw] = {};
             uint32_t raw_par[kNumRaw] = {};
-            int scl_issued[kNumScl] = {};
-            uint32_t scl_par[kNumScl] = {};
             bool first = true;
             for (int tile = tile_first; tile < num_tiles; tile += tile_step) {
                 const int m0 = (tile / tiles_n) * BM, n0 = (tile % tiles_n) * BN;
@@ -275,32 +270,24 @@ gemm_tc_kernel(const __grid_constant__ TmaMaps maps, float* __restrict__ C,
                         goto producer_done;
                     const uint32_t raw = sbase + kOffRaw + rr.slot * kRawStage;
                     if (!(first && inject_timeout)) {   // test hook: withhold this arrival
-                        mbar_arrive_expect_tx(bars.raw_full(rr.slot), kRawTx);
-                        tma_load_2d(raw, &maps.a, bars.raw_full(rr.slot), sb * 256, m0);
-                        tma_load_2d(raw + kRawASub, &maps.a, bars.raw_full(rr.slot), sb * 256 + 128, m0);
-                        tma_load_2d(raw + kRawA, &maps.b, bars.raw_full(rr.slot), sb * 144, n0);
+                        const uint32_t fb = bars.raw_full(rr.slot);
+                        mbar_arrive_expect_tx(fb, kRawTx);
+                        tma_load_2d(raw, &maps.a, fb, sb * 256, m0);
+                        tma_load_2d(raw + kRawASub, &maps.a, fb, sb * 256 + 128, m0);
+                        tma_load_2d(raw + kOffRawB, &maps.b, fb, sb * 144, n0);
+                        tma_load_2d(raw + kOffRawDa, &maps.da, fb, sb * 8, m0);
+                        tma_load_2d(raw + kOffRawSa, &maps.sa, fb, sb * 8, m0);
                         raw_issued[rr.slot] = 1;
                         raw_par[rr.slot] = rr.phase;
                     }
                     first = false;
                     rr.next();
-                    if (!wait_bounded(bars.scl_empty(sr.slot), sr.phase ^ 1u, abort_flag, status))
-                        goto producer_done;
-                    const uint32_t scl = sbase + kOffScl + sr.slot * kSclStage;
-                    mbar_arrive_expect_tx(bars.scl_tma(sr.slot), kSclTx);
-                    tma_load_2d(scl, &maps.da, bars.scl_tma(sr.slot), sb * 8, m0);
-                    tma_load_2d(scl + kSclDa, &maps.sa, bars.scl_tma(sr.slot), sb * 8, m0);
-                    scl_issued[sr.slot] = 1;
-                    scl_par[sr.slot] = sr.phase;
-                    sr.next();
                 }
             }
         producer_done:
             // Let every copy already issued land before the CTA can exit.
             for (int s = 0; s < kNumRaw; ++s)
                 if (raw_issued[s]) wait_drain(bars.raw_full(s), raw_par[s], status);
-            for (int s = 0; s < kNumScl; ++s)
-                if (scl_issued[s]) wait_drain(bars.scl_tma(s), scl_par[s], status);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------- MMA issuer
@@ -355,10 +342,10 @@ gemm_tc_kernel(const __grid_constant__ TmaMaps maps, float* __restrict__ C,
             for (int sb = sb_lo; sb < sb_hi; ++sb) {
                 if (!wait_bounded(bars.raw_full(rr.slot), rr.phase, abort_flag, status)) goto scl_done;
                 if (!wait_bounded(bars.scl_empty(sr.slot), sr.phase ^ 1u, abort_flag, status)) goto scl_done;
-                if (!wait_bounded(bars.scl_tma(sr.slot), sr.phase, abort_flag, status)) goto scl_done;
                 {
-                    const uint32_t rawB = sbase + kOffRaw + rr.slot * kRawStage + kRawA;
-                    const uint32_t scl = sbase + kOffScl + sr.slot * kSclStage;
+                    const uint32_t rawB = sbase + kOffRaw + rr.slot * kRawStage + kOffRawB;
+                    const uint32_t rawDa = sbase + kOffRaw + rr.slot * kRawStage + kOffRawDa;
+                    const uint32_t rawSa = sbase + kOffRaw + rr.slot * kRawStage + kOffRawSa;
                     float* colf = reinterpret_cast<float*>(smem + kOffScl + sr.slot * kSclStage + kOffSclCol);
                     float2* row2 = reinterpret_cast<float2*>(smem + kOffScl + sr.slot * kSclStage + kOffSclRow);
 #pragma unroll
@@ -383,9 +370,9 @@ gemm_tc_kernel(const __grid_constant__ TmaMaps maps, float* __restrict__ C,
                             cp[c * (BN * 2)] = d * float(sc) * kDsvScale;
                             cp[c * (BN * 2) + 2] = -(dmin * float(m));
                         }
-                        const uint4 da0 = ld_shared_v4(scl + t * 32), da1 = ld_shared_v4(scl + t * 32 + 16);
-                        const uint4 sa0 = ld_shared_v4(scl + kSclDa + t * 32);
-                        const uint4 sa1 = ld_shared_v4(scl + kSclDa + t * 32 + 16);
+                        const uint4 da0 = ld_shared_v4(rawDa + t * 32), da1 = ld_shared_v4(rawDa + t * 32 + 16);
+                        const uint4 sa0 = ld_shared_v4(rawSa + t * 32);
+                        const uint4 sa1 = ld_shared_v4(rawSa + t * 32 + 16);
                         const uint32_t dav[8] = {da0.x, da0.y, da0.z, da0.w, da1.x, da1.y, da1.z, da1.w};
                         const uint32_t sav[8] = {sa0.x, sa0.y, sa0.z, sa0.w, sa1.x, sa1.y, sa1.z, sa1.w};
 #pragma unroll
@@ -415,7 +402,7 @@ gemm_tc_kernel(const __grid_constant__ TmaMaps maps, float* __restrict__ C,
             for (int sb = sb_lo; sb < sb_hi; ++sb) {
                 if (!wait_bounded(bars.raw_full(rr.slot), rr.phase, abort_flag, status)) goto conv_done;
                 const uint32_t raw = sbase + kOffRaw + rr.slot * kRawStage;
-                const uint32_t rawB = raw + kRawA + t * 144 + 16;
+                const uint32_t rawB = raw + kOffRawB + t * 144 + 16;
                 for (int q = 0; q < 4; ++q) {   // chunk pair q = chunks 2q, 2q+1
                     if (!wait_bounded(bars.op_empty(orr.slot), orr.phase ^ 1u, abort_flag, status))
                         goto conv_done;
