@@ -1,38 +1,50 @@
 // q4_K x q8_1 GEMM on the 5th-generation tensor cores (tcgen05) of sm_103a.
 //
 // Math (web page "20 . r15 -- f32-accumulate mma probe (dead end) + rank-1
-// term2 rescale", section 2.1): for every 32-k chunk c the exact integer dot
-// S_ij = sum_k a_ik * v_jk (|S| <= 32*127*15, section 2.3) is rescaled into
-// f32:  acc_ij += (da_ic * dsv_jc) * S_ij + dma_ic * dmv_jc, dsv = d*sc,
-// dmv = -dmin*m, dma = da*sa once per token row and chunk (the rank-1 fold,
-// page "21 . r16 -- Narrow kernel gets the rank-1 fold", section 2.1).
+// term2 rescale", section 2.1): for every 32-k chunk c
+//     C_ij += (da_ic * d_j * sc_jc) * S_ij + dma_ic * dmv_jc,
+// S_ij = sum_k a_ik * v_jk the exact integer dot of the chunk, dmv = -dmin*m,
+// dma = da*sa once per token row and chunk (the rank-1 fold, page "21 . r16 --
+// Narrow kernel gets the rank-1 fold", section 2.1).  This kernel regroups the
+// same sum so that the CUDA cores do one fused multiply-add per output and
+// chunk:
+//   * the 6-bit scale sc goes into the weight operand: the MMA computes the
+//     integer S'_ij = sc_jc * S_ij (|S'| <= 32*127*63*15 < 2^22, still exact);
+//   * the per-row scale is applied per chunk, the per-super-block d once per
+//     super-block: acc_ij += d_j * sum_c da_ic * S'_ijc;
+//   * the second term, a (K/32)-long f32 contraction of dma with dmv, runs on
+//     the tensor core in tf32 with both factors split into a high and a low
+//     tf32 part (hi*hi + hi*lo + lo*hi, relative error ~2^-21) into its own
+//     tensor-memory accumulator, read once per tile.
 //
 // sm_103a has no integer kind for tcgen05.mma, so the integers go through
-// kind::f16: every quant a in [-127, 127] and nibble v in [0, 15] is an exact
-// fp16 value, every product and partial sum is an integer below 2^24, so the
-// f32 accumulator in tensor memory holds S exactly (checked bit for bit by the
-// S dump).  The nibbles are written as fp16 subnormals v * 2^-24 (just the
-// zero-extended nibble bits, no arithmetic); the 2^24 is folded into dsv.
+// kind::f16: every quant a in [-127, 127] is an exact fp16 value, and the
+// weight factor sc*v <= 945 is written as the fp16 subnormal sc*v * 2^-24
+// (just the integer in the mantissa bits); every product and partial sum is
+// an integer multiple of 2^-24 below 2^-2, so the f32 accumulator holds
+// S' * 2^-24 exactly.  The 2^24 is folded into d.  The S dump (kDump) leaves
+// sc out and returns S itself, bit for bit.
 //
 // One CTA per SM, persistent over 128 (tokens) x 128 (weight rows) tiles,
 // warp-specialised (16 warps; setmaxnreg moves registers to the epilogue):
 //   warp 0      TMA producer: per 256-k super-block the raw int8 A tile (two
 //               128-byte-swizzled boxes), the raw 144-byte q4_K rows, and the
 //               da / sa slices, all zero-filled past M / N.
-//   warp 1      MMA issuer (one thread): per chunk two K=16 MMAs into one of
-//               four 128-column f32 tensor-memory buffers.
-//   warps 2-3   scale tables per super-block: dsv/dmv per weight row and
-//               chunk, (da, dma = da*sa) per token row and chunk.
+//   warp 1      MMA issuer (one thread): per chunk two K=16 f16 MMAs into one
+//               of three 128-column f32 tensor-memory buffers; per super-block
+//               three K=8 tf32 MMAs of the second term into a fourth buffer.
+//   warps 2-3   per super-block: the epilogue's tables (da per row and chunk,
+//               d * 2^24 per weight row) and the split tf32 operands of the
+//               second term (dma per token row, dmv per weight row).
 //   warps 4-7   operand converters: int8 -> fp16 (exact, via the 1024-offset
-//               bit pattern and one fp16 subtraction) and nibble -> fp16 into
-//               the 128-byte-swizzled K-major layout, one 64-k chunk pair at a
-//               time, one row per thread.
-//   warps 8-15  epilogue: per chunk tcgen05.ld of the S tile (16x256b shape:
-//               each thread holds 4 rows x 16 columns, so one column-scale load
-//               serves four rows), the rescale with the fold in packed f32x2
-//               arithmetic, the next tensor-memory load issued before the
-//               current part is computed; C stored at the end of a tile.
-// Within a chunk the k order of both operands is permuted identically
+//               bit pattern and one fp16 subtraction) and nibble * sc -> fp16
+//               subnormal into the 128-byte-swizzled K-major layout, one 64-k
+//               chunk pair at a time, one row per thread.
+//   warps 8-15  epilogue: thread = token row, 64 columns; per chunk four
+//               32x32b.x16 tensor-memory loads (the next in flight while the
+//               current one is used) and 32 packed f32x2 FMAs; per
+//               super-block 32 more for d; C stored at the end of a tile.
+// Within a chunk the k order of both f16 operands is permuted identically
 // (groups of four as 0,2,1,3) so that both unpacks are plain byte/nibble
 // moves; a dot product does not depend on the order of its terms.
 #include <cuda.h>
@@ -49,15 +61,17 @@ namespace {
 using namespace mmq::ptx;
 
 constexpr int BM = 128, BN = 128;
-constexpr int kNumRaw = 2, kNumScl = 2, kNumOp = 2, kNumTm = 4;
+constexpr int kNumRaw = 2, kNumScl = 3, kNumOp = 2, kNumTm = 3;
 constexpr int kSclWarp0 = 2, kNumSclWarps = 2, kConvWarp0 = 4, kNumConvWarps = 4;
 constexpr int kEpiWarp0 = 8, kNumEpiWarps = 8;
 constexpr int kThreads = (kEpiWarp0 + kNumEpiWarps) * 32;   // 512
-// Register split: warpgroups 0-1 (producer, MMA, scale tables, converters)
-// give up registers to warpgroups 2-3 (epilogue).  Launch budget: 512 x 128.
-constexpr uint32_t kRegsLow = 72, kRegsHigh = 184, kRegsLaunch = 128;
+// Register split: warpgroups 0-1 (producer, MMA, tables, converters) give up
+// registers to warpgroups 2-3 (epilogue).  Launch budget: 512 x 128.
+constexpr uint32_t kRegsLow = 80, kRegsHigh = 176, kRegsLaunch = 128;
 static_assert(256 * kRegsLow + 256 * kRegsHigh <= kThreads * kRegsLaunch, "register split");
-constexpr uint32_t kTmemCols = 512;                          // kNumTm x BN
+constexpr uint32_t kTmemCols = 512;                          // kNumTm x BN + BN (second term)
+constexpr uint32_t kTmemMin = kNumTm * BN;                   // column of the second-term accumulator
+static_assert(kTmemMin + BN <= kTmemCols, "tensor memory budget");
 
 // Shared memory map (offsets from a 1024-byte aligned base).
 constexpr int kRawASub = BM * 128;                   // 16 KB: 128 rows x 128 B, swizzled
@@ -67,29 +81,31 @@ constexpr int kRawDa = BM * 8 * 4;                   // da [128][8] f32
 constexpr int kRawSa = BM * 8 * 4;                   // sa [128][8] i32
 constexpr int kOffRawB = kRawA, kOffRawDa = kRawA + kRawB, kOffRawSa = kOffRawDa + kRawDa;
 constexpr int kRawStage = kOffRawSa + kRawSa;        // 58 KB: everything one super-block needs from HBM
-constexpr int kSclCol = 8 * BN * 8;                  // [8 chunks][64 column pairs] float4
-                                                     //   {dsv_2p, dsv_2p+1, dmv_2p, dmv_2p+1}
-constexpr int kSclRow = 8 * BM * 8;                  // [8 chunks][128 rows] float2 {da, da*sa}
-constexpr int kOffSclCol = 0;
-constexpr int kOffSclRow = kOffSclCol + kSclCol;
-constexpr int kSclStage = kOffSclRow + kSclRow;      // 16 KB of scale tables (no copies land here)
 constexpr int kOpTile = 128 * 128;                   // 128 rows x 64 fp16 (128 B), swizzled
 constexpr int kOpStage = 2 * kOpTile;                // A + B
+constexpr int kMinTile = 128 * 128;                  // 128 rows x 32 tf32 slots (24 used), swizzled
+constexpr int kMinStage = 2 * kMinTile;              // dma parts + dmv parts
+constexpr int kSclDa = 8 * BM * 4;                   // da [8 chunks][128 rows] f32
+constexpr int kSclD = BN * 4;                        // d * 2^24 [128 weight rows] f32
+constexpr int kSclStage = kSclDa + kSclD;            // 4.5 KB
 constexpr int kOffRaw = 0;
-constexpr int kOffScl = kOffRaw + kNumRaw * kRawStage;
-constexpr int kOffOp = kOffScl + kNumScl * kSclStage;
-constexpr int kOffBar = kOffOp + kNumOp * kOpStage;
-// barriers: raw_full, raw_empty, scl_col, scl_empty, op_full, op_empty, tm_full, tm_empty
-constexpr int kNumBars = 2 * kNumRaw + 2 * kNumScl + 2 * kNumOp + 2 * kNumTm;
+constexpr int kOffOp = kOffRaw + kNumRaw * kRawStage;
+constexpr int kOffMin = kOffOp + kNumOp * kOpStage;
+constexpr int kOffScl = kOffMin + kMinStage;
+constexpr int kOffBar = kOffScl + kNumScl * kSclStage;
+// barriers: raw full/empty, op full/empty, tm full/empty, scl full/empty,
+// min full/empty, dmin full/empty
+constexpr int kNumBars = 2 * kNumRaw + 2 * kNumOp + 2 * kNumTm + 2 * kNumScl + 4;
 constexpr int kOffMisc = kOffBar + kNumBars * 8;     // tmem slot, abort flag
 constexpr int kSmemBytes = kOffMisc + 16 + 1024;     // + alignment slack
-static_assert(kOffOp % 1024 == 0, "operand tiles need 1024-byte alignment");
-static_assert(kRawStage % 1024 == 0 && kSclStage % 1024 == 0, "stage alignment");
+static_assert(kOffOp % 1024 == 0 && kOffMin % 1024 == 0, "operand tiles need 1024-byte alignment");
+static_assert(kRawStage % 1024 == 0 && kSclStage % 16 == 0, "stage alignment");
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 
 constexpr uint32_t kRawTx = kRawStage;
 constexpr uint32_t kIdesc = idesc_f16_f32(BM, BN);
-constexpr float kDsvScale = 16777216.0f;             // 2^24: nibbles are fp16 subnormals
+constexpr uint32_t kIdescTf32 = idesc_tf32_f32(BM, BN);
+constexpr float kSubnormalScale = 16777216.0f;       // 2^24: weight factors are fp16 subnormals
 
 struct TmaMaps {
     CUtensorMap a, b, da, sa;
@@ -97,20 +113,22 @@ struct TmaMaps {
 
 struct Bars {
     uint32_t base;
-    __device__ uint32_t raw_full(int s) const { return base + 8 * s; }
-    __device__ uint32_t raw_empty(int s) const { return base + 8 * (kNumRaw + s); }
-    __device__ uint32_t scl_col(int s) const { return base + 8 * (2 * kNumRaw + s); }
-    __device__ uint32_t scl_empty(int s) const { return base + 8 * (2 * kNumRaw + kNumScl + s); }
-    __device__ uint32_t op_full(int s) const { return base + 8 * (2 * kNumRaw + 2 * kNumScl + s); }
-    __device__ uint32_t op_empty(int s) const {
-        return base + 8 * (2 * kNumRaw + 2 * kNumScl + kNumOp + s);
+    __device__ uint32_t at(int i) const { return base + 8 * i; }
+    __device__ uint32_t raw_full(int s) const { return at(s); }
+    __device__ uint32_t raw_empty(int s) const { return at(kNumRaw + s); }
+    __device__ uint32_t op_full(int s) const { return at(2 * kNumRaw + s); }
+    __device__ uint32_t op_empty(int s) const { return at(2 * kNumRaw + kNumOp + s); }
+    __device__ uint32_t tm_full(int s) const { return at(2 * kNumRaw + 2 * kNumOp + s); }
+    __device__ uint32_t tm_empty(int s) const { return at(2 * kNumRaw + 2 * kNumOp + kNumTm + s); }
+    __device__ uint32_t scl_full(int s) const { return at(2 * kNumRaw + 2 * kNumOp + 2 * kNumTm + s); }
+    __device__ uint32_t scl_empty(int s) const {
+        return at(2 * kNumRaw + 2 * kNumOp + 2 * kNumTm + kNumScl + s);
     }
-    __device__ uint32_t tm_full(int s) const {
-        return base + 8 * (2 * kNumRaw + 2 * kNumScl + 2 * kNumOp + s);
-    }
-    __device__ uint32_t tm_empty(int s) const {
-        return base + 8 * (2 * kNumRaw + 2 * kNumScl + 2 * kNumOp + kNumTm + s);
-    }
+    static constexpr int kMin0 = 2 * kNumRaw + 2 * kNumOp + 2 * kNumTm + 2 * kNumScl;
+    __device__ uint32_t min_full() const { return at(kMin0); }
+    __device__ uint32_t min_empty() const { return at(kMin0 + 1); }
+    __device__ uint32_t dmin_full() const { return at(kMin0 + 2); }
+    __device__ uint32_t dmin_empty() const { return at(kMin0 + 3); }
 };
 
 // Ring position: slot index and the parity of the current pass over the ring.
@@ -143,11 +161,34 @@ __device__ __forceinline__ void cvt_a4(uint32_t w, uint32_t& h02, uint32_t& h13)
     h13 = *reinterpret_cast<uint32_t*>(&y);
 }
 
+// 6-bit scales / mins of a q4_K super-block (12 bytes s[0..11] as three
+// words), four per word, one per byte: sub-blocks 0-3 are the low six bits
+// of s[0..3] / s[4..7]; sub-blocks 4-7 take their low four bits from s[8..11]
+// (low / high nibble) and their top two bits from the top of s[0..3] / s[4..7].
+__device__ __forceinline__ uint32_t sc_lo4(uint32_t s0) { return s0 & 0x3F3F3F3Fu; }
+__device__ __forceinline__ uint32_t sc_hi4(uint32_t s0, uint32_t s2) {
+    return (s2 & 0x0F0F0F0Fu) | ((s0 >> 2) & 0x30303030u);
+}
+__device__ __forceinline__ uint32_t m_lo4(uint32_t s1) { return s1 & 0x3F3F3F3Fu; }
+__device__ __forceinline__ uint32_t m_hi4(uint32_t s1, uint32_t s2) {
+    return ((s2 >> 4) & 0x0F0F0F0Fu) | ((s1 >> 2) & 0x30303030u);
+}
+
+// x = hi + lo with hi = x truncated to tf32 (low 13 mantissa bits cleared);
+// lo = x - hi is exact in f32.
+__device__ __forceinline__ void split_tf32(float x, float& hi, float& lo) {
+    hi = __uint_as_float(__float_as_uint(x) & 0xFFFFE000u);
+    lo = x - hi;
+}
+
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
                                              uint32_t d) {
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
                  "r"(d)
                  : "memory");
+}
+__device__ __forceinline__ void st_shared_v4f(uint32_t addr, float a, float b, float c, float d) {
+    st_shared_v4(addr, __float_as_uint(a), __float_as_uint(b), __float_as_uint(c), __float_as_uint(d));
 }
 
 __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
@@ -176,21 +217,35 @@ __device__ __forceinline__ float4 ld_dsmem_v4(uint32_t addr) {
     return v;
 }
 
-// Epilogue thread's 4 rows x 16 columns of the 128x128 tile (m0, n0) -> C.
-__device__ __forceinline__ void store_tile(float* C, const uint64_t (&acc)[4][8], int M, int N, int m0,
-                                           int n0, int quarter, int colhalf, int tq, int tr4) {
+// One 16-column part of a chunk: asb[8p + j] (+)= da * S'[16p + 2j, +1].
+template <int P>
+__device__ __forceinline__ void chunk_part(uint64_t (&asb)[32], const uint32_t (&b)[16], uint64_t da2) {
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-        const int64_t gr = int64_t(m0) + quarter * 32 + tq + 8 * k;
-        if (gr < M) {
-            float* crow = C + gr * N;
+    for (int j = 0; j < 8; ++j) asb[8 * P + j] = ffma2(pack2u(b[2 * j], b[2 * j + 1]), da2, asb[8 * P + j]);
+}
+
+// S dump of one 16-column part (block dots, bit for bit).
+__device__ __forceinline__ void dump_part(int32_t* S, const uint32_t (&b)[16], int64_t gr, int gc0, int M,
+                                          int N, int nb, int kb) {
+    if (gr >= M) return;
 #pragma unroll
-            for (int g = 0; g < 8; ++g) {
-                const int gc = n0 + colhalf * 64 + 8 * g + 2 * tr4;
-                if (gc < N)
-                    *reinterpret_cast<float2*>(crow + gc) = make_float2(lo_f(acc[k][g]), hi_f(acc[k][g]));
-            }
-        }
+    for (int j = 0; j < 16; ++j)
+        if (gc0 + j < N)
+            S[(gr * N + gc0 + j) * int64_t(nb) + kb] = int32_t(__uint_as_float(b[j]) * kSubnormalScale);
+}
+
+// Epilogue thread's row x 64 columns of the 128x128 tile (m0, n0) -> C.
+__device__ __forceinline__ void store_tile(float* C, const uint64_t (&acc)[32], int M, int N, int m0,
+                                           int n0, int row, int colhalf) {
+    const int64_t gr = int64_t(m0) + row;
+    if (gr >= M) return;
+    float* crow = C + gr * N;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        const int gc = n0 + colhalf * 64 + 4 * i;   // N % 4 == 0: all four columns or none
+        if (gc < N)
+            *reinterpret_cast<float4*>(crow + gc) =
+                make_float4(lo_f(acc[2 * i]), hi_f(acc[2 * i]), lo_f(acc[2 * i + 1]), hi_f(acc[2 * i + 1]));
     }
 }
 
@@ -224,10 +279,6 @@ gemm_tc_kernel(const __grid_constant__ TmaMaps maps, float* __restrict__ C,
             mbar_init(bars.raw_full(s), 1);
             mbar_init(bars.raw_empty(s), kNumConvWarps + kNumSclWarps);
         }
-        for (int s = 0; s < kNumScl; ++s) {
-            mbar_init(bars.scl_col(s), kNumSclWarps);
-            mbar_init(bars.scl_empty(s), kNumEpiWarps);
-        }
         for (int s = 0; s < kNumOp; ++s) {
             mbar_init(bars.op_full(s), kNumConvWarps);
             mbar_init(bars.op_empty(s), 1);
@@ -236,6 +287,14 @@ gemm_tc_kernel(const __grid_constant__ TmaMaps maps, float* __restrict__ C,
             mbar_init(bars.tm_full(s), 1);
             mbar_init(bars.tm_empty(s), kNumEpiWarps);
         }
+        for (int s = 0; s < kNumScl; ++s) {
+            mbar_init(bars.scl_full(s), kNumSclWarps);
+            mbar_init(bars.scl_empty(s), kNumEpiWarps);
+        }
+        mbar_init(bars.min_full(), kNumSclWarps);
+        mbar_init(bars.min_empty(), 1);
+        mbar_init(bars.dmin_full(), 1);
+        mbar_init(bars.dmin_empty(), kNumEpiWarps);
         *abort_flag = 0;
         fence_barrier_init();
         fence_proxy_async_smem();
@@ -294,9 +353,10 @@ gemm_tc_kernel(const __grid_constant__ TmaMaps maps, float* __restrict__ C,
         if (lane == 0) {
             Ring<kNumOp> orr;
             Ring<kNumTm> tr;
-            int issued = 0;
-            int last_slot = 0;
-            uint32_t last_par = 0;
+            Ring<1> mr, dr;
+            uint32_t last_bar = 0, last_par = 0;   // most recent commit, drained on exit
+            const uint32_t dmin = tmem_base + kTmemMin;
+            const uint32_t minA = sbase + kOffMin, minB = minA + kMinTile;
             for (int tile = tile_first; tile < num_tiles; tile += tile_step) {
                 for (int sb = sb_lo; sb < sb_hi; ++sb) {
                     for (int q = 0; q < 4; ++q) {
@@ -317,82 +377,124 @@ gemm_tc_kernel(const __grid_constant__ TmaMaps maps, float* __restrict__ C,
                                         kIdesc, uint32_t(kk));
                             }
                             mma_commit(bars.tm_full(tr.slot));
-                            issued = 1;
-                            last_slot = tr.slot;
+                            last_bar = bars.tm_full(tr.slot);
                             last_par = tr.phase;
                             tr.next();
                         }
                         mma_commit(bars.op_empty(orr.slot));
                         orr.next();
                     }
-                }
-            }
-        mma_done:
-            if (issued) wait_drain(bars.tm_full(last_slot), last_par, status);
-        }
-    } else if (warp < kConvWarp0) {
-        // ------------------------------------------------------ scale tables
-        // Weight rows: dsv = d*sc (times 2^24 for the subnormal nibbles) and
-        // dmv = -dmin*m, exact in f32, as column pairs {dsv0, dsv1, dmv0, dmv1};
-        // token rows: {da, dma = da*sa}, the rank-1 fold once per row and chunk.
-        const int ts = threadIdx.x - kSclWarp0 * 32;   // 0..63: rows ts and ts + 64
-        Ring<kNumRaw> rr;
-        Ring<kNumScl> sr;
-        for (int tile = tile_first; tile < num_tiles; tile += tile_step) {
-            for (int sb = sb_lo; sb < sb_hi; ++sb) {
-                if (!wait_bounded(bars.raw_full(rr.slot), rr.phase, abort_flag, status)) goto scl_done;
-                if (!wait_bounded(bars.scl_empty(sr.slot), sr.phase ^ 1u, abort_flag, status)) goto scl_done;
-                {
-                    const uint32_t rawB = sbase + kOffRaw + rr.slot * kRawStage + kOffRawB;
-                    const uint32_t rawDa = sbase + kOffRaw + rr.slot * kRawStage + kOffRawDa;
-                    const uint32_t rawSa = sbase + kOffRaw + rr.slot * kRawStage + kOffRawSa;
-                    float* colf = reinterpret_cast<float*>(smem + kOffScl + sr.slot * kSclStage + kOffSclCol);
-                    float2* row2 = reinterpret_cast<float2*>(smem + kOffScl + sr.slot * kSclStage + kOffSclRow);
+                    if (!kDump) {
+                        // second term of this super-block: three K=8 tf32 MMAs
+                        if (!wait_bounded(bars.min_full(), mr.phase, abort_flag, status)) goto mma_done;
+                        if (sb == sb_lo &&
+                            !wait_bounded(bars.dmin_empty(), dr.phase ^ 1u, abort_flag, status))
+                            goto mma_done;
+                        tc_fence_after();
 #pragma unroll
-                    for (int rh = 0; rh < 2; ++rh) {
-                        const int t = ts + 64 * rh;
-                        const uint4 hdr = ld_shared_v4(rawB + t * 144);   // d, dmin, s[0..11]
-                        const float d = __half2float(__ushort_as_half(uint16_t(hdr.x & 0xFFFFu)));
-                        const float dmin = __half2float(__ushort_as_half(uint16_t(hdr.x >> 16)));
-                        const uint32_t s0 = hdr.y, s1 = hdr.z, s2 = hdr.w;   // s[0..3], s[4..7], s[8..11]
-                        float* cp = colf + (t >> 1) * 4 + (t & 1);
-#pragma unroll
-                        for (int c = 0; c < 8; ++c) {
-                            uint32_t sc, m;
-                            if (c < 4) {
-                                sc = (s0 >> (8 * c)) & 63u;
-                                m = (s1 >> (8 * c)) & 63u;
-                            } else {
-                                const int b = 8 * (c - 4);
-                                sc = ((s2 >> b) & 15u) | (((s0 >> (b + 6)) & 3u) << 4);
-                                m = ((s2 >> (b + 4)) & 15u) | (((s1 >> (b + 6)) & 3u) << 4);
-                            }
-                            cp[c * (BN * 2)] = d * float(sc) * kDsvScale;
-                            cp[c * (BN * 2) + 2] = -(dmin * float(m));
-                        }
-                        const uint4 da0 = ld_shared_v4(rawDa + t * 32), da1 = ld_shared_v4(rawDa + t * 32 + 16);
-                        const uint4 sa0 = ld_shared_v4(rawSa + t * 32);
-                        const uint4 sa1 = ld_shared_v4(rawSa + t * 32 + 16);
-                        const uint32_t dav[8] = {da0.x, da0.y, da0.z, da0.w, da1.x, da1.y, da1.z, da1.w};
-                        const uint32_t sav[8] = {sa0.x, sa0.y, sa0.z, sa0.w, sa1.x, sa1.y, sa1.z, sa1.w};
-#pragma unroll
-                        for (int c = 0; c < 8; ++c) {
-                            const float da = __uint_as_float(dav[c]);
-                            row2[c * BM + t] = make_float2(da, da * float(int32_t(sav[c])));
+                        for (int j = 0; j < 3; ++j)
+                            mma_tf32(dmin, smem_desc_sw128(minA + 32 * j), smem_desc_sw128(minB + 32 * j),
+                                     kIdescTf32, uint32_t(sb > sb_lo || j > 0));
+                        mma_commit(bars.min_empty());
+                        last_bar = bars.min_empty();
+                        last_par = mr.phase;
+                        mr.next();
+                        if (sb == sb_hi - 1) {
+                            mma_commit(bars.dmin_full());
+                            dr.next();
                         }
                     }
                 }
-                __syncwarp();
-                if (lane == 0) {
-                    mbar_arrive(bars.scl_col(sr.slot));
-                    mbar_arrive(bars.raw_empty(rr.slot));
+            }
+        mma_done:
+            if (last_bar) wait_drain(last_bar, last_par, status);
+        }
+    } else if (warp < kConvWarp0) {
+        // ------------------------------------------- tables and second term
+        const int ts = threadIdx.x - kSclWarp0 * 32;   // 0..63: rows ts and ts + 64
+        Ring<kNumRaw> rr;
+        Ring<kNumScl> sr;
+        Ring<1> mr;
+        for (int tile = tile_first; tile < num_tiles; tile += tile_step) {
+            for (int sb = sb_lo; sb < sb_hi; ++sb) {
+                if (!wait_bounded(bars.raw_full(rr.slot), rr.phase, abort_flag, status)) goto scl_done;
+                {
+                    const uint32_t raw = sbase + kOffRaw + rr.slot * kRawStage;
+                    if (!wait_bounded(bars.scl_empty(sr.slot), sr.phase ^ 1u, abort_flag, status))
+                        goto scl_done;
+                    float* dat = reinterpret_cast<float*>(smem + kOffScl + sr.slot * kSclStage);
+                    float* dtab = dat + 8 * BM;
+#pragma unroll
+                    for (int rh = 0; rh < 2; ++rh) {
+                        const int t = ts + 64 * rh;
+                        const uint4 d0 = ld_shared_v4(raw + kOffRawDa + t * 32);
+                        const uint4 d1 = ld_shared_v4(raw + kOffRawDa + t * 32 + 16);
+                        const uint32_t dv[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
+#pragma unroll
+                        for (int c = 0; c < 8; ++c) dat[c * BM + t] = __uint_as_float(dv[c]);
+                        const uint32_t h0 = ld_shared_v4(raw + kOffRawB + t * 144).x;
+                        dtab[t] = __half2float(__ushort_as_half(uint16_t(h0 & 0xFFFFu))) * kSubnormalScale;
+                    }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bars.scl_full(sr.slot));
+                    sr.next();
+                    if (!kDump) {
+                        if (!wait_bounded(bars.min_empty(), mr.phase ^ 1u, abort_flag, status)) goto scl_done;
+                        const uint32_t minA = sbase + kOffMin, minB = minA + kMinTile;
+#pragma unroll
+                        for (int rh = 0; rh < 2; ++rh) {
+                            const int t = ts + 64 * rh;
+                            const int sw = t & 7;
+                            // token row t: dma = da * sa per chunk, split hi / lo
+                            const uint4 d0 = ld_shared_v4(raw + kOffRawDa + t * 32);
+                            const uint4 d1 = ld_shared_v4(raw + kOffRawDa + t * 32 + 16);
+                            const uint4 s0 = ld_shared_v4(raw + kOffRawSa + t * 32);
+                            const uint4 s1 = ld_shared_v4(raw + kOffRawSa + t * 32 + 16);
+                            const uint32_t dv[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
+                            const uint32_t sv[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+                            float ah[8], al[8];
+#pragma unroll
+                            for (int c = 0; c < 8; ++c)
+                                split_tf32(__uint_as_float(dv[c]) * float(int32_t(sv[c])), ah[c], al[c]);
+                            // k slots: 0-7 hi, 8-15 hi, 16-23 lo (against hi, lo, hi of dmv)
+                            const uint32_t ra = minA + t * 128;
+                            st_shared_v4f(ra + ((0 ^ sw) << 4), ah[0], ah[1], ah[2], ah[3]);
+                            st_shared_v4f(ra + ((1 ^ sw) << 4), ah[4], ah[5], ah[6], ah[7]);
+                            st_shared_v4f(ra + ((2 ^ sw) << 4), ah[0], ah[1], ah[2], ah[3]);
+                            st_shared_v4f(ra + ((3 ^ sw) << 4), ah[4], ah[5], ah[6], ah[7]);
+                            st_shared_v4f(ra + ((4 ^ sw) << 4), al[0], al[1], al[2], al[3]);
+                            st_shared_v4f(ra + ((5 ^ sw) << 4), al[4], al[5], al[6], al[7]);
+                            // weight row t: dmv = -dmin * m per chunk (exact in f32), split hi / lo
+                            const uint4 hdr = ld_shared_v4(raw + kOffRawB + t * 144);
+                            const float dmn = __half2float(__ushort_as_half(uint16_t(hdr.x >> 16)));
+                            const uint32_t mlo = m_lo4(hdr.z), mhi = m_hi4(hdr.z, hdr.w);
+                            float bh[8], bl[8];
+#pragma unroll
+                            for (int c = 0; c < 8; ++c) {
+                                const uint32_t mv = ((c < 4 ? mlo : mhi) >> (8 * (c & 3))) & 0xFFu;
+                                split_tf32(-(dmn * float(mv)), bh[c], bl[c]);
+                            }
+                            const uint32_t rb = minB + t * 128;
+                            st_shared_v4f(rb + ((0 ^ sw) << 4), bh[0], bh[1], bh[2], bh[3]);
+                            st_shared_v4f(rb + ((1 ^ sw) << 4), bh[4], bh[5], bh[6], bh[7]);
+                            st_shared_v4f(rb + ((2 ^ sw) << 4), bl[0], bl[1], bl[2], bl[3]);
+                            st_shared_v4f(rb + ((3 ^ sw) << 4), bl[4], bl[5], bl[6], bl[7]);
+                            st_shared_v4f(rb + ((4 ^ sw) << 4), bh[0], bh[1], bh[2], bh[3]);
+                            st_shared_v4f(rb + ((5 ^ sw) << 4), bh[4], bh[5], bh[6], bh[7]);
+                        }
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(bars.min_full());
+                        mr.next();
+                    }
                 }
-                sr.next();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bars.raw_empty(rr.slot));
                 rr.next();
             }
         }
     scl_done:;
-    } else if (warp < kEpiWarp0) {
+    } else {
         // -------------------------------------------------------- converters
         const int t = threadIdx.x - kConvWarp0 * 32;   // 0..127: this thread's row
         const int sw = t & 7;
@@ -403,9 +505,19 @@ gemm_tc_kernel(const __grid_constant__ TmaMaps maps, float* __restrict__ C,
                 if (!wait_bounded(bars.raw_full(rr.slot), rr.phase, abort_flag, status)) goto conv_done;
                 const uint32_t raw = sbase + kOffRaw + rr.slot * kRawStage;
                 const uint32_t rawB = raw + kOffRawB + t * 144 + 16;
+                uint32_t scw_lo = 0x01010101u, scw_hi = 0x01010101u;   // the S dump keeps sc out
+                if (!kDump) {
+                    const uint4 hdr = ld_shared_v4(raw + kOffRawB + t * 144);
+                    scw_lo = sc_lo4(hdr.y);
+                    scw_hi = sc_hi4(hdr.y, hdr.w);
+                }
                 for (int q = 0; q < 4; ++q) {   // chunk pair q = chunks 2q, 2q+1
                     if (!wait_bounded(bars.op_empty(orr.slot), orr.phase ^ 1u, abort_flag, status))
                         goto conv_done;
+                    const uint32_t scw = q < 2 ? scw_lo : scw_hi;
+                    const uint32_t sh = 16u * uint32_t(q & 1);
+                    const uint32_t sca = (scw >> sh) & 0xFFu;          // chunk 2q: low nibbles
+                    const uint32_t scb = (scw >> (sh + 8u)) & 0xFFu;   // chunk 2q+1: high nibbles
                     const uint32_t opA = sbase + kOffOp + orr.slot * kOpStage + t * 128;
                     const uint32_t opB = opA + kOpTile;
                     uint4 wa[4], wb[2];
@@ -431,10 +543,12 @@ gemm_tc_kernel(const __grid_constant__ TmaMaps maps, float* __restrict__ C,
                         uint32_t lo[8], hi[8];
 #pragma unroll
                         for (int u = 0; u < 4; ++u) {
-                            lo[2 * u] = ww[u] & 0x000F000Fu;            // {e0, e2} low nibbles
-                            lo[2 * u + 1] = (ww[u] >> 8) & 0x000F000Fu; // {e1, e3}
-                            hi[2 * u] = (ww[u] >> 4) & 0x000F000Fu;
-                            hi[2 * u + 1] = (ww[u] >> 12) & 0x000F000Fu;
+                            // two nibbles per 32-bit word, one per 16-bit half; times sc
+                            // (<= 63 * 15 = 945, no carry into the upper half)
+                            lo[2 * u] = (ww[u] & 0x000F000Fu) * sca;            // {e0, e2} low nibbles
+                            lo[2 * u + 1] = ((ww[u] >> 8) & 0x000F000Fu) * sca; // {e1, e3}
+                            hi[2 * u] = ((ww[u] >> 4) & 0x000F000Fu) * scb;
+                            hi[2 * u + 1] = ((ww[u] >> 12) & 0x000F000Fu) * scb;
                         }
                         st_shared_v4(opB + (((2 * G) ^ sw) << 4), lo[0], lo[1], lo[2], lo[3]);
                         st_shared_v4(opB + (((2 * G + 1) ^ sw) << 4), lo[4], lo[5], lo[6], lo[7]);
@@ -460,117 +574,108 @@ gemm_tc_kernel(const __grid_constant__ TmaMaps maps, float* __restrict__ C,
     } else {
         setmaxnreg_inc<kRegsHigh>();
         // ---------------------------------------------------------- epilogue
-        // Thread t of a warp holds, per chunk, rows quarter*32 + t/4 + 8k
-        // (k = 0..3) x columns colhalf*64 + 8g + 2(t%4) + {0,1} (g = 0..7).
-        // A chunk is read from tensor memory in two parts (lanes +0..15 give
-        // rows k = 0,1; lanes +16..31 give k = 2,3); the load of the next part
-        // is in flight while the current one is computed.
+        // Thread = token row quarter*32 + lane (the tensor-memory lane quarter
+        // this warp may read) x 64 columns colhalf*64 + [0, 64).
         const int ew = warp - kEpiWarp0;
-        const int quarter = warp & 3;                  // tensor-memory lanes this warp may read
-        const int colhalf = ew >> 2;                   // columns [64*colhalf, +64)
-        const int tq = lane >> 2, tr4 = lane & 3;
-        const uint32_t tlane0 = uint32_t(quarter * 32) << 16, tlane1 = uint32_t(quarter * 32 + 16) << 16;
+        const int quarter = warp & 3;
+        const int colhalf = ew >> 2;
+        const int row = quarter * 32 + lane;
+        const uint32_t tlane = uint32_t(quarter * 32) << 16;
+        const int nb = K / 32;
         Ring<kNumScl> sr;
         Ring<kNumTm> tr;
-        uint64_t acc[4][8];
+        Ring<1> dr;
+        uint64_t acc[32], asb[32];
         for (int tile = tile_first; tile < num_tiles; tile += tile_step) {
             const int m0 = (tile / tiles_n) * BM, n0 = (tile % tiles_n) * BN;
 #pragma unroll
-            for (int k = 0; k < 4; ++k)
-#pragma unroll
-                for (int g = 0; g < 8; ++g) acc[k][g] = 0ull;
-            uint32_t b0[32], b1[32];
-            // prologue: first part of the tile's first chunk
-            if (!wait_bounded(bars.scl_col(sr.slot), sr.phase, abort_flag, status)) goto epi_done;
-            if (!wait_bounded(bars.tm_full(tr.slot), tr.phase, abort_flag, status)) goto epi_done;
-            tc_fence_after();
-            tmem_ld_16x256b_x8(tmem_base + tlane0 + uint32_t(tr.slot * BN + colhalf * 64), b0);
-            tmem_wait_ld();
+            for (int i = 0; i < 32; ++i) acc[i] = 0ull;
             for (int sb = sb_lo; sb < sb_hi; ++sb) {
-                const uint8_t* scl = smem + kOffScl + sr.slot * kSclStage;
-                const float4* col4 = reinterpret_cast<const float4*>(scl + kOffSclCol);
-                const float2* row2 = reinterpret_cast<const float2*>(scl + kOffSclRow);
+                if (!wait_bounded(bars.scl_full(sr.slot), sr.phase, abort_flag, status)) goto epi_done;
+                const float* dat = reinterpret_cast<const float*>(smem + kOffScl + sr.slot * kSclStage);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) asb[i] = 0ull;
                 for (int c = 0; c < 8; ++c) {
-                    float4 cs[8];
-#pragma unroll
-                    for (int g = 0; g < 8; ++g) cs[g] = col4[c * 64 + colhalf * 32 + 4 * g + tr4];
-                    float2 rr[4];
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) rr[k] = row2[c * BM + quarter * 32 + tq + 8 * k];
-                    // second part of this chunk, then compute the first part
-                    tmem_ld_16x256b_x8(tmem_base + tlane1 + uint32_t(tr.slot * BN + colhalf * 64), b1);
-#pragma unroll
-                    for (int kk = 0; kk < 2; ++kk) {
-                        if (kDump) {
-                            const int64_t gr = int64_t(m0) + quarter * 32 + tq + 8 * kk;
-#pragma unroll
-                            for (int g = 0; g < 8; ++g)
-#pragma unroll
-                                for (int e = 0; e < 2; ++e) {
-                                    const int64_t gc = int64_t(n0) + colhalf * 64 + 8 * g + 2 * tr4 + e;
-                                    if (gr < M && gc < N)
-                                        S[(gr * N + gc) * (K / 32) + sb * 8 + c] =
-                                            int32_t(__uint_as_float(b0[4 * g + 2 * kk + e]) * kDsvScale);
-                                }
-                        } else {
-                            const uint64_t da2 = pack2(rr[kk].x, rr[kk].x), dma2 = pack2(rr[kk].y, rr[kk].y);
-#pragma unroll
-                            for (int g = 0; g < 8; ++g) {
-                                const uint64_t c1 = fmul2(da2, pack2(cs[g].x, cs[g].y));
-                                const uint64_t a = ffma2(c1, pack2u(b0[4 * g + 2 * kk], b0[4 * g + 2 * kk + 1]), acc[kk][g]);
-                                acc[kk][g] = ffma2(dma2, pack2(cs[g].z, cs[g].w), a);
-                            }
-                        }
-                    }
-                    tmem_wait_ld();
-                    // the whole S tile of this chunk is in registers: hand the buffer back
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(bars.tm_empty(tr.slot));
-                    tr.next();
-                    const bool last_in_sb = (c == 7);
-                    const bool has_next = !(last_in_sb && sb == sb_hi - 1);
-                    if (last_in_sb) {   // scale tables of this super-block no longer needed
+                    const float da = dat[c * BM + row];
+                    const uint64_t da2 = pack2(da, da);
+                    if (!wait_bounded(bars.tm_full(tr.slot), tr.phase, abort_flag, status)) goto epi_done;
+                    tc_fence_after();
+                    const uint32_t ta = tmem_base + tlane + uint32_t(tr.slot * BN + colhalf * 64);
+                    uint32_t b0[16], b1[16];
+                    tmem_ld_32x32b_x16(ta, b0);
+                    tmem_wait_ld(b0);
+                    tmem_ld_32x32b_x16(ta + 16, b1);
+                    if (kDump) {
+                        const int64_t gr = int64_t(m0) + row;
+                        const int gc = n0 + colhalf * 64, kb = sb * 8 + c;
+                        dump_part(S, b0, gr, gc, M, N, nb, kb);
+                        tmem_wait_ld(b1);
+                        tmem_ld_32x32b_x16(ta + 32, b0);
+                        dump_part(S, b1, gr, gc + 16, M, N, nb, kb);
+                        tmem_wait_ld(b0);
+                        tmem_ld_32x32b_x16(ta + 48, b1);
+                        dump_part(S, b0, gr, gc + 32, M, N, nb, kb);
+                        tmem_wait_ld(b1);
+                        tc_fence_before();
                         __syncwarp();
-                        if (lane == 0) mbar_arrive(bars.scl_empty(sr.slot));
-                        sr.next();
+                        if (lane == 0) mbar_arrive(bars.tm_empty(tr.slot));
+                        tr.next();
+                        dump_part(S, b1, gr, gc + 48, M, N, nb, kb);
+                    } else {
+                        chunk_part<0>(asb, b0, da2);
+                        tmem_wait_ld(b1);
+                        tmem_ld_32x32b_x16(ta + 32, b0);
+                        chunk_part<1>(asb, b1, da2);
+                        tmem_wait_ld(b0);
+                        tmem_ld_32x32b_x16(ta + 48, b1);
+                        chunk_part<2>(asb, b0, da2);
+                        tmem_wait_ld(b1);
+                        // the whole S' tile of this chunk is in registers: hand the buffer back
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(bars.tm_empty(tr.slot));
+                        tr.next();
+                        chunk_part<3>(asb, b1, da2);
                     }
-                    if (has_next) {
-                        if (last_in_sb &&
-                            !wait_bounded(bars.scl_col(sr.slot), sr.phase, abort_flag, status))
-                            goto epi_done;
-                        if (!wait_bounded(bars.tm_full(tr.slot), tr.phase, abort_flag, status)) goto epi_done;
-                        tc_fence_after();
-                        tmem_ld_16x256b_x8(tmem_base + tlane0 + uint32_t(tr.slot * BN + colhalf * 64), b0);
-                    }
-#pragma unroll
-                    for (int kk = 0; kk < 2; ++kk) {
-                        const int k = 2 + kk;
-                        if (kDump) {
-                            const int64_t gr = int64_t(m0) + quarter * 32 + tq + 8 * k;
-#pragma unroll
-                            for (int g = 0; g < 8; ++g)
-#pragma unroll
-                                for (int e = 0; e < 2; ++e) {
-                                    const int64_t gc = int64_t(n0) + colhalf * 64 + 8 * g + 2 * tr4 + e;
-                                    if (gr < M && gc < N)
-                                        S[(gr * N + gc) * (K / 32) + sb * 8 + c] =
-                                            int32_t(__uint_as_float(b1[4 * g + 2 * kk + e]) * kDsvScale);
-                                }
-                        } else {
-                            const uint64_t da2 = pack2(rr[k].x, rr[k].x), dma2 = pack2(rr[k].y, rr[k].y);
-#pragma unroll
-                            for (int g = 0; g < 8; ++g) {
-                                const uint64_t c1 = fmul2(da2, pack2(cs[g].x, cs[g].y));
-                                const uint64_t a = ffma2(c1, pack2u(b1[4 * g + 2 * kk], b1[4 * g + 2 * kk + 1]), acc[k][g]);
-                                acc[k][g] = ffma2(dma2, pack2(cs[g].z, cs[g].w), a);
-                            }
-                        }
-                    }
-                    if (has_next) tmem_wait_ld();
                 }
+                if (!kDump) {   // acc += d * 2^24 * asb for this super-block
+                    const float4* dcol = reinterpret_cast<const float4*>(dat + 8 * BM + colhalf * 64);
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const float4 dv = dcol[i];
+                        acc[2 * i] = ffma2(pack2(dv.x, dv.y), asb[2 * i], acc[2 * i]);
+                        acc[2 * i + 1] = ffma2(pack2(dv.z, dv.w), asb[2 * i + 1], acc[2 * i + 1]);
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bars.scl_empty(sr.slot));
+                sr.next();
             }
-            if (!kDump && split == 1) store_tile(C, acc, M, N, m0, n0, quarter, colhalf, tq, tr4);
+            if (!kDump) {
+                // second term, accumulated by the tensor core over this tile's super-blocks
+                if (!wait_bounded(bars.dmin_full(), dr.phase, abort_flag, status)) goto epi_done;
+                tc_fence_after();
+                const uint32_t ta = tmem_base + tlane + kTmemMin + uint32_t(colhalf * 64);
+                const uint64_t one2 = pack2(1.0f, 1.0f);
+                uint32_t b0[16], b1[16];
+                tmem_ld_32x32b_x16(ta, b0);
+                tmem_wait_ld(b0);
+                tmem_ld_32x32b_x16(ta + 16, b1);
+                chunk_part<0>(acc, b0, one2);
+                tmem_wait_ld(b1);
+                tmem_ld_32x32b_x16(ta + 32, b0);
+                chunk_part<1>(acc, b1, one2);
+                tmem_wait_ld(b0);
+                tmem_ld_32x32b_x16(ta + 48, b1);
+                chunk_part<2>(acc, b0, one2);
+                tmem_wait_ld(b1);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bars.dmin_empty());
+                dr.next();
+                chunk_part<3>(acc, b1, one2);
+                if (split == 1) store_tile(C, acc, M, N, m0, n0, row, colhalf);
+            }
         }
     epi_done:;
         if (split > 1) {
@@ -579,26 +684,22 @@ gemm_tc_kernel(const __grid_constant__ TmaMaps maps, float* __restrict__ C,
             const int e = threadIdx.x - kEpiWarp0 * 32;   // 0..255
             float4* mine = reinterpret_cast<float4*>(smem + kOffRaw) + e * 16;
 #pragma unroll
-            for (int k = 0; k < 4; ++k)
-#pragma unroll
-                for (int g = 0; g < 8; g += 2)
-                    mine[k * 4 + g / 2] = make_float4(lo_f(acc[k][g]), hi_f(acc[k][g]),
-                                                      lo_f(acc[k][g + 1]), hi_f(acc[k][g + 1]));
+            for (int i = 0; i < 16; ++i)
+                mine[i] = make_float4(lo_f(acc[2 * i]), hi_f(acc[2 * i]), lo_f(acc[2 * i + 1]),
+                                      hi_f(acc[2 * i + 1]));
             cluster_sync_all();
             if (rank == 0 && !kDump) {
                 for (int r = 1; r < split; ++r) {
                     const uint32_t remote = map_shared_rank(sbase + kOffRaw + uint32_t(e) * 256u, uint32_t(r));
 #pragma unroll
-                    for (int k = 0; k < 4; ++k)
-#pragma unroll
-                        for (int g = 0; g < 8; g += 2) {
-                            const float4 v = ld_dsmem_v4(remote + uint32_t(k * 4 + g / 2) * 16u);
-                            acc[k][g] = pack2(lo_f(acc[k][g]) + v.x, hi_f(acc[k][g]) + v.y);
-                            acc[k][g + 1] = pack2(lo_f(acc[k][g + 1]) + v.z, hi_f(acc[k][g + 1]) + v.w);
-                        }
+                    for (int i = 0; i < 16; ++i) {
+                        const float4 v = ld_dsmem_v4(remote + uint32_t(i) * 16u);
+                        acc[2 * i] = pack2(lo_f(acc[2 * i]) + v.x, hi_f(acc[2 * i]) + v.y);
+                        acc[2 * i + 1] = pack2(lo_f(acc[2 * i + 1]) + v.z, hi_f(acc[2 * i + 1]) + v.w);
+                    }
                 }
                 const int m0 = (tile_first / tiles_n) * BM, n0 = (tile_first % tiles_n) * BN;
-                store_tile(C, acc, M, N, m0, n0, quarter, colhalf, tq, tr4);
+                store_tile(C, acc, M, N, m0, n0, row, colhalf);
             }
             cluster_sync_all();   // remote partials stay alive until rank 0 has read them
         }

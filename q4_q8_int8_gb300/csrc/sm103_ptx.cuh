@@ -133,6 +133,17 @@ __device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a_desc, uint64
         : "memory");
 }
 
+// D[tmem] (+)= A[smem] * B[smem]^T, kind::tf32 (32-bit containers, the tensor
+// core reads sign, exponent and the top 10 mantissa bits; f32 accumulate).
+__device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                         uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // Arrive on `bar` once all tcgen05 operations issued so far by this thread complete.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
     asm volatile(
@@ -142,6 +153,17 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
 
 __device__ __forceinline__ void tmem_wait_ld() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// The same wait, with the 16 destination registers of the load it waits for
+// passed through it, so that no use of them can be scheduled before it.
+__device__ __forceinline__ void tmem_wait_ld(uint32_t (&r)[16]) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
+                   "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
+                   "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15])
+                 :
+                 : "memory");
 }
 
 // 32 lanes x 32 consecutive 32-bit columns: thread t gets lane (base lane + t),
@@ -252,6 +274,15 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
 __host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N) {
     return (1u << 4)                         // D format: f32
            | (0u << 7) | (0u << 10)          // A, B format: f16
+           | (0u << 15) | (0u << 16)         // A, B K-major
+           | (uint32_t(N >> 3) << 17)        // N / 8
+           | (uint32_t(M >> 4) << 24);       // M / 16
+}
+
+// Instruction descriptor, kind::tf32: tf32 A and B, f32 D, both K-major.
+__host__ __device__ constexpr uint32_t idesc_tf32_f32(int M, int N) {
+    return (1u << 4)                         // D format: f32
+           | (2u << 7) | (2u << 10)          // A, B format: tf32
            | (0u << 15) | (0u << 16)         // A, B K-major
            | (uint32_t(N >> 3) << 17)        // N / 8
            | (uint32_t(M >> 4) << 24);       // M / 16
