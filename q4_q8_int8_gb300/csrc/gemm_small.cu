@@ -137,7 +137,7 @@ gemm_small_kernel(const __grid_constant__ SmallMaps maps, float* __restrict__ C,
     constexpr int mp = NF * 8;
     const Layout L = Layout::make(NF, G, split);
     const uint32_t bar0 = sbase + L.bar_off;
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.bar_off + 8 * G);
+    const AbortFlag abort_flag{sbase + uint32_t(L.bar_off + 8 * G)};
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int grp = warp >> 2, gt = threadIdx.x & 127;   // group, thread within the group
@@ -155,7 +155,7 @@ gemm_small_kernel(const __grid_constant__ SmallMaps maps, float* __restrict__ C,
 
     if (threadIdx.x == 0) {
         for (int q = 0; q < G; ++q) mbar_init(bar0 + 8 * q, 1);
-        *abort_flag = 0;
+        abort_flag.set(0u);
         fence_barrier_init();
         fence_proxy_async_smem();
     }
@@ -271,7 +271,7 @@ gemm_small_kernel(const __grid_constant__ SmallMaps maps, float* __restrict__ C,
             }
         }
         group_sync(grp);   // the group is done reading its stage
-        if (*abort_flag) break;
+        if (abort_flag.raised()) break;
         if (gt == 0 && i + G < nmine) {
             fence_proxy_async_smem();
             issue(i + G);

@@ -200,6 +200,15 @@ __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
     return v;
 }
 
+__device__ __forceinline__ void st_shared_u32(uint32_t addr, uint32_t v) {
+    asm volatile("st.shared.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+__device__ __forceinline__ uint32_t ld_shared_u32(uint32_t addr) {
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    return v;
+}
+
 __device__ __forceinline__ void cluster_sync_all() {
     asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
 }
@@ -259,7 +268,7 @@ gemm_tc_kernel(const __grid_constant__ TmaMaps maps, float* __restrict__ C,
     const uint32_t sbase = smem_u32(smem);
     const Bars bars{sbase + kOffBar};
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
+    const AbortFlag abort_flag{sbase + kOffMisc + 4};
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nsb = K / 256;
@@ -295,7 +304,7 @@ gemm_tc_kernel(const __grid_constant__ TmaMaps maps, float* __restrict__ C,
         mbar_init(bars.min_empty(), 1);
         mbar_init(bars.dmin_full(), 1);
         mbar_init(bars.dmin_empty(), kNumEpiWarps);
-        *abort_flag = 0;
+        abort_flag.set(0u);
         fence_barrier_init();
         fence_proxy_async_smem();
         prefetch_tmap(&maps.a);
@@ -422,8 +431,8 @@ gemm_tc_kernel(const __grid_constant__ TmaMaps maps, float* __restrict__ C,
                     const uint32_t raw = sbase + kOffRaw + rr.slot * kRawStage;
                     if (!wait_bounded(bars.scl_empty(sr.slot), sr.phase ^ 1u, abort_flag, status))
                         goto scl_done;
-                    float* dat = reinterpret_cast<float*>(smem + kOffScl + sr.slot * kSclStage);
-                    float* dtab = dat + 8 * BM;
+                    const uint32_t dat = sbase + kOffScl + sr.slot * kSclStage;   // da [8][128]
+                    const uint32_t dtab = dat + kSclDa;                              // d * 2^24 [128]
 #pragma unroll
                     for (int rh = 0; rh < 2; ++rh) {
                         const int t = ts + 64 * rh;
@@ -431,9 +440,11 @@ gemm_tc_kernel(const __grid_constant__ TmaMaps maps, float* __restrict__ C,
                         const uint4 d1 = ld_shared_v4(raw + kOffRawDa + t * 32 + 16);
                         const uint32_t dv[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
 #pragma unroll
-                        for (int c = 0; c < 8; ++c) dat[c * BM + t] = __uint_as_float(dv[c]);
+                        for (int c = 0; c < 8; ++c) st_shared_u32(dat + uint32_t(c * BM + t) * 4u, dv[c]);
                         const uint32_t h0 = ld_shared_v4(raw + kOffRawB + t * 144).x;
-                        dtab[t] = __half2float(__ushort_as_half(uint16_t(h0 & 0xFFFFu))) * kSubnormalScale;
+                        st_shared_u32(dtab + uint32_t(t) * 4u,
+                                      __float_as_uint(__half2float(__ushort_as_half(uint16_t(h0 & 0xFFFFu))) *
+                                                      kSubnormalScale));
                     }
                     __syncwarp();
                     if (lane == 0) mbar_arrive(bars.scl_full(sr.slot));
@@ -592,11 +603,11 @@ gemm_tc_kernel(const __grid_constant__ TmaMaps maps, float* __restrict__ C,
             for (int i = 0; i < 32; ++i) acc[i] = 0ull;
             for (int sb = sb_lo; sb < sb_hi; ++sb) {
                 if (!wait_bounded(bars.scl_full(sr.slot), sr.phase, abort_flag, status)) goto epi_done;
-                const float* dat = reinterpret_cast<const float*>(smem + kOffScl + sr.slot * kSclStage);
+                const uint32_t dat = sbase + kOffScl + sr.slot * kSclStage;
 #pragma unroll
                 for (int i = 0; i < 32; ++i) asb[i] = 0ull;
                 for (int c = 0; c < 8; ++c) {
-                    const float da = dat[c * BM + row];
+                    const float da = __uint_as_float(ld_shared_u32(dat + uint32_t(c * BM + row) * 4u));
                     const uint64_t da2 = pack2(da, da);
                     if (!wait_bounded(bars.tm_full(tr.slot), tr.phase, abort_flag, status)) goto epi_done;
                     tc_fence_after();
@@ -639,12 +650,12 @@ gemm_tc_kernel(const __grid_constant__ TmaMaps maps, float* __restrict__ C,
                     }
                 }
                 if (!kDump) {   // acc += d * 2^24 * asb for this super-block
-                    const float4* dcol = reinterpret_cast<const float4*>(dat + 8 * BM + colhalf * 64);
+                    const uint32_t dcol = dat + kSclDa + uint32_t(colhalf * 64) * 4u;
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
-                        const float4 dv = dcol[i];
-                        acc[2 * i] = ffma2(pack2(dv.x, dv.y), asb[2 * i], acc[2 * i]);
-                        acc[2 * i + 1] = ffma2(pack2(dv.z, dv.w), asb[2 * i + 1], acc[2 * i + 1]);
+                        const uint4 dv = ld_shared_v4(dcol + 16u * i);
+                        acc[2 * i] = ffma2(pack2u(dv.x, dv.y), asb[2 * i], acc[2 * i]);
+                        acc[2 * i + 1] = ffma2(pack2u(dv.z, dv.w), asb[2 * i + 1], acc[2 * i + 1]);
                     }
                 }
                 __syncwarp();

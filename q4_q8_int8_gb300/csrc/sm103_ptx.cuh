@@ -54,18 +54,32 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// A CTA-wide abort flag: one 32-bit word of shared memory, read and written
+// with shared-space volatile accesses.
+struct AbortFlag {
+    uint32_t addr;
+    __device__ __forceinline__ bool raised() const {
+        uint32_t v;
+        asm volatile("ld.volatile.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+        return v != 0;
+    }
+    __device__ __forceinline__ void set(uint32_t v) const {
+        asm volatile("st.volatile.shared.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+    }
+};
+
 // Wait for phase `parity` of `bar`.  Returns false (without waiting further)
 // if another thread of the CTA already aborted, or after kWaitLimitNs, in
 // which case it raises the CTA's abort flag and the device status word.
-__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity,
-                                             volatile int* abort_flag, int* status) {
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, AbortFlag abort_flag,
+                                             int* status) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer();
     while (true) {
         if (mbar_try_wait(bar, parity)) return true;
-        if (*abort_flag) return false;
+        if (abort_flag.raised()) return false;
         if (globaltimer() - t0 > kWaitLimitNs) {
-            *abort_flag = 1;
+            abort_flag.set(1u);
             atomicCAS(status, 0, MMQ_ERR_DEVICE_TIMEOUT);
             return false;
         }
