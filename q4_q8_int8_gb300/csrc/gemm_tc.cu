@@ -12,10 +12,11 @@
 //     integer S'_ij = sc_jc * S_ij (|S'| <= 32*127*63*15 < 2^22, still exact);
 //   * the per-row scale is applied per chunk, the per-super-block d once per
 //     super-block: acc_ij += d_j * sum_c da_ic * S'_ijc;
-//   * the second term, a (K/32)-long f32 contraction of dma with dmv, runs on
-//     the tensor core in tf32 with both factors split into a high and a low
-//     tf32 part (hi*hi + hi*lo + lo*hi, relative error ~2^-21) into its own
-//     tensor-memory accumulator, read once per tile.
+//   * the second term, per super-block an 8-long f32 contraction of dma with
+//     dmv, runs on the tensor core in tf32 with both factors split into a
+//     high and a low tf32 part (hi*hi + hi*lo + lo*hi, relative error ~2^-21)
+//     and reaches the epilogue as a ninth tensor-memory buffer per
+//     super-block, added as it is.
 //
 // sm_103a has no integer kind for tcgen05.mma, so the integers go through
 // kind::f16: every quant a in [-127, 127] is an exact fp16 value, and the
@@ -31,8 +32,8 @@
 //               128-byte-swizzled boxes), the raw 144-byte q4_K rows, and the
 //               da / sa slices, all zero-filled past M / N.
 //   warp 1      MMA issuer (one thread): per chunk two K=16 f16 MMAs into one
-//               of three 128-column f32 tensor-memory buffers; per super-block
-//               three K=8 tf32 MMAs of the second term into a fourth buffer.
+//               of four 128-column f32 tensor-memory buffers; per super-block
+//               three K=8 tf32 MMAs of the second term into the next buffer.
 //   warps 2-3   per super-block: the epilogue's tables (da per row and chunk,
 //               d * 2^24 per weight row) and the split tf32 operands of the
 //               second term (dma per token row, dmv per weight row).
@@ -40,10 +41,10 @@
 //               bit pattern and one fp16 subtraction) and nibble * sc -> fp16
 //               subnormal into the 128-byte-swizzled K-major layout, one 64-k
 //               chunk pair at a time, one row per thread.
-//   warps 8-15  epilogue: thread = token row, 64 columns; per chunk four
-//               32x32b.x16 tensor-memory loads (the next in flight while the
-//               current one is used) and 32 packed f32x2 FMAs; per
-//               super-block 32 more for d; C stored at the end of a tile.
+//   warps 8-15  epilogue: thread = token row, 64 columns; per chunk two
+//               32x32b.x32 tensor-memory loads and 32 packed f32x2 FMAs; per
+//               super-block 32 more for d and 32 adds of the second term; C
+//               stored at the end of a tile.
 // Within a chunk the k order of both f16 operands is permuted identically
 // (groups of four as 0,2,1,3) so that both unpacks are plain byte/nibble
 // moves; a dot product does not depend on the order of its terms.
@@ -61,7 +62,7 @@ namespace {
 using namespace mmq::ptx;
 
 constexpr int BM = 128, BN = 128;
-constexpr int kNumRaw = 2, kNumScl = 3, kNumOp = 2, kNumTm = 3;
+constexpr int kNumRaw = 2, kNumScl = 3, kNumOp = 2, kNumTm = 4;
 constexpr int kSclWarp0 = 2, kNumSclWarps = 2, kConvWarp0 = 4, kNumConvWarps = 4;
 constexpr int kEpiWarp0 = 8, kNumEpiWarps = 8;
 constexpr int kThreads = (kEpiWarp0 + kNumEpiWarps) * 32;   // 512
@@ -69,9 +70,8 @@ constexpr int kThreads = (kEpiWarp0 + kNumEpiWarps) * 32;   // 512
 // registers to warpgroups 2-3 (epilogue).  Launch budget: 512 x 128.
 constexpr uint32_t kRegsLow = 80, kRegsHigh = 176, kRegsLaunch = 128;
 static_assert(256 * kRegsLow + 256 * kRegsHigh <= kThreads * kRegsLaunch, "register split");
-constexpr uint32_t kTmemCols = 512;                          // kNumTm x BN + BN (second term)
-constexpr uint32_t kTmemMin = kNumTm * BN;                   // column of the second-term accumulator
-static_assert(kTmemMin + BN <= kTmemCols, "tensor memory budget");
+constexpr uint32_t kTmemCols = 512;                          // kNumTm x BN
+static_assert(kNumTm * BN <= int(kTmemCols), "tensor memory budget");
 
 // Shared memory map (offsets from a 1024-byte aligned base).
 constexpr int kRawASub = BM * 128;                   // 16 KB: 128 rows x 128 B, swizzled
@@ -93,9 +93,8 @@ constexpr int kOffOp = kOffRaw + kNumRaw * kRawStage;
 constexpr int kOffMin = kOffOp + kNumOp * kOpStage;
 constexpr int kOffScl = kOffMin + kMinStage;
 constexpr int kOffBar = kOffScl + kNumScl * kSclStage;
-// barriers: raw full/empty, op full/empty, tm full/empty, scl full/empty,
-// min full/empty, dmin full/empty
-constexpr int kNumBars = 2 * kNumRaw + 2 * kNumOp + 2 * kNumTm + 2 * kNumScl + 4;
+// barriers: raw full/empty, op full/empty, tm full/empty, scl full/empty, min full/empty
+constexpr int kNumBars = 2 * kNumRaw + 2 * kNumOp + 2 * kNumTm + 2 * kNumScl + 2;
 constexpr int kOffMisc = kOffBar + kNumBars * 8;     // tmem slot, abort flag
 constexpr int kSmemBytes = kOffMisc + 16 + 1024;     // + alignment slack
 static_assert(kOffOp % 1024 == 0 && kOffMin % 1024 == 0, "operand tiles need 1024-byte alignment");
@@ -127,8 +126,6 @@ struct Bars {
     static constexpr int kMin0 = 2 * kNumRaw + 2 * kNumOp + 2 * kNumTm + 2 * kNumScl;
     __device__ uint32_t min_full() const { return at(kMin0); }
     __device__ uint32_t min_empty() const { return at(kMin0 + 1); }
-    __device__ uint32_t dmin_full() const { return at(kMin0 + 2); }
-    __device__ uint32_t dmin_empty() const { return at(kMin0 + 3); }
 };
 
 // Ring position: slot index and the parity of the current pass over the ring.
@@ -226,11 +223,11 @@ __device__ __forceinline__ float4 ld_dsmem_v4(uint32_t addr) {
     return v;
 }
 
-// One 16-column part of a chunk: asb[8p + j] (+)= da * S'[16p + 2j, +1].
-template <int P>
-__device__ __forceinline__ void chunk_part(uint64_t (&asb)[32], const uint32_t (&b)[16], uint64_t da2) {
+// One 32-column half of a buffer: acc[16h + j] += m * D[32h + 2j, +1].
+template <int H>
+__device__ __forceinline__ void half_fma(uint64_t (&acc)[32], const uint32_t (&b)[32], uint64_t m2) {
 #pragma unroll
-    for (int j = 0; j < 8; ++j) asb[8 * P + j] = ffma2(pack2u(b[2 * j], b[2 * j + 1]), da2, asb[8 * P + j]);
+    for (int j = 0; j < 16; ++j) acc[16 * H + j] = ffma2(pack2u(b[2 * j], b[2 * j + 1]), m2, acc[16 * H + j]);
 }
 
 // S dump of one 16-column part (block dots, bit for bit).
@@ -302,8 +299,6 @@ gemm_tc_kernel(const __grid_constant__ TmaMaps maps, float* __restrict__ C,
         }
         mbar_init(bars.min_full(), kNumSclWarps);
         mbar_init(bars.min_empty(), 1);
-        mbar_init(bars.dmin_full(), 1);
-        mbar_init(bars.dmin_empty(), kNumEpiWarps);
         abort_flag.set(0u);
         fence_barrier_init();
         fence_proxy_async_smem();
@@ -362,9 +357,8 @@ gemm_tc_kernel(const __grid_constant__ TmaMaps maps, float* __restrict__ C,
         if (lane == 0) {
             Ring<kNumOp> orr;
             Ring<kNumTm> tr;
-            Ring<1> mr, dr;
+            Ring<1> mr;
             uint32_t last_bar = 0, last_par = 0;   // most recent commit, drained on exit
-            const uint32_t dmin = tmem_base + kTmemMin;
             const uint32_t minA = sbase + kOffMin, minB = minA + kMinTile;
             for (int tile = tile_first; tile < num_tiles; tile += tile_step) {
                 for (int sb = sb_lo; sb < sb_hi; ++sb) {
@@ -394,24 +388,23 @@ gemm_tc_kernel(const __grid_constant__ TmaMaps maps, float* __restrict__ C,
                         orr.next();
                     }
                     if (!kDump) {
-                        // second term of this super-block: three K=8 tf32 MMAs
+                        // second term of this super-block: three K=8 tf32 MMAs into the
+                        // next buffer, handed to the epilogue like a ninth chunk
                         if (!wait_bounded(bars.min_full(), mr.phase, abort_flag, status)) goto mma_done;
-                        if (sb == sb_lo &&
-                            !wait_bounded(bars.dmin_empty(), dr.phase ^ 1u, abort_flag, status))
+                        if (!wait_bounded(bars.tm_empty(tr.slot), tr.phase ^ 1u, abort_flag, status))
                             goto mma_done;
                         tc_fence_after();
+                        const uint32_t d = tmem_base + uint32_t(tr.slot * BN);
 #pragma unroll
                         for (int j = 0; j < 3; ++j)
-                            mma_tf32(dmin, smem_desc_sw128(minA + 32 * j), smem_desc_sw128(minB + 32 * j),
-                                     kIdescTf32, uint32_t(sb > sb_lo || j > 0));
+                            mma_tf32(d, smem_desc_sw128(minA + 32 * j), smem_desc_sw128(minB + 32 * j),
+                                     kIdescTf32, uint32_t(j));
+                        mma_commit(bars.tm_full(tr.slot));
                         mma_commit(bars.min_empty());
                         last_bar = bars.min_empty();
                         last_par = mr.phase;
                         mr.next();
-                        if (sb == sb_hi - 1) {
-                            mma_commit(bars.dmin_full());
-                            dr.next();
-                        }
+                        tr.next();
                     }
                 }
             }
@@ -456,42 +449,38 @@ gemm_tc_kernel(const __grid_constant__ TmaMaps maps, float* __restrict__ C,
                         for (int rh = 0; rh < 2; ++rh) {
                             const int t = ts + 64 * rh;
                             const int sw = t & 7;
-                            // token row t: dma = da * sa per chunk, split hi / lo
-                            const uint4 d0 = ld_shared_v4(raw + kOffRawDa + t * 32);
-                            const uint4 d1 = ld_shared_v4(raw + kOffRawDa + t * 32 + 16);
-                            const uint4 s0 = ld_shared_v4(raw + kOffRawSa + t * 32);
-                            const uint4 s1 = ld_shared_v4(raw + kOffRawSa + t * 32 + 16);
-                            const uint32_t dv[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
-                            const uint32_t sv[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
-                            float ah[8], al[8];
-#pragma unroll
-                            for (int c = 0; c < 8; ++c)
-                                split_tf32(__uint_as_float(dv[c]) * float(int32_t(sv[c])), ah[c], al[c]);
-                            // k slots: 0-7 hi, 8-15 hi, 16-23 lo (against hi, lo, hi of dmv)
+                            // token row t: dma = da * sa per chunk, split hi / lo; k slots
+                            // 0-7 hi, 8-15 hi, 16-23 lo (against hi, lo, hi of dmv); four
+                            // chunks (one 16-byte granule) at a time
                             const uint32_t ra = minA + t * 128;
-                            st_shared_v4f(ra + ((0 ^ sw) << 4), ah[0], ah[1], ah[2], ah[3]);
-                            st_shared_v4f(ra + ((1 ^ sw) << 4), ah[4], ah[5], ah[6], ah[7]);
-                            st_shared_v4f(ra + ((2 ^ sw) << 4), ah[0], ah[1], ah[2], ah[3]);
-                            st_shared_v4f(ra + ((3 ^ sw) << 4), ah[4], ah[5], ah[6], ah[7]);
-                            st_shared_v4f(ra + ((4 ^ sw) << 4), al[0], al[1], al[2], al[3]);
-                            st_shared_v4f(ra + ((5 ^ sw) << 4), al[4], al[5], al[6], al[7]);
+#pragma unroll
+                            for (int h = 0; h < 2; ++h) {
+                                const uint4 dv = ld_shared_v4(raw + kOffRawDa + t * 32 + 16 * h);
+                                const uint4 sv = ld_shared_v4(raw + kOffRawSa + t * 32 + 16 * h);
+                                float ah[4], al[4];
+                                split_tf32(__uint_as_float(dv.x) * float(int32_t(sv.x)), ah[0], al[0]);
+                                split_tf32(__uint_as_float(dv.y) * float(int32_t(sv.y)), ah[1], al[1]);
+                                split_tf32(__uint_as_float(dv.z) * float(int32_t(sv.z)), ah[2], al[2]);
+                                split_tf32(__uint_as_float(dv.w) * float(int32_t(sv.w)), ah[3], al[3]);
+                                st_shared_v4f(ra + (((0 + h) ^ sw) << 4), ah[0], ah[1], ah[2], ah[3]);
+                                st_shared_v4f(ra + (((2 + h) ^ sw) << 4), ah[0], ah[1], ah[2], ah[3]);
+                                st_shared_v4f(ra + (((4 + h) ^ sw) << 4), al[0], al[1], al[2], al[3]);
+                            }
                             // weight row t: dmv = -dmin * m per chunk (exact in f32), split hi / lo
                             const uint4 hdr = ld_shared_v4(raw + kOffRawB + t * 144);
                             const float dmn = __half2float(__ushort_as_half(uint16_t(hdr.x >> 16)));
-                            const uint32_t mlo = m_lo4(hdr.z), mhi = m_hi4(hdr.z, hdr.w);
-                            float bh[8], bl[8];
-#pragma unroll
-                            for (int c = 0; c < 8; ++c) {
-                                const uint32_t mv = ((c < 4 ? mlo : mhi) >> (8 * (c & 3))) & 0xFFu;
-                                split_tf32(-(dmn * float(mv)), bh[c], bl[c]);
-                            }
                             const uint32_t rb = minB + t * 128;
-                            st_shared_v4f(rb + ((0 ^ sw) << 4), bh[0], bh[1], bh[2], bh[3]);
-                            st_shared_v4f(rb + ((1 ^ sw) << 4), bh[4], bh[5], bh[6], bh[7]);
-                            st_shared_v4f(rb + ((2 ^ sw) << 4), bl[0], bl[1], bl[2], bl[3]);
-                            st_shared_v4f(rb + ((3 ^ sw) << 4), bl[4], bl[5], bl[6], bl[7]);
-                            st_shared_v4f(rb + ((4 ^ sw) << 4), bh[0], bh[1], bh[2], bh[3]);
-                            st_shared_v4f(rb + ((5 ^ sw) << 4), bh[4], bh[5], bh[6], bh[7]);
+#pragma unroll
+                            for (int h = 0; h < 2; ++h) {
+                                const uint32_t mw = h == 0 ? m_lo4(hdr.z) : m_hi4(hdr.z, hdr.w);
+                                float bh[4], bl[4];
+#pragma unroll
+                                for (int i = 0; i < 4; ++i)
+                                    split_tf32(-(dmn * float((mw >> (8 * i)) & 0xFFu)), bh[i], bl[i]);
+                                st_shared_v4f(rb + (((0 + h) ^ sw) << 4), bh[0], bh[1], bh[2], bh[3]);
+                                st_shared_v4f(rb + (((2 + h) ^ sw) << 4), bl[0], bl[1], bl[2], bl[3]);
+                                st_shared_v4f(rb + (((4 + h) ^ sw) << 4), bh[0], bh[1], bh[2], bh[3]);
+                            }
                         }
                         fence_proxy_async_smem();
                         __syncwarp();
@@ -595,7 +584,6 @@ gemm_tc_kernel(const __grid_constant__ TmaMaps maps, float* __restrict__ C,
         const int nb = K / 32;
         Ring<kNumScl> sr;
         Ring<kNumTm> tr;
-        Ring<1> dr;
         uint64_t acc[32], asb[32];
         for (int tile = tile_first; tile < num_tiles; tile += tile_step) {
             const int m0 = (tile / tiles_n) * BM, n0 = (tile % tiles_n) * BN;
@@ -612,13 +600,13 @@ gemm_tc_kernel(const __grid_constant__ TmaMaps maps, float* __restrict__ C,
                     if (!wait_bounded(bars.tm_full(tr.slot), tr.phase, abort_flag, status)) goto epi_done;
                     tc_fence_after();
                     const uint32_t ta = tmem_base + tlane + uint32_t(tr.slot * BN + colhalf * 64);
-                    uint32_t b0[16], b1[16];
-                    tmem_ld_32x32b_x16(ta, b0);
-                    tmem_wait_ld(b0);
-                    tmem_ld_32x32b_x16(ta + 16, b1);
                     if (kDump) {
                         const int64_t gr = int64_t(m0) + row;
                         const int gc = n0 + colhalf * 64, kb = sb * 8 + c;
+                        uint32_t b0[16], b1[16];
+                        tmem_ld_32x32b_x16(ta, b0);
+                        tmem_wait_ld(b0);
+                        tmem_ld_32x32b_x16(ta + 16, b1);
                         dump_part(S, b0, gr, gc, M, N, nb, kb);
                         tmem_wait_ld(b1);
                         tmem_ld_32x32b_x16(ta + 32, b0);
@@ -633,23 +621,22 @@ gemm_tc_kernel(const __grid_constant__ TmaMaps maps, float* __restrict__ C,
                         tr.next();
                         dump_part(S, b1, gr, gc + 48, M, N, nb, kb);
                     } else {
-                        chunk_part<0>(asb, b0, da2);
-                        tmem_wait_ld(b1);
-                        tmem_ld_32x32b_x16(ta + 32, b0);
-                        chunk_part<1>(asb, b1, da2);
-                        tmem_wait_ld(b0);
-                        tmem_ld_32x32b_x16(ta + 48, b1);
-                        chunk_part<2>(asb, b0, da2);
-                        tmem_wait_ld(b1);
+                        uint32_t b[32];
+                        tmem_ld_32x32b_x32(ta, b);
+                        tmem_wait_ld(b);
+                        half_fma<0>(asb, b, da2);
+                        tmem_ld_32x32b_x32(ta + 32, b);
+                        tmem_wait_ld(b);
                         // the whole S' tile of this chunk is in registers: hand the buffer back
                         tc_fence_before();
                         __syncwarp();
                         if (lane == 0) mbar_arrive(bars.tm_empty(tr.slot));
                         tr.next();
-                        chunk_part<3>(asb, b1, da2);
+                        half_fma<1>(asb, b, da2);
                     }
                 }
-                if (!kDump) {   // acc += d * 2^24 * asb for this super-block
+                if (!kDump) {
+                    // acc += d * 2^24 * asb for this super-block
                     const uint32_t dcol = dat + kSclDa + uint32_t(colhalf * 64) * 4u;
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
@@ -657,36 +644,28 @@ gemm_tc_kernel(const __grid_constant__ TmaMaps maps, float* __restrict__ C,
                         acc[2 * i] = ffma2(pack2u(dv.x, dv.y), asb[2 * i], acc[2 * i]);
                         acc[2 * i + 1] = ffma2(pack2u(dv.z, dv.w), asb[2 * i + 1], acc[2 * i + 1]);
                     }
+                    // acc += the second term of this super-block (the ninth buffer)
+                    if (!wait_bounded(bars.tm_full(tr.slot), tr.phase, abort_flag, status)) goto epi_done;
+                    tc_fence_after();
+                    const uint32_t ta = tmem_base + tlane + uint32_t(tr.slot * BN + colhalf * 64);
+                    const uint64_t one2 = pack2(1.0f, 1.0f);
+                    uint32_t b[32];
+                    tmem_ld_32x32b_x32(ta, b);
+                    tmem_wait_ld(b);
+                    half_fma<0>(acc, b, one2);
+                    tmem_ld_32x32b_x32(ta + 32, b);
+                    tmem_wait_ld(b);
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bars.tm_empty(tr.slot));
+                    tr.next();
+                    half_fma<1>(acc, b, one2);
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bars.scl_empty(sr.slot));
                 sr.next();
             }
-            if (!kDump) {
-                // second term, accumulated by the tensor core over this tile's super-blocks
-                if (!wait_bounded(bars.dmin_full(), dr.phase, abort_flag, status)) goto epi_done;
-                tc_fence_after();
-                const uint32_t ta = tmem_base + tlane + kTmemMin + uint32_t(colhalf * 64);
-                const uint64_t one2 = pack2(1.0f, 1.0f);
-                uint32_t b0[16], b1[16];
-                tmem_ld_32x32b_x16(ta, b0);
-                tmem_wait_ld(b0);
-                tmem_ld_32x32b_x16(ta + 16, b1);
-                chunk_part<0>(acc, b0, one2);
-                tmem_wait_ld(b1);
-                tmem_ld_32x32b_x16(ta + 32, b0);
-                chunk_part<1>(acc, b1, one2);
-                tmem_wait_ld(b0);
-                tmem_ld_32x32b_x16(ta + 48, b1);
-                chunk_part<2>(acc, b0, one2);
-                tmem_wait_ld(b1);
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bars.dmin_empty());
-                dr.next();
-                chunk_part<3>(acc, b1, one2);
-                if (split == 1) store_tile(C, acc, M, N, m0, n0, row, colhalf);
-            }
+            if (!kDump && split == 1) store_tile(C, acc, M, N, m0, n0, row, colhalf);
         }
     epi_done:;
         if (split > 1) {
