@@ -15,7 +15,7 @@
 //   * the second term, per super-block an 8-long f32 contraction of dma with
 //     dmv, runs on the tensor core in tf32 with both factors split into a
 //     high and a low tf32 part (hi*hi + hi*lo + lo*hi, relative error ~2^-21)
-//     and reaches the epilogue as a ninth tensor-memory buffer per
+//     and reaches the epilogue as a fifth tensor-memory hand-off per
 //     super-block, added as it is.
 //
 // sm_103a has no integer kind for tcgen05.mma, so the integers go through
@@ -31,9 +31,10 @@
 //   warp 0      TMA producer: per 256-k super-block the raw int8 A tile (two
 //               128-byte-swizzled boxes), the raw 144-byte q4_K rows, and the
 //               da / sa slices, all zero-filled past M / N.
-//   warp 1      MMA issuer (one thread): per chunk two K=16 f16 MMAs into one
-//               of four 128-column f32 tensor-memory buffers; per super-block
-//               three K=8 tf32 MMAs of the second term into the next buffer.
+//   warp 1      MMA issuer (one thread): per operand stage (two chunks) four
+//               K=16 f16 MMAs into one of two 256-column f32 tensor-memory
+//               slots, one hand-off per stage; per super-block three K=8 tf32
+//               MMAs of the second term into the next slot.
 //   warps 2-3   per super-block: the epilogue's tables (da per row and chunk,
 //               d * 2^24 per weight row) and the split tf32 operands of the
 //               second term (dma per token row, dmv per weight row).
@@ -42,9 +43,10 @@
 //               subnormal into the 128-byte-swizzled K-major layout, one 64-k
 //               chunk pair at a time, one row per thread.
 //   warps 8-15  epilogue: thread = token row, 64 columns; per chunk two
-//               32x32b.x32 tensor-memory loads and 32 packed f32x2 FMAs; per
-//               super-block 32 more for d and 32 adds of the second term; C
-//               stored at the end of a tile.
+//               32x32b.x32 tensor-memory loads and 32 packed f32x2 FMAs, one
+//               wait and one release per two chunks; per super-block 32 more
+//               for d and 32 adds of the second term; C stored at the end of
+//               a tile.
 // Within a chunk the k order of both f16 operands is permuted identically
 // (groups of four as 0,2,1,3) so that both unpacks are plain byte/nibble
 // moves; a dot product does not depend on the order of its terms.
@@ -62,7 +64,7 @@ namespace {
 using namespace mmq::ptx;
 
 constexpr int BM = 128, BN = 128;
-constexpr int kNumRaw = 2, kNumScl = 3, kNumOp = 2, kNumTm = 4;
+constexpr int kNumRaw = 2, kNumScl = 3, kNumOp = 2, kNumTm = 2;
 constexpr int kSclWarp0 = 2, kNumSclWarps = 2, kConvWarp0 = 4, kNumConvWarps = 4;
 constexpr int kEpiWarp0 = 8, kNumEpiWarps = 8;
 constexpr int kThreads = (kEpiWarp0 + kNumEpiWarps) * 32;   // 512
@@ -70,8 +72,11 @@ constexpr int kThreads = (kEpiWarp0 + kNumEpiWarps) * 32;   // 512
 // registers to warpgroups 2-3 (epilogue).  Launch budget: 512 x 128.
 constexpr uint32_t kRegsLow = 80, kRegsHigh = 176, kRegsLaunch = 128;
 static_assert(256 * kRegsLow + 256 * kRegsHigh <= kThreads * kRegsLaunch, "register split");
-constexpr uint32_t kTmemCols = 512;                          // kNumTm x BN
-static_assert(kNumTm * BN <= int(kTmemCols), "tensor memory budget");
+// Tensor memory: kNumTm slots, each two 128-column f32 buffers (the two
+// chunks of one operand stage, or the second term in the first of them).
+constexpr int kSlotCols = 2 * BN;
+constexpr uint32_t kTmemCols = 512;
+static_assert(kNumTm * kSlotCols <= int(kTmemCols), "tensor memory budget");
 
 // Shared memory map (offsets from a 1024-byte aligned base).
 constexpr int kRawASub = BM * 128;                   // 16 KB: 128 rows x 128 B, swizzled
@@ -362,39 +367,38 @@ gemm_tc_kernel(const __grid_constant__ TmaMaps maps, float* __restrict__ C,
             const uint32_t minA = sbase + kOffMin, minB = minA + kMinTile;
             for (int tile = tile_first; tile < num_tiles; tile += tile_step) {
                 for (int sb = sb_lo; sb < sb_hi; ++sb) {
-                    for (int q = 0; q < 4; ++q) {
+                    for (int q = 0; q < 4; ++q) {   // operand stage q: chunks 2q, 2q+1
                         if (!wait_bounded(bars.op_full(orr.slot), orr.phase, abort_flag, status))
+                            goto mma_done;
+                        if (!wait_bounded(bars.tm_empty(tr.slot), tr.phase ^ 1u, abort_flag, status))
                             goto mma_done;
                         tc_fence_after();
                         const uint32_t opA = sbase + kOffOp + orr.slot * kOpStage;
                         const uint32_t opB = opA + kOpTile;
-                        for (int h = 0; h < 2; ++h) {
-                            if (!wait_bounded(bars.tm_empty(tr.slot), tr.phase ^ 1u, abort_flag, status))
-                                goto mma_done;
-                            tc_fence_after();
-                            const uint32_t d = tmem_base + uint32_t(tr.slot * BN);
+                        const uint32_t d0 = tmem_base + uint32_t(tr.slot * kSlotCols);
+#pragma unroll
+                        for (int h = 0; h < 2; ++h)
 #pragma unroll
                             for (int kk = 0; kk < 2; ++kk) {
                                 const uint32_t koff = uint32_t(h * 64 + kk * 32);   // bytes within the 128-B row
-                                mma_f16(d, smem_desc_sw128(opA + koff), smem_desc_sw128(opB + koff),
-                                        kIdesc, uint32_t(kk));
+                                mma_f16(d0 + uint32_t(h * BN), smem_desc_sw128(opA + koff),
+                                        smem_desc_sw128(opB + koff), kIdesc, uint32_t(kk));
                             }
-                            mma_commit(bars.tm_full(tr.slot));
-                            last_bar = bars.tm_full(tr.slot);
-                            last_par = tr.phase;
-                            tr.next();
-                        }
+                        mma_commit(bars.tm_full(tr.slot));
                         mma_commit(bars.op_empty(orr.slot));
+                        last_bar = bars.op_empty(orr.slot);
+                        last_par = orr.phase;
+                        tr.next();
                         orr.next();
                     }
                     if (!kDump) {
                         // second term of this super-block: three K=8 tf32 MMAs into the
-                        // next buffer, handed to the epilogue like a ninth chunk
+                        // next slot, handed to the epilogue like a fifth stage
                         if (!wait_bounded(bars.min_full(), mr.phase, abort_flag, status)) goto mma_done;
                         if (!wait_bounded(bars.tm_empty(tr.slot), tr.phase ^ 1u, abort_flag, status))
                             goto mma_done;
                         tc_fence_after();
-                        const uint32_t d = tmem_base + uint32_t(tr.slot * BN);
+                        const uint32_t d = tmem_base + uint32_t(tr.slot * kSlotCols);
 #pragma unroll
                         for (int j = 0; j < 3; ++j)
                             mma_tf32(d, smem_desc_sw128(minA + 32 * j), smem_desc_sw128(minB + 32 * j),
@@ -594,45 +598,58 @@ gemm_tc_kernel(const __grid_constant__ TmaMaps maps, float* __restrict__ C,
                 const uint32_t dat = sbase + kOffScl + sr.slot * kSclStage;
 #pragma unroll
                 for (int i = 0; i < 32; ++i) asb[i] = 0ull;
-                for (int c = 0; c < 8; ++c) {
-                    const float da = __uint_as_float(ld_shared_u32(dat + uint32_t(c * BM + row) * 4u));
-                    const uint64_t da2 = pack2(da, da);
+                for (int q = 0; q < 4; ++q) {   // operand stage q: chunks 2q, 2q+1 in one slot
+                    const float da0 = __uint_as_float(ld_shared_u32(dat + uint32_t(2 * q * BM + row) * 4u));
                     if (!wait_bounded(bars.tm_full(tr.slot), tr.phase, abort_flag, status)) goto epi_done;
                     tc_fence_after();
-                    const uint32_t ta = tmem_base + tlane + uint32_t(tr.slot * BN + colhalf * 64);
+                    const uint32_t ta = tmem_base + tlane + uint32_t(tr.slot * kSlotCols + colhalf * 64);
                     if (kDump) {
                         const int64_t gr = int64_t(m0) + row;
-                        const int gc = n0 + colhalf * 64, kb = sb * 8 + c;
+                        const int gc = n0 + colhalf * 64;
                         uint32_t b0[16], b1[16];
-                        tmem_ld_32x32b_x16(ta, b0);
-                        tmem_wait_ld(b0);
-                        tmem_ld_32x32b_x16(ta + 16, b1);
-                        dump_part(S, b0, gr, gc, M, N, nb, kb);
-                        tmem_wait_ld(b1);
-                        tmem_ld_32x32b_x16(ta + 32, b0);
-                        dump_part(S, b1, gr, gc + 16, M, N, nb, kb);
-                        tmem_wait_ld(b0);
-                        tmem_ld_32x32b_x16(ta + 48, b1);
-                        dump_part(S, b0, gr, gc + 32, M, N, nb, kb);
-                        tmem_wait_ld(b1);
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            const int kb = sb * 8 + 2 * q + h;
+                            const uint32_t th = ta + uint32_t(h * BN);
+                            tmem_ld_32x32b_x16(th, b0);
+                            tmem_wait_ld(b0);
+                            tmem_ld_32x32b_x16(th + 16, b1);
+                            dump_part(S, b0, gr, gc, M, N, nb, kb);
+                            tmem_wait_ld(b1);
+                            tmem_ld_32x32b_x16(th + 32, b0);
+                            dump_part(S, b1, gr, gc + 16, M, N, nb, kb);
+                            tmem_wait_ld(b0);
+                            tmem_ld_32x32b_x16(th + 48, b1);
+                            dump_part(S, b0, gr, gc + 32, M, N, nb, kb);
+                            tmem_wait_ld(b1);
+                            dump_part(S, b1, gr, gc + 48, M, N, nb, kb);
+                        }
                         tc_fence_before();
                         __syncwarp();
                         if (lane == 0) mbar_arrive(bars.tm_empty(tr.slot));
                         tr.next();
-                        dump_part(S, b1, gr, gc + 48, M, N, nb, kb);
                     } else {
+                        const uint64_t da02 = pack2(da0, da0);
                         uint32_t b[32];
                         tmem_ld_32x32b_x32(ta, b);
                         tmem_wait_ld(b);
-                        half_fma<0>(asb, b, da2);
+                        half_fma<0>(asb, b, da02);
                         tmem_ld_32x32b_x32(ta + 32, b);
                         tmem_wait_ld(b);
-                        // the whole S' tile of this chunk is in registers: hand the buffer back
+                        half_fma<1>(asb, b, da02);
+                        const float da1 = __uint_as_float(ld_shared_u32(dat + uint32_t((2 * q + 1) * BM + row) * 4u));
+                        const uint64_t da12 = pack2(da1, da1);
+                        tmem_ld_32x32b_x32(ta + BN, b);
+                        tmem_wait_ld(b);
+                        half_fma<0>(asb, b, da12);
+                        tmem_ld_32x32b_x32(ta + BN + 32, b);
+                        tmem_wait_ld(b);
+                        // both S' tiles of this stage are in registers: hand the slot back
                         tc_fence_before();
                         __syncwarp();
                         if (lane == 0) mbar_arrive(bars.tm_empty(tr.slot));
                         tr.next();
-                        half_fma<1>(asb, b, da2);
+                        half_fma<1>(asb, b, da12);
                     }
                 }
                 if (!kDump) {
@@ -644,10 +661,10 @@ gemm_tc_kernel(const __grid_constant__ TmaMaps maps, float* __restrict__ C,
                         acc[2 * i] = ffma2(pack2u(dv.x, dv.y), asb[2 * i], acc[2 * i]);
                         acc[2 * i + 1] = ffma2(pack2u(dv.z, dv.w), asb[2 * i + 1], acc[2 * i + 1]);
                     }
-                    // acc += the second term of this super-block (the ninth buffer)
+                    // acc += the second term of this super-block (the fifth slot use)
                     if (!wait_bounded(bars.tm_full(tr.slot), tr.phase, abort_flag, status)) goto epi_done;
                     tc_fence_after();
-                    const uint32_t ta = tmem_base + tlane + uint32_t(tr.slot * BN + colhalf * 64);
+                    const uint32_t ta = tmem_base + tlane + uint32_t(tr.slot * kSlotCols + colhalf * 64);
                     const uint64_t one2 = pack2(1.0f, 1.0f);
                     uint32_t b[32];
                     tmem_ld_32x32b_x32(ta, b);
