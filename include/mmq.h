@@ -116,17 +116,20 @@ int mmq_q4K_gemm(mmq_q8_1_t aq, const uint8_t* bq4k, float* C, int64_t M,
 #define MMQ_PATH_TC 2       /* tcgen05 kernel (exact integers in fp16, f32   */
                             /* accumulation in tensor memory)               */
 #define MMQ_PATH_SMALL_M 3  /* weight-streaming kernel for few tokens       */
+#define MMQ_PATH_TC_PAIR 4  /* tcgen05 kernel on CTA pairs (one M=256 MMA    */
+                            /* over two SMs; 256 x 128 output tiles)        */
 
 /* Same as mmq_q4K_gemm with an explicit kernel.  MMQ_ERR_ARG if `path` is
  * unknown or the kernel does not accept the shape (the small-M kernel takes
- * M <= 64). */
+ * M <= 64).  The automatic choice: M <= 64 -> small-M, else the one-CTA
+ * tcgen05 kernel (which splits K over a cluster when tiles are few). */
 int mmq_q4K_gemm_path(mmq_q8_1_t aq, const uint8_t* bq4k, float* C, int64_t M,
                       int64_t N, int64_t K, int path, void* stream);
 
 /* Debug/test dump of the exact per-chunk integer dots (page r15 section 2.1:
  * S_ij = sum_k a_int[i,k] * v[j,k]; section 2.3: |S| <= 32*127*15) computed
  * by the same unpack and MMA code as the GEMM kernel selected by `path`
- * (MMQ_PATH_MMA_S8 or MMQ_PATH_TC).  S int32 [M][N][K/32].  Same shape
+ * (MMQ_PATH_MMA_S8, MMQ_PATH_TC or MMQ_PATH_TC_PAIR).  S int32 [M][N][K/32].  Same shape
  * rules as the GEMM. */
 int mmq_q4K_block_dots(mmq_q8_1_t aq, const uint8_t* bq4k, int32_t* S,
                        int64_t M, int64_t N, int64_t K, int path, void* stream);

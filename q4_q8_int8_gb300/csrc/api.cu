@@ -124,11 +124,19 @@ size_t mmq_q4K_bytes(int64_t N, int64_t K) {
     return size_t(N) * size_t(K / 256) * 144;
 }
 
+// The automatic kernel choice (shape only): few tokens -> weight streaming,
+// else the one-CTA tcgen05 kernel. (The CTA-pair kernel is measured slower
+// on every shape tried so far and is only taken on request.)
+static int auto_path(int64_t M, int64_t N, bool dump) {
+    (void)N;
+    return (M <= mmq::kSmallMMax && !dump) ? MMQ_PATH_SMALL_M : MMQ_PATH_TC;
+}
+
 static int run_gemm(mmq_q8_1_t aq, const uint8_t* w, float* C, int32_t* S, int64_t M,
                     int64_t N, int64_t K, int path, cudaStream_t s) {
     int* status = mmq::status_word_ptr();
     if (!status) return MMQ_ERR_CUDA;
-    if (path == MMQ_PATH_AUTO) path = (M <= mmq::kSmallMMax && !S) ? MMQ_PATH_SMALL_M : MMQ_PATH_TC;
+    if (path == MMQ_PATH_AUTO) path = auto_path(M, N, S != nullptr);
     switch (path) {
         case MMQ_PATH_MMA_S8:
             return from_cuda(mmq::launch_gemm_mma_s8(aq, w, C, S, M, N, K, status, s));
@@ -138,6 +146,13 @@ static int run_gemm(mmq_q8_1_t aq, const uint8_t* w, float* C, int32_t* S, int64
             const int inject = t_inject_timeout;
             t_inject_timeout = 0;
             return from_cuda(mmq::launch_gemm_tc(aq, w, C, S, M, N, K, status, inject, s));
+        }
+        case MMQ_PATH_TC_PAIR: {
+            int rc = mmq::tc2_gemm_check_resources();
+            if (rc) return rc;
+            const int inject = t_inject_timeout;
+            t_inject_timeout = 0;
+            return from_cuda(mmq::launch_gemm_tc2(aq, w, C, S, M, N, K, status, inject, s));
         }
         case MMQ_PATH_SMALL_M:
             if (S || M > mmq::kSmallMMax) return MMQ_ERR_ARG;
@@ -154,7 +169,7 @@ int mmq_q4K_gemm(mmq_q8_1_t aq, const uint8_t* bq4k, float* C, int64_t M, int64_
 
 int mmq_q4K_gemm_path(mmq_q8_1_t aq, const uint8_t* bq4k, float* C, int64_t M, int64_t N,
                       int64_t K, int path, void* stream) {
-    if (path < MMQ_PATH_AUTO || path > MMQ_PATH_SMALL_M) return MMQ_ERR_ARG;
+    if (path < MMQ_PATH_AUTO || path > MMQ_PATH_TC_PAIR) return MMQ_ERR_ARG;
     if (path == MMQ_PATH_SMALL_M && M > mmq::kSmallMMax) return MMQ_ERR_ARG;
     int rc = check_gemm_args(aq, bq4k, C, M, N, K);
     if (rc) return rc;
@@ -163,7 +178,7 @@ int mmq_q4K_gemm_path(mmq_q8_1_t aq, const uint8_t* bq4k, float* C, int64_t M, i
 
 int mmq_q4K_block_dots(mmq_q8_1_t aq, const uint8_t* bq4k, int32_t* S, int64_t M, int64_t N,
                        int64_t K, int path, void* stream) {
-    if (path != MMQ_PATH_MMA_S8 && path != MMQ_PATH_TC) return MMQ_ERR_ARG;
+    if (path != MMQ_PATH_MMA_S8 && path != MMQ_PATH_TC && path != MMQ_PATH_TC_PAIR) return MMQ_ERR_ARG;
     int rc = check_gemm_args(aq, bq4k, S, M, N, K);
     if (rc) return rc;
     return run_gemm(aq, bq4k, nullptr, S, M, N, K, path, static_cast<cudaStream_t>(stream));

@@ -22,6 +22,11 @@ int tc_gemm_check_resources();   // MMQ_OK or MMQ_ERR_RESOURCE
 cudaError_t launch_gemm_tc(mmq_q8_1_t aq, const uint8_t* w, float* C,
                            int32_t* S, int64_t M, int64_t N, int64_t K,
                            int* status, int inject_timeout, cudaStream_t s);
+int tc2_gemm_check_resources();  // MMQ_OK or MMQ_ERR_RESOURCE
+int64_t tc2_pair_tiles(int64_t M, int64_t N);
+cudaError_t launch_gemm_tc2(mmq_q8_1_t aq, const uint8_t* w, float* C,
+                            int32_t* S, int64_t M, int64_t N, int64_t K,
+                            int* status, int inject_timeout, cudaStream_t s);
 cudaError_t launch_gemm_small_m(mmq_q8_1_t aq, const uint8_t* w, float* C,
                                 int64_t M, int64_t N, int64_t K, int* status,
                                 cudaStream_t s);

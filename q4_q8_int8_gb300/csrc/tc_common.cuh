@@ -1,0 +1,179 @@
+// Pieces shared by the tcgen05 GEMM kernels (one CTA and CTA-pair forms):
+// operand unpack arithmetic, shared-memory and cluster accessors, the
+// epilogue's packed FMA and stores, and the host-side tensor-map encoder.
+#pragma once
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_fp16.h>
+
+#include <mutex>
+
+#include "sm103_ptx.cuh"
+
+namespace mmq {
+namespace tc {
+
+using namespace mmq::ptx;
+
+constexpr float kSubnormalScale = 16777216.0f;   // 2^24: weight factors are fp16 subnormals
+
+// Ring position: slot index and the parity of the current pass over the ring.
+template <int N>
+struct Ring {
+    int slot = 0;
+    uint32_t phase = 0;
+    __device__ void next() {
+        if (++slot == N) {
+            slot = 0;
+            phase ^= 1u;
+        }
+    }
+};
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+    uint32_t d;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+    return d;
+}
+
+// Four int8 (a0 a1 a2 a3) -> fp16 pairs {a0, a2} and {a1, a3}, exact:
+// 0x6400 | (a ^ 0x80) is the fp16 1024 + (a + 128); subtracting 1152 leaves a.
+__device__ __forceinline__ void cvt_a4(uint32_t w, uint32_t& h02, uint32_t& h13) {
+    const uint32_t u = w ^ 0x80808080u;
+    const __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));
+    __half2 x = __hsub2(*reinterpret_cast<const __half2*>(&(h02 = prmt(u, 0x64646464u, 0x4240u))), bias);
+    __half2 y = __hsub2(*reinterpret_cast<const __half2*>(&(h13 = prmt(u, 0x64646464u, 0x4341u))), bias);
+    h02 = *reinterpret_cast<uint32_t*>(&x);
+    h13 = *reinterpret_cast<uint32_t*>(&y);
+}
+
+// 6-bit scales / mins of a q4_K super-block (12 bytes s[0..11] as three
+// words), four per word, one per byte: sub-blocks 0-3 are the low six bits
+// of s[0..3] / s[4..7]; sub-blocks 4-7 take their low four bits from s[8..11]
+// (low / high nibble) and their top two bits from the top of s[0..3] / s[4..7].
+__device__ __forceinline__ uint32_t sc_lo4(uint32_t s0) { return s0 & 0x3F3F3F3Fu; }
+__device__ __forceinline__ uint32_t sc_hi4(uint32_t s0, uint32_t s2) {
+    return (s2 & 0x0F0F0F0Fu) | ((s0 >> 2) & 0x30303030u);
+}
+__device__ __forceinline__ uint32_t m_lo4(uint32_t s1) { return s1 & 0x3F3F3F3Fu; }
+__device__ __forceinline__ uint32_t m_hi4(uint32_t s1, uint32_t s2) {
+    return ((s2 >> 4) & 0x0F0F0F0Fu) | ((s1 >> 2) & 0x30303030u);
+}
+
+// x = hi + lo with hi = x truncated to tf32 (low 13 mantissa bits cleared);
+// lo = x - hi is exact in f32.
+__device__ __forceinline__ void split_tf32(float x, float& hi, float& lo) {
+    hi = __uint_as_float(__float_as_uint(x) & 0xFFFFE000u);
+    lo = x - hi;
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
+                 "r"(d)
+                 : "memory");
+}
+__device__ __forceinline__ void st_shared_v4f(uint32_t addr, float a, float b, float c, float d) {
+    st_shared_v4(addr, __float_as_uint(a), __float_as_uint(b), __float_as_uint(c), __float_as_uint(d));
+}
+
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(addr)
+                 : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_shared_u32(uint32_t addr, uint32_t v) {
+    asm volatile("st.shared.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+__device__ __forceinline__ uint32_t ld_shared_u32(uint32_t addr) {
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t map_shared_rank(uint32_t saddr, uint32_t rank) {
+    uint32_t d;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(d) : "r"(saddr), "r"(rank));
+    return d;
+}
+__device__ __forceinline__ float4 ld_dsmem_v4(uint32_t addr) {
+    float4 v;
+    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(addr)
+                 : "memory");
+    return v;
+}
+
+// One 32-column half of a buffer: acc[16h + j] += m * D[32h + 2j, +1].
+template <int H>
+__device__ __forceinline__ void half_fma(uint64_t (&acc)[32], const uint32_t (&b)[32], uint64_t m2) {
+#pragma unroll
+    for (int j = 0; j < 16; ++j) acc[16 * H + j] = ffma2(pack2u(b[2 * j], b[2 * j + 1]), m2, acc[16 * H + j]);
+}
+
+// S dump of one 16-column part (block dots, bit for bit).
+__device__ __forceinline__ void dump_part(int32_t* S, const uint32_t (&b)[16], int64_t gr, int gc0, int M,
+                                          int N, int nb, int kb) {
+    if (gr >= M) return;
+#pragma unroll
+    for (int j = 0; j < 16; ++j)
+        if (gc0 + j < N)
+            S[(gr * N + gc0 + j) * int64_t(nb) + kb] = int32_t(__uint_as_float(b[j]) * kSubnormalScale);
+}
+
+// Epilogue thread's row x 64 columns of the 128x128 tile (m0, n0) -> C.
+__device__ __forceinline__ void store_tile(float* C, const uint64_t (&acc)[32], int M, int N, int m0,
+                                           int n0, int row, int colhalf) {
+    const int64_t gr = int64_t(m0) + row;
+    if (gr >= M) return;
+    float* crow = C + gr * N;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        const int gc = n0 + colhalf * 64 + 4 * i;   // N % 4 == 0: all four columns or none
+        if (gc < N)
+            *reinterpret_cast<float4*>(crow + gc) =
+                make_float4(lo_f(acc[2 * i]), hi_f(acc[2 * i]), lo_f(acc[2 * i + 1]), hi_f(acc[2 * i + 1]));
+    }
+}
+
+// ------------------------------------------------------------------- host
+inline PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+        else
+            cudaGetLastError();
+    });
+    return fn;
+}
+
+inline bool encode_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t inner,
+               uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
+               CUtensorMapSwizzle sw) {
+    auto fn = get_encode();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {inner, outer};
+    const cuuint64_t strides[1] = {row_bytes};
+    const cuuint32_t box[2] = {box_inner, box_outer};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace tc
+}  // namespace mmq

@@ -11,8 +11,10 @@ from tests.gpu_util import require_gpu, to_dev
 pytestmark = pytest.mark.gpu
 
 
-def test_injected_timeout_is_reported_and_context_survives():
+@pytest.mark.parametrize("path_name", ["MMQ_PATH_TC", "MMQ_PATH_TC_PAIR"])
+def test_injected_timeout_is_reported_and_context_survives(path_name):
     mmq = require_gpu()
+    path = getattr(mmq, path_name)
     M, N, K = 128, 256, 512
     x = synthetic.activations(M, K, 5)
     blk = synthetic.q4K_weights(N, K, 6)
@@ -20,11 +22,11 @@ def test_injected_timeout_is_reported_and_context_survives():
     w = to_dev(blk.reshape(-1))
     assert mmq.status() == 0
     mmq.mmq_debug_inject_timeout(True)
-    mmq.q4K_gemm(aq, w, N, path=mmq.MMQ_PATH_TC)
+    mmq.q4K_gemm(aq, w, N, path=path)
     assert mmq.status() == mmq.MMQ_ERR_DEVICE_TIMEOUT
     assert mmq.status() == 0   # read-and-clear
     # the next launch is unaffected and correct
-    C = mmq.q4K_gemm(aq, w, N, path=mmq.MMQ_PATH_TC).cpu().numpy()
+    C = mmq.q4K_gemm(aq, w, N, path=path).cpu().numpy()
     assert mmq.status() == 0
     q, da, sa = oracle.quantize_q8_1(x)
     C_ref, _, T = oracle.gemm(q, da, sa, blk, N)

@@ -20,7 +20,7 @@ RTOL, ATOL = 1e-4, 1e-6
 
 def _paths():
     import q4_q8_int8_gb300 as mmq
-    return [mmq.MMQ_PATH_MMA_S8, mmq.MMQ_PATH_TC]
+    return [mmq.MMQ_PATH_MMA_S8, mmq.MMQ_PATH_TC, mmq.MMQ_PATH_TC_PAIR]
 
 
 def _paths_for(M):
@@ -48,7 +48,7 @@ def _full_check(x, blk, N, path):
     return C
 
 
-@pytest.mark.parametrize("path_name", ["MMQ_PATH_MMA_S8", "MMQ_PATH_TC"])
+@pytest.mark.parametrize("path_name", ["MMQ_PATH_MMA_S8", "MMQ_PATH_TC", "MMQ_PATH_TC_PAIR"])
 @pytest.mark.parametrize("M,N,K", [(128, 256, 512), (77, 132, 768), (1, 4, 256), (130, 260, 2816),
                                    (256, 128, 256)])
 def test_block_dots_bit_exact(path_name, M, N, K):
@@ -63,7 +63,7 @@ def test_block_dots_bit_exact(path_name, M, N, K):
     assert (S == oracle.block_dots(q, blk, N)).all()
 
 
-@pytest.mark.parametrize("path_name", ["MMQ_PATH_MMA_S8", "MMQ_PATH_TC"])
+@pytest.mark.parametrize("path_name", ["MMQ_PATH_MMA_S8", "MMQ_PATH_TC", "MMQ_PATH_TC_PAIR"])
 @pytest.mark.parametrize("sign", [1, -1])
 def test_block_dots_extremes(path_name, sign):
     # all quants at +-127 and all nibbles at 15: |S| reaches 32*127*15 = 60960
@@ -77,7 +77,7 @@ def test_block_dots_extremes(path_name, sign):
     assert (S == sign * 60960).all()
 
 
-@pytest.mark.parametrize("path_name", ["MMQ_PATH_MMA_S8", "MMQ_PATH_TC"])
+@pytest.mark.parametrize("path_name", ["MMQ_PATH_MMA_S8", "MMQ_PATH_TC", "MMQ_PATH_TC_PAIR"])
 @pytest.mark.parametrize("M,N,K", [(128, 256, 512), (77, 132, 768), (300, 388, 1280), (1, 4, 256),
                                    (64, 128, 2816)])
 def test_gemm_full_small(path_name, M, N, K):
@@ -95,7 +95,7 @@ def test_gemm_small_m_full():
         _full_check(x, blk, 260, mmq.MMQ_PATH_SMALL_M)
 
 
-@pytest.mark.parametrize("path_name", ["MMQ_PATH_MMA_S8", "MMQ_PATH_TC"])
+@pytest.mark.parametrize("path_name", ["MMQ_PATH_MMA_S8", "MMQ_PATH_TC", "MMQ_PATH_TC_PAIR"])
 @pytest.mark.parametrize("name", ["q_proj", "down", "gate_up"])
 def test_gemm_full_size_sampled(path_name, name):
     mmq = require_gpu()
@@ -125,7 +125,8 @@ def test_gemm_sweep_auto_sampled(M):
     assert oracle.within_tolerance(C[rows, cols], C_ref, T, RTOL, ATOL).all()
 
 
-@pytest.mark.parametrize("path_name", ["MMQ_PATH_MMA_S8", "MMQ_PATH_TC", "MMQ_PATH_SMALL_M"])
+@pytest.mark.parametrize("path_name", ["MMQ_PATH_MMA_S8", "MMQ_PATH_TC", "MMQ_PATH_TC_PAIR",
+                                       "MMQ_PATH_SMALL_M"])
 def test_every_output_written_and_deterministic(path_name):
     import torch
     mmq = require_gpu()
@@ -147,7 +148,8 @@ def test_every_output_written_and_deterministic(path_name):
     assert torch.equal(C1.view(torch.int32), C2.view(torch.int32))
 
 
-@pytest.mark.parametrize("path_name", ["MMQ_PATH_MMA_S8", "MMQ_PATH_TC", "MMQ_PATH_SMALL_M"])
+@pytest.mark.parametrize("path_name", ["MMQ_PATH_MMA_S8", "MMQ_PATH_TC", "MMQ_PATH_TC_PAIR",
+                                       "MMQ_PATH_SMALL_M"])
 def test_worked_examples_exact(path_name):
     mmq = require_gpu()
     path = getattr(mmq, path_name)
