@@ -30,6 +30,19 @@ SHAPES = {
 }
 SWEEP_M = (1, 16, 77, 128, 512, 2047, 8192)
 
+# The 7B prefill linear stack: 32 layers, each with these GEMMs as (name, K, N);
+# every (layer, GEMM) has its own weights and its own activations.
+STACK_LAYERS = 32
+STACK_TOKENS = 2048
+STACK_GEMMS = (("q", 4096, 4096), ("k", 4096, 4096), ("v", 4096, 4096), ("o", 4096, 4096),
+               ("gate", 4096, 11008), ("up", 4096, 11008), ("down", 11008, 4096))
+
+
+def stack_seeds(layer: int, g: int):
+    """(weight seed, activation seed) of GEMM g of `layer` in the stack."""
+    s = 3000 + 7 * layer + g
+    return s, 1_000_000 + s
+
 
 def activations(M: int, K: int, seed: int, outlier_frac: float = 0.0,
                 outlier_scale: float = 20.0) -> np.ndarray:
