@@ -480,10 +480,14 @@ cudaError_t launch_nf(const SmallMaps& maps, float* C, int64_t M, int64_t N, int
     cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
     const int64_t row_tiles = (N + kRows - 1) / kRows;
     const int nsb = int(K / 256);
-    // Split K over a cluster so that about two CTAs land on every SM, within
-    // the shared-memory budget of the landing area.
+    // Split K over a cluster so that every SM gets a CTA: about two per SM
+    // for one token fragment, about one for more (each CTA converts the
+    // tokens of its super-blocks, so more CTAs per weight row cost more
+    // conversion; measured on 4096 x 4096: M = 8 fastest at two per SM,
+    // M = 16..64 at one), within the shared-memory budget of the landing area.
+    const int64_t per_sm = NF == 1 ? 2 : 1;
     int split = 1;
-    while (split < kMaxSplit && row_tiles * split * 2 <= 2 * int64_t(nsm) && split * 2 <= nsb &&
+    while (split < kMaxSplit && row_tiles * split * 2 <= per_sm * int64_t(nsm) && split * 2 <= nsb &&
            Layout::make(NF, G, split * 2).total + 1024 <= optin)
         split *= 2;
     const int smem = Layout::make(NF, G, split).total + 1024;   // + alignment slack
