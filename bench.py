@@ -42,7 +42,7 @@ def parse():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="mine", choices=["mine", "reference"])
     ap.add_argument("--workload", default="q_proj", choices=sorted(WORKLOADS))
-    ap.add_argument("--path", default="auto", choices=["auto", "mma_s8", "tc", "small_m"])
+    ap.add_argument("--path", default="auto", choices=["auto", "mma_s8", "tc", "tc_pair", "small_m"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="target seconds of oracle work for the CPU baseline sample")
@@ -276,7 +276,7 @@ def run_mine(args, rank, world, local_rank):
     mmq_build.build()
     mmq.load_library()
     path = {"auto": mmq.MMQ_PATH_AUTO, "mma_s8": mmq.MMQ_PATH_MMA_S8, "tc": mmq.MMQ_PATH_TC,
-            "small_m": mmq.MMQ_PATH_SMALL_M}[args.path]
+            "tc_pair": mmq.MMQ_PATH_TC_PAIR, "small_m": mmq.MMQ_PATH_SMALL_M}[args.path]
 
     M, K, N = WORKLOADS[args.workload]
     # Inputs: R independent sets rotated step by step so that every step reads
@@ -342,7 +342,9 @@ def run_mine(args, rank, world, local_rank):
 
     step_ms = evs[0][0].elapsed_time(evs[-1][2]) / args.steps
     q_ms = float(np.mean([e[0].elapsed_time(e[1]) for e in evs]))
-    g_ms = float(np.mean([e[1].elapsed_time(e[2]) for e in evs]))
+    g_all = np.array([e[1].elapsed_time(e[2]) for e in evs])
+    g_ms = float(np.mean(g_all))
+    g_dist = {"median": float(np.median(g_all)), "min": float(g_all.min()), "max": float(g_all.max())}
     t = torch.tensor([step_ms, q_ms, g_ms], device=dev)
     if world > 1:
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
@@ -397,6 +399,7 @@ def run_mine(args, rank, world, local_rank):
         used_path = mmq.MMQ_PATH_SMALL_M if M <= mmq.SMALL_M_MAX else mmq.MMQ_PATH_TC
     kname = {mmq.MMQ_PATH_MMA_S8: ("gemm_mma_s8", "gemm_mma.cu"),
              mmq.MMQ_PATH_TC: ("gemm_tc", "gemm_tc.cu"),
+             mmq.MMQ_PATH_TC_PAIR: ("gemm_tc2", "gemm_tc2.cu"),
              mmq.MMQ_PATH_SMALL_M: ("gemm_small_m", "gemm_small.cu")}[used_path]
     src_hash = kernel_source_hash([kname[1], "sm103_ptx.cuh"])
     traffic = recorded_traffic(kname[0], src_hash)
@@ -407,7 +410,7 @@ def run_mine(args, rank, world, local_rank):
         roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
                 "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json hbm copy)"}
-    elif used_path == mmq.MMQ_PATH_TC:
+    elif used_path in (mmq.MMQ_PATH_TC, mmq.MMQ_PATH_TC_PAIR):
         # The exact integer contraction runs on the tensor pipe as kind::f16
         # MMAs (2 flops per MAC); the kernel is timed inside a long loop, so
         # the denominator is the sustained measured bf16 (= f16 rate) peak.
@@ -426,6 +429,15 @@ def run_mine(args, rank, world, local_rank):
                 "frac": achieved / peak, "traffic": traffic,
                 "peak_source": "measured int8 mma.sync peak (profiles/peaks.json)"}
     roof["kernel"] = kname[0]
+    # The epilogue's FP32 ceiling, reported beside the tensor roofline: per
+    # output and 32-k chunk the tcgen05 kernel does one FMA (2 flops), plus
+    # per super-block one FMA for d and one add of the second term (0.5 flop
+    # per chunk); the other kernels do the pages' 1 FMUL + 2 FFMA (5 flops).
+    alu_flops = (2.5 if used_path in (mmq.MMQ_PATH_TC, mmq.MMQ_PATH_TC_PAIR) else 5.0) * macs / 32
+    alu_peak = micro["sms"] * 128 * 2 * sm_mhz * 1e6 / 1e12
+    alu = {"flops_per_launch": alu_flops, "achieved_tflops": alu_flops / (g_ms * 1e-3) / 1e12,
+           "peak_tflops": alu_peak, "frac": alu_flops / (g_ms * 1e-3) / 1e12 / alu_peak,
+           "peak_source": f"derived: {micro['sms']} SMs x 128 FP32 lanes x 2 x {sm_mhz:.0f} MHz"}
     roof["algorithmic_bytes_per_launch"] = alg_bytes
     roof["algorithmic_macs_per_launch"] = macs
     int8_frac = 2 * gemm_tmacs / micro["int8_mma_sync_tops"]
@@ -443,7 +455,7 @@ def run_mine(args, rank, world, local_rank):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "int8xu4->f32 (fp16-exact ints on tensor cores)"
-        if used_path == mmq.MMQ_PATH_TC else "s8xs8->s32, f32 rescale",
+        if used_path in (mmq.MMQ_PATH_TC, mmq.MMQ_PATH_TC_PAIR) else "s8xs8->s32, f32 rescale",
         "data": "synthetic",
         "config": {"workload": f"{args.workload} M={M} K={K} N={N}", "global_batch_tokens": M * world,
                    "parallelism": f"independent problem per GPU x{world}",
@@ -451,8 +463,10 @@ def run_mine(args, rank, world, local_rank):
                    "path": args.path},
         "us_per_gmac": step_ms * 1e3 / (macs / 1e9),
         "gemm_only": {"tmacs": gemm_tmacs, "us_per_gmac": g_ms * 1e3 / (macs / 1e9), "ms": g_ms,
+                      "ms_over_steps": g_dist,
                       "frac_of_int8_peak": int8_frac,
                       "int8_peak_source": "measured mma.sync s8 peak, profiles/peaks.json"},
+        "epilogue_alu": alu,
         "prepass": {"ms": q_ms, "gbs": (M * K * 4 + M * K * 1.25) / (q_ms * 1e-3) / 1e9},
         "roofline": roof,
         "cpu_baseline": cpu,
