@@ -1,13 +1,17 @@
 // Peak-rate microbenchmarks for the roofline denominators this library needs
 // and the driver does not measure: the warp-level int8 tensor rate
 // (mma.sync m16n8k32 s8 -> s32) and the FP32 FMA rates (scalar and f32x2)
-// that bound the per-chunk rescale epilogue.  Prints one JSON line.
+// that bound the per-chunk rescale epilogue; tensor-memory load rates; and
+// the latencies of the tcgen05 GEMM's MMA-issue / mbarrier hand-off chain.
+// Prints JSON lines.
 //
 // Each kernel runs long chains of independent instructions per warp on every
 // SM; timing is by CUDA events around a single launch after a warm-up.
 #include <cuda_runtime.h>
 #include <cstdio>
 #include <cstdint>
+
+#include "../csrc/sm103_ptx.cuh"
 
 #define CK(x) do { cudaError_t e = (x); if (e != cudaSuccess) { \
     fprintf(stderr, "%s: %s\n", #x, cudaGetErrorString(e)); return 1; } } while (0)
@@ -144,6 +148,125 @@ __global__ void hmma_loop(int iters, int* out) {
     if (s == 1234.5f) out[0] = 1;
 }
 
+// ---- hand-off latencies on one SM (one CTA of 512 threads): the cost of
+// the tcgen05 GEMM's producer/consumer chain with no work in it.
+//   test 0: one 128x128x16 f16 MMA + commit into an idle tensor pipe
+//   test 1: four such MMAs + commit
+//   test 2: mbarrier try_wait on an already completed phase
+//   test 3/4/5: two tensor-memory slots handed between one issuing thread and
+//   eight consumer warps; the issuer waits "slot empty" (8 arrivals) and then
+//   signals "slot full" by a commit with no MMA (3), a plain arrive (4), or a
+//   commit after four MMAs into the slot (5); consumers wait "full", arrive "empty".
+// out[0] = issue cycles, out[1] = total cycles (per iteration after dividing).
+__device__ __forceinline__ long long clock64_now() {
+    long long c;
+    asm volatile("mov.u64 %0, %%clock64;" : "=l"(c));
+    return c;
+}
+__device__ __forceinline__ bool spin_wait(uint32_t bar, uint32_t par) {
+    const long long t0 = clock64_now();
+    while (!mmq::ptx::mbar_try_wait(bar, par))
+        if (clock64_now() - t0 > (1ll << 30)) return false;
+    return true;
+}
+
+template <int kTest>
+__global__ void __launch_bounds__(512, 1) handoff_loop(int iters, long long* out) {
+    using namespace mmq::ptx;
+    extern __shared__ __align__(1024) uint8_t hsm[];
+    uint8_t* s = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(hsm) + 1023) & ~uintptr_t(1023));
+    const uint32_t sb = smem_u32(s);
+    uint32_t* slot = reinterpret_cast<uint32_t*>(s + 32768);
+    const uint32_t done = sb + 32768 + 64, full = done + 8, empty = done + 24;   // full/empty: 2 slots each
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int i = threadIdx.x; i < 8192; i += blockDim.x) reinterpret_cast<uint32_t*>(s)[i] = 0;
+    if (threadIdx.x == 0) {
+        mbar_init(done, 1);
+        mbar_init(full, 1);
+        mbar_init(full + 8, 1);
+        mbar_init(empty, 8);
+        mbar_init(empty + 8, 8);
+        fence_barrier_init();
+    }
+    fence_proxy_async_smem();
+    __syncthreads();
+    if (warp == 0) {
+        tmem_alloc(smem_u32(slot), 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tb = *slot;
+    const uint32_t idesc = idesc_f16_f32(128, 128);
+    const uint64_t dA = smem_desc_sw128(sb), dB = smem_desc_sw128(sb + 16384);
+    bool ok = true;
+    if (kTest <= 1) {
+        if (warp == 1 && lane == 0) {
+            long long tiss = 0, tall = 0;
+            for (int i = 0; i < iters && ok; ++i) {
+                const long long t0 = clock64_now();
+                for (int j = 0; j < (kTest == 0 ? 1 : 4); ++j)
+                    mma_f16(tb + uint32_t((j >> 1) * 128), dA + uint64_t(2 * (j & 1)), dB + uint64_t(2 * (j & 1)),
+                            idesc, uint32_t(j & 1));
+                mma_commit(done);
+                const long long t1 = clock64_now();
+                ok = spin_wait(done, uint32_t(i & 1));
+                tiss += t1 - t0;
+                tall += clock64_now() - t0;
+            }
+            out[0] = tiss;
+            out[1] = tall;
+        }
+    } else if (kTest == 2) {
+        if (warp == 1 && lane == 0) {
+            mbar_arrive(done);
+            int n = 0;
+            const long long t0 = clock64_now();
+            for (int i = 0; i < iters; ++i) n += mbar_try_wait(done, 0u) ? 1 : 0;
+            out[0] = out[1] = clock64_now() - t0;
+            if (n != iters) ok = false;
+        }
+    } else {
+        if (warp == 1 && lane == 0) {
+            const long long t0 = clock64_now();
+            for (int u = 0; u < iters && ok; ++u) {
+                const uint32_t sl = uint32_t(u & 1) * 8u, ph = uint32_t(u >> 1) & 1u;
+                ok = spin_wait(empty + sl, ph ^ 1u);
+                tc_fence_after();
+                if (kTest == 5)
+                    for (int j = 0; j < 4; ++j)
+                        mma_f16(tb + uint32_t((u & 1) * 256 + (j >> 1) * 128), dA + uint64_t(2 * (j & 1)),
+                                dB + uint64_t(2 * (j & 1)), idesc, uint32_t(j & 1));
+                if (kTest == 4) mbar_arrive(full + sl);
+                else mma_commit(full + sl);
+            }
+            out[0] = out[1] = clock64_now() - t0;
+            if (kTest == 5) {
+                mma_commit(done);
+                ok = ok && spin_wait(done, 0u);
+            }
+        } else if (warp >= 8) {
+            for (int u = 0; u < iters && ok; ++u) {
+                const uint32_t sl = uint32_t(u & 1) * 8u, ph = uint32_t(u >> 1) & 1u;
+                ok = spin_wait(full + sl, ph);
+                tc_fence_after();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(empty + sl);
+            }
+        }
+    }
+    if (!ok) out[2] = 1;
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tb, 512);
+    }
+}
+
 int main() {
     int dev = 0, nsm = 0, clk = 0;
     CK(cudaGetDevice(&dev));
@@ -223,6 +346,29 @@ int main() {
         run_t(tmem_ld_loop<0, 1>, 16, 1, "32x32b.x32") || run_t(tmem_ld_loop<0, 2>, 8, 2, "32x32b.x32") ||
         run_t(tmem_ld_loop<1, 1>, 8, 1, "16x256b.x8") || run_t(tmem_ld_loop<1, 1>, 16, 1, "16x256b.x8") ||
         run_t(tmem_ld_loop<1, 2>, 8, 2, "16x256b.x8"))
+        return 1;
+
+    // hand-off latencies (cycles per iteration on one SM)
+    long long* dl;
+    CK(cudaMalloc(&dl, 3 * sizeof(long long)));
+    auto run_h = [&](void (*k)(int, long long*), int iters, const char* name) -> int {
+        const int smem = 32768 + 1024 + 128;
+        if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) return 1;
+        CK(cudaMemset(dl, 0, 3 * sizeof(long long)));
+        k<<<1, 512, smem>>>(iters, dl);
+        CK(cudaDeviceSynchronize());
+        long long h[3];
+        CK(cudaMemcpy(h, dl, sizeof(h), cudaMemcpyDeviceToHost));
+        printf("{\"handoff\": \"%s\", \"issue_cycles\": %.1f, \"cycles\": %.1f, \"timed_out\": %lld}\n", name,
+               double(h[0]) / iters, double(h[1]) / iters, h[2]);
+        return 0;
+    };
+    if (run_h(handoff_loop<0>, 512, "1 MMA 128x128x16 + commit, idle pipe") ||
+        run_h(handoff_loop<1>, 512, "4 MMAs + commit, idle pipe") ||
+        run_h(handoff_loop<2>, 4096, "try_wait on a completed phase") ||
+        run_h(handoff_loop<3>, 2048, "2-slot hand-off, commit without MMA, 8 consumer warps") ||
+        run_h(handoff_loop<4>, 2048, "2-slot hand-off, plain arrive, 8 consumer warps") ||
+        run_h(handoff_loop<5>, 2048, "2-slot hand-off, 4 MMAs + commit, 8 consumer warps"))
         return 1;
     return 0;
 }
