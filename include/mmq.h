@@ -126,6 +126,18 @@ int mmq_q4K_gemm(mmq_q8_1_t aq, const uint8_t* bq4k, float* C, int64_t M,
 int mmq_q4K_gemm_path(mmq_q8_1_t aq, const uint8_t* bq4k, float* C, int64_t M,
                       int64_t N, int64_t K, int path, void* stream);
 
+/* The GEMM with its output also quantized to q8_1, so that a following GEMM
+ * needs no separate prepass: `out` describes an [M][N] q8_1 buffer
+ * (mmq_q8_1_bytes(M, N); N % 32 == 0) and receives exactly what
+ * mmq_quantize_q8_1 would produce from the f32 result (per 32 output
+ * columns: da = amax/127, q = roundf(c/da) clamped to +-127, sa = sum q).
+ * For M > 64 the tcgen05 kernel quantizes in its epilogue and C may be NULL
+ * (then no f32 result is stored).  For M <= 64 C is required: the small-M
+ * kernel writes C and a quantize pass over it follows on the same stream.
+ * Otherwise as mmq_q4K_gemm (same argument rules and error codes). */
+int mmq_q4K_gemm_q8_1(mmq_q8_1_t aq, const uint8_t* bq4k, float* C, mmq_q8_1_t out,
+                      int64_t M, int64_t N, int64_t K, void* stream);
+
 /* Debug/test dump of the exact per-chunk integer dots (page r15 section 2.1:
  * S_ij = sum_k a_int[i,k] * v[j,k]; section 2.3: |S| <= 32*127*15) computed
  * by the same unpack and MMA code as the GEMM kernel selected by `path`

@@ -34,7 +34,7 @@ SMALL_M_MAX = 64
 # Every symbol include/mmq.h declares.
 EXPORTS = (
     "mmq_q8_1_bytes", "mmq_q8_1_view", "mmq_quantize_q8_1", "mmq_q4K_bytes",
-    "mmq_pack_q4K", "mmq_q4K_gemm", "mmq_q4K_gemm_path", "mmq_q4K_block_dots",
+    "mmq_pack_q4K", "mmq_q4K_gemm", "mmq_q4K_gemm_path", "mmq_q4K_gemm_q8_1", "mmq_q4K_block_dots",
     "mmq_status", "mmq_strerror", "mmq_debug_inject_timeout",
 )
 
@@ -71,6 +71,7 @@ def load_library(path: str = LIB_PATH):
                 "mmq_pack_q4K": ([P, P, P, P, P, I, I, P], ctypes.c_int),
                 "mmq_q4K_gemm": ([Q, P, P, I, I, I, P], ctypes.c_int),
                 "mmq_q4K_gemm_path": ([Q, P, P, I, I, I, ctypes.c_int, P], ctypes.c_int),
+                "mmq_q4K_gemm_q8_1": ([Q, P, P, Q, I, I, I, P], ctypes.c_int),
                 "mmq_q4K_block_dots": ([Q, P, P, I, I, I, ctypes.c_int, P], ctypes.c_int),
                 "mmq_status": ([P], ctypes.c_int),
                 "mmq_strerror": ([ctypes.c_int], ctypes.c_char_p),
@@ -111,6 +112,10 @@ def mmq_q4K_gemm(aq, bq4k, C, M, N, K, stream):
 
 def mmq_q4K_gemm_path(aq, bq4k, C, M, N, K, path, stream):
     return load_library().mmq_q4K_gemm_path(aq, bq4k, C, M, N, K, path, stream)
+
+
+def mmq_q4K_gemm_q8_1(aq, bq4k, C, out, M, N, K, stream):
+    return load_library().mmq_q4K_gemm_q8_1(aq, bq4k, C, out, M, N, K, stream)
 
 
 def mmq_q4K_block_dots(aq, bq4k, S, M, N, K, path, stream):
@@ -176,6 +181,21 @@ def q4K_gemm(aq, w, N: int, path: int = MMQ_PATH_AUTO, out=None, stream=None):
                              ctypes.c_void_p(C.data_ptr()), M, N, K, path, _stream_ptr(stream)),
            "mmq_q4K_gemm")
     return C
+
+
+def q4K_gemm_q8_1(aq, w, N: int, with_c: bool = True, out=None, stream=None):
+    """GEMM whose result is also quantized to q8_1 ([M][N] q8_1 triple, ready
+    as the next GEMM's activations); returns (C or None, (qs, da, sa))."""
+    import torch
+    qs, da, sa = aq
+    M, K = qs.shape
+    C = torch.empty((M, N), dtype=torch.float32, device=qs.device) if with_c else None
+    o = out if out is not None else empty_q8_1(M, N, qs.device)
+    _check(mmq_q4K_gemm_q8_1(q8_1_struct(qs, da, sa), ctypes.c_void_p(w.data_ptr()),
+                             ctypes.c_void_p(C.data_ptr() if C is not None else 0), q8_1_struct(*o),
+                             M, N, K, _stream_ptr(stream)),
+           "mmq_q4K_gemm_q8_1")
+    return C, o
 
 
 def q4K_block_dots(aq, w, N: int, path: int = MMQ_PATH_MMA_S8, out=None, stream=None):

@@ -133,7 +133,8 @@ static int auto_path(int64_t M, int64_t N, bool dump) {
 }
 
 static int run_gemm(mmq_q8_1_t aq, const uint8_t* w, float* C, int32_t* S, int64_t M,
-                    int64_t N, int64_t K, int path, cudaStream_t s) {
+                    int64_t N, int64_t K, int path, cudaStream_t s,
+                    mmq_q8_1_t q8out = mmq_q8_1_t{nullptr, nullptr, nullptr}) {
     int* status = mmq::status_word_ptr();
     if (!status) return MMQ_ERR_CUDA;
     if (path == MMQ_PATH_AUTO) path = auto_path(M, N, S != nullptr);
@@ -145,7 +146,7 @@ static int run_gemm(mmq_q8_1_t aq, const uint8_t* w, float* C, int32_t* S, int64
             if (rc) return rc;
             const int inject = t_inject_timeout;
             t_inject_timeout = 0;
-            return from_cuda(mmq::launch_gemm_tc(aq, w, C, S, M, N, K, status, inject, s));
+            return from_cuda(mmq::launch_gemm_tc(aq, w, C, q8out, S, M, N, K, status, inject, s));
         }
         case MMQ_PATH_TC_PAIR: {
             int rc = mmq::tc2_gemm_check_resources();
@@ -174,6 +175,23 @@ int mmq_q4K_gemm_path(mmq_q8_1_t aq, const uint8_t* bq4k, float* C, int64_t M, i
     int rc = check_gemm_args(aq, bq4k, C, M, N, K);
     if (rc) return rc;
     return run_gemm(aq, bq4k, C, nullptr, M, N, K, path, static_cast<cudaStream_t>(stream));
+}
+
+int mmq_q4K_gemm_q8_1(mmq_q8_1_t aq, const uint8_t* bq4k, float* C, mmq_q8_1_t out, int64_t M,
+                      int64_t N, int64_t K, void* stream) {
+    int rc = check_q8(out);
+    if (rc) return rc;
+    if (N % 32 != 0) return MMQ_ERR_ARG;
+    const bool small = M <= mmq::kSmallMMax;
+    if (small && !C) return MMQ_ERR_ARG;   // the small-M kernel writes C, then it is quantized
+    rc = check_gemm_args(aq, bq4k, C ? static_cast<const void*>(C) : static_cast<const void*>(out.qs), M, N, K);
+    if (rc) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (small) {
+        if ((rc = run_gemm(aq, bq4k, C, nullptr, M, N, K, MMQ_PATH_SMALL_M, s))) return rc;
+        return from_cuda(mmq::launch_quantize_q8_1(C, M, N, out, s));
+    }
+    return run_gemm(aq, bq4k, C, nullptr, M, N, K, MMQ_PATH_TC, s, out);
 }
 
 int mmq_q4K_block_dots(mmq_q8_1_t aq, const uint8_t* bq4k, int32_t* S, int64_t M, int64_t N,

@@ -134,9 +134,11 @@ struct Bars {
     __device__ uint32_t min_empty() const { return at(kMin0 + 1); }
 };
 
-template <bool kDump>
+// kDump: write the exact block dots S instead of C; kQ8: also (or only, C
+// == nullptr) write the result quantized to q8_1.
+template <bool kDump, bool kQ8>
 __global__ void __launch_bounds__(kThreads, 1)
-gemm_tc_kernel(const __grid_constant__ TmaMaps maps, float* __restrict__ C,
+gemm_tc_kernel(const __grid_constant__ TmaMaps maps, float* __restrict__ C, mmq_q8_1_t q8out,
                int32_t* __restrict__ S, int M, int N, int K, int split, int* status, int inject_timeout) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -559,7 +561,10 @@ gemm_tc_kernel(const __grid_constant__ TmaMaps maps, float* __restrict__ C,
                 if (lane == 0) mbar_arrive(bars.scl_empty(sr.slot));
                 sr.next();
             }
-            if (!kDump && split == 1) store_tile(C, acc, M, N, m0, n0, row, colhalf);
+            if (!kDump && split == 1) {
+                if (!kQ8 || C) store_tile(C, acc, M, N, m0, n0, row, colhalf);
+                if (kQ8) store_tile_q8_1(q8out, acc, M, N, m0, n0, row, colhalf);
+            }
         }
     epi_done:;
         if (split > 1) {
@@ -583,7 +588,8 @@ gemm_tc_kernel(const __grid_constant__ TmaMaps maps, float* __restrict__ C,
                     }
                 }
                 const int m0 = (tile_first / tiles_n) * BM, n0 = (tile_first % tiles_n) * BN;
-                store_tile(C, acc, M, N, m0, n0, row, colhalf);
+                if (!kQ8 || C) store_tile(C, acc, M, N, m0, n0, row, colhalf);
+                if (kQ8) store_tile_q8_1(q8out, acc, M, N, m0, n0, row, colhalf);
             }
             cluster_sync_all();   // remote partials stay alive until rank 0 has read them
         }
@@ -612,7 +618,7 @@ int tc_gemm_check_resources() {
     return optin >= kSmemBytes ? MMQ_OK : MMQ_ERR_RESOURCE;
 }
 
-cudaError_t launch_gemm_tc(mmq_q8_1_t aq, const uint8_t* w, float* C, int32_t* S, int64_t M,
+cudaError_t launch_gemm_tc(mmq_q8_1_t aq, const uint8_t* w, float* C, mmq_q8_1_t q8out, int32_t* S, int64_t M,
                            int64_t N, int64_t K, int* status, int inject_timeout, cudaStream_t s) {
     TmaMaps maps;
     const uint64_t nb = uint64_t(K / 32), nsb = uint64_t(K / 256);
@@ -632,8 +638,9 @@ cudaError_t launch_gemm_tc(mmq_q8_1_t aq, const uint8_t* w, float* C, int32_t* S
     // kRegsLaunch registers per thread; refuse anything else.
     {
         cudaFuncAttributes fa;
-        cudaError_t e = S ? cudaFuncGetAttributes(&fa, gemm_tc_kernel<true>)
-                          : cudaFuncGetAttributes(&fa, gemm_tc_kernel<false>);
+        cudaError_t e = cudaFuncGetAttributes(&fa, S ? gemm_tc_kernel<true, false>
+                                                   : (q8out.qs ? gemm_tc_kernel<false, true>
+                                                               : gemm_tc_kernel<false, false>));
         if (e != cudaSuccess) return e;
         if (fa.numRegs != int(kRegsLaunch)) return cudaErrorInvalidConfiguration;
     }
@@ -642,7 +649,8 @@ cudaError_t launch_gemm_tc(mmq_q8_1_t aq, const uint8_t* w, float* C, int32_t* S
     int split = 1;
     if (tiles * 2 <= nsm)
         while (split < 8 && tiles * split * 2 <= nsm && split * 2 <= int64_t(nsb)) split *= 2;
-    auto k = S ? gemm_tc_kernel<true> : gemm_tc_kernel<false>;
+    auto k = S ? gemm_tc_kernel<true, false>
+               : (q8out.qs ? gemm_tc_kernel<false, true> : gemm_tc_kernel<false, false>);
     cudaError_t e;
     if ((e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes)))
         return e;
@@ -658,7 +666,7 @@ cudaError_t launch_gemm_tc(mmq_q8_1_t aq, const uint8_t* w, float* C, int32_t* S
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, k, maps, C, S, int(M), int(N), int(K), split, status, inject_timeout);
+    e = cudaLaunchKernelEx(&cfg, k, maps, C, q8out, S, int(M), int(N), int(K), split, status, inject_timeout);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }

@@ -19,7 +19,8 @@ cudaError_t launch_gemm_mma_s8(mmq_q8_1_t aq, const uint8_t* w, float* C,
                                int32_t* S, int64_t M, int64_t N, int64_t K,
                                int* status, cudaStream_t s);
 int tc_gemm_check_resources();   // MMQ_OK or MMQ_ERR_RESOURCE
-cudaError_t launch_gemm_tc(mmq_q8_1_t aq, const uint8_t* w, float* C,
+// q8out.qs == nullptr: no q8_1 output; C == nullptr: no f32 output.
+cudaError_t launch_gemm_tc(mmq_q8_1_t aq, const uint8_t* w, float* C, mmq_q8_1_t q8out,
                            int32_t* S, int64_t M, int64_t N, int64_t K,
                            int* status, int inject_timeout, cudaStream_t s);
 int tc2_gemm_check_resources();  // MMQ_OK or MMQ_ERR_RESOURCE

@@ -144,6 +144,56 @@ __device__ __forceinline__ void store_tile(float* C, const uint64_t (&acc)[32], 
     }
 }
 
+// The same row x 64 columns quantized to q8_1 (two 32-column blocks of an
+// [M][N] q8_1 output, N % 32 == 0): per block amax, da = amax / 127 (IEEE
+// division), q = roundf(c / da) clamped to +-127, sa = sum of q; da == 0
+// gives q = 0 and sa = 0.  The same operation as the q8_1 prepass on the
+// stored f32 values (web page "20 . r15 -- f32-accumulate mma probe (dead
+// end) + rank-1 term2 rescale", section 2.1, for the format).
+__device__ __forceinline__ void store_tile_q8_1(mmq_q8_1_t out, const uint64_t (&acc)[32], int M, int N,
+                                                int m0, int n0, int row, int colhalf) {
+    const int64_t gr = int64_t(m0) + row;
+    if (gr >= M) return;
+#pragma unroll
+    for (int blk = 0; blk < 2; ++blk) {
+        const int gc = n0 + colhalf * 64 + 32 * blk;
+        if (gc >= N) continue;
+        float v[32];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            v[2 * i] = lo_f(acc[16 * blk + i]);
+            v[2 * i + 1] = hi_f(acc[16 * blk + i]);
+        }
+        float amax = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
+        const float d = __fdiv_rn(amax, 127.0f);
+        uint32_t w[8];
+        int sum = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            uint32_t word = 0;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                int q = 0;
+                if (d != 0.0f) {
+                    q = int(roundf(__fdiv_rn(v[4 * i + e], d)));
+                    q = q > 127 ? 127 : (q < -127 ? -127 : q);
+                }
+                sum += q;
+                word |= (uint32_t(q) & 0xFFu) << (8 * e);
+            }
+            w[i] = word;
+        }
+        int8_t* qrow = out.qs + gr * N + gc;
+        *reinterpret_cast<uint4*>(qrow) = make_uint4(w[0], w[1], w[2], w[3]);
+        *reinterpret_cast<uint4*>(qrow + 16) = make_uint4(w[4], w[5], w[6], w[7]);
+        const int64_t bi = gr * (N / 32) + gc / 32;
+        out.da[bi] = d;
+        out.sa[bi] = sum;
+    }
+}
+
 // ------------------------------------------------------------------- host
 inline PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;

@@ -9,7 +9,12 @@ activation sets per input width is reused round-robin during the timed
 passes (every weight matrix is distinct, so nothing of the weight stream is
 served from L2).
 
-  python -m q4_q8_int8_gb300.tools.stack [--passes 3] [--path auto]
+With --fused every GEMM writes its result as q8_1 from its epilogue
+(mmq_q4K_gemm_q8_1 without the f32 output) and reads q8_1 activations that
+were quantized once before timing: the stack as it runs when each GEMM's
+output prepass is folded into the producing GEMM.
+
+  python -m q4_q8_int8_gb300.tools.stack [--passes 3] [--path auto] [--fused]
 """
 from __future__ import annotations
 
@@ -31,6 +36,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=1)
     ap.add_argument("--path", default="auto", choices=sorted(PATHS))
     ap.add_argument("--layers", type=int, default=synthetic.STACK_LAYERS)
+    ap.add_argument("--fused", action="store_true")
     args = ap.parse_args()
     build.build()
     mmq.load_library()
@@ -49,9 +55,17 @@ def main():
             _, xseed = synthetic.stack_seeds(i, 0 if K == 4096 else 6)
             xs.append(synthetic.torch_activations(M, K, xseed, dev, 0.01))
         pool[K] = (xs, [mmq.empty_q8_1(M, K, dev) for _ in xs])
-    outs = {N: torch.empty((M, N), device=dev) for N in sorted({N for _, _, N in synthetic.STACK_GEMMS})}
+    Ns = sorted({N for _, _, N in synthetic.STACK_GEMMS})
+    outs = {N: torch.empty((M, N), device=dev) for N in Ns}
+    outs_q8 = {N: mmq.q8_1_struct(*mmq.empty_q8_1(M, N, dev)) for N in Ns}
     sp = mmq._stream_ptr()
     structs = {K: [mmq.q8_1_struct(*aq) for aq in pool[K][1]] for K in pool}
+    if args.fused:   # activations quantized once, outside the timed passes
+        for K in pool:
+            for x, aqs in zip(pool[K][0], structs[K]):
+                rc = mmq.mmq_quantize_q8_1(ctypes.c_void_p(x.data_ptr()), M, K, aqs, sp)
+                if rc:
+                    raise mmq.MMQError(rc, "quantize")
 
     def one_pass(ev=None):
         for i, (K, N, w) in enumerate(weights):
@@ -59,13 +73,17 @@ def main():
             aqs = structs[K][i % 8]
             if ev is not None:
                 ev[i][0].record()
-            rc = mmq.mmq_quantize_q8_1(ctypes.c_void_p(x.data_ptr()), M, K, aqs, sp)
-            if rc:
-                raise mmq.MMQError(rc, "quantize")
+            if not args.fused:
+                rc = mmq.mmq_quantize_q8_1(ctypes.c_void_p(x.data_ptr()), M, K, aqs, sp)
+                if rc:
+                    raise mmq.MMQError(rc, "quantize")
             if ev is not None:
                 ev[i][1].record()
-            rc = mmq.mmq_q4K_gemm_path(aqs, ctypes.c_void_p(w.data_ptr()),
-                                       ctypes.c_void_p(outs[N].data_ptr()), M, N, K, path, sp)
+            if args.fused:
+                rc = mmq.mmq_q4K_gemm_q8_1(aqs, ctypes.c_void_p(w.data_ptr()), None, outs_q8[N], M, N, K, sp)
+            else:
+                rc = mmq.mmq_q4K_gemm_path(aqs, ctypes.c_void_p(w.data_ptr()),
+                                           ctypes.c_void_p(outs[N].data_ptr()), M, N, K, path, sp)
             if rc:
                 raise mmq.MMQError(rc, "gemm")
             if ev is not None:
@@ -95,7 +113,7 @@ def main():
     print(json.dumps({
         "workload": f"7B prefill stack: {args.layers} layers x (q,k,v,o 4096x4096; gate,up 4096->11008; "
                     f"down 11008->4096), M={M}",
-        "path": args.path, "passes": args.passes,
+        "path": args.path, "passes": args.passes, "fused_requantize": args.fused,
         "stack_ms": {"min": best, "median": sorted(t_stack)[len(t_stack) // 2], "max": max(t_stack)},
         "equivalent_tok_s": M / (best * 1e-3),
         "tmacs_with_prepass": macs / (best * 1e-3) / 1e12,
