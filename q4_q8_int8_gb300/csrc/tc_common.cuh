@@ -8,6 +8,7 @@
 
 #include <mutex>
 
+#include "q8_round.cuh"
 #include "sm103_ptx.cuh"
 
 namespace mmq {
@@ -146,8 +147,8 @@ __device__ __forceinline__ void store_tile(float* C, const uint64_t (&acc)[32], 
 
 // The same row x 64 columns quantized to q8_1 (two 32-column blocks of an
 // [M][N] q8_1 output, N % 32 == 0): per block amax, da = amax / 127 (IEEE
-// division), q = roundf(c / da) clamped to +-127, sa = sum of q; da == 0
-// gives q = 0 and sa = 0.  The same operation as the q8_1 prepass on the
+// division), q = roundf(c / da) (the quotient of IEEE division, as in the
+// prepass) clamped to +-127, sa = sum of q; da == 0 gives q = 0 and sa = 0.  The same operation as the q8_1 prepass on the
 // stored f32 values (web page "20 . r15 -- f32-accumulate mma probe (dead
 // end) + rank-1 term2 rescale", section 2.1, for the format).
 __device__ __forceinline__ void store_tile_q8_1(mmq_q8_1_t out, const uint64_t (&acc)[32], int M, int N,
@@ -168,6 +169,21 @@ __device__ __forceinline__ void store_tile_q8_1(mmq_q8_1_t out, const uint64_t (
 #pragma unroll
         for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
         const float d = __fdiv_rn(amax, 127.0f);
+        int qv[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) qv[i] = 0;   // a zero scale gives zero quants
+        if (d != 0.0f) {
+            // the prepass's rounding: reciprocal fast path, IEEE division where
+            // a quotient lies too close to a half-integer (or d is subnormal)
+            bool redo = d < 0x1p-126f;
+            const float r = __frcp_rn(d);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) qv[i] = q8::quant_fast(v[i], r, redo);
+            if (redo) {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) qv[i] = q8::quant_exact(v[i], d);
+            }
+        }
         uint32_t w[8];
         int sum = 0;
 #pragma unroll
@@ -175,11 +191,7 @@ __device__ __forceinline__ void store_tile_q8_1(mmq_q8_1_t out, const uint64_t (
             uint32_t word = 0;
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                int q = 0;
-                if (d != 0.0f) {
-                    q = int(roundf(__fdiv_rn(v[4 * i + e], d)));
-                    q = q > 127 ? 127 : (q < -127 ? -127 : q);
-                }
+                const int q = q8::clamp127(qv[4 * i + e]);
                 sum += q;
                 word |= (uint32_t(q) & 0xFFu) << (8 * e);
             }
