@@ -56,16 +56,18 @@ struct SmallMaps {
 };
 
 // Shared-memory layout for NF token fragments (mp = 8*NF tokens) and G warp
-// groups.  Group q owns one TMA stage and one work area:
+// groups.  Group q owns D TMA stages and one work area:
 //   stage  [0, kW) raw q4_K rows | [aoff, +2*mp*128) token quants as two
 //          128-byte-swizzled boxes | [doff, +mp*32) da [mp][8] | [soff, +mp*32) sa
 //   work   [0, NF*8*32*16) fp16 token fragments [f][c][lane] (4 x u32 each) |
 //          [fbytes, +8*NF*4*16) token scales [c][f][j] {da_t0, da_t1, dma_t0, dma_t1}
-// then the split-K landing area (partials pushed by cluster ranks 1..S-1:
-// [rank-1][128 threads][NF] float4), barriers and the abort flag.
+// With D = 2 stages a group's next super-block is in flight while it
+// computes the current one.  Then come the split-K landing area (partials
+// pushed by cluster ranks 1..S-1: [rank-1][128 threads][NF] float4), the
+// G*D stage barriers and the abort flag.
 struct Layout {
     int aoff, doff, soff, stage, fbytes, work, stages_off, work_off, red_off, bar_off, total;
-    __host__ __device__ static Layout make(int nf, int groups, int split) {
+    __host__ __device__ static Layout make(int nf, int groups, int depth, int split) {
         Layout L;
         const int mp = 8 * nf;
         L.aoff = ((kW + 1023) / 1024) * 1024;
@@ -75,10 +77,10 @@ struct Layout {
         L.fbytes = nf * 8 * 32 * 16;
         L.work = L.fbytes + 8 * nf * 4 * 16;
         L.stages_off = 0;
-        L.work_off = groups * L.stage;
+        L.work_off = groups * depth * L.stage;
         L.red_off = L.work_off + groups * L.work;
         L.bar_off = L.red_off + (split - 1) * 128 * nf * 16;
-        L.total = L.bar_off + 8 * groups + 16;
+        L.total = L.bar_off + 8 * groups * depth + 16;
         return L;
     }
 };
@@ -126,7 +128,7 @@ __device__ __forceinline__ void group_sync(int group) {   // the 4 warps (128 th
     asm volatile("bar.sync %0, 128;" ::"r"(group + 1) : "memory");
 }
 
-template <int NF, int G>
+template <int NF, int G, int D>
 __global__ void __launch_bounds__(G * 128)
 gemm_small_kernel(const __grid_constant__ SmallMaps maps, float* __restrict__ C, int M, int N,
                   int K, int split, int* status) {
@@ -135,9 +137,9 @@ gemm_small_kernel(const __grid_constant__ SmallMaps maps, float* __restrict__ C,
                                                ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
     constexpr int mp = NF * 8;
-    const Layout L = Layout::make(NF, G, split);
+    const Layout L = Layout::make(NF, G, D, split);
     const uint32_t bar0 = sbase + L.bar_off;
-    const AbortFlag abort_flag{sbase + uint32_t(L.bar_off + 8 * G)};
+    const AbortFlag abort_flag{sbase + uint32_t(L.bar_off + 8 * G * D)};
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int grp = warp >> 2, gt = threadIdx.x & 127;   // group, thread within the group
@@ -148,34 +150,38 @@ gemm_small_kernel(const __grid_constant__ SmallMaps maps, float* __restrict__ C,
     const int sb_begin = (nsb * rank) / split, sb_end = (nsb * (rank + 1)) / split;
     const int nmine = sb_end - sb_begin;
     const uint32_t stage_tx = uint32_t(kW + 2 * mp * 128 + 2 * mp * 32);
-    const uint32_t bar = bar0 + 8 * grp;
-    uint8_t* st = smem + L.stages_off + grp * L.stage;
-    const uint32_t st_s = sbase + L.stages_off + grp * L.stage;
+    // stage `slot` of this group and its barrier
+    auto stage_off = [&](int slot) { return L.stages_off + (grp * D + slot) * L.stage; };
+    auto stage_bar = [&](int slot) { return bar0 + 8u * uint32_t(grp * D + slot); };
     uint8_t* work = smem + L.work_off + grp * L.work;
 
     if (threadIdx.x == 0) {
-        for (int q = 0; q < G; ++q) mbar_init(bar0 + 8 * q, 1);
+        for (int q = 0; q < G * D; ++q) mbar_init(bar0 + 8 * q, 1);
         abort_flag.set(0u);
         fence_barrier_init();
         fence_proxy_async_smem();
     }
     __syncthreads();
 
-    // group leader issues the TMA of super-block sb_begin + i into its stage
+    // group leader issues the TMA of super-block sb_begin + i (the group's
+    // round (i - grp) / G) into stage round % D
+    int last_issued[D];   // leader only: last round issued into each stage
+#pragma unroll
+    for (int q = 0; q < D; ++q) last_issued[q] = -1;
     auto issue = [&](int i) {
         const int sb = sb_begin + i;
+        const int round = (i - grp) / G, slot = round % D;
+        const uint32_t bar = stage_bar(slot), st_s = sbase + uint32_t(stage_off(slot));
         mbar_arrive_expect_tx(bar, stage_tx);
         tma_load_2d(st_s, &maps.w, bar, sb * 144, n0);
         tma_load_2d(st_s + L.aoff, &maps.a, bar, sb * 256, 0);
         tma_load_2d(st_s + L.aoff + mp * 128, &maps.a, bar, sb * 256 + 128, 0);
         tma_load_2d(st_s + L.doff, &maps.da, bar, sb * 8, 0);
         tma_load_2d(st_s + L.soff, &maps.sa, bar, sb * 8, 0);
+        last_issued[slot] = round;
     };
-    int last_issued = -1;   // leader only
-    if (gt == 0 && grp < nmine) {
-        issue(grp);
-        last_issued = grp;
-    }
+    if (gt == 0)
+        for (int q = 0; q < D && grp + q * G < nmine; ++q) issue(grp + q * G);
 
     uint64_t acc[NF][2];   // per token fragment: rows g (tokens 2j, 2j+1) and g + 8
 #pragma unroll
@@ -184,9 +190,12 @@ gemm_small_kernel(const __grid_constant__ SmallMaps maps, float* __restrict__ C,
     const int r0 = (warp & 3) * 16 + g;   // this thread's weight rows r0 and r0 + 8 (within the CTA)
     int pass = 0;
     for (int i = grp; i < nmine; i += G, ++pass) {
+        const int slot = pass % D;
+        const uint8_t* st = smem + stage_off(slot);
         // A timed-out wait raises the CTA abort flag; the exit is decided after
         // a group barrier, so the group's threads leave together.
-        const bool landed = wait_bounded(bar, uint32_t(pass & 1), abort_flag, status);
+        const bool landed =
+            wait_bounded(stage_bar(slot), uint32_t((pass / D) & 1), abort_flag, status);
         if (landed) {
             // ---- tokens: fp16 fragments and (da, dma) once for the group
             for (int e = gt; e < NF * 8 * 32; e += 128) {
@@ -270,17 +279,19 @@ gemm_small_kernel(const __grid_constant__ SmallMaps maps, float* __restrict__ C,
                 }
             }
         }
-        group_sync(grp);   // the group is done reading its stage
+        group_sync(grp);   // the group is done reading this stage
         if (abort_flag.raised()) break;
-        if (gt == 0 && i + G < nmine) {
+        if (gt == 0 && i + D * G < nmine) {
             fence_proxy_async_smem();
-            issue(i + G);
-            last_issued = i + G;
+            issue(i + D * G);
         }
     }
-    if (gt == 0 && last_issued >= 0) {
-        // the group's last copy must land before its stage memory is reused or the CTA exits
-        wait_drain(bar, uint32_t(((last_issued - grp) / G) & 1), status);
+    if (gt == 0) {
+        // the group's last copies must land before its stage memory is reused or the CTA exits
+#pragma unroll
+        for (int q = 0; q < D; ++q)
+            if (last_issued[q] >= 0)
+                wait_drain(stage_bar(q), uint32_t((last_issued[q] / D) & 1), status);
     }
     __syncthreads();
 
@@ -471,7 +482,7 @@ bool encode(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t i
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int NF, int G>
+template <int NF, int G, int D>
 cudaError_t launch_nf(const SmallMaps& maps, float* C, int64_t M, int64_t N, int64_t K, int* status,
                       cudaStream_t s) {
     int dev = 0, nsm = 0, optin = 0;
@@ -488,11 +499,11 @@ cudaError_t launch_nf(const SmallMaps& maps, float* C, int64_t M, int64_t N, int
     const int64_t per_sm = NF == 1 ? 2 : 1;
     int split = 1;
     while (split < kMaxSplit && row_tiles * split * 2 <= per_sm * int64_t(nsm) && split * 2 <= nsb &&
-           Layout::make(NF, G, split * 2).total + 1024 <= optin)
+           Layout::make(NF, G, D, split * 2).total + 1024 <= optin)
         split *= 2;
-    const int smem = Layout::make(NF, G, split).total + 1024;   // + alignment slack
+    const int smem = Layout::make(NF, G, D, split).total + 1024;   // + alignment slack
     if (smem > optin) return cudaErrorInvalidConfiguration;
-    auto k = gemm_small_kernel<NF, G>;
+    auto k = gemm_small_kernel<NF, G, D>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
@@ -540,14 +551,14 @@ cudaError_t launch_gemm_small_m(mmq_q8_1_t aq, const uint8_t* w, float* C, int64
                 CU_TENSOR_MAP_SWIZZLE_NONE))
         return cudaErrorInvalidValue;
     switch (nf) {
-        case 1: return launch_nf<1, 4>(maps, C, M, N, K, status, s);
-        case 2: return launch_nf<2, 4>(maps, C, M, N, K, status, s);
-        case 3: return launch_nf<3, 4>(maps, C, M, N, K, status, s);
-        case 4: return launch_nf<4, 4>(maps, C, M, N, K, status, s);
-        case 5: return launch_nf<5, 2>(maps, C, M, N, K, status, s);
-        case 6: return launch_nf<6, 2>(maps, C, M, N, K, status, s);
-        case 7: return launch_nf<7, 2>(maps, C, M, N, K, status, s);
-        default: return launch_nf<8, 2>(maps, C, M, N, K, status, s);
+        case 1: return launch_nf<1, 4, 1>(maps, C, M, N, K, status, s);
+        case 2: return launch_nf<2, 4, 2>(maps, C, M, N, K, status, s);
+        case 3: return launch_nf<3, 4, 2>(maps, C, M, N, K, status, s);
+        case 4: return launch_nf<4, 4, 1>(maps, C, M, N, K, status, s);
+        case 5: return launch_nf<5, 2, 2>(maps, C, M, N, K, status, s);
+        case 6: return launch_nf<6, 2, 2>(maps, C, M, N, K, status, s);
+        case 7: return launch_nf<7, 2, 2>(maps, C, M, N, K, status, s);
+        default: return launch_nf<8, 2, 2>(maps, C, M, N, K, status, s);
     }
 }
 
