@@ -118,6 +118,9 @@ int mmq_q4K_gemm(mmq_q8_1_t aq, const uint8_t* bq4k, float* C, int64_t M,
 #define MMQ_PATH_SMALL_M 3  /* weight-streaming kernel for few tokens       */
 #define MMQ_PATH_TC_PAIR 4  /* tcgen05 kernel on CTA pairs (one M=256 MMA    */
                             /* over two SMs; 256 x 128 output tiles)        */
+#define MMQ_PATH_TC_SMALL 5 /* tcgen05 kernel for few tokens: 128 weight     */
+                            /* rows on the MMA's M side, 16/32/64 tokens on */
+                            /* its N side; accepts any M (token tiles of 64) */
 
 /* Same as mmq_q4K_gemm with an explicit kernel.  MMQ_ERR_ARG if `path` is
  * unknown or the kernel does not accept the shape (the small-M kernel takes

@@ -29,6 +29,7 @@ MMQ_PATH_MMA_S8 = 1
 MMQ_PATH_TC = 2
 MMQ_PATH_SMALL_M = 3
 MMQ_PATH_TC_PAIR = 4
+MMQ_PATH_TC_SMALL = 5
 SMALL_M_MAX = 64
 
 # Every symbol include/mmq.h declares.

@@ -158,6 +158,12 @@ static int run_gemm(mmq_q8_1_t aq, const uint8_t* w, float* C, int32_t* S, int64
         case MMQ_PATH_SMALL_M:
             if (S || M > mmq::kSmallMMax) return MMQ_ERR_ARG;
             return from_cuda(mmq::launch_gemm_small_m(aq, w, C, M, N, K, status, s));
+        case MMQ_PATH_TC_SMALL: {
+            if (S) return MMQ_ERR_ARG;
+            const int inject = t_inject_timeout;
+            t_inject_timeout = 0;
+            return from_cuda(mmq::launch_gemm_tc_small(aq, w, C, M, N, K, status, inject, s));
+        }
         default:
             return MMQ_ERR_ARG;
     }
@@ -170,7 +176,7 @@ int mmq_q4K_gemm(mmq_q8_1_t aq, const uint8_t* bq4k, float* C, int64_t M, int64_
 
 int mmq_q4K_gemm_path(mmq_q8_1_t aq, const uint8_t* bq4k, float* C, int64_t M, int64_t N,
                       int64_t K, int path, void* stream) {
-    if (path < MMQ_PATH_AUTO || path > MMQ_PATH_TC_PAIR) return MMQ_ERR_ARG;
+    if (path < MMQ_PATH_AUTO || path > MMQ_PATH_TC_SMALL) return MMQ_ERR_ARG;
     if (path == MMQ_PATH_SMALL_M && M > mmq::kSmallMMax) return MMQ_ERR_ARG;
     int rc = check_gemm_args(aq, bq4k, C, M, N, K);
     if (rc) return rc;

@@ -31,6 +31,10 @@ cudaError_t launch_gemm_tc2(mmq_q8_1_t aq, const uint8_t* w, float* C,
 cudaError_t launch_gemm_small_m(mmq_q8_1_t aq, const uint8_t* w, float* C,
                                 int64_t M, int64_t N, int64_t K, int* status,
                                 cudaStream_t s);
+// tcgen05 kernel for few tokens: 128 weight rows x 16/32/64 tokens per CTA.
+cudaError_t launch_gemm_tc_small(mmq_q8_1_t aq, const uint8_t* w, float* C,
+                                 int64_t M, int64_t N, int64_t K, int* status,
+                                 int inject_timeout, cudaStream_t s);
 constexpr int64_t kSmallMMax = 64;
 
 }  // namespace mmq

@@ -2,7 +2,9 @@
 // and the driver does not measure: the warp-level int8 tensor rate
 // (mma.sync m16n8k32 s8 -> s32) and the FP32 FMA rates (scalar and f32x2)
 // that bound the per-chunk rescale epilogue; tensor-memory load rates; and
-// the latencies of the tcgen05 GEMM's MMA-issue / mbarrier hand-off chain.
+// the latencies of the tcgen05 GEMM's MMA-issue / mbarrier hand-off chain,
+// the issue cost of one tcgen05 MMA by its N, and what an MMA-issuing
+// thread's loop of waits, MMAs and commits costs per operand stage.
 // Prints JSON lines.
 //
 // Each kernel runs long chains of independent instructions per warp on every
@@ -267,6 +269,132 @@ __global__ void __launch_bounds__(512, 1) handoff_loop(int iters, long long* out
     }
 }
 
+// ---- tcgen05 MMA issue cost by shape: one thread issues `nmma` f16 MMAs of
+// 128 x N x 16 back to back (accumulating into N columns), one commit, and
+// waits for it; out[0] = issue cycles, out[1] = cycles until the commit
+// arrived, summed over iterations.
+template <int N>
+__global__ void __launch_bounds__(128, 1) mma_burst(int iters, int nmma, long long* out) {
+    using namespace mmq::ptx;
+    extern __shared__ __align__(1024) uint8_t msm[];
+    uint8_t* s = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(msm) + 1023) & ~uintptr_t(1023));
+    const uint32_t sb = smem_u32(s);
+    uint32_t* slot = reinterpret_cast<uint32_t*>(s + 49152);
+    const uint32_t done = sb + 49152 + 64;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int i = threadIdx.x; i < 12288; i += blockDim.x) reinterpret_cast<uint32_t*>(s)[i] = 0;
+    if (threadIdx.x == 0) {
+        mbar_init(done, 1);
+        fence_barrier_init();
+    }
+    fence_proxy_async_smem();
+    __syncthreads();
+    if (warp == 0) {
+        tmem_alloc(smem_u32(slot), 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tb = *slot;
+    const uint32_t idesc = idesc_f16_f32(128, N);
+    const uint64_t dA = smem_desc_sw128(sb), dB = smem_desc_sw128(sb + 16384);
+    bool ok = true;
+    if (warp == 1 && lane == 0) {
+        long long tiss = 0, tall = 0;
+        for (int i = 0; i < iters && ok; ++i) {
+            const long long t0 = clock64_now();
+            for (int j = 0; j < nmma; ++j)
+                mma_f16(tb, dA + uint64_t(2 * (j & 3)), dB + uint64_t(2 * (j & 3)), idesc, uint32_t(j != 0));
+            mma_commit(done);
+            const long long t1 = clock64_now();
+            ok = spin_wait(done, uint32_t(i & 1));
+            tiss += t1 - t0;
+            tall += clock64_now() - t0;
+        }
+        out[0] = tiss;
+        out[1] = tall;
+    }
+    if (!ok) out[2] = 1;
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tb, 512);
+    }
+}
+
+// ---- the MMA-issuing thread's loop shape: per "operand stage" four
+// 128 x N x 16 MMAs from one of four rotating operand buffers into rotating
+// tensor-memory columns, with (kMode & 1) an mbarrier try_wait (on a phase
+// completed before the loop) and tcgen05.fence::after_thread_sync first,
+// (kMode & 2) the same only every fourth stage, (kMode & 4) two commits
+// after.  out[0] = issue cycles over all stages.  Every mbarrier here has
+// an arrival count of 1.
+template <int kMode, int N>
+__global__ void __launch_bounds__(128, 1) mma_stage_loop(int stages, long long* out) {
+    using namespace mmq::ptx;
+    extern __shared__ __align__(1024) uint8_t lsm[];
+    uint8_t* s = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(lsm) + 1023) & ~uintptr_t(1023));
+    const uint32_t sb = smem_u32(s);
+    constexpr int kOp = 16384 + N * 128, kNumOp = 4;
+    uint32_t* slot = reinterpret_cast<uint32_t*>(s + kNumOp * kOp);
+    const uint32_t bars = sb + kNumOp * kOp + 64;   // ready, done, 4 x c, 4 x d
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int i = threadIdx.x; i < kNumOp * kOp / 4; i += blockDim.x) reinterpret_cast<uint32_t*>(s)[i] = 0;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < 10; ++i) mbar_init(bars + 8 * i, 1);
+        fence_barrier_init();
+    }
+    fence_proxy_async_smem();
+    __syncthreads();
+    if (threadIdx.x == 0) mbar_arrive(bars);   // phase 0 of "ready" completes
+    if (warp == 0) {
+        tmem_alloc(smem_u32(slot), 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tb = *slot;
+    const uint32_t idesc = idesc_f16_f32(128, N);
+    bool ok = true;
+    if (warp == 1 && lane == 0) {
+        const long long t0 = clock64_now();
+        for (int st = 0; st < stages && ok; ++st) {
+            if ((kMode & 1) || ((kMode & 2) && (st & 3) == 0)) {
+                ok = spin_wait(bars, 0u);
+                tc_fence_after();
+            }
+            const uint64_t dA = smem_desc_sw128(sb + (st & 3) * kOp), dB = dA + uint64_t(16384 >> 4);
+            const uint32_t d0 = tb + uint32_t((st & (256 / (2 * N) - 1)) * 2 * N);
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+#pragma unroll
+                for (int kk = 0; kk < 2; ++kk)
+                    mma_f16(d0 + uint32_t(h * N), dA + uint64_t((h * 64 + kk * 32) >> 4),
+                            dB + uint64_t((h * 64 + kk * 32) >> 4), idesc, uint32_t(kk));
+            if (kMode & 4) {
+                mma_commit(bars + 16 + 8 * (st & 3));
+                mma_commit(bars + 48 + 8 * (st & 3));
+            }
+        }
+        mma_commit(bars + 8);
+        out[0] = clock64_now() - t0;
+        ok = ok && spin_wait(bars + 8, 0u);
+        out[1] = clock64_now() - t0;
+    }
+    if (!ok) out[2] = 1;
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tb, 512);
+    }
+}
+
 int main() {
     int dev = 0, nsm = 0, clk = 0;
     CK(cudaGetDevice(&dev));
@@ -369,6 +497,48 @@ int main() {
         run_h(handoff_loop<3>, 2048, "2-slot hand-off, commit without MMA, 8 consumer warps") ||
         run_h(handoff_loop<4>, 2048, "2-slot hand-off, plain arrive, 8 consumer warps") ||
         run_h(handoff_loop<5>, 2048, "2-slot hand-off, 4 MMAs + commit, 8 consumer warps"))
+        return 1;
+
+    // MMA issue cost by N (cycles per MMA on one SM)
+    auto run_m = [&](void (*k)(int, int, long long*), int n, int nmma) -> int {
+        const int smem = 49152 + 1024 + 128;
+        if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) return 1;
+        CK(cudaMemset(dl, 0, 3 * sizeof(long long)));
+        const int iters = 256;
+        k<<<1, 128, smem>>>(iters, nmma, dl);
+        CK(cudaDeviceSynchronize());
+        long long h[3];
+        CK(cudaMemcpy(h, dl, sizeof(h), cudaMemcpyDeviceToHost));
+        printf("{\"mma_burst\": \"128x%dx16 f16\", \"mmas\": %d, \"issue_cycles_per_mma\": %.1f, "
+               "\"cycles_per_mma\": %.1f, \"timed_out\": %lld}\n",
+               n, nmma, double(h[0]) / iters / nmma, double(h[1]) / iters / nmma, h[2]);
+        return 0;
+    };
+    for (int nmma : {4, 32})
+        if (run_m(mma_burst<16>, 16, nmma) || run_m(mma_burst<32>, 32, nmma) || run_m(mma_burst<64>, 64, nmma) ||
+            run_m(mma_burst<128>, 128, nmma) || run_m(mma_burst<256>, 256, nmma))
+            return 1;
+
+    // the MMA thread's loop shape (cycles per operand stage of four MMAs)
+    auto run_l = [&](void (*k)(int, long long*), const char* name) -> int {
+        const int smem = 4 * 32768 + 1024 + 512;   // four 32 KB operand buffers + barriers
+        if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) return 1;
+        CK(cudaMemset(dl, 0, 3 * sizeof(long long)));
+        const int stages = 64;
+        k<<<1, 128, smem>>>(stages, dl);
+        CK(cudaDeviceSynchronize());
+        long long h[3];
+        CK(cudaMemcpy(h, dl, sizeof(h), cudaMemcpyDeviceToHost));
+        printf("{\"mma_stage_loop\": \"%s\", \"issue_cycles_per_stage\": %.1f, \"timed_out\": %lld}\n", name,
+               double(h[0]) / stages, h[2]);
+        return 0;
+    };
+    if (run_l(mma_stage_loop<0, 16>, "N=16: four MMAs per stage") ||
+        run_l(mma_stage_loop<1, 16>, "N=16: + try_wait and fence per stage") ||
+        run_l(mma_stage_loop<2, 16>, "N=16: + try_wait and fence every fourth stage") ||
+        run_l(mma_stage_loop<5, 16>, "N=16: + try_wait, fence and two commits per stage") ||
+        run_l(mma_stage_loop<0, 128>, "N=128: four MMAs per stage") ||
+        run_l(mma_stage_loop<5, 128>, "N=128: + try_wait, fence and two commits per stage"))
         return 1;
     return 0;
 }

@@ -22,7 +22,7 @@ import q4_q8_int8_gb300 as mmq
 from q4_q8_int8_gb300 import build, synthetic
 
 PATHS = {"auto": mmq.MMQ_PATH_AUTO, "tc": mmq.MMQ_PATH_TC, "mma_s8": mmq.MMQ_PATH_MMA_S8,
-         "small_m": mmq.MMQ_PATH_SMALL_M}
+         "small_m": mmq.MMQ_PATH_SMALL_M, "tc_pair": mmq.MMQ_PATH_TC_PAIR, "tc_small": mmq.MMQ_PATH_TC_SMALL}
 
 
 def shapes():

@@ -118,6 +118,7 @@ def test_argument_errors_before_device(lib):
     assert mmq.mmq_q4K_gemm_path(good, w, C, 65, 4, 256, mmq.MMQ_PATH_SMALL_M, None) == mmq.MMQ_ERR_ARG
     assert mmq.mmq_q4K_gemm_path(good, w, C, 1, 4, 256, 9, None) == mmq.MMQ_ERR_ARG
     assert mmq.mmq_q4K_block_dots(good, w, C, 1, 4, 256, mmq.MMQ_PATH_SMALL_M, None) == mmq.MMQ_ERR_ARG
+    assert mmq.mmq_q4K_block_dots(good, w, C, 1, 4, 256, mmq.MMQ_PATH_TC_SMALL, None) == mmq.MMQ_ERR_ARG
     # alignment
     assert mmq.mmq_q4K_gemm(Q(0x10004, 0x20000, 0x30000), w, C, 1, 4, 256, None) == mmq.MMQ_ERR_ALIGN
     assert mmq.mmq_q4K_gemm(good, ctypes.c_void_p(0x40008), C, 1, 4, 256, None) == mmq.MMQ_ERR_ALIGN

@@ -11,11 +11,12 @@ from tests.gpu_util import require_gpu, to_dev
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("path_name", ["MMQ_PATH_TC", "MMQ_PATH_TC_PAIR"])
-def test_injected_timeout_is_reported_and_context_survives(path_name):
+@pytest.mark.parametrize("path_name,M", [("MMQ_PATH_TC", 128), ("MMQ_PATH_TC_PAIR", 128),
+                                         ("MMQ_PATH_TC_SMALL", 16), ("MMQ_PATH_TC_SMALL", 128)])
+def test_injected_timeout_is_reported_and_context_survives(path_name, M):
     mmq = require_gpu()
     path = getattr(mmq, path_name)
-    M, N, K = 128, 256, 512
+    N, K = 256, 512
     x = synthetic.activations(M, K, 5)
     blk = synthetic.q4K_weights(N, K, 6)
     aq = mmq.quantize_q8_1(to_dev(x))

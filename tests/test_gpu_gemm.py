@@ -77,7 +77,8 @@ def test_block_dots_extremes(path_name, sign):
     assert (S == sign * 60960).all()
 
 
-@pytest.mark.parametrize("path_name", ["MMQ_PATH_MMA_S8", "MMQ_PATH_TC", "MMQ_PATH_TC_PAIR"])
+@pytest.mark.parametrize("path_name", ["MMQ_PATH_MMA_S8", "MMQ_PATH_TC", "MMQ_PATH_TC_PAIR",
+                                       "MMQ_PATH_TC_SMALL"])
 @pytest.mark.parametrize("M,N,K", [(128, 256, 512), (77, 132, 768), (300, 388, 1280), (1, 4, 256),
                                    (64, 128, 2816)])
 def test_gemm_full_small(path_name, M, N, K):
@@ -87,15 +88,35 @@ def test_gemm_full_small(path_name, M, N, K):
     _full_check(x, blk, N, getattr(mmq, path_name))
 
 
-def test_gemm_small_m_full():
+@pytest.mark.parametrize("path_name", ["MMQ_PATH_SMALL_M", "MMQ_PATH_TC_SMALL"])
+def test_gemm_small_m_full(path_name):
     mmq = require_gpu()
-    for M in (1, 2, 3, 4, 5, 7, 8, 9, 16, 33, 64):
+    for M in (1, 2, 3, 4, 5, 7, 8, 9, 15, 16, 17, 31, 32, 33, 48, 63, 64):
         x = synthetic.activations(M, 1024, 71 + M, 0.01)
         blk = synthetic.q4K_weights(260, 1024, 81)
-        _full_check(x, blk, 260, mmq.MMQ_PATH_SMALL_M)
+        _full_check(x, blk, 260, getattr(mmq, path_name))
 
 
-@pytest.mark.parametrize("path_name", ["MMQ_PATH_MMA_S8", "MMQ_PATH_TC", "MMQ_PATH_TC_PAIR"])
+@pytest.mark.parametrize("M,N,K", [(1, 4096, 4096), (16, 4096, 4096), (64, 4096, 4096),
+                                   (40, 4096, 11008), (16, 11008, 4096), (9, 388, 256)])
+def test_tc_small_full_size_sampled(M, N, K):
+    # the few-token tcgen05 kernel at full decode / sweep sizes (cluster split-K up to 4)
+    mmq = require_gpu()
+    x = synthetic.activations(M, K, 111 + M, 0.01)
+    blk = synthetic.q4K_weights(N, K, 121 + K % 7)
+    _, aq, w = _dev_inputs(x, blk)
+    C = mmq.q4K_gemm(aq, w, N, path=mmq.MMQ_PATH_TC_SMALL).cpu().numpy()
+    assert mmq.status() == 0
+    assert np.isfinite(C).all()
+    q, da, sa = oracle.quantize_q8_1(x)
+    rows, cols = sample_points(M, N, 3000, 7)
+    C_ref, _, T = oracle.gemm_sampled(q, da, sa, blk, N, rows, cols)
+    ok = oracle.within_tolerance(C[rows, cols], C_ref, T, RTOL, ATOL)
+    assert ok.all(), f"{(~ok).sum()} sampled outputs outside tolerance"
+
+
+@pytest.mark.parametrize("path_name", ["MMQ_PATH_MMA_S8", "MMQ_PATH_TC", "MMQ_PATH_TC_PAIR",
+                                       "MMQ_PATH_TC_SMALL"])
 @pytest.mark.parametrize("name", ["q_proj", "down", "gate_up"])
 def test_gemm_full_size_sampled(path_name, name):
     mmq = require_gpu()
@@ -126,11 +147,11 @@ def test_gemm_sweep_auto_sampled(M):
 
 
 @pytest.mark.parametrize("path_name", ["MMQ_PATH_MMA_S8", "MMQ_PATH_TC", "MMQ_PATH_TC_PAIR",
-                                       "MMQ_PATH_SMALL_M"])
+                                       "MMQ_PATH_SMALL_M", "MMQ_PATH_TC_SMALL"])
 def test_every_output_written_and_deterministic(path_name):
     import torch
     mmq = require_gpu()
-    M, N, K = (37 if path_name == "MMQ_PATH_SMALL_M" else 200), 516, 1024
+    M, N, K = (37 if path_name in ("MMQ_PATH_SMALL_M", "MMQ_PATH_TC_SMALL") else 200), 516, 1024
     x = synthetic.activations(M, K, 91, 0.01)
     blk = synthetic.q4K_weights(N, K, 92)
     _, aq, w = _dev_inputs(x, blk)
@@ -149,7 +170,7 @@ def test_every_output_written_and_deterministic(path_name):
 
 
 @pytest.mark.parametrize("path_name", ["MMQ_PATH_MMA_S8", "MMQ_PATH_TC", "MMQ_PATH_TC_PAIR",
-                                       "MMQ_PATH_SMALL_M"])
+                                       "MMQ_PATH_SMALL_M", "MMQ_PATH_TC_SMALL"])
 def test_worked_examples_exact(path_name):
     mmq = require_gpu()
     path = getattr(mmq, path_name)
