@@ -42,8 +42,9 @@ def parse():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="mine", choices=["mine", "reference"])
     ap.add_argument("--workload", default="q_proj", choices=sorted(WORKLOADS))
-    ap.add_argument("--path", default="auto", choices=["auto", "mma_s8", "tc", "tc_pair", "small_m"])
+    ap.add_argument("--path", default="auto", choices=["auto", "mma_s8", "tc", "tc_pair", "small_m", "tc_small"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-control", action="store_true", help="skip the dequantize-then-dense control timing")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="target seconds of oracle work for the CPU baseline sample")
     return ap.parse_args()
@@ -276,7 +277,8 @@ def run_mine(args, rank, world, local_rank):
     mmq_build.build()
     mmq.load_library()
     path = {"auto": mmq.MMQ_PATH_AUTO, "mma_s8": mmq.MMQ_PATH_MMA_S8, "tc": mmq.MMQ_PATH_TC,
-            "tc_pair": mmq.MMQ_PATH_TC_PAIR, "small_m": mmq.MMQ_PATH_SMALL_M}[args.path]
+            "tc_pair": mmq.MMQ_PATH_TC_PAIR, "small_m": mmq.MMQ_PATH_SMALL_M,
+            "tc_small": mmq.MMQ_PATH_TC_SMALL}[args.path]
 
     M, K, N = WORKLOADS[args.workload]
     # Inputs: R independent sets rotated step by step so that every step reads
@@ -384,6 +386,52 @@ def run_mine(args, rank, world, local_rank):
         torch.distributed.all_reduce(te, op=torch.distributed.ReduceOp.MAX)
     e2e_ms = te.item()
 
+    # ---- the dequantize-then-dense control path on the same inputs (rank 0)
+    control = None
+    if rank == 0 and not args.no_control:
+        xh16 = [torch.empty((M, K), dtype=torch.float16, device=dev) for _ in range(R)]
+        wh16 = [torch.empty((N, K), dtype=torch.float16, device=dev) for _ in range(R)]
+
+        def ctrl_step(i, ev=None):
+            r = i % R
+            if ev is not None:
+                ev[0].record(stream)
+            mmq.convert_f16(xs[r], out=xh16[r], stream=stream)
+            if ev is not None:
+                ev[1].record(stream)
+            mmq.dequantize_q4K_f16(ws[r], N, K, out=wh16[r], stream=stream)
+            if ev is not None:
+                ev[2].record(stream)
+            mmq.gemm_f16(xh16[r], wh16[r], out=Cs[r], stream=stream)
+            if ev is not None:
+                ev[3].record(stream)
+
+        for i in range(3):
+            ctrl_step(i)
+        torch.cuda.synchronize(dev)
+        cn = max(3, min(args.steps, 20))
+        cev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(cn)]
+        for i in range(cn):
+            ctrl_step(3 + i, cev[i])
+        torch.cuda.synchronize(dev)
+        if mmq.status(stream) != 0:
+            raise RuntimeError("device status error in the control path")
+        c_conv = float(np.mean([e[0].elapsed_time(e[1]) for e in cev]))
+        c_deq = float(np.mean([e[1].elapsed_time(e[2]) for e in cev]))
+        c_gemm = float(np.mean([e[2].elapsed_time(e[3]) for e in cev]))
+        pk = measured_peaks()
+        control = {
+            "what": "x -> fp16, q4_K -> fp16 (dequantize), dense tcgen05 fp16 GEMM with f32 accumulation",
+            "convert_ms": c_conv, "dequant_ms": c_deq, "gemm_f16_ms": c_gemm,
+            "total_ms": c_conv + c_deq + c_gemm,
+            "gemm_f16_tflops": 2.0 * M * N * K / (c_gemm * 1e-3) / 1e12,
+            "gemm_f16_frac_of_burst": 2.0 * M * N * K / (c_gemm * 1e-3) / 1e12 / pk["bf16_tflops"],
+            "dequant_gbs": N * K * (0.5625 + 2) / (c_deq * 1e-3) / 1e9,
+            "convert_gbs": M * K * 6 / (c_conv * 1e-3) / 1e9,
+            "mmq_step_over_control": step_ms / (c_conv + c_deq + c_gemm),
+            "gpu_launches": 3 * cn,
+        }
+
     if rank != 0:
         if world > 1:
             torch.distributed.destroy_process_group()
@@ -400,7 +448,8 @@ def run_mine(args, rank, world, local_rank):
     kname = {mmq.MMQ_PATH_MMA_S8: ("gemm_mma_s8", "gemm_mma.cu"),
              mmq.MMQ_PATH_TC: ("gemm_tc", "gemm_tc.cu"),
              mmq.MMQ_PATH_TC_PAIR: ("gemm_tc2", "gemm_tc2.cu"),
-             mmq.MMQ_PATH_SMALL_M: ("gemm_small_m", "gemm_small.cu")}[used_path]
+             mmq.MMQ_PATH_SMALL_M: ("gemm_small_m", "gemm_small.cu"),
+             mmq.MMQ_PATH_TC_SMALL: ("gemm_tc_small", "gemm_tc_small.cu")}[used_path]
     src_hash = kernel_source_hash([kname[1], "sm103_ptx.cuh"])
     traffic = recorded_traffic(kname[0], src_hash)
     alg_bytes = 0.5625 * N * K + 1.25 * M * K + 4 * M * N
@@ -410,7 +459,7 @@ def run_mine(args, rank, world, local_rank):
         roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
                 "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json hbm copy)"}
-    elif used_path in (mmq.MMQ_PATH_TC, mmq.MMQ_PATH_TC_PAIR):
+    elif used_path in (mmq.MMQ_PATH_TC, mmq.MMQ_PATH_TC_PAIR, mmq.MMQ_PATH_TC_SMALL):
         # The exact integer contraction runs on the tensor pipe as kind::f16
         # MMAs (2 flops per MAC); the kernel is timed inside a long loop, so
         # the denominator is the sustained measured bf16 (= f16 rate) peak.
@@ -434,6 +483,8 @@ def run_mine(args, rank, world, local_rank):
     # per super-block one FMA for d and one add of the second term (0.5 flop
     # per chunk); the other kernels do the pages' 1 FMUL + 2 FFMA (5 flops).
     alu_flops = (2.5 if used_path in (mmq.MMQ_PATH_TC, mmq.MMQ_PATH_TC_PAIR) else 5.0) * macs / 32
+    if used_path == mmq.MMQ_PATH_TC_SMALL:
+        alu_flops = 4.0 * macs / 32   # one FMA with da and one with dma * dmv per output and chunk
     alu_peak = micro["sms"] * 128 * 2 * sm_mhz * 1e6 / 1e12
     alu = {"flops_per_launch": alu_flops, "achieved_tflops": alu_flops / (g_ms * 1e-3) / 1e12,
            "peak_tflops": alu_peak, "frac": alu_flops / (g_ms * 1e-3) / 1e12 / alu_peak,
@@ -455,7 +506,8 @@ def run_mine(args, rank, world, local_rank):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "int8xu4->f32 (fp16-exact ints on tensor cores)"
-        if used_path in (mmq.MMQ_PATH_TC, mmq.MMQ_PATH_TC_PAIR) else "s8xs8->s32, f32 rescale",
+        if used_path in (mmq.MMQ_PATH_TC, mmq.MMQ_PATH_TC_PAIR, mmq.MMQ_PATH_TC_SMALL)
+        else "s8xs8->s32, f32 rescale",
         "data": "synthetic",
         "config": {"workload": f"{args.workload} M={M} K={K} N={N}", "global_batch_tokens": M * world,
                    "parallelism": f"independent problem per GPU x{world}",
@@ -474,6 +526,7 @@ def run_mine(args, rank, world, local_rank):
                 "h2d_bytes_per_step": M * K * 4, "d2h_bytes_per_step": M * N * 4,
                 "ms_per_step": e2e_ms},
         "gpu_launches": 2 * args.steps,
+        "control": control,
         "clocks": clk,
         "clocks_window": "from warm-up start to timed-region end",
         "wall_s_timed": wall,

@@ -149,6 +149,33 @@ int mmq_q4K_gemm_q8_1(mmq_q8_1_t aq, const uint8_t* bq4k, float* C, mmq_q8_1_t o
 int mmq_q4K_block_dots(mmq_q8_1_t aq, const uint8_t* bq4k, int32_t* S,
                        int64_t M, int64_t N, int64_t K, int path, void* stream);
 
+/* ---- The dequantize-then-dense control path (the f16 GEMM path the pages
+ * measure MMQ against: page r12, the landing note comparing MMQ with the f16
+ * default GEMM path; its dequantize step a bandwidth kernel as audited on
+ * page "Round 31 Track C Audit: dq_f16 (dense_mm.metal) & DW<F>
+ * (mma.metal)", section 2.1).  fp16 values travel as their uint16_t bits. */
+
+/* q4_K weights -> fp16, row-major [N][K] (caller-owned, N*K*2 bytes): element
+ * k of sub-block c of a super-block is fp16(f32(d*sc_c*v_k - dmin*m_c)), the
+ * difference rounded once to f32 (both products are exact in f32) and then
+ * to fp16, round to nearest even both times.  N >= 1, K % 256 == 0;
+ * pointers 16-byte aligned.  Bit-for-bit reproducible. */
+int mmq_dequantize_q4K_f16(const uint8_t* bq4k, uint16_t* wh, int64_t N,
+                           int64_t K, void* stream);
+
+/* x float[n] -> fp16 (round to nearest even); n % 4 == 0, pointers 16-byte
+ * aligned. */
+int mmq_convert_f32_f16(const float* x, uint16_t* xh, int64_t n, void* stream);
+
+/* Dense C[M][N] = A[M][K] . B[N][K]^T with fp16 A, B (row-major, K
+ * contiguous) and f32 C (row-major, overwritten), on the tcgen05 tensor cores
+ * with f32 accumulation.  M, N >= 1, N % 4 == 0, K % 64 == 0; pointers
+ * 16-byte aligned.  Each C value is the sum of K exact products accumulated
+ * in f32; results are bitwise deterministic run to run.  MMQ_ERR_RESOURCE if
+ * the device's shared memory per block is too small. */
+int mmq_gemm_f16(const uint16_t* A, const uint16_t* B, float* C, int64_t M,
+                 int64_t N, int64_t K, void* stream);
+
 /* Synchronizes `stream`, then returns and clears the current device's status
  * word: MMQ_OK, or MMQ_ERR_DEVICE_TIMEOUT if a kernel's bounded wait gave up
  * since the last call (that kernel's output is then invalid), or

@@ -36,6 +36,7 @@ SMALL_M_MAX = 64
 EXPORTS = (
     "mmq_q8_1_bytes", "mmq_q8_1_view", "mmq_quantize_q8_1", "mmq_q4K_bytes",
     "mmq_pack_q4K", "mmq_q4K_gemm", "mmq_q4K_gemm_path", "mmq_q4K_gemm_q8_1", "mmq_q4K_block_dots",
+    "mmq_dequantize_q4K_f16", "mmq_convert_f32_f16", "mmq_gemm_f16",
     "mmq_status", "mmq_strerror", "mmq_debug_inject_timeout",
 )
 
@@ -74,6 +75,9 @@ def load_library(path: str = LIB_PATH):
                 "mmq_q4K_gemm_path": ([Q, P, P, I, I, I, ctypes.c_int, P], ctypes.c_int),
                 "mmq_q4K_gemm_q8_1": ([Q, P, P, Q, I, I, I, P], ctypes.c_int),
                 "mmq_q4K_block_dots": ([Q, P, P, I, I, I, ctypes.c_int, P], ctypes.c_int),
+                "mmq_dequantize_q4K_f16": ([P, P, I, I, P], ctypes.c_int),
+                "mmq_convert_f32_f16": ([P, P, I, P], ctypes.c_int),
+                "mmq_gemm_f16": ([P, P, P, I, I, I, P], ctypes.c_int),
                 "mmq_status": ([P], ctypes.c_int),
                 "mmq_strerror": ([ctypes.c_int], ctypes.c_char_p),
                 "mmq_debug_inject_timeout": ([ctypes.c_int], None),
@@ -209,6 +213,47 @@ def q4K_block_dots(aq, w, N: int, path: int = MMQ_PATH_MMA_S8, out=None, stream=
                               ctypes.c_void_p(S.data_ptr()), M, N, K, path, _stream_ptr(stream)),
            "mmq_q4K_block_dots")
     return S
+
+
+def mmq_dequantize_q4K_f16(bq4k, wh, N, K, stream):
+    return load_library().mmq_dequantize_q4K_f16(bq4k, wh, N, K, stream)
+
+
+def mmq_convert_f32_f16(x, xh, n, stream):
+    return load_library().mmq_convert_f32_f16(x, xh, n, stream)
+
+
+def mmq_gemm_f16(A, B, C, M, N, K, stream):
+    return load_library().mmq_gemm_f16(A, B, C, M, N, K, stream)
+
+
+def dequantize_q4K_f16(w, N: int, K: int, out=None, stream=None):
+    """q4_K bytes of an N x K matrix (CUDA uint8) -> float16 [N][K]."""
+    import torch
+    wh = out if out is not None else torch.empty((N, K), dtype=torch.float16, device=w.device)
+    _check(mmq_dequantize_q4K_f16(ctypes.c_void_p(w.data_ptr()), ctypes.c_void_p(wh.data_ptr()), N, K,
+                                  _stream_ptr(stream)), "mmq_dequantize_q4K_f16")
+    return wh
+
+
+def convert_f16(x, out=None, stream=None):
+    """float32 CUDA tensor -> float16 of the same shape (round to nearest even)."""
+    import torch
+    xh = out if out is not None else torch.empty(x.shape, dtype=torch.float16, device=x.device)
+    _check(mmq_convert_f32_f16(ctypes.c_void_p(x.data_ptr()), ctypes.c_void_p(xh.data_ptr()), x.numel(),
+                               _stream_ptr(stream)), "mmq_convert_f32_f16")
+    return xh
+
+
+def gemm_f16(a, b, out=None, stream=None):
+    """a float16 [M][K], b float16 [N][K] (CUDA) -> a . b^T as float32 [M][N]."""
+    import torch
+    M, K = a.shape
+    N = b.shape[0]
+    C = out if out is not None else torch.empty((M, N), dtype=torch.float32, device=a.device)
+    _check(mmq_gemm_f16(ctypes.c_void_p(a.data_ptr()), ctypes.c_void_p(b.data_ptr()),
+                        ctypes.c_void_p(C.data_ptr()), M, N, K, _stream_ptr(stream)), "mmq_gemm_f16")
+    return C
 
 
 def status(stream=None) -> int:

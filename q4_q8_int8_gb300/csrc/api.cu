@@ -208,6 +208,41 @@ int mmq_q4K_block_dots(mmq_q8_1_t aq, const uint8_t* bq4k, int32_t* S, int64_t M
     return run_gemm(aq, bq4k, nullptr, S, M, N, K, path, static_cast<cudaStream_t>(stream));
 }
 
+int mmq_dequantize_q4K_f16(const uint8_t* bq4k, uint16_t* wh, int64_t N, int64_t K, void* stream) {
+    if (!bq4k || !wh) return MMQ_ERR_ARG;
+    if (N < 1 || K < 256 || (K % 256) != 0) return MMQ_ERR_ARG;
+    if (N > (int64_t(1) << 31) - 1 || K > (int64_t(1) << 31) - 1 || N * (K / 64) > (int64_t(1) << 36))
+        return MMQ_ERR_ARG;
+    if (!aligned16(bq4k) || !aligned16(wh)) return MMQ_ERR_ALIGN;
+    int rc = check_device();
+    if (rc) return rc;
+    return from_cuda(mmq::launch_dequantize_q4K_f16(bq4k, wh, N, K, static_cast<cudaStream_t>(stream)));
+}
+
+int mmq_convert_f32_f16(const float* x, uint16_t* xh, int64_t n, void* stream) {
+    if (!x || !xh) return MMQ_ERR_ARG;
+    if (n < 4 || (n % 4) != 0 || n > (int64_t(1) << 38)) return MMQ_ERR_ARG;
+    if (!aligned16(x) || !aligned16(xh)) return MMQ_ERR_ALIGN;
+    int rc = check_device();
+    if (rc) return rc;
+    return from_cuda(mmq::launch_convert_f16(x, xh, n, static_cast<cudaStream_t>(stream)));
+}
+
+int mmq_gemm_f16(const uint16_t* A, const uint16_t* B, float* C, int64_t M, int64_t N, int64_t K,
+                 void* stream) {
+    if (!A || !B || !C) return MMQ_ERR_ARG;
+    if (M < 1 || N < 1 || K < 64 || (K % 64) != 0 || (N % 4) != 0) return MMQ_ERR_ARG;
+    if (M > (int64_t(1) << 31) - 1 || N > (int64_t(1) << 31) - 1 || K > (int64_t(1) << 31) - 1)
+        return MMQ_ERR_ARG;
+    if (!aligned16(A) || !aligned16(B) || !aligned16(C)) return MMQ_ERR_ALIGN;
+    int rc = check_device();
+    if (rc) return rc;
+    if ((rc = mmq::dense_gemm_check_resources())) return rc;
+    int* status = mmq::status_word_ptr();
+    if (!status) return MMQ_ERR_CUDA;
+    return from_cuda(mmq::launch_gemm_f16(A, B, C, M, N, K, status, static_cast<cudaStream_t>(stream)));
+}
+
 int mmq_status(void* stream) {
     int* p = mmq::status_word_ptr();
     if (!p) return MMQ_ERR_CUDA;

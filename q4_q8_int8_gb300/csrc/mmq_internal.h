@@ -35,6 +35,13 @@ cudaError_t launch_gemm_small_m(mmq_q8_1_t aq, const uint8_t* w, float* C,
 cudaError_t launch_gemm_tc_small(mmq_q8_1_t aq, const uint8_t* w, float* C,
                                  int64_t M, int64_t N, int64_t K, int* status,
                                  int inject_timeout, cudaStream_t s);
+// The dequantize-then-dense control path (dense.cu).
+cudaError_t launch_dequantize_q4K_f16(const uint8_t* w, uint16_t* out, int64_t N, int64_t K,
+                                      cudaStream_t s);
+cudaError_t launch_convert_f16(const float* x, uint16_t* out, int64_t n, cudaStream_t s);
+int dense_gemm_check_resources();   // MMQ_OK or MMQ_ERR_RESOURCE
+cudaError_t launch_gemm_f16(const uint16_t* A, const uint16_t* B, float* C, int64_t M, int64_t N,
+                            int64_t K, int* status, cudaStream_t s);
 constexpr int64_t kSmallMMax = 64;
 
 }  // namespace mmq

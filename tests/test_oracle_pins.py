@@ -276,3 +276,71 @@ class TestGemmExamples:
         cols = rng.integers(0, N, 40)
         Cs, C64s, Ts = oracle.gemm_sampled(q, da, sa, blk, N, rows, cols)
         assert (Cs == C[rows, cols]).all() and (C64s == C64[rows, cols]).all() and (Ts == T[rows, cols]).all()
+
+
+# ---------------------------------------------------------------------------
+# Control path (dequantize to fp16, dense GEMM): oracle.dense
+# ---------------------------------------------------------------------------
+def _golden_dequant_rows():
+    rows = []
+    for line in open(os.path.join(os.path.dirname(__file__), "golden", "dequant_f16_values.txt")):
+        line = line.strip()
+        if not line or line.startswith("#"):
+            continue
+        f = line.split()
+        rows.append((int(f[0], 16), int(f[1], 16), int(f[2]), int(f[3]), int(f[4]), float(f[5])))
+    return rows
+
+
+def test_dense_dequant_golden_values():
+    from oracle import dense
+    rows = _golden_dequant_rows()
+    assert len(rows) >= 5
+    N, K = len(rows), 256
+    d = np.array([[np.array(r[0], np.uint16).view(np.float16)] for r in rows])
+    dmin = np.array([[np.array(r[1], np.uint16).view(np.float16)] for r in rows])
+    sc = np.array([[r[2]] * 8 for r in rows])
+    m = np.array([[r[3]] * 8 for r in rows])
+    v = np.array([[r[4]] * K for r in rows])
+    blk = q4k_layout.encode(d, dmin, sc, m, v)
+    w = dense.dequantize_q4K_f16(blk, N, K)
+    assert w.dtype == np.float16
+    for j, r in enumerate(rows):
+        assert (w[j] == np.float16(r[5])).all(), (r, w[j][:4])
+
+
+def test_dense_dequant_matches_fraction_definition():
+    # random fields: fp16(float32-rounded exact difference) computed with Fractions
+    from fractions import Fraction
+    from oracle import dense
+    rng = np.random.default_rng(11)
+    N, K = 6, 512
+    d = rng.uniform(1e-3, 4.0, (N, 2)).astype(np.float16)
+    dmin = rng.uniform(1e-3, 4.0, (N, 2)).astype(np.float16)
+    sc = rng.integers(0, 64, (N, 16))
+    m = rng.integers(0, 64, (N, 16))
+    v = rng.integers(0, 16, (N, K))
+    blk = q4k_layout.encode(d, dmin, sc, m, v)
+    w = dense.dequantize_q4K_f16(blk, N, K)
+    for j in range(N):
+        for k in range(0, K, 7):
+            sb, c = k // 256, k // 32
+            exact = (Fraction(float(d[j, sb])) * int(sc[j, c]) * int(v[j, k])
+                     - Fraction(float(dmin[j, sb])) * int(m[j, c]))
+            f32 = np.float32(float(exact))      # exact fits a double; one rounding to float32
+            assert w[j, k] == np.float16(f32), (j, k, exact)
+
+
+def test_dense_gemm_integer_matrices_exact():
+    # small integers are exact in fp16 and every sum is exact in float64
+    from oracle import dense
+    rng = np.random.default_rng(12)
+    A = rng.integers(-8, 9, (5, 64))
+    B = rng.integers(-8, 9, (3, 64))
+    C, T = dense.gemm_f16(A.astype(np.float16), B.astype(np.float16))
+    assert C.shape == (5, 3)
+    assert (C == A @ B.T).all()
+    assert (T == np.abs(A) @ np.abs(B).T).all()
+    Cs, Ts = dense.gemm_f16_sampled(A.astype(np.float16), B.astype(np.float16), [4, 0, 2], [0, 2, 1])
+    assert (Cs == np.array([C[4, 0], C[0, 2], C[2, 1]])).all()
+    assert (Ts == np.array([T[4, 0], T[0, 2], T[2, 1]])).all()
