@@ -141,6 +141,29 @@ int mmq_q4K_gemm_path(mmq_q8_1_t aq, const uint8_t* bq4k, float* C, int64_t M,
 int mmq_q4K_gemm_q8_1(mmq_q8_1_t aq, const uint8_t* bq4k, float* C, mmq_q8_1_t out,
                       int64_t M, int64_t N, int64_t K, void* stream);
 
+/* The gate and up projections of a SwiGLU FFN block in one GEMM, with the
+ * activation and the q8_1 quantization of its output in the epilogue, so
+ * that the down projection gets its q8_1 input with no separate pass (the
+ * fused-neighbour idea of page r12's prepass/transpose work).  bq4k_gu holds
+ * the q4_K bytes of a 2F x K matrix whose rows alternate gate row f and up
+ * row f (mmq_interleave_rows_q4K builds it once, at load time).  With g, u
+ * the two GEMM results (the same arithmetic as mmq_q4K_gemm), the output is
+ *     h = silu(g) * u = g / (1 + exp(-g)) * u           (f32, IEEE ops)
+ * quantized to q8_1 exactly as mmq_quantize_q8_1 would quantize h: `out`
+ * describes an [M][F] q8_1 buffer.  hf (may be NULL) receives h, f32
+ * [M][F].  F % 32 == 0; other rules as mmq_q4K_gemm (N = 2F).  Runs the
+ * tcgen05 kernel for every M. */
+int mmq_q4K_gemm_swiglu_q8_1(mmq_q8_1_t aq, const uint8_t* bq4k_gu, float* hf,
+                             mmq_q8_1_t out, int64_t M, int64_t F, int64_t K,
+                             void* stream);
+
+/* out = the rows of gate and up (q4_K bytes, F x K each) interleaved: row 2f
+ * of out is gate row f, row 2f + 1 up row f.  Any mix of host and device
+ * pointers (two strided copies on `stream`); out is 2 * F * (K/256) * 144
+ * bytes. */
+int mmq_interleave_rows_q4K(const uint8_t* gate, const uint8_t* up, uint8_t* out,
+                            int64_t F, int64_t K, void* stream);
+
 /* Debug/test dump of the exact per-chunk integer dots (page r15 section 2.1:
  * S_ij = sum_k a_int[i,k] * v[j,k]; section 2.3: |S| <= 32*127*15) computed
  * by the same unpack and MMA code as the GEMM kernel selected by `path`

@@ -37,6 +37,7 @@ EXPORTS = (
     "mmq_q8_1_bytes", "mmq_q8_1_view", "mmq_quantize_q8_1", "mmq_q4K_bytes",
     "mmq_pack_q4K", "mmq_q4K_gemm", "mmq_q4K_gemm_path", "mmq_q4K_gemm_q8_1", "mmq_q4K_block_dots",
     "mmq_dequantize_q4K_f16", "mmq_convert_f32_f16", "mmq_gemm_f16",
+    "mmq_q4K_gemm_swiglu_q8_1", "mmq_interleave_rows_q4K",
     "mmq_status", "mmq_strerror", "mmq_debug_inject_timeout",
 )
 
@@ -78,6 +79,8 @@ def load_library(path: str = LIB_PATH):
                 "mmq_dequantize_q4K_f16": ([P, P, I, I, P], ctypes.c_int),
                 "mmq_convert_f32_f16": ([P, P, I, P], ctypes.c_int),
                 "mmq_gemm_f16": ([P, P, P, I, I, I, P], ctypes.c_int),
+                "mmq_q4K_gemm_swiglu_q8_1": ([Q, P, P, Q, I, I, I, P], ctypes.c_int),
+                "mmq_interleave_rows_q4K": ([P, P, P, I, I, P], ctypes.c_int),
                 "mmq_status": ([P], ctypes.c_int),
                 "mmq_strerror": ([ctypes.c_int], ctypes.c_char_p),
                 "mmq_debug_inject_timeout": ([ctypes.c_int], None),
@@ -225,6 +228,39 @@ def mmq_convert_f32_f16(x, xh, n, stream):
 
 def mmq_gemm_f16(A, B, C, M, N, K, stream):
     return load_library().mmq_gemm_f16(A, B, C, M, N, K, stream)
+
+
+def mmq_q4K_gemm_swiglu_q8_1(aq, bq4k_gu, hf, out, M, F, K, stream):
+    return load_library().mmq_q4K_gemm_swiglu_q8_1(aq, bq4k_gu, hf, out, M, F, K, stream)
+
+
+def mmq_interleave_rows_q4K(gate, up, out, F, K, stream):
+    return load_library().mmq_interleave_rows_q4K(gate, up, out, F, K, stream)
+
+
+def interleave_rows_q4K(gate, up, F: int, K: int, out=None, stream=None):
+    """gate, up: q4_K bytes of F x K matrices (CUDA uint8) -> rows interleaved (2F x K)."""
+    import torch
+    o = out if out is not None else torch.empty(2 * gate.numel(), dtype=torch.uint8, device=gate.device)
+    _check(mmq_interleave_rows_q4K(ctypes.c_void_p(gate.data_ptr()), ctypes.c_void_p(up.data_ptr()),
+                                   ctypes.c_void_p(o.data_ptr()), F, K, _stream_ptr(stream)),
+           "mmq_interleave_rows_q4K")
+    return o
+
+
+def q4K_gemm_swiglu_q8_1(aq, w_gu, F: int, with_h: bool = False, out=None, stream=None):
+    """silu(x.gate^T) * (x.up^T) quantized to q8_1 ([M][F] triple); w_gu from
+    interleave_rows_q4K.  Returns (h f32 or None, (qs, da, sa))."""
+    import torch
+    qs, da, sa = aq
+    M, K = qs.shape
+    h = torch.empty((M, F), dtype=torch.float32, device=qs.device) if with_h else None
+    o = out if out is not None else empty_q8_1(M, F, qs.device)
+    _check(mmq_q4K_gemm_swiglu_q8_1(q8_1_struct(qs, da, sa), ctypes.c_void_p(w_gu.data_ptr()),
+                                    ctypes.c_void_p(h.data_ptr() if h is not None else 0), q8_1_struct(*o),
+                                    M, F, K, _stream_ptr(stream)),
+           "mmq_q4K_gemm_swiglu_q8_1")
+    return h, o
 
 
 def dequantize_q4K_f16(w, N: int, K: int, out=None, stream=None):

@@ -200,6 +200,37 @@ int mmq_q4K_gemm_q8_1(mmq_q8_1_t aq, const uint8_t* bq4k, float* C, mmq_q8_1_t o
     return run_gemm(aq, bq4k, C, nullptr, M, N, K, MMQ_PATH_TC, s, out);
 }
 
+int mmq_q4K_gemm_swiglu_q8_1(mmq_q8_1_t aq, const uint8_t* bq4k_gu, float* hf, mmq_q8_1_t out, int64_t M,
+                             int64_t F, int64_t K, void* stream) {
+    int rc = check_q8(out);
+    if (rc) return rc;
+    if (F < 32 || (F % 32) != 0 || F > (int64_t(1) << 30)) return MMQ_ERR_ARG;
+    if ((rc = check_gemm_args(aq, bq4k_gu, out.qs, M, 2 * F, K))) return rc;
+    if (hf && !aligned16(hf)) return MMQ_ERR_ALIGN;
+    if ((rc = mmq::tc_gemm_check_resources())) return rc;
+    int* status = mmq::status_word_ptr();
+    if (!status) return MMQ_ERR_CUDA;
+    const int inject = t_inject_timeout;
+    t_inject_timeout = 0;
+    return from_cuda(mmq::launch_gemm_tc(aq, bq4k_gu, hf, out, nullptr, M, 2 * F, K, status, inject,
+                                         static_cast<cudaStream_t>(stream), true));
+}
+
+int mmq_interleave_rows_q4K(const uint8_t* gate, const uint8_t* up, uint8_t* out, int64_t F, int64_t K,
+                            void* stream) {
+    if (!gate || !up || !out) return MMQ_ERR_ARG;
+    if (F < 1 || K < 256 || (K % 256) != 0 || F > (int64_t(1) << 30) || K > (int64_t(1) << 31) - 1)
+        return MMQ_ERR_ARG;
+    int rc = check_device();
+    if (rc) return rc;
+    const size_t pitch = size_t(K / 256) * 144;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaMemcpy2DAsync(out, 2 * pitch, gate, pitch, pitch, size_t(F), cudaMemcpyDefault, s);
+    if (e == cudaSuccess)
+        e = cudaMemcpy2DAsync(out + pitch, 2 * pitch, up, pitch, pitch, size_t(F), cudaMemcpyDefault, s);
+    return from_cuda(e);
+}
+
 int mmq_q4K_block_dots(mmq_q8_1_t aq, const uint8_t* bq4k, int32_t* S, int64_t M, int64_t N,
                        int64_t K, int path, void* stream) {
     if (path != MMQ_PATH_MMA_S8 && path != MMQ_PATH_TC && path != MMQ_PATH_TC_PAIR) return MMQ_ERR_ARG;

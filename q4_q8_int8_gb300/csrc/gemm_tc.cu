@@ -134,9 +134,11 @@ struct Bars {
     __device__ uint32_t min_empty() const { return at(kMin0 + 1); }
 };
 
+// kGlu: the weight rows alternate gate / up rows; write SwiGLU(gate, up)
+// quantized to q8_1 (and, if C is not null, as f32 [M][N/2] into C).
 // kDump: write the exact block dots S instead of C; kQ8: also (or only, C
 // == nullptr) write the result quantized to q8_1.
-template <bool kDump, bool kQ8>
+template <bool kDump, bool kQ8, bool kGlu = false>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_tc_kernel(const __grid_constant__ TmaMaps maps, float* __restrict__ C, mmq_q8_1_t q8out,
                int32_t* __restrict__ S, int M, int N, int K, int split, int* status, int inject_timeout) {
@@ -562,8 +564,12 @@ gemm_tc_kernel(const __grid_constant__ TmaMaps maps, float* __restrict__ C, mmq_
                 sr.next();
             }
             if (!kDump && split == 1) {
-                if (!kQ8 || C) store_tile(C, acc, M, N, m0, n0, row, colhalf);
-                if (kQ8) store_tile_q8_1(q8out, acc, M, N, m0, n0, row, colhalf);
+                if (kGlu) {
+                    store_tile_swiglu_q8_1(q8out, C, acc, M, N / 2, m0, n0, row, colhalf);
+                } else {
+                    if (!kQ8 || C) store_tile(C, acc, M, N, m0, n0, row, colhalf);
+                    if (kQ8) store_tile_q8_1(q8out, acc, M, N, m0, n0, row, colhalf);
+                }
             }
         }
     epi_done:;
@@ -588,8 +594,12 @@ gemm_tc_kernel(const __grid_constant__ TmaMaps maps, float* __restrict__ C, mmq_
                     }
                 }
                 const int m0 = (tile_first / tiles_n) * BM, n0 = (tile_first % tiles_n) * BN;
-                if (!kQ8 || C) store_tile(C, acc, M, N, m0, n0, row, colhalf);
-                if (kQ8) store_tile_q8_1(q8out, acc, M, N, m0, n0, row, colhalf);
+                if (kGlu) {
+                    store_tile_swiglu_q8_1(q8out, C, acc, M, N / 2, m0, n0, row, colhalf);
+                } else {
+                    if (!kQ8 || C) store_tile(C, acc, M, N, m0, n0, row, colhalf);
+                    if (kQ8) store_tile_q8_1(q8out, acc, M, N, m0, n0, row, colhalf);
+                }
             }
             cluster_sync_all();   // remote partials stay alive until rank 0 has read them
         }
@@ -619,7 +629,7 @@ int tc_gemm_check_resources() {
 }
 
 cudaError_t launch_gemm_tc(mmq_q8_1_t aq, const uint8_t* w, float* C, mmq_q8_1_t q8out, int32_t* S, int64_t M,
-                           int64_t N, int64_t K, int* status, int inject_timeout, cudaStream_t s) {
+                           int64_t N, int64_t K, int* status, int inject_timeout, cudaStream_t s, bool swiglu) {
     TmaMaps maps;
     const uint64_t nb = uint64_t(K / 32), nsb = uint64_t(K / 256);
     if (!encode_2d(&maps.a, CU_TENSOR_MAP_DATA_TYPE_UINT8, aq.qs, uint64_t(K), uint64_t(M),
@@ -639,6 +649,7 @@ cudaError_t launch_gemm_tc(mmq_q8_1_t aq, const uint8_t* w, float* C, mmq_q8_1_t
     {
         cudaFuncAttributes fa;
         cudaError_t e = cudaFuncGetAttributes(&fa, S ? gemm_tc_kernel<true, false>
+                                                   : swiglu ? gemm_tc_kernel<false, true, true>
                                                    : (q8out.qs ? gemm_tc_kernel<false, true>
                                                                : gemm_tc_kernel<false, false>));
         if (e != cudaSuccess) return e;
@@ -650,6 +661,7 @@ cudaError_t launch_gemm_tc(mmq_q8_1_t aq, const uint8_t* w, float* C, mmq_q8_1_t
     if (tiles * 2 <= nsm)
         while (split < 8 && tiles * split * 2 <= nsm && split * 2 <= int64_t(nsb)) split *= 2;
     auto k = S ? gemm_tc_kernel<true, false>
+               : swiglu ? gemm_tc_kernel<false, true, true>
                : (q8out.qs ? gemm_tc_kernel<false, true> : gemm_tc_kernel<false, false>);
     cudaError_t e;
     if ((e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes)))

@@ -20,9 +20,11 @@ cudaError_t launch_gemm_mma_s8(mmq_q8_1_t aq, const uint8_t* w, float* C,
                                int* status, cudaStream_t s);
 int tc_gemm_check_resources();   // MMQ_OK or MMQ_ERR_RESOURCE
 // q8out.qs == nullptr: no q8_1 output; C == nullptr: no f32 output.
+// swiglu: the N weight rows alternate gate / up; q8out receives the [M][N/2]
+// q8_1 of silu(gate) * up and C (may be null) the same values in f32.
 cudaError_t launch_gemm_tc(mmq_q8_1_t aq, const uint8_t* w, float* C, mmq_q8_1_t q8out,
                            int32_t* S, int64_t M, int64_t N, int64_t K,
-                           int* status, int inject_timeout, cudaStream_t s);
+                           int* status, int inject_timeout, cudaStream_t s, bool swiglu = false);
 int tc2_gemm_check_resources();  // MMQ_OK or MMQ_ERR_RESOURCE
 int64_t tc2_pair_tiles(int64_t M, int64_t N);
 cudaError_t launch_gemm_tc2(mmq_q8_1_t aq, const uint8_t* w, float* C,

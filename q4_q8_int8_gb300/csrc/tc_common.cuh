@@ -145,12 +145,54 @@ __device__ __forceinline__ void store_tile(float* C, const uint64_t (&acc)[32], 
     }
 }
 
+// One q8_1 block from 32 f32 values: amax, da = amax / 127 (IEEE division),
+// q = roundf(c / da) (the quotient of IEEE division, as in the prepass)
+// clamped to +-127, sa = sum of q; da == 0 gives q = 0 and sa = 0 (web page
+// "20 . r15 -- f32-accumulate mma probe (dead end) + rank-1 term2 rescale",
+// section 2.1, for the format).  Writes 32 quants at qrow (16-byte aligned).
+__device__ __forceinline__ void quantize_block32(const float (&v)[32], int8_t* qrow, float* da_out,
+                                                 int32_t* sa_out) {
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
+    const float d = __fdiv_rn(amax, 127.0f);
+    int qv[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) qv[i] = 0;   // a zero scale gives zero quants
+    if (d != 0.0f) {
+        // the prepass's rounding: reciprocal fast path, IEEE division where
+        // a quotient lies too close to a half-integer (or d is subnormal)
+        bool redo = d < 0x1p-126f;
+        const float r = __frcp_rn(d);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) qv[i] = q8::quant_fast(v[i], r, redo);
+        if (redo) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) qv[i] = q8::quant_exact(v[i], d);
+        }
+    }
+    uint32_t w[8];
+    int sum = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        uint32_t word = 0;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int q = q8::clamp127(qv[4 * i + e]);
+            sum += q;
+            word |= (uint32_t(q) & 0xFFu) << (8 * e);
+        }
+        w[i] = word;
+    }
+    *reinterpret_cast<uint4*>(qrow) = make_uint4(w[0], w[1], w[2], w[3]);
+    *reinterpret_cast<uint4*>(qrow + 16) = make_uint4(w[4], w[5], w[6], w[7]);
+    *da_out = d;
+    *sa_out = sum;
+}
+
 // The same row x 64 columns quantized to q8_1 (two 32-column blocks of an
-// [M][N] q8_1 output, N % 32 == 0): per block amax, da = amax / 127 (IEEE
-// division), q = roundf(c / da) (the quotient of IEEE division, as in the
-// prepass) clamped to +-127, sa = sum of q; da == 0 gives q = 0 and sa = 0.  The same operation as the q8_1 prepass on the
-// stored f32 values (web page "20 . r15 -- f32-accumulate mma probe (dead
-// end) + rank-1 term2 rescale", section 2.1, for the format).
+// [M][N] q8_1 output, N % 32 == 0): the same operation as the q8_1 prepass
+// on the stored f32 values.
 __device__ __forceinline__ void store_tile_q8_1(mmq_q8_1_t out, const uint64_t (&acc)[32], int M, int N,
                                                 int m0, int n0, int row, int colhalf) {
     const int64_t gr = int64_t(m0) + row;
@@ -165,45 +207,36 @@ __device__ __forceinline__ void store_tile_q8_1(mmq_q8_1_t out, const uint64_t (
             v[2 * i] = lo_f(acc[16 * blk + i]);
             v[2 * i + 1] = hi_f(acc[16 * blk + i]);
         }
-        float amax = 0.0f;
-#pragma unroll
-        for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
-        const float d = __fdiv_rn(amax, 127.0f);
-        int qv[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) qv[i] = 0;   // a zero scale gives zero quants
-        if (d != 0.0f) {
-            // the prepass's rounding: reciprocal fast path, IEEE division where
-            // a quotient lies too close to a half-integer (or d is subnormal)
-            bool redo = d < 0x1p-126f;
-            const float r = __frcp_rn(d);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) qv[i] = q8::quant_fast(v[i], r, redo);
-            if (redo) {
-#pragma unroll
-                for (int i = 0; i < 32; ++i) qv[i] = q8::quant_exact(v[i], d);
-            }
-        }
-        uint32_t w[8];
-        int sum = 0;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            uint32_t word = 0;
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int q = q8::clamp127(qv[4 * i + e]);
-                sum += q;
-                word |= (uint32_t(q) & 0xFFu) << (8 * e);
-            }
-            w[i] = word;
-        }
-        int8_t* qrow = out.qs + gr * N + gc;
-        *reinterpret_cast<uint4*>(qrow) = make_uint4(w[0], w[1], w[2], w[3]);
-        *reinterpret_cast<uint4*>(qrow + 16) = make_uint4(w[4], w[5], w[6], w[7]);
         const int64_t bi = gr * (N / 32) + gc / 32;
-        out.da[bi] = d;
-        out.sa[bi] = sum;
+        quantize_block32(v, out.qs + gr * N + gc, out.da + bi, out.sa + bi);
     }
+}
+
+// SwiGLU of an interleaved gate / up tile, quantized to q8_1: the weight rows
+// of the GEMM alternate gate_f, up_f, so each packed pair acc[i] of this
+// thread's 64 columns is (g, u) of one feature, and the 32 features
+// (n0 + 64 colhalf) / 2 + i form one q8_1 block of the [M][F] output
+// (F % 32 == 0):  h = silu(g) * u = g / (1 + exp(-g)) * u in f32.  hf, if
+// not null, receives h as f32 [M][F].
+__device__ __forceinline__ void store_tile_swiglu_q8_1(mmq_q8_1_t out, float* hf, const uint64_t (&acc)[32],
+                                                       int M, int F, int m0, int n0, int row, int colhalf) {
+    const int64_t gr = int64_t(m0) + row;
+    const int f0 = (n0 + colhalf * 64) / 2;
+    if (gr >= M || f0 >= F) return;
+    float h[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+        const float g = lo_f(acc[i]), u = hi_f(acc[i]);
+        h[i] = __fmul_rn(__fdiv_rn(g, __fadd_rn(1.0f, expf(-g))), u);
+    }
+    if (hf) {
+        float* hrow = hf + gr * F + f0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            *reinterpret_cast<float4*>(hrow + 4 * i) = make_float4(h[4 * i], h[4 * i + 1], h[4 * i + 2], h[4 * i + 3]);
+    }
+    const int64_t bi = gr * (F / 32) + f0 / 32;
+    quantize_block32(h, out.qs + gr * F + f0, out.da + bi, out.sa + bi);
 }
 
 // ------------------------------------------------------------------- host

@@ -14,7 +14,12 @@ With --fused every GEMM writes its result as q8_1 from its epilogue
 were quantized once before timing: the stack as it runs when each GEMM's
 output prepass is folded into the producing GEMM.
 
-  python -m q4_q8_int8_gb300.tools.stack [--passes 3] [--path auto] [--fused]
+With --swiglu (implies --fused) each layer's gate and up weights are
+interleaved once at set-up and run as one GEMM whose epilogue applies
+silu(gate) * up and quantizes to q8_1 (mmq_q4K_gemm_swiglu_q8_1); that
+output is the down projection's input, as in a SwiGLU FFN block.
+
+  python -m q4_q8_int8_gb300.tools.stack [--passes 3] [--path auto] [--fused] [--swiglu]
 """
 from __future__ import annotations
 
@@ -37,17 +42,31 @@ def main():
     ap.add_argument("--path", default="auto", choices=sorted(PATHS))
     ap.add_argument("--layers", type=int, default=synthetic.STACK_LAYERS)
     ap.add_argument("--fused", action="store_true")
+    ap.add_argument("--swiglu", action="store_true")
     args = ap.parse_args()
+    if args.swiglu:
+        args.fused = True
     build.build()
     mmq.load_library()
     dev = torch.device("cuda", 0)
     M = synthetic.STACK_TOKENS
     path = PATHS[args.path]
-    weights = []
+    weights = []   # (K, N, bytes, kind); kind "glu": N = 2F interleaved gate / up rows
+    names = [n for n, _, _ in synthetic.STACK_GEMMS]
     for layer in range(args.layers):
-        for g, (_, K, N) in enumerate(synthetic.STACK_GEMMS):
+        pending = {}
+        for g, (name, K, N) in enumerate(synthetic.STACK_GEMMS):
             ws, _ = synthetic.stack_seeds(layer, g)
-            weights.append((K, N, synthetic.torch_q4K_weights(N, K, ws, dev).view(-1)))
+            w = synthetic.torch_q4K_weights(N, K, ws, dev).view(-1)
+            if args.swiglu and name in ("gate", "up"):
+                pending[name] = w
+                if len(pending) == 2:
+                    weights.append((K, 2 * N, mmq.interleave_rows_q4K(pending["gate"], pending["up"], N, K), "glu"))
+                    del pending
+                    pending = {}
+                continue
+            weights.append((K, N, w, "down" if (args.swiglu and name == "down") else "gemm"))
+    assert not args.swiglu or {"gate", "up", "down"} <= set(names)
     pool = {}
     for K in sorted({K for _, K, _ in synthetic.STACK_GEMMS}):
         xs = []
@@ -58,6 +77,8 @@ def main():
     Ns = sorted({N for _, _, N in synthetic.STACK_GEMMS})
     outs = {N: torch.empty((M, N), device=dev) for N in Ns}
     outs_q8 = {N: mmq.q8_1_struct(*mmq.empty_q8_1(M, N, dev)) for N in Ns}
+    F = max(Ns)
+    glu_out = mmq.q8_1_struct(*mmq.empty_q8_1(M, F, dev))   # the down projection's input
     sp = mmq._stream_ptr()
     structs = {K: [mmq.q8_1_struct(*aq) for aq in pool[K][1]] for K in pool}
     if args.fused:   # activations quantized once, outside the timed passes
@@ -68,9 +89,9 @@ def main():
                     raise mmq.MMQError(rc, "quantize")
 
     def one_pass(ev=None):
-        for i, (K, N, w) in enumerate(weights):
+        for i, (K, N, w, kind) in enumerate(weights):
             x = pool[K][0][i % 8]
-            aqs = structs[K][i % 8]
+            aqs = glu_out if kind == "down" else structs[K][i % 8]
             if ev is not None:
                 ev[i][0].record()
             if not args.fused:
@@ -79,7 +100,10 @@ def main():
                     raise mmq.MMQError(rc, "quantize")
             if ev is not None:
                 ev[i][1].record()
-            if args.fused:
+            if kind == "glu":
+                rc = mmq.mmq_q4K_gemm_swiglu_q8_1(aqs, ctypes.c_void_p(w.data_ptr()), None, glu_out, M, N // 2,
+                                                  K, sp)
+            elif args.fused:
                 rc = mmq.mmq_q4K_gemm_q8_1(aqs, ctypes.c_void_p(w.data_ptr()), None, outs_q8[N], M, N, K, sp)
             else:
                 rc = mmq.mmq_q4K_gemm_path(aqs, ctypes.c_void_p(w.data_ptr()),
@@ -108,18 +132,18 @@ def main():
     t_gemm = sum(b.elapsed_time(c) for _, b, c in ev)
     if mmq.status() != 0:
         raise RuntimeError("device status error")
-    macs = sum(M * K * N for K, N, _ in weights)
+    macs = sum(M * K * N for K, N, _, _ in weights)
     best = min(t_stack)
     print(json.dumps({
         "workload": f"7B prefill stack: {args.layers} layers x (q,k,v,o 4096x4096; gate,up 4096->11008; "
                     f"down 11008->4096), M={M}",
-        "path": args.path, "passes": args.passes, "fused_requantize": args.fused,
+        "path": args.path, "passes": args.passes, "fused_requantize": args.fused, "fused_swiglu": args.swiglu,
         "stack_ms": {"min": best, "median": sorted(t_stack)[len(t_stack) // 2], "max": max(t_stack)},
         "equivalent_tok_s": M / (best * 1e-3),
         "tmacs_with_prepass": macs / (best * 1e-3) / 1e12,
         "gemm_only_ms": t_gemm, "gemm_only_tmacs": macs / (t_gemm * 1e-3) / 1e12,
         "prepass_ms": t_pre, "gmac": macs / 1e9,
-        "weights_gb": sum(w.numel() for _, _, w in weights) / 1e9,
+        "weights_gb": sum(w.numel() for _, _, w, _ in weights) / 1e9,
     }))
 
 

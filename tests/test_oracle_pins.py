@@ -344,3 +344,18 @@ def test_dense_gemm_integer_matrices_exact():
     Cs, Ts = dense.gemm_f16_sampled(A.astype(np.float16), B.astype(np.float16), [4, 0, 2], [0, 2, 1])
     assert (Cs == np.array([C[4, 0], C[0, 2], C[2, 1]])).all()
     assert (Ts == np.array([T[4, 0], T[0, 2], T[2, 1]])).all()
+
+
+# ---------------------------------------------------------------------------
+# SwiGLU epilogue: oracle.ffn
+# ---------------------------------------------------------------------------
+def test_ffn_silu_closed_forms():
+    from oracle import ffn
+    assert ffn.silu(0.0) == 0.0
+    assert abs(ffn.silu(np.log(3.0)) - 0.75 * np.log(3.0)) < 1e-15      # sigmoid(ln 3) = 3/4
+    x = np.linspace(-20, 20, 81)
+    assert np.allclose(ffn.silu(x) - ffn.silu(-x), x, rtol=0, atol=1e-13)  # x s(x) - (-x) s(-x) = x
+    assert abs(ffn.silu(40.0) - 40.0) < 1e-15 * 40 * 1e3                  # sigmoid(40) = 1 - 4e-18
+    assert ffn.silu(-800.0) == 0.0 or abs(ffn.silu(-800.0)) < 1e-300
+    g = np.array([1.0, -2.0]); u = np.array([3.0, 0.5])
+    assert np.allclose(ffn.swiglu(g, u), [3.0 / (1 + np.exp(-1.0)), 0.5 * -2.0 / (1 + np.exp(2.0))])
