@@ -450,7 +450,7 @@ def run_mine(args, rank, world, local_rank):
              mmq.MMQ_PATH_TC_PAIR: ("gemm_tc2", "gemm_tc2.cu"),
              mmq.MMQ_PATH_SMALL_M: ("gemm_small_m", "gemm_small.cu"),
              mmq.MMQ_PATH_TC_SMALL: ("gemm_tc_small", "gemm_tc_small.cu")}[used_path]
-    src_hash = kernel_source_hash([kname[1], "sm103_ptx.cuh"])
+    src_hash = kernel_source_hash([kname[1], "sm103_ptx.cuh", "tc_common.cuh", "q8_round.cuh"])
     traffic = recorded_traffic(kname[0], src_hash)
     alg_bytes = 0.5625 * N * K + 1.25 * M * K + 4 * M * N
     sm_mhz = (clk or {}).get("sm_mhz") or micro["sm_max_mhz"]
