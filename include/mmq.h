@@ -199,6 +199,43 @@ int mmq_convert_f32_f16(const float* x, uint16_t* xh, int64_t n, void* stream);
 int mmq_gemm_f16(const uint16_t* A, const uint16_t* B, float* C, int64_t M,
                  int64_t N, int64_t K, void* stream);
 
+/* ---- q6_K weights (the family the pages' MMQ line moved to next: page r15,
+ * "Proof of pattern portability").  The pages print no layout; this library
+ * takes the customary 210-byte super-block of 256 weights: ql[128] (low
+ * nibbles), qh[64] (high bit pairs), int8 scales[16] (one per 16 weights),
+ * fp16 d.  Quant q in [-32, 31] is stored as u = q + 32; element
+ * 128n + 32r + l (n < 2, r < 4, l < 32) keeps the low 4 bits of u in nibble
+ * r/2 of ql[64n + 32(r%2) + l] and the top 2 bits in bits 2r, 2r+1 of
+ * qh[32n + l].  The weight is d * sc * q (no minimum term). */
+
+/* Bytes of the customary layout (0 if N < 1 or K % 256 != 0). */
+size_t mmq_q6K_bytes(int64_t N, int64_t K);
+
+/* Host packer: q int8 [N][K] in [-32, 31], sc int8 [N][K/16], d fp16 bits
+ * [N][K/256] -> mmq_q6K_bytes(N, K) bytes, row j's super-blocks contiguous.
+ * MMQ_ERR_ARG on a quant out of range. */
+int mmq_pack_q6K(const int8_t* q_host, const int8_t* sc_host, const uint16_t* d_host,
+                 int64_t N, int64_t K, uint8_t* out_host);
+
+/* Bytes of the device layout the q6_K GEMM reads: each super-block padded to
+ * 224 bytes (14 zero bytes after d), so that rows are whole 16-byte pieces. */
+size_t mmq_q6K_dev_bytes(int64_t N, int64_t K);
+
+/* Customary layout (device memory, any alignment) -> device layout (dst
+ * 16-byte aligned), once at load time. */
+int mmq_repack_q6K(const uint8_t* src, uint8_t* dst, int64_t N, int64_t K, void* stream);
+
+/* C = A . W^T for q8_1 activations and q6_K weights in the device layout:
+ * per 16-weight sub-block s of the 32-element q8_1 block c,
+ * C_ij += da_ic * d_j * sc_js * S_ijs with S the exact int32 dot (warp-level
+ * int8 tensor MMAs).  Shape rules and tolerance as mmq_q4K_gemm. */
+int mmq_q6K_gemm(mmq_q8_1_t aq, const uint8_t* bq6k_dev, float* C, int64_t M,
+                 int64_t N, int64_t K, void* stream);
+
+/* The exact per-16 dots S int32 [M][N][K/16] of the same kernel. */
+int mmq_q6K_block_dots(mmq_q8_1_t aq, const uint8_t* bq6k_dev, int32_t* S,
+                       int64_t M, int64_t N, int64_t K, void* stream);
+
 /* Synchronizes `stream`, then returns and clears the current device's status
  * word: MMQ_OK, or MMQ_ERR_DEVICE_TIMEOUT if a kernel's bounded wait gave up
  * since the last call (that kernel's output is then invalid), or

@@ -38,6 +38,8 @@ EXPORTS = (
     "mmq_pack_q4K", "mmq_q4K_gemm", "mmq_q4K_gemm_path", "mmq_q4K_gemm_q8_1", "mmq_q4K_block_dots",
     "mmq_dequantize_q4K_f16", "mmq_convert_f32_f16", "mmq_gemm_f16",
     "mmq_q4K_gemm_swiglu_q8_1", "mmq_interleave_rows_q4K",
+    "mmq_q6K_bytes", "mmq_pack_q6K", "mmq_q6K_dev_bytes", "mmq_repack_q6K", "mmq_q6K_gemm",
+    "mmq_q6K_block_dots",
     "mmq_status", "mmq_strerror", "mmq_debug_inject_timeout",
 )
 
@@ -81,6 +83,12 @@ def load_library(path: str = LIB_PATH):
                 "mmq_gemm_f16": ([P, P, P, I, I, I, P], ctypes.c_int),
                 "mmq_q4K_gemm_swiglu_q8_1": ([Q, P, P, Q, I, I, I, P], ctypes.c_int),
                 "mmq_interleave_rows_q4K": ([P, P, P, I, I, P], ctypes.c_int),
+                "mmq_q6K_bytes": ([I, I], S),
+                "mmq_pack_q6K": ([P, P, P, I, I, P], ctypes.c_int),
+                "mmq_q6K_dev_bytes": ([I, I], S),
+                "mmq_repack_q6K": ([P, P, I, I, P], ctypes.c_int),
+                "mmq_q6K_gemm": ([Q, P, P, I, I, I, P], ctypes.c_int),
+                "mmq_q6K_block_dots": ([Q, P, P, I, I, I, P], ctypes.c_int),
                 "mmq_status": ([P], ctypes.c_int),
                 "mmq_strerror": ([ctypes.c_int], ctypes.c_char_p),
                 "mmq_debug_inject_timeout": ([ctypes.c_int], None),
@@ -261,6 +269,74 @@ def q4K_gemm_swiglu_q8_1(aq, w_gu, F: int, with_h: bool = False, out=None, strea
                                     M, F, K, _stream_ptr(stream)),
            "mmq_q4K_gemm_swiglu_q8_1")
     return h, o
+
+
+def mmq_q6K_bytes(N, K):
+    return load_library().mmq_q6K_bytes(N, K)
+
+
+def mmq_pack_q6K(q, sc, d, N, K, out):
+    return load_library().mmq_pack_q6K(q, sc, d, N, K, out)
+
+
+def mmq_q6K_dev_bytes(N, K):
+    return load_library().mmq_q6K_dev_bytes(N, K)
+
+
+def mmq_repack_q6K(src, dst, N, K, stream):
+    return load_library().mmq_repack_q6K(src, dst, N, K, stream)
+
+
+def mmq_q6K_gemm(aq, w, C, M, N, K, stream):
+    return load_library().mmq_q6K_gemm(aq, w, C, M, N, K, stream)
+
+
+def mmq_q6K_block_dots(aq, w, S, M, N, K, stream):
+    return load_library().mmq_q6K_block_dots(aq, w, S, M, N, K, stream)
+
+
+def pack_q6K(q, sc, d_bits):
+    """Host packer (numpy): q int8 [N][K], sc int8 [N][K/16], d fp16 bits [N][K/256] -> bytes."""
+    import numpy as np
+    q = np.ascontiguousarray(q, np.int8)
+    N, K = q.shape
+    sc = np.ascontiguousarray(sc, np.int8)
+    d_bits = np.ascontiguousarray(d_bits, np.uint16)
+    out = np.empty((N, K // 256, 210), np.uint8)
+    ptr = lambda a: a.ctypes.data_as(ctypes.c_void_p)
+    _check(mmq_pack_q6K(ptr(q), ptr(sc), ptr(d_bits), N, K, ptr(out)), "mmq_pack_q6K")
+    return out
+
+
+def repack_q6K(w, N: int, K: int, out=None, stream=None):
+    """Customary q6_K bytes (CUDA uint8) -> the device layout the q6_K GEMM reads."""
+    import torch
+    o = out if out is not None else torch.empty(N * (K // 256) * 224, dtype=torch.uint8, device=w.device)
+    _check(mmq_repack_q6K(ctypes.c_void_p(w.data_ptr()), ctypes.c_void_p(o.data_ptr()), N, K,
+                          _stream_ptr(stream)), "mmq_repack_q6K")
+    return o
+
+
+def q6K_gemm(aq, w_dev, N: int, out=None, stream=None):
+    """aq = (qs, da, sa); w_dev q6_K bytes in the device layout -> C float32 [M][N]."""
+    import torch
+    qs, da, sa = aq
+    M, K = qs.shape
+    C = out if out is not None else torch.empty((M, N), dtype=torch.float32, device=qs.device)
+    _check(mmq_q6K_gemm(q8_1_struct(qs, da, sa), ctypes.c_void_p(w_dev.data_ptr()), ctypes.c_void_p(C.data_ptr()),
+                        M, N, K, _stream_ptr(stream)), "mmq_q6K_gemm")
+    return C
+
+
+def q6K_block_dots(aq, w_dev, N: int, out=None, stream=None):
+    """Exact per-16 int32 dots S [M][N][K/16]."""
+    import torch
+    qs, da, sa = aq
+    M, K = qs.shape
+    S = out if out is not None else torch.empty((M, N, K // 16), dtype=torch.int32, device=qs.device)
+    _check(mmq_q6K_block_dots(q8_1_struct(qs, da, sa), ctypes.c_void_p(w_dev.data_ptr()),
+                              ctypes.c_void_p(S.data_ptr()), M, N, K, _stream_ptr(stream)), "mmq_q6K_block_dots")
+    return S
 
 
 def dequantize_q4K_f16(w, N: int, K: int, out=None, stream=None):

@@ -274,6 +274,34 @@ int mmq_gemm_f16(const uint16_t* A, const uint16_t* B, float* C, int64_t M, int6
     return from_cuda(mmq::launch_gemm_f16(A, B, C, M, N, K, status, static_cast<cudaStream_t>(stream)));
 }
 
+size_t mmq_q6K_dev_bytes(int64_t N, int64_t K) {
+    if (N < 1 || K < 256 || (K % 256) != 0) return 0;
+    return size_t(N) * size_t(K / 256) * 224;
+}
+
+int mmq_repack_q6K(const uint8_t* src, uint8_t* dst, int64_t N, int64_t K, void* stream) {
+    if (!src || !dst) return MMQ_ERR_ARG;
+    if (N < 1 || K < 256 || (K % 256) != 0 || N * (K / 256) > (int64_t(1) << 34)) return MMQ_ERR_ARG;
+    if (!aligned16(dst)) return MMQ_ERR_ALIGN;
+    int rc = check_device();
+    if (rc) return rc;
+    return from_cuda(mmq::launch_repack_q6K(src, dst, N, K, static_cast<cudaStream_t>(stream)));
+}
+
+int mmq_q6K_gemm(mmq_q8_1_t aq, const uint8_t* bq6k_dev, float* C, int64_t M, int64_t N, int64_t K,
+                 void* stream) {
+    int rc = check_gemm_args(aq, bq6k_dev, C, M, N, K);
+    if (rc) return rc;
+    return from_cuda(mmq::launch_gemm_q6k(aq, bq6k_dev, C, nullptr, M, N, K, static_cast<cudaStream_t>(stream)));
+}
+
+int mmq_q6K_block_dots(mmq_q8_1_t aq, const uint8_t* bq6k_dev, int32_t* S, int64_t M, int64_t N, int64_t K,
+                       void* stream) {
+    int rc = check_gemm_args(aq, bq6k_dev, S, M, N, K);
+    if (rc) return rc;
+    return from_cuda(mmq::launch_gemm_q6k(aq, bq6k_dev, nullptr, S, M, N, K, static_cast<cudaStream_t>(stream)));
+}
+
 int mmq_status(void* stream) {
     int* p = mmq::status_word_ptr();
     if (!p) return MMQ_ERR_CUDA;

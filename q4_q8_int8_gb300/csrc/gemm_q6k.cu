@@ -1,0 +1,296 @@
+// q6_K x q8_1 GEMM on warp-level integer MMA, and the load-time repack of
+// q6_K weights into a 16-byte aligned device layout.
+//
+// q6_K is the weight family the pages' MMQ line moved to next (web page "20
+// . r15 -- f32-accumulate mma probe (dead end) + rank-1 term2 rescale",
+// section "Proof of pattern portability"), on warp-level mma.sync kernels.
+// Weights: 256-element super-blocks with an fp16 d, an int8 scale per 16
+// consecutive elements, and 6-bit quants stored as u = q + 32 (q in
+// [-32, 31]); no minimum, so the rescale has one term.  Per 16-element
+// sub-block s the integer MMA produces S_is exactly (|S| <= 16*127*32), then
+//     acc_ij += (da_i,s/2 * d_j * sc_j,s) * S_ijs.
+//
+// Device layout (mmq_repack_q6K): each customary 210-byte super-block padded
+// to 224 bytes (ql[128], qh[64], scales[16], d, 14 zero bytes), so that a row
+// of super-blocks is a whole number of 16-byte pieces for cp.async.
+//
+// Design (the control kernel's shape, gemm_mma.cu): CTA tile 128 tokens x
+// 128 weight rows, 8 warps as 2 x 4, 16 MMA chains per warp; one super-block
+// per cp.async stage (3 in flight).  A fragments by ldmatrix from int8 rows;
+// the m16n8k32 A fragment's two halves are the m16n8k16 fragments of the
+// chunk's two sub-blocks.  B fragments are built from the raw bytes: for
+// chunk c = 4n + r of a super-block, the four quants of a fragment register
+// are nibble r/2 of one ql word and bit pair r of one qh word, and
+// __vsub4(u, 32) makes them int8.  The s32 accumulators are seeded with the
+// bits of 1.5 * 2^23, so one FADD recovers S as a float.
+#include <cuda_fp16.h>
+
+#include "mmq_internal.h"
+
+namespace {
+
+constexpr int BM = 128, BN = 128, kThreads = 256, kStages = 3;
+constexpr int kQ6Bytes = 210, kQ6DevBytes = 224;
+constexpr int kARowBytes = 272;                        // 256 + 16 pad
+constexpr int kAStage = BM * kARowBytes;               // 34816
+constexpr int kWStage = BN * kQ6DevBytes;              // 28672
+constexpr int kDaStage = BM * 8 * 4;                   // 4096
+constexpr int kStageBytes = kAStage + kWStage + kDaStage;
+constexpr int kSmemBytes = kStages * kStageBytes + 16 * 128 * 4 + 8 * 128 * 4;   // + d*sc and da tables
+constexpr uint32_t kBiasBits = 0x4B400000u;            // 12582912.0f
+constexpr float kBias = 12582912.0f;
+static_assert(kSmemBytes <= 232448, "shared memory budget");
+
+// ---------------------------------------------------------------- repack
+// One thread per 16-byte piece of the padded layout (14 per super-block).
+__global__ void __launch_bounds__(256) repack_q6K_kernel(const uint8_t* __restrict__ src,
+                                                         uint8_t* __restrict__ dst, int64_t pieces) {
+    const int64_t p = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (p >= pieces) return;
+    const int64_t sbi = p / 14;
+    const int off = int(p - sbi * 14) * 16;
+    const uint8_t* s = src + sbi * kQ6Bytes + off;
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        uint32_t v = 0;
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+            const int o = off + 4 * i + b;
+            v |= uint32_t(o < kQ6Bytes ? s[4 * i + b] : 0) << (8 * b);
+        }
+        w[i] = v;
+    }
+    *reinterpret_cast<uint4*>(dst + sbi * kQ6DevBytes + off) = make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid) {
+    const int n = valid ? 16 : 0;
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src), "r"(n));
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N)); }
+
+__device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                            uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+
+// m16n8k16 s8 x s8 -> s32, accumulate in place.
+__device__ __forceinline__ void mma_s8_k16(uint32_t (&c)[4], uint32_t a0, uint32_t a1, uint32_t b) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.s32.s8.s8.s32 {%0,%1,%2,%3}, {%4,%5}, {%6}, {%0,%1,%2,%3};\n"
+        : "+r"(c[0]), "+r"(c[1]), "+r"(c[2]), "+r"(c[3])
+        : "r"(a0), "r"(a1), "r"(b));
+}
+
+__device__ __forceinline__ void load_stage(uint32_t st, const mmq_q8_1_t& aq, const uint8_t* w, int64_t M,
+                                           int64_t N, int64_t K, int64_t m0, int64_t n0, int64_t sb) {
+    const int t = threadIdx.x;
+    const int64_t nsb = K / 256, nb = K / 32;
+#pragma unroll
+    for (int i = 0; i < (BM * 16) / kThreads; ++i) {   // A: 128 rows x 16 pieces
+        const int piece = t + i * kThreads;
+        const int r = piece >> 4, seg = piece & 15;
+        const bool ok = (m0 + r) < M;
+        const int8_t* src = ok ? aq.qs + (m0 + r) * K + sb * 256 + seg * 16 : aq.qs;
+        cp_async16(st + r * kARowBytes + seg * 16, src, ok);
+    }
+    for (int piece = t; piece < BN * 14; piece += kThreads) {   // W: 128 rows x 14 pieces
+        const int r = piece / 14, seg = piece - r * 14;
+        const bool ok = (n0 + r) < N;
+        const uint8_t* src = ok ? w + ((n0 + r) * nsb + sb) * kQ6DevBytes + seg * 16 : w;
+        cp_async16(st + kAStage + r * kQ6DevBytes + seg * 16, src, ok);
+    }
+    {   // da: 128 rows x 2 pieces
+        const int r = t >> 1, seg = t & 1;
+        const bool ok = (m0 + r) < M;
+        const float* sd = ok ? aq.da + (m0 + r) * nb + sb * 8 + seg * 4 : aq.da;
+        cp_async16(st + kAStage + kWStage + r * 32 + seg * 16, sd, ok);
+    }
+}
+
+template <bool kDump>
+__global__ void __launch_bounds__(kThreads, 1)
+gemm_q6k_kernel(mmq_q8_1_t aq, const uint8_t* __restrict__ w, float* __restrict__ C, int32_t* __restrict__ S,
+                int64_t M, int64_t N, int64_t K) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    const uint32_t sbase = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
+    float* colsc = reinterpret_cast<float*>(smem + kStages * kStageBytes);   // d * sc [16][128]
+    float* rowda = colsc + 16 * 128;                                        // da [8][128]
+
+    const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+    const int wm = warp & 1, wn = warp >> 1;
+    const int64_t m0 = int64_t(blockIdx.y) * BM, n0 = int64_t(blockIdx.x) * BN;
+    const int64_t nsb = K / 256;
+    const int64_t ns16 = K / 16;
+
+    float acc[4][4][4];
+#pragma unroll
+    for (int a = 0; a < 4; ++a)
+#pragma unroll
+        for (int b = 0; b < 4; ++b)
+#pragma unroll
+            for (int r = 0; r < 4; ++r) acc[a][b][r] = 0.0f;
+
+#pragma unroll
+    for (int s = 0; s < kStages - 1; ++s) {
+        if (s < nsb) load_stage(sbase + s * kStageBytes, aq, w, M, N, K, m0, n0, s);
+        cp_async_commit();
+    }
+
+    for (int64_t sb = 0; sb < nsb; ++sb) {
+        cp_async_wait<kStages - 2>();
+        __syncthreads();   // stage sb visible; everyone is done with sb-1
+        {
+            const int64_t nx = sb + kStages - 1;
+            if (nx < nsb) load_stage(sbase + (nx % kStages) * kStageBytes, aq, w, M, N, K, m0, n0, nx);
+            cp_async_commit();
+        }
+        const int st = int(sb % kStages);
+        const uint8_t* sA = smem + st * kStageBytes;
+        const uint8_t* sW = sA + kAStage;
+        const float* sDa = reinterpret_cast<const float*>(sW + kWStage);
+
+        if (!kDump) {
+            {   // d * sc per weight row and sub-block (exact in f32: 11 x 8 bits)
+                const int n = t >> 1, s8 = (t & 1) * 8;
+                const uint8_t* blk = sW + n * kQ6DevBytes;
+                const float d = __half2float(__ushort_as_half(uint16_t(blk[208] | (blk[209] << 8))));
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+                    colsc[(s8 + k) * 128 + n] = d * float(int8_t(blk[192 + s8 + k]));
+            }
+            {   // da per token row and chunk
+                const int r = t >> 1, c4 = (t & 1) * 4;
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc) rowda[(c4 + cc) * 128 + r] = sDa[r * 8 + c4 + cc];
+            }
+            __syncthreads();
+        }
+
+        const uint32_t aRowAddr = sbase + st * kStageBytes +
+                                  (wm * 64 + (lane & 7) + ((lane >> 3) & 1) * 8) * kARowBytes + (lane >> 4) * 16;
+#pragma unroll 1
+        for (int n = 0; n < 2; ++n) {   // half n of the super-block: chunks 4n .. 4n + 3
+#pragma unroll 1
+            for (int r = 0; r < 4; ++r) {
+                const int c = 4 * n + r;   // chunk within the super-block
+                // this chunk's ql word (nibble r / 2) and qh word (bit pair r) per fragment and half
+                uint32_t qlw[4][2], qhw[4][2];
+#pragma unroll
+                for (int fn = 0; fn < 4; ++fn) {
+                    const uint8_t* row = sW + (wn * 32 + fn * 8 + (lane >> 2)) * kQ6DevBytes;
+#pragma unroll
+                    for (int kh = 0; kh < 2; ++kh) {
+                        const int l = 16 * kh + (lane & 3) * 4;
+                        qlw[fn][kh] = *reinterpret_cast<const uint32_t*>(row + 64 * n + 32 * (r & 1) + l);
+                        qhw[fn][kh] = *reinterpret_cast<const uint32_t*>(row + 128 + 32 * n + l);
+                    }
+                }
+                uint32_t af[4][4];
+#pragma unroll
+                for (int fm = 0; fm < 4; ++fm)
+                    ldmatrix_x4(aRowAddr + fm * 16 * kARowBytes + c * 32, af[fm][0], af[fm][1], af[fm][2],
+                                af[fm][3]);
+#pragma unroll 1
+                for (int kh = 0; kh < 2; ++kh) {   // sub-block 2c + kh
+                    uint32_t ci[4][4][4];
+#pragma unroll
+                    for (int fm = 0; fm < 4; ++fm)
+#pragma unroll
+                        for (int fn = 0; fn < 4; ++fn)
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) ci[fm][fn][i] = kDump ? 0u : kBiasBits;
+#pragma unroll
+                    for (int fn = 0; fn < 4; ++fn) {
+                        // selects, not run-time indexing, keep these arrays in registers
+                        const uint32_t lw = kh ? qlw[fn][1] : qlw[fn][0], hw = kh ? qhw[fn][1] : qhw[fn][0];
+                        const uint32_t u = ((lw >> (4 * (r >> 1))) & 0x0F0F0F0Fu) | (((hw >> (2 * r)) & 0x03030303u) << 4);
+                        const uint32_t b = __vsub4(u, 0x20202020u);   // u - 32 per byte: int8 quants
+#pragma unroll
+                        for (int fm = 0; fm < 4; ++fm)
+                            mma_s8_k16(ci[fm][fn], kh ? af[fm][2] : af[fm][0], kh ? af[fm][3] : af[fm][1], b);
+                    }
+                    const int s16 = 2 * c + kh;
+                    if (kDump) {
+#pragma unroll
+                        for (int fm = 0; fm < 4; ++fm)
+#pragma unroll
+                            for (int fn = 0; fn < 4; ++fn)
+#pragma unroll
+                                for (int i = 0; i < 4; ++i) {
+                                    const int64_t row = m0 + wm * 64 + fm * 16 + (lane >> 2) + (i >> 1) * 8;
+                                    const int64_t col = n0 + wn * 32 + fn * 8 + (lane & 3) * 2 + (i & 1);
+                                    if (row < M && col < N)
+                                        S[(row * N + col) * ns16 + sb * 16 + s16] = int32_t(ci[fm][fn][i]);
+                                }
+                    } else {
+                        float da[4][2];
+#pragma unroll
+                        for (int fm = 0; fm < 4; ++fm)
+#pragma unroll
+                            for (int hr = 0; hr < 2; ++hr)
+                                da[fm][hr] = rowda[c * 128 + wm * 64 + fm * 16 + (lane >> 2) + hr * 8];
+#pragma unroll
+                        for (int fn = 0; fn < 4; ++fn) {
+                            const float2 ds = *reinterpret_cast<const float2*>(
+                                &colsc[s16 * 128 + wn * 32 + fn * 8 + (lane & 3) * 2]);
+#pragma unroll
+                            for (int fm = 0; fm < 4; ++fm)
+#pragma unroll
+                                for (int i = 0; i < 4; ++i) {
+                                    const float sv = __uint_as_float(ci[fm][fn][i]) - kBias;
+                                    acc[fm][fn][i] = fmaf(da[fm][i >> 1] * ((i & 1) ? ds.y : ds.x), sv,
+                                                          acc[fm][fn][i]);
+                                }
+                        }
+                    }
+                }
+            }
+        }
+    }
+    cp_async_wait<0>();
+
+    if (!kDump) {
+#pragma unroll
+        for (int fm = 0; fm < 4; ++fm)
+#pragma unroll
+            for (int fn = 0; fn < 4; ++fn)
+#pragma unroll
+                for (int hr = 0; hr < 2; ++hr) {
+                    const int64_t row = m0 + wm * 64 + fm * 16 + (lane >> 2) + hr * 8;
+                    const int64_t col = n0 + wn * 32 + fn * 8 + (lane & 3) * 2;
+                    if (row < M && col < N)
+                        *reinterpret_cast<float2*>(C + row * N + col) =
+                            make_float2(acc[fm][fn][2 * hr], acc[fm][fn][2 * hr + 1]);
+                }
+    }
+}
+
+}  // namespace
+
+namespace mmq {
+
+cudaError_t launch_repack_q6K(const uint8_t* src, uint8_t* dst, int64_t N, int64_t K, cudaStream_t s) {
+    const int64_t pieces = N * (K / 256) * 14;
+    const int64_t blocks = (pieces + 255) / 256;
+    repack_q6K_kernel<<<unsigned(blocks), 256, 0, s>>>(src, dst, pieces);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_gemm_q6k(mmq_q8_1_t aq, const uint8_t* w, float* C, int32_t* S, int64_t M, int64_t N,
+                            int64_t K, cudaStream_t s) {
+    const dim3 grid(unsigned((N + BN - 1) / BN), unsigned((M + BM - 1) / BM));
+    if (grid.y > 65535u) return cudaErrorInvalidConfiguration;
+    auto k = S ? gemm_q6k_kernel<true> : gemm_q6k_kernel<false>;
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess) return e;
+    k<<<grid, kThreads, kSmemBytes, s>>>(aq, w, C, S, M, N, K);
+    return cudaGetLastError();
+}
+
+}  // namespace mmq

@@ -44,6 +44,10 @@ cudaError_t launch_convert_f16(const float* x, uint16_t* out, int64_t n, cudaStr
 int dense_gemm_check_resources();   // MMQ_OK or MMQ_ERR_RESOURCE
 cudaError_t launch_gemm_f16(const uint16_t* A, const uint16_t* B, float* C, int64_t M, int64_t N,
                             int64_t K, int* status, cudaStream_t s);
+// q6_K x q8_1 (gemm_q6k.cu): S != nullptr dumps the per-16 dots instead of C.
+cudaError_t launch_repack_q6K(const uint8_t* src, uint8_t* dst, int64_t N, int64_t K, cudaStream_t s);
+cudaError_t launch_gemm_q6k(mmq_q8_1_t aq, const uint8_t* w, float* C, int32_t* S, int64_t M,
+                            int64_t N, int64_t K, cudaStream_t s);
 constexpr int64_t kSmallMMax = 64;
 
 }  // namespace mmq

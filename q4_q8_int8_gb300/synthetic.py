@@ -68,6 +68,35 @@ def q4K_weights(N: int, K: int, seed: int, d_lo: float = 1e-3,
     return blk
 
 
+Q6K_BLOCK_BYTES = 210
+
+
+def q6K_weights(N: int, K: int, seed: int, d_lo: float = 1e-4,
+                d_hi: float = 1e-3) -> np.ndarray:
+    """Customary q6_K super-blocks [N][K/256][210]: uniform random bytes for
+    the quant bits (so u = q + 32 ~ U{0..63}) and the int8 scales, fp16 d ~
+    U(d_lo, d_hi) in bytes 208-209."""
+    assert K % QK_K == 0
+    nsb = K // QK_K
+    rng = np.random.Generator(np.random.PCG64(seed))
+    blk = rng.integers(0, 256, size=(N, nsb, Q6K_BLOCK_BYTES), dtype=np.uint8)
+    d = rng.uniform(d_lo, d_hi, size=(N, nsb)).astype(np.float16)
+    blk[:, :, 208:210] = d.view(np.uint8).reshape(N, nsb, 2)
+    return blk
+
+
+def torch_q6K_weights(N: int, K: int, seed: int, device, d_lo: float = 1e-4, d_hi: float = 1e-3):
+    """Device-side variant of q6K_weights (same recipe, torch Philox stream)."""
+    import torch
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    nsb = K // QK_K
+    blk = torch.randint(0, 256, (N, nsb, Q6K_BLOCK_BYTES), dtype=torch.uint8, device=device, generator=g)
+    d = (torch.rand((N, nsb), device=device, generator=g) * (d_hi - d_lo) + d_lo).half()
+    blk[:, :, 208:210] = d.view(torch.uint8).view(N, nsb, 2)
+    return blk
+
+
 def config_inputs(name: str, M: int | None = None):
     """(x, blk, N) for a named workload; seeds fixed per workload."""
     if name == "tiny":

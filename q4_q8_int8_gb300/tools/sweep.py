@@ -7,7 +7,10 @@ and uses CUDA events on the launching stream after warm-up.  The reported
 kernel time replays the launches from a CUDA graph (no host launch cost);
 the plain stream-launch time is reported beside it.
 
-  python -m q4_q8_int8_gb300.tools.sweep [--reps 50] [--paths auto,tc,mma_s8,small_m]
+The path "q6k" times the q6_K x q8_1 GEMM (mmq_q6K_gemm) on q6_K weights
+of the same shapes, repacked once to the device layout before timing.
+
+  python -m q4_q8_int8_gb300.tools.sweep [--reps 50] [--paths auto,tc,mma_s8,small_m,q6k]
 """
 from __future__ import annotations
 
@@ -22,7 +25,8 @@ import q4_q8_int8_gb300 as mmq
 from q4_q8_int8_gb300 import build, synthetic
 
 PATHS = {"auto": mmq.MMQ_PATH_AUTO, "tc": mmq.MMQ_PATH_TC, "mma_s8": mmq.MMQ_PATH_MMA_S8,
-         "small_m": mmq.MMQ_PATH_SMALL_M, "tc_pair": mmq.MMQ_PATH_TC_PAIR, "tc_small": mmq.MMQ_PATH_TC_SMALL}
+         "small_m": mmq.MMQ_PATH_SMALL_M, "tc_pair": mmq.MMQ_PATH_TC_PAIR, "tc_small": mmq.MMQ_PATH_TC_SMALL,
+         "q6k": "q6k"}
 
 
 def shapes():
@@ -34,20 +38,29 @@ def shapes():
 
 
 def time_gemm(M, K, N, path, reps, dev, graph=True):
-    set_bytes = N * K * 0.5625 + M * K * 1.25 + M * N * 4 + M * K * 4
+    q6 = path == "q6k"
+    set_bytes = N * K * (0.875 if q6 else 0.5625) + M * K * 1.25 + M * N * 4 + M * K * 4
     R = max(2, math.ceil(2 * 129e6 / set_bytes) + 1)
     R = min(R, 64)
-    ws = [synthetic.torch_q4K_weights(N, K, 100 + r, dev).view(-1) for r in range(R)]
+    if q6:
+        ws = [mmq.repack_q6K(synthetic.torch_q6K_weights(N, K, 100 + r, dev).view(-1), N, K) for r in range(R)]
+    else:
+        ws = [synthetic.torch_q4K_weights(N, K, 100 + r, dev).view(-1) for r in range(R)]
     xs = [synthetic.torch_activations(M, K, 200 + r, dev) for r in range(R)]
     aqs = [mmq.quantize_q8_1(x) for x in xs]
     Cs = [torch.empty((M, N), device=dev) for _ in range(R)]
     sp = mmq._stream_ptr()
     structs = [mmq.q8_1_struct(*aq) for aq in aqs]
 
+    def gemm_call(r, stream_ptr):
+        if q6:
+            return mmq.mmq_q6K_gemm(structs[r], ctypes.c_void_p(ws[r].data_ptr()),
+                                    ctypes.c_void_p(Cs[r].data_ptr()), M, N, K, stream_ptr)
+        return mmq.mmq_q4K_gemm_path(structs[r], ctypes.c_void_p(ws[r].data_ptr()),
+                                     ctypes.c_void_p(Cs[r].data_ptr()), M, N, K, path, stream_ptr)
+
     def launch(i):
-        r = i % R
-        rc = mmq.mmq_q4K_gemm_path(structs[r], ctypes.c_void_p(ws[r].data_ptr()),
-                                   ctypes.c_void_p(Cs[r].data_ptr()), M, N, K, path, sp)
+        rc = gemm_call(i % R, sp)
         if rc:
             raise mmq.MMQError(rc, "gemm")
 
@@ -82,9 +95,7 @@ def time_gemm(M, K, N, path, reps, dev, graph=True):
                 for i in range(reps):
                     r = i % R
                     if label == "gemm":
-                        rc = mmq.mmq_q4K_gemm_path(structs[r], ctypes.c_void_p(ws[r].data_ptr()),
-                                                   ctypes.c_void_p(Cs[r].data_ptr()), M, N, K, path,
-                                                   global_sp)
+                        rc = gemm_call(r, global_sp)
                     else:
                         rc = mmq.mmq_quantize_q8_1(ctypes.c_void_p(xs[r].data_ptr()), M, K,
                                                    structs[r], global_sp)
@@ -125,7 +136,7 @@ def main():
             t, R = time_gemm(M, K, N, path, args.reps, dev, graph=not args.no_graph)
             ms = t["gemm_graph"]
             macs = M * N * K
-            gbytes = (N * K * 0.5625 + M * K * 1.25 + M * N * 4) / 1e9
+            gbytes = (N * K * (0.875 if path == "q6k" else 0.5625) + M * K * 1.25 + M * N * 4) / 1e9
             print(json.dumps({
                 "workload": name, "M": M, "K": K, "N": N, "path": pname,
                 "gemm_us": ms * 1e3, "tmacs": macs / (ms * 1e-3) / 1e12,

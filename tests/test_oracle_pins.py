@@ -359,3 +359,97 @@ def test_ffn_silu_closed_forms():
     assert ffn.silu(-800.0) == 0.0 or abs(ffn.silu(-800.0)) < 1e-300
     g = np.array([1.0, -2.0]); u = np.array([3.0, 0.5])
     assert np.allclose(ffn.swiglu(g, u), [3.0 / (1 + np.exp(-1.0)), 0.5 * -2.0 / (1 + np.exp(2.0))])
+
+
+# ---------------------------------------------------------------------------
+# q6_K x q8_1: oracle.q6k
+# ---------------------------------------------------------------------------
+def _q6k_golden():
+    vals = {}
+    for line in open(os.path.join(os.path.dirname(__file__), "golden", "q6k_bytes.txt")):
+        line = line.strip()
+        if line and not line.startswith("#"):
+            f = line.split()
+            vals[int(f[0])] = int(f[1], 16)
+    return vals
+
+
+def _q6k_golden_fields():
+    e = np.arange(256)
+    q = (e % 64 - 32)[None, :]
+    sc = (np.arange(16) - 8)[None, :]
+    return q, sc, np.ones((1, 1))
+
+
+def test_q6k_hand_packed_bytes():
+    from oracle import q6k
+    from tests import q6k_layout
+    q, sc, d = _q6k_golden_fields()
+    blk = q6k_layout.encode(q, sc, d).reshape(-1)
+    for off, v in _q6k_golden().items():
+        assert blk[off] == v, (off, hex(blk[off]), hex(v))
+    u = q6k.unpack_q6K(blk, 1, 256)
+    assert (u["q"] == q).all() and (u["sc"] == sc).all() and (u["d"] == 1.0).all()
+
+
+def test_q6k_round_trip_random_fields():
+    from oracle import q6k
+    from tests import q6k_layout
+    rng = np.random.default_rng(21)
+    N, K = 5, 768
+    q = rng.integers(-32, 32, (N, K))
+    sc = rng.integers(-128, 128, (N, K // 16))
+    d = rng.uniform(-2, 2, (N, K // 256)).astype(np.float16)
+    u = q6k.unpack_q6K(q6k_layout.encode(q, sc, d), N, K)
+    assert (u["q"] == q).all() and (u["sc"] == sc).all() and (u["d"] == d.astype(np.float64)).all()
+
+
+def test_q6k_block_dots_brute_force():
+    from oracle import q6k
+    from tests import q6k_layout
+    rng = np.random.default_rng(22)
+    M, N, K = 3, 4, 512
+    qa = rng.integers(-127, 128, (M, K)).astype(np.int8)
+    q = rng.integers(-32, 32, (N, K))
+    blk = q6k_layout.encode(q, rng.integers(-128, 128, (N, K // 16)), np.ones((N, 2)))
+    S = q6k.block_dots16(qa, blk, N)
+    for i in range(M):
+        for j in range(N):
+            for s in range(K // 16):
+                assert S[i, j, s] == sum(int(qa[i, 16 * s + k]) * int(q[j, 16 * s + k]) for k in range(16))
+
+
+def test_q6k_worked_examples():
+    from oracle import q6k
+    from tests import q6k_layout
+    M, N, K = 1, 3, 256
+    # x = 1 everywhere: q8_1 gives da = fl32(1/127), q = 127 in every block
+    x = np.ones((M, K), np.float32)
+    qa, da, _ = oracle.quantize_q8_1(x)
+    assert (qa == 127).all() and (da == np.float32(1.0) / np.float32(127.0)).all()
+    q = np.array([[31] * K, [0] * K, [-32] * K])          # stored u = 63, 32, 0
+    sc = np.array([[1] * 16, [5] * 16, [-128] * 16])
+    blk = q6k_layout.encode(q, sc, np.array([[1.0], [3.0], [0.5]]))
+    C, C64, T = q6k.gemm(qa, da, blk, N)
+    da64 = float(da[0, 0])
+    assert C64[0, 0] == 256 * 127 * 31 * da64                # 8 blocks x 2 halves x 16 x 127 x 31 x 1
+    assert C64[0, 1] == 0.0                                  # q = 0: no minimum term to leave behind
+    assert C64[0, 2] == 256 * 127 * (-32) * (-128) * 0.5 * da64
+    assert (T[0] == np.abs(C64[0])).all()                    # all products of one sign per row
+
+
+def test_q6k_gemm_equals_dequantized_dot():
+    from oracle import q6k
+    from tests import q6k_layout
+    rng = np.random.default_rng(23)
+    M, N, K = 4, 5, 512
+    x = rng.standard_normal((M, K)).astype(np.float32)
+    qa, da, _ = oracle.quantize_q8_1(x)
+    blk = q6k_layout.encode(rng.integers(-32, 32, (N, K)), rng.integers(-128, 128, (N, K // 16)),
+                            rng.uniform(1e-3, 1e-2, (N, 2)))
+    C, C64, T = q6k.gemm(qa, da, blk, N)
+    D = q6k.dequant_dot(qa, da, blk, N)
+    assert np.allclose(C64, D, rtol=1e-12, atol=1e-12 * np.abs(T).max())
+    Cs, C64s, Ts = q6k.gemm(qa, da, blk, N, rows=[3, 0, 2], cols=[1, 4, 0])
+    assert np.allclose(C64s, C64[[3, 0, 2], [1, 4, 0]], rtol=1e-14, atol=0)
+    assert np.allclose(Ts, T[[3, 0, 2], [1, 4, 0]], rtol=1e-14, atol=0)
