@@ -236,6 +236,37 @@ int mmq_q6K_gemm(mmq_q8_1_t aq, const uint8_t* bq6k_dev, float* C, int64_t M,
 int mmq_q6K_block_dots(mmq_q8_1_t aq, const uint8_t* bq6k_dev, int32_t* S,
                        int64_t M, int64_t N, int64_t K, void* stream);
 
+/* ---- GGUF interop (host).  Reads and writes the tensors of GGUF files
+ * (versions 2 and 3, little endian), the file format the customary q4_K /
+ * q6_K super-block layouts come from.  Files are untrusted input: every
+ * length and offset is checked against the file size; a file that does not
+ * parse gives MMQ_ERR_ARG.  Tensor types (GGUF numbering): */
+#define MMQ_GGUF_F32 0
+#define MMQ_GGUF_F16 1
+#define MMQ_GGUF_Q4_K 12
+#define MMQ_GGUF_Q6_K 14
+typedef struct mmq_gguf mmq_gguf;
+
+/* Parse the header and tensor table of `path`; *out owns the open file
+ * until mmq_gguf_close.  Tensors of other types are listed with nbytes 0. */
+int mmq_gguf_open(const char* path, mmq_gguf** out);
+void mmq_gguf_close(mmq_gguf* h);
+int64_t mmq_gguf_tensor_count(const mmq_gguf* h);
+/* Index of the tensor called `name`, or -1. */
+int mmq_gguf_find(const mmq_gguf* h, const char* name);
+/* Name (truncated to name_cap - 1 bytes, NUL-terminated), type, number of
+ * dims and dims (dims4[0] the contiguous one; unused entries 1) and the
+ * byte size of tensor i (0 if its type is not one of the four above). */
+int mmq_gguf_tensor_info(const mmq_gguf* h, int64_t i, char* name, size_t name_cap,
+                         uint32_t* type, uint32_t* ndim, int64_t* dims4, uint64_t* nbytes);
+/* Copy tensor i's bytes into host memory (cap >= its nbytes). */
+int mmq_gguf_read(mmq_gguf* h, int64_t i, void* dst_host, uint64_t cap);
+/* Write n two-dimensional tensors (dims2[2i] the contiguous dim, dims2[2i+1]
+ * the rows) with general.alignment = 32.  For q4_K / q6_K the bytes are the
+ * customary super-blocks (mmq_pack_q4K / mmq_pack_q6K output). */
+int mmq_gguf_write(const char* path, int64_t n, const char* const* names,
+                   const uint32_t* types, const int64_t* dims2, const void* const* data);
+
 /* Synchronizes `stream`, then returns and clears the current device's status
  * word: MMQ_OK, or MMQ_ERR_DEVICE_TIMEOUT if a kernel's bounded wait gave up
  * since the last call (that kernel's output is then invalid), or

@@ -31,6 +31,7 @@ MMQ_PATH_SMALL_M = 3
 MMQ_PATH_TC_PAIR = 4
 MMQ_PATH_TC_SMALL = 5
 SMALL_M_MAX = 64
+MMQ_GGUF_F32, MMQ_GGUF_F16, MMQ_GGUF_Q4_K, MMQ_GGUF_Q6_K = 0, 1, 12, 14
 
 # Every symbol include/mmq.h declares.
 EXPORTS = (
@@ -40,6 +41,8 @@ EXPORTS = (
     "mmq_q4K_gemm_swiglu_q8_1", "mmq_interleave_rows_q4K",
     "mmq_q6K_bytes", "mmq_pack_q6K", "mmq_q6K_dev_bytes", "mmq_repack_q6K", "mmq_q6K_gemm",
     "mmq_q6K_block_dots",
+    "mmq_gguf_open", "mmq_gguf_close", "mmq_gguf_tensor_count", "mmq_gguf_find", "mmq_gguf_tensor_info",
+    "mmq_gguf_read", "mmq_gguf_write",
     "mmq_status", "mmq_strerror", "mmq_debug_inject_timeout",
 )
 
@@ -89,6 +92,17 @@ def load_library(path: str = LIB_PATH):
                 "mmq_repack_q6K": ([P, P, I, I, P], ctypes.c_int),
                 "mmq_q6K_gemm": ([Q, P, P, I, I, I, P], ctypes.c_int),
                 "mmq_q6K_block_dots": ([Q, P, P, I, I, I, P], ctypes.c_int),
+                "mmq_gguf_open": ([ctypes.c_char_p, ctypes.POINTER(P)], ctypes.c_int),
+                "mmq_gguf_close": ([P], None),
+                "mmq_gguf_tensor_count": ([P], I),
+                "mmq_gguf_find": ([P, ctypes.c_char_p], ctypes.c_int),
+                "mmq_gguf_tensor_info": ([P, I, ctypes.c_char_p, S, ctypes.POINTER(ctypes.c_uint32),
+                                          ctypes.POINTER(ctypes.c_uint32), ctypes.POINTER(ctypes.c_int64),
+                                          ctypes.POINTER(ctypes.c_uint64)], ctypes.c_int),
+                "mmq_gguf_read": ([P, I, P, ctypes.c_uint64], ctypes.c_int),
+                "mmq_gguf_write": ([ctypes.c_char_p, I, ctypes.POINTER(ctypes.c_char_p),
+                                    ctypes.POINTER(ctypes.c_uint32), ctypes.POINTER(ctypes.c_int64),
+                                    ctypes.POINTER(P)], ctypes.c_int),
                 "mmq_status": ([P], ctypes.c_int),
                 "mmq_strerror": ([ctypes.c_int], ctypes.c_char_p),
                 "mmq_debug_inject_timeout": ([ctypes.c_int], None),
@@ -337,6 +351,44 @@ def q6K_block_dots(aq, w_dev, N: int, out=None, stream=None):
     _check(mmq_q6K_block_dots(q8_1_struct(qs, da, sa), ctypes.c_void_p(w_dev.data_ptr()),
                               ctypes.c_void_p(S.data_ptr()), M, N, K, _stream_ptr(stream)), "mmq_q6K_block_dots")
     return S
+
+
+def gguf_write(path: str, tensors):
+    """tensors: list of (name, type, ne0, ne1, numpy buffer) -> a GGUF file."""
+    import numpy as np
+    lib = load_library()
+    n = len(tensors)
+    bufs = [np.ascontiguousarray(t[4]) for t in tensors]
+    names = (ctypes.c_char_p * n)(*[t[0].encode() for t in tensors])
+    types = (ctypes.c_uint32 * n)(*[t[1] for t in tensors])
+    dims = (ctypes.c_int64 * (2 * n))(*[v for t in tensors for v in (t[2], t[3])])
+    data = (ctypes.c_void_p * n)(*[b.ctypes.data_as(ctypes.c_void_p) for b in bufs])
+    _check(lib.mmq_gguf_write(path.encode(), n, names, types, dims, data), "mmq_gguf_write")
+
+
+def gguf_read(path: str):
+    """A GGUF file -> {name: (type, dims tuple, numpy uint8 bytes)} for the
+    F32 / F16 / Q4_K / Q6_K tensors (others listed with empty bytes)."""
+    import numpy as np
+    lib = load_library()
+    h = ctypes.c_void_p()
+    _check(lib.mmq_gguf_open(path.encode(), ctypes.byref(h)), "mmq_gguf_open")
+    try:
+        out = {}
+        for i in range(lib.mmq_gguf_tensor_count(h)):
+            name = ctypes.create_string_buffer(256)
+            t, nd = ctypes.c_uint32(), ctypes.c_uint32()
+            dims = (ctypes.c_int64 * 4)()
+            nb = ctypes.c_uint64()
+            _check(lib.mmq_gguf_tensor_info(h, i, name, 256, ctypes.byref(t), ctypes.byref(nd), dims,
+                                            ctypes.byref(nb)), "mmq_gguf_tensor_info")
+            buf = np.empty(nb.value, np.uint8)
+            if nb.value:
+                _check(lib.mmq_gguf_read(h, i, buf.ctypes.data_as(ctypes.c_void_p), nb.value), "mmq_gguf_read")
+            out[name.value.decode()] = (t.value, tuple(dims[:nd.value]), buf)
+        return out
+    finally:
+        lib.mmq_gguf_close(h)
 
 
 def dequantize_q4K_f16(w, N: int, K: int, out=None, stream=None):
