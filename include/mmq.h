@@ -110,6 +110,7 @@ int mmq_pack_q4K(const uint8_t* v_host, const uint8_t* sc_host,
 int mmq_q4K_gemm(mmq_q8_1_t aq, const uint8_t* bq4k, float* C, int64_t M,
                  int64_t N, int64_t K, void* stream);
 
+
 /* Kernel selection for mmq_q4K_gemm_path (testing and A/B timing). */
 #define MMQ_PATH_AUTO 0
 #define MMQ_PATH_MMA_S8 1   /* warp-level mma.sync s8 x s8 -> s32 kernel    */
@@ -135,8 +136,10 @@ int mmq_q4K_gemm_path(mmq_q8_1_t aq, const uint8_t* bq4k, float* C, int64_t M,
  * mmq_quantize_q8_1 would produce from the f32 result (per 32 output
  * columns: da = amax/127, q = roundf(c/da) clamped to +-127, sa = sum q).
  * For M > 64 the tcgen05 kernel quantizes in its epilogue and C may be NULL
- * (then no f32 result is stored).  For M <= 64 C is required: the small-M
- * kernel writes C and a quantize pass over it follows on the same stream.
+ * (then no f32 result is stored).  For M <= 4 the dot-product kernel runs in
+ * clusters of 8 CTAs (32 output columns) and quantizes in its epilogue; C
+ * may be NULL.  For 4 < M <= 64 C is required: the small-M kernel writes C
+ * and a quantize pass over it follows on the same stream.
  * Otherwise as mmq_q4K_gemm (same argument rules and error codes). */
 int mmq_q4K_gemm_q8_1(mmq_q8_1_t aq, const uint8_t* bq4k, float* C, mmq_q8_1_t out,
                       int64_t M, int64_t N, int64_t K, void* stream);
@@ -275,6 +278,15 @@ int mmq_status(void* stream);
 
 /* Static text for an MMQ_* code. */
 const char* mmq_strerror(int code);
+
+/* Programmatic dependent launch (process-wide, default off): when enabled,
+ * the q8_1 prepass and the few-token GEMM kernels (M <= 64) are launched so
+ * that each may start while the previous kernel on its stream finishes.  A
+ * kernel so launched issues only its weight loads before it waits for the
+ * previous grid to complete; it reads activations and writes its outputs
+ * only after that wait, so results are the same either way.  Hides most of
+ * the per-kernel start cost in a decode-style sequence of small GEMMs. */
+void mmq_set_programmatic_launch(int enable);
 
 /* Test hook: when nonzero, the next tensor-core GEMM launch on this host
  * thread withholds one producer arrival so that its consumers' bounded

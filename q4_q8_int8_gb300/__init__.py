@@ -43,7 +43,7 @@ EXPORTS = (
     "mmq_q6K_block_dots",
     "mmq_gguf_open", "mmq_gguf_close", "mmq_gguf_tensor_count", "mmq_gguf_find", "mmq_gguf_tensor_info",
     "mmq_gguf_read", "mmq_gguf_write",
-    "mmq_status", "mmq_strerror", "mmq_debug_inject_timeout",
+    "mmq_status", "mmq_strerror", "mmq_debug_inject_timeout", "mmq_set_programmatic_launch",
 )
 
 
@@ -106,6 +106,7 @@ def load_library(path: str = LIB_PATH):
                 "mmq_status": ([P], ctypes.c_int),
                 "mmq_strerror": ([ctypes.c_int], ctypes.c_char_p),
                 "mmq_debug_inject_timeout": ([ctypes.c_int], None),
+                "mmq_set_programmatic_launch": ([ctypes.c_int], None),
             }
             for name, (args, res) in sigs.items():
                 f = getattr(lib, name)
@@ -162,6 +163,10 @@ def mmq_strerror(code):
 
 def mmq_debug_inject_timeout(enable):
     load_library().mmq_debug_inject_timeout(1 if enable else 0)
+
+
+def mmq_set_programmatic_launch(enable):
+    load_library().mmq_set_programmatic_launch(1 if enable else 0)
 
 
 def strerror(code: int) -> str:

@@ -15,6 +15,7 @@ int* g_status_addr[kMaxDevices];       // device address of g_status_word
 signed char g_arch_ok[kMaxDevices];    // 0 unknown, 1 sm_103, -1 other
 
 thread_local int t_inject_timeout = 0;
+std::atomic<int> g_programmatic_launch{0};
 
 int current_device(int* dev) {
     if (cudaGetDevice(dev) != cudaSuccess) { cudaGetLastError(); return MMQ_ERR_CUDA; }
@@ -69,6 +70,8 @@ int from_cuda(cudaError_t e) {
 }  // namespace
 
 namespace mmq {
+
+bool programmatic_launch_enabled() { return g_programmatic_launch.load(std::memory_order_relaxed) != 0; }
 
 int* status_word_ptr() {
     int dev;
@@ -189,10 +192,11 @@ int mmq_q4K_gemm_q8_1(mmq_q8_1_t aq, const uint8_t* bq4k, float* C, mmq_q8_1_t o
     if (rc) return rc;
     if (N % 32 != 0) return MMQ_ERR_ARG;
     const bool small = M <= mmq::kSmallMMax;
-    if (small && !C) return MMQ_ERR_ARG;   // the small-M kernel writes C, then it is quantized
+    if (small && M > 4 && !C) return MMQ_ERR_ARG;   // the mma.sync kernel writes C, then it is quantized
     rc = check_gemm_args(aq, bq4k, C ? static_cast<const void*>(C) : static_cast<const void*>(out.qs), M, N, K);
     if (rc) return rc;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (M <= 4) return from_cuda(mmq::launch_gemv_q8_1(aq, bq4k, C, out, M, N, K, s));   // one kernel
     if (small) {
         if ((rc = run_gemm(aq, bq4k, C, nullptr, M, N, K, MMQ_PATH_SMALL_M, s))) return rc;
         return from_cuda(mmq::launch_quantize_q8_1(C, M, N, out, s));
@@ -332,5 +336,7 @@ const char* mmq_strerror(int code) {
 }
 
 void mmq_debug_inject_timeout(int enable) { t_inject_timeout = enable ? 1 : 0; }
+
+void mmq_set_programmatic_launch(int enable) { g_programmatic_launch.store(enable ? 1 : 0); }
 
 }  // extern "C"

@@ -40,6 +40,7 @@
 
 #include "mmq_internal.h"
 #include "sm103_ptx.cuh"
+#include "q8_round.cuh"
 
 namespace {
 
@@ -140,6 +141,7 @@ gemm_small_kernel(const __grid_constant__ SmallMaps maps, float* __restrict__ C,
     const Layout L = Layout::make(NF, G, D, split);
     const uint32_t bar0 = sbase + L.bar_off;
     const AbortFlag abort_flag{sbase + uint32_t(L.bar_off + 8 * G * D)};
+    griddep_launch_dependents();
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int grp = warp >> 2, gt = threadIdx.x & 127;   // group, thread within the group
@@ -168,20 +170,34 @@ gemm_small_kernel(const __grid_constant__ SmallMaps maps, float* __restrict__ C,
     int last_issued[D];   // leader only: last round issued into each stage
 #pragma unroll
     for (int q = 0; q < D; ++q) last_issued[q] = -1;
-    auto issue = [&](int i) {
-        const int sb = sb_begin + i;
+    // the weight copy (which sets the stage's expected bytes) and the token
+    // copies of one round, issued separately so that the first rounds'
+    // weights can stream before the programmatic-launch wait
+    auto issue_w = [&](int i) {
         const int round = (i - grp) / G, slot = round % D;
         const uint32_t bar = stage_bar(slot), st_s = sbase + uint32_t(stage_off(slot));
         mbar_arrive_expect_tx(bar, stage_tx);
-        tma_load_2d(st_s, &maps.w, bar, sb * 144, n0);
+        tma_load_2d(st_s, &maps.w, bar, (sb_begin + i) * 144, n0);
+        last_issued[slot] = round;
+    };
+    auto issue_a = [&](int i) {
+        const int sb = sb_begin + i;
+        const int slot = ((i - grp) / G) % D;
+        const uint32_t bar = stage_bar(slot), st_s = sbase + uint32_t(stage_off(slot));
         tma_load_2d(st_s + L.aoff, &maps.a, bar, sb * 256, 0);
         tma_load_2d(st_s + L.aoff + mp * 128, &maps.a, bar, sb * 256 + 128, 0);
         tma_load_2d(st_s + L.doff, &maps.da, bar, sb * 8, 0);
         tma_load_2d(st_s + L.soff, &maps.sa, bar, sb * 8, 0);
-        last_issued[slot] = round;
+    };
+    auto issue = [&](int i) {
+        issue_w(i);
+        issue_a(i);
     };
     if (gt == 0)
-        for (int q = 0; q < D && grp + q * G < nmine; ++q) issue(grp + q * G);
+        for (int q = 0; q < D && grp + q * G < nmine; ++q) issue_w(grp + q * G);
+    griddep_wait();   // the previous kernel's outputs (tokens) are complete
+    if (gt == 0)
+        for (int q = 0; q < D && grp + q * G < nmine; ++q) issue_a(grp + q * G);
 
     uint64_t acc[NF][2];   // per token fragment: rows g (tokens 2j, 2j+1) and g + 8
 #pragma unroll
@@ -345,10 +361,9 @@ gemm_small_kernel(const __grid_constant__ SmallMaps maps, float* __restrict__ C,
     }
 }
 
-
 // ---------------------------------------------------------------------------
-// M <= 4 tokens: one warp per weight row, a plain streaming dot product.
-// Lane l takes the row's chunk pairs l, l+32, ...: 32 nibble bytes (chunk 2p
+// M <= 4 tokens: a plain streaming dot product, one warp per few weight rows.
+// Lane l takes each row's chunk pairs l, l+32, ...: 32 nibble bytes (chunk 2p
 // in the low nibbles, 2p+1 in the high ones, both in natural k order) plus
 // the super-block header.  S comes from dp4a (unsigned nibble bytes x signed
 // int8 quants, exact int32), then the per-chunk rescale with the fold; the
@@ -360,98 +375,232 @@ __device__ __forceinline__ int dp4a_us(uint32_t a_u8, uint32_t b_s8, int c) {
     return d;
 }
 
-template <int MT>
+// q8_1 of one 32-element block held by 8 lanes (one float4 each; the
+// group's lanes xor-reduce amax and the sum): the rounding of the prepass
+// (reciprocal with an exactness check, IEEE division where a quotient lies
+// too close to a half-integer), so the bits equal quantize-after-store.
+__device__ __forceinline__ uint32_t quantize_group8(float4 v, float& d, int& sum) {
+    using namespace mmq::q8;
+    float amax = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
+    d = __fdiv_rn(amax, 127.0f);
+    int q0 = 0, q1 = 0, q2 = 0, q3 = 0;   // a zero scale gives zero quants
+    if (d != 0.0f) {
+        bool redo = d < 0x1p-126f;
+        const float r = __frcp_rn(d);
+        q0 = quant_fast(v.x, r, redo);
+        q1 = quant_fast(v.y, r, redo);
+        q2 = quant_fast(v.z, r, redo);
+        q3 = quant_fast(v.w, r, redo);
+        if (redo) {
+            q0 = quant_exact(v.x, d);
+            q1 = quant_exact(v.y, d);
+            q2 = quant_exact(v.z, d);
+            q3 = quant_exact(v.w, d);
+        }
+    }
+    q0 = clamp127(q0);
+    q1 = clamp127(q1);
+    q2 = clamp127(q2);
+    q3 = clamp127(q3);
+    sum = q0 + q1 + q2 + q3;
+    sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+    sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+    sum += __shfl_xor_sync(0xffffffffu, sum, 4);
+    return (uint32_t(q0) & 0xFFu) | ((uint32_t(q1) & 0xFFu) << 8) | ((uint32_t(q2) & 0xFFu) << 16) |
+           ((uint32_t(q3) & 0xFFu) << 24);
+}
+
+constexpr int kQC = 8;   // CTAs (of 4 weight rows) per cluster: one q8_1 block of outputs
+
+__device__ __forceinline__ void st_dsmem_f32(uint32_t addr, float v) {
+    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+
+// One warp per R consecutive weight rows: each activation load (the token's
+// 64 quants of a chunk pair, its two da and sa) serves R rows, so the
+// activation traffic through L1 is 1/R of one row per warp.  R rows x the
+// lane's pair of weights (48 bytes each) are all requested before any is
+// used.  Per (row, token) the arithmetic is the same for every R: the same
+// fmaf sequence per pair in the lane, the same xor-shuffle tree.
+//
+// kQ8: the result is also written as q8_1 (the next GEMM's activations,
+// with the bits of a prepass over C): launched in clusters of 8 / R CTAs,
+// whose 32 consecutive output rows form one q8_1 block per token; each warp
+// pushes its rows' sums into rank 0's shared memory and rank 0 quantizes
+// the block.  C may then be null.
+template <int MT, int R, bool kQ8>
 __global__ void __launch_bounds__(128)
-gemv_dp4a_kernel(mmq_q8_1_t aq, const uint8_t* __restrict__ w, float* __restrict__ C, int M,
-                 int N, int K) {
-    constexpr int kU = 2;   // chunk pairs per lane per batch; all their loads are issued first
+gemv_dp4a_kernel(mmq_q8_1_t aq, const uint8_t* __restrict__ w, float* __restrict__ C, mmq_q8_1_t out,
+                 int M, int N, int K) {
+    constexpr int kCluster = 8 / R;   // kQ8: CTAs per 32 output rows
+    __shared__ __align__(16) float red[kQ8 ? MT : 1][32];   // kQ8, rank 0: the cluster's outputs [t][row]
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int row = blockIdx.x * 4 + warp;
-    if (row >= N) return;
+    const int row0 = (blockIdx.x * 4 + warp) * R;   // this warp's rows row0 .. row0 + R - 1
+    griddep_launch_dependents();
+    if (!kQ8 && row0 >= N) return;   // (with kQ8 every row exists: N % 32 == 0)
+    if (kQ8) asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");   // this CTA has started
     const int nsb = K / 256, npairs = K / 64, nb = K / 32;
-    const uint8_t* wrow = w + int64_t(row) * nsb * 144;
-    float acc[MT];
+    float acc[MT][R];
 #pragma unroll
-    for (int t = 0; t < MT; ++t) acc[t] = 0.0f;
-    for (int base = 0; base < npairs; base += 32 * kU) {
-        uint4 hdr[kU], q0[kU], q1[kU];
+    for (int t = 0; t < MT; ++t)
 #pragma unroll
-        for (int u = 0; u < kU; ++u) {
-            const int pr = base + lane + 32 * u;
-            if (pr < npairs) {
-                const uint8_t* blk = wrow + (pr >> 2) * 144;
-                hdr[u] = __ldg(reinterpret_cast<const uint4*>(blk));
-                q0[u] = __ldcs(reinterpret_cast<const uint4*>(blk + 16 + 32 * (pr & 3)));
-                q1[u] = __ldcs(reinterpret_cast<const uint4*>(blk + 32 + 32 * (pr & 3)));
+        for (int r = 0; r < R; ++r) acc[t][r] = 0.0f;
+    for (int base = 0; base < npairs; base += 32) {
+        const int pr = base + lane;
+        const int p = pr & 3;
+        uint4 hdr[R], q0[R], q1[R];
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            if (pr < npairs && row0 + r < N) {
+                const uint8_t* blk = w + (int64_t(row0 + r) * nsb + (pr >> 2)) * 144;
+                hdr[r] = __ldg(reinterpret_cast<const uint4*>(blk));
+                q0[r] = __ldcs(reinterpret_cast<const uint4*>(blk + 16 + 32 * p));
+                q1[r] = __ldcs(reinterpret_cast<const uint4*>(blk + 32 + 32 * p));
+            } else {
+                hdr[r] = q0[r] = q1[r] = make_uint4(0u, 0u, 0u, 0u);   // contributes 0
             }
         }
+        // weights stream in while the previous kernel (programmatic dependent
+        // launch) finishes; activations and C only after it has
+        if (base == 0) griddep_wait();
+        if (pr >= npairs) continue;
+        float dsv[R][2], dmv[R][2];
 #pragma unroll
-        for (int u = 0; u < kU; ++u) {
-            const int pr = base + lane + 32 * u;
-            if (pr >= npairs) continue;
-            const int p = pr & 3;
-            const float d = __half2float(__ushort_as_half(uint16_t(hdr[u].x & 0xFFFFu)));
-            const float dmin = __half2float(__ushort_as_half(uint16_t(hdr[u].x >> 16)));
-            float dsv[2], dmv[2];
+        for (int r = 0; r < R; ++r) {
+            const float d = __half2float(__ushort_as_half(uint16_t(hdr[r].x & 0xFFFFu)));
+            const float dmin = __half2float(__ushort_as_half(uint16_t(hdr[r].x >> 16)));
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 const int c = 2 * p + h;   // sub-block within the super-block
                 uint32_t sc, m;
                 if (c < 4) {
-                    sc = (hdr[u].y >> (8 * c)) & 63u;
-                    m = (hdr[u].z >> (8 * c)) & 63u;
+                    sc = (hdr[r].y >> (8 * c)) & 63u;
+                    m = (hdr[r].z >> (8 * c)) & 63u;
                 } else {
                     const int bsh = 8 * (c - 4);
-                    sc = ((hdr[u].w >> bsh) & 15u) | (((hdr[u].y >> (bsh + 6)) & 3u) << 4);
-                    m = ((hdr[u].w >> (bsh + 4)) & 15u) | (((hdr[u].z >> (bsh + 6)) & 3u) << 4);
+                    sc = ((hdr[r].w >> bsh) & 15u) | (((hdr[r].y >> (bsh + 6)) & 3u) << 4);
+                    m = ((hdr[r].w >> (bsh + 4)) & 15u) | (((hdr[r].z >> (bsh + 6)) & 3u) << 4);
                 }
-                dsv[h] = d * float(sc);
-                dmv[h] = -(dmin * float(m));
+                dsv[r][h] = d * float(sc);
+                dmv[r][h] = -(dmin * float(m));
             }
-            const uint32_t wv[8] = {q0[u].x, q0[u].y, q0[u].z, q0[u].w, q1[u].x, q1[u].y, q1[u].z, q1[u].w};
-            uint32_t lo[8], hi[8];
+        }
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                lo[e] = wv[e] & 0x0F0F0F0Fu;          // chunk 2p, natural k order
-                hi[e] = (wv[e] >> 4) & 0x0F0F0F0Fu;   // chunk 2p + 1
-            }
+        for (int t = 0; t < MT; ++t) {
+            if (t < M) {
+                const int8_t* qt = aq.qs + int64_t(t) * K + 64 * pr;
+                const uint4 a0 = __ldg(reinterpret_cast<const uint4*>(qt));
+                const uint4 a1 = __ldg(reinterpret_cast<const uint4*>(qt + 16));
+                const uint4 a2 = __ldg(reinterpret_cast<const uint4*>(qt + 32));
+                const uint4 a3 = __ldg(reinterpret_cast<const uint4*>(qt + 48));
+                const float2 da = __ldg(reinterpret_cast<const float2*>(aq.da + int64_t(t) * nb + 2 * pr));
+                const int2 sa = __ldg(reinterpret_cast<const int2*>(aq.sa + int64_t(t) * nb + 2 * pr));
 #pragma unroll
-            for (int t = 0; t < MT; ++t) {
-                if (t < M) {
-                    const int8_t* qt = aq.qs + int64_t(t) * K + 64 * pr;
-                    const uint4 a0 = __ldg(reinterpret_cast<const uint4*>(qt));
-                    const uint4 a1 = __ldg(reinterpret_cast<const uint4*>(qt + 16));
-                    const uint4 a2 = __ldg(reinterpret_cast<const uint4*>(qt + 32));
-                    const uint4 a3 = __ldg(reinterpret_cast<const uint4*>(qt + 48));
+                for (int r = 0; r < R; ++r) {
+                    // chunk 2p in the low nibbles, 2p + 1 in the high ones, natural k order
+                    const uint32_t wv[8] = {q0[r].x, q0[r].y, q0[r].z, q0[r].w, q1[r].x, q1[r].y, q1[r].z, q1[r].w};
+                    const uint32_t av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+                    const uint32_t bv[8] = {a2.x, a2.y, a2.z, a2.w, a3.x, a3.y, a3.z, a3.w};
                     int s0 = 0, s1 = 0;
-                    s0 = dp4a_us(lo[0], a0.x, s0); s0 = dp4a_us(lo[1], a0.y, s0);
-                    s0 = dp4a_us(lo[2], a0.z, s0); s0 = dp4a_us(lo[3], a0.w, s0);
-                    s0 = dp4a_us(lo[4], a1.x, s0); s0 = dp4a_us(lo[5], a1.y, s0);
-                    s0 = dp4a_us(lo[6], a1.z, s0); s0 = dp4a_us(lo[7], a1.w, s0);
-                    s1 = dp4a_us(hi[0], a2.x, s1); s1 = dp4a_us(hi[1], a2.y, s1);
-                    s1 = dp4a_us(hi[2], a2.z, s1); s1 = dp4a_us(hi[3], a2.w, s1);
-                    s1 = dp4a_us(hi[4], a3.x, s1); s1 = dp4a_us(hi[5], a3.y, s1);
-                    s1 = dp4a_us(hi[6], a3.z, s1); s1 = dp4a_us(hi[7], a3.w, s1);
-                    const float2 da = __ldg(reinterpret_cast<const float2*>(aq.da + int64_t(t) * nb + 2 * pr));
-                    const int2 sa = __ldg(reinterpret_cast<const int2*>(aq.sa + int64_t(t) * nb + 2 * pr));
-                    float a = acc[t];
-                    a = fmaf(da.x * dsv[0], float(s0), a);
-                    a = fmaf(da.x * float(sa.x), dmv[0], a);   // rank-1 fold: dma = da*sa
-                    a = fmaf(da.y * dsv[1], float(s1), a);
-                    a = fmaf(da.y * float(sa.y), dmv[1], a);
-                    acc[t] = a;
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        s0 = dp4a_us(wv[e] & 0x0F0F0F0Fu, av[e], s0);
+                        s1 = dp4a_us((wv[e] >> 4) & 0x0F0F0F0Fu, bv[e], s1);
+                    }
+                    float a = acc[t][r];
+                    a = fmaf(da.x * dsv[r][0], float(s0), a);
+                    a = fmaf(da.x * float(sa.x), dmv[r][0], a);   // rank-1 fold: dma = da*sa
+                    a = fmaf(da.y * dsv[r][1], float(s1), a);
+                    a = fmaf(da.y * float(sa.y), dmv[r][1], a);
+                    acc[t][r] = a;
                 }
             }
         }
     }
 #pragma unroll
     for (int t = 0; t < MT; ++t) {
-        float a = acc[t];
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
-        if (lane == 0 && t < M) C[int64_t(t) * N + row] = a;
+        for (int r = 0; r < R; ++r) {
+            float a = acc[t][r];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
+            if (lane == 0 && t < M && row0 + r < N && C) C[int64_t(t) * N + row0 + r] = a;
+            acc[t][r] = a;
+        }
+    }
+    if constexpr (kQ8) {
+        const uint32_t rank = cluster_ctarank();
+        asm volatile("barrier.cluster.wait.aligned;" ::: "memory");   // every CTA of the cluster has started
+        if (lane == 0) {
+#pragma unroll
+            for (int t = 0; t < MT; ++t)
+#pragma unroll
+                for (int r = 0; r < R; ++r)
+                    if (t < M)
+                        st_dsmem_f32(map_shared_rank(smem_u32(&red[t][(rank * 4 + warp) * R + r]), 0), acc[t][r]);
+        }
+        cluster_sync();   // the 32 rows' sums are in rank 0
+        if (rank == 0 && warp == 0) {
+            const int t = lane >> 3, part = lane & 7;   // 8 lanes per token
+            const float4 v = t < M ? *reinterpret_cast<const float4*>(&red[t < MT ? t : 0][part * 4])
+                                   : make_float4(0.f, 0.f, 0.f, 0.f);
+            float d;
+            int sum;
+            const uint32_t word = quantize_group8(v, d, sum);
+            const int blk = int(blockIdx.x / kCluster);   // output columns 32 blk .. 32 blk + 31
+            if (t < M) {
+                *reinterpret_cast<uint32_t*>(out.qs + int64_t(t) * N + 32 * blk + part * 4) = word;
+                if (part == 0) {
+                    out.da[int64_t(t) * (N / 32) + blk] = d;
+                    out.sa[int64_t(t) * (N / 32) + blk] = sum;
+                }
+            }
+        }
     }
 }
+
+// Rows per warp of the dot-product kernel.  Measured on the 7B decode chain
+// (224 dependent GEMMs, programmatic launch): R = 4 beats 1, 2 and (at one
+// token) 8 for 1, 2 and 4 tokens.
+constexpr int kGemvRows = 4;
+
+template <int MT, bool kQ8>
+cudaError_t launch_gemv(mmq_q8_1_t aq, const uint8_t* w, float* C, mmq_q8_1_t out, int64_t M, int64_t N, int64_t K,
+                        cudaStream_t s) {
+    constexpr int R = kGemvRows;
+    cudaLaunchAttribute attr[2];
+    const unsigned grid = unsigned((N + 4 * R - 1) / (4 * R));
+    cudaLaunchConfig_t cfg = mmq::launch_config(dim3(grid), dim3(128), 0, s, attr);
+    if (kQ8) {   // grid = N / (4R) is a multiple of 8 / R when N % 32 == 0
+        attr[cfg.numAttrs].id = cudaLaunchAttributeClusterDimension;
+        attr[cfg.numAttrs].val.clusterDim.x = 8 / R;
+        attr[cfg.numAttrs].val.clusterDim.y = 1;
+        attr[cfg.numAttrs].val.clusterDim.z = 1;
+        ++cfg.numAttrs;
+    }
+    return cudaLaunchKernelEx(&cfg, gemv_dp4a_kernel<MT, R, kQ8>, aq, w, C, out, int(M), int(N), int(K));
+}
+
+}  // namespace
+
+namespace mmq {
+
+cudaError_t launch_gemv_q8_1(mmq_q8_1_t aq, const uint8_t* w, float* C, mmq_q8_1_t out, int64_t M, int64_t N,
+                             int64_t K, cudaStream_t s) {
+    if (M < 1 || M > 4 || N % 32 != 0) return cudaErrorInvalidValue;
+    switch (M) {
+        case 1: return launch_gemv<1, true>(aq, w, C, out, M, N, K, s);
+        case 2: return launch_gemv<2, true>(aq, w, C, out, M, N, K, s);
+        default: return launch_gemv<4, true>(aq, w, C, out, M, N, K, s);
+    }
+}
+
+}  // namespace mmq
+
+namespace {
 
 PFN_cuTensorMapEncodeTiled_v12000 get_encode_small() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -506,18 +655,14 @@ cudaError_t launch_nf(const SmallMaps& maps, float* C, int64_t M, int64_t N, int
     auto k = gemm_small_kernel<NF, G, D>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(unsigned(row_tiles * split));
-    cfg.blockDim = dim3(G * 128);
-    cfg.dynamicSmemBytes = size_t(smem);
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = unsigned(split);
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cudaLaunchAttribute attr[2];
+    cudaLaunchConfig_t cfg = mmq::launch_config(dim3(unsigned(row_tiles * split)), dim3(G * 128), size_t(smem), s,
+                                                attr);
+    attr[cfg.numAttrs].id = cudaLaunchAttributeClusterDimension;
+    attr[cfg.numAttrs].val.clusterDim.x = unsigned(split);
+    attr[cfg.numAttrs].val.clusterDim.y = 1;
+    attr[cfg.numAttrs].val.clusterDim.z = 1;
+    cfg.numAttrs += 1;
     return cudaLaunchKernelEx(&cfg, k, maps, C, int(M), int(N), int(K), split, status);
 }
 
@@ -529,13 +674,12 @@ cudaError_t launch_gemm_small_m(mmq_q8_1_t aq, const uint8_t* w, float* C, int64
                                 int64_t K, int* status, cudaStream_t s) {
     if (M > kMaxTok) return cudaErrorInvalidValue;
     if (M <= 4) {   // a few tokens: streaming dot products on dp4a
-        const unsigned grid = unsigned((N + 3) / 4);
+        const mmq_q8_1_t none = {nullptr, nullptr, nullptr};
         switch (M) {
-            case 1: gemv_dp4a_kernel<1><<<grid, 128, 0, s>>>(aq, w, C, int(M), int(N), int(K)); break;
-            case 2: gemv_dp4a_kernel<2><<<grid, 128, 0, s>>>(aq, w, C, int(M), int(N), int(K)); break;
-            default: gemv_dp4a_kernel<4><<<grid, 128, 0, s>>>(aq, w, C, int(M), int(N), int(K)); break;
+            case 1: return launch_gemv<1, false>(aq, w, C, none, M, N, K, s);
+            case 2: return launch_gemv<2, false>(aq, w, C, none, M, N, K, s);
+            default: return launch_gemv<4, false>(aq, w, C, none, M, N, K, s);
         }
-        return cudaGetLastError();
     }
     const int nf = int((M + 7) / 8);
     const uint32_t mp = uint32_t(nf * 8);

@@ -7,6 +7,31 @@
 
 namespace mmq {
 
+// Programmatic dependent launch for the kernels that support it (the q8_1
+// prepass and the few-token GEMMs): off unless mmq_set_programmatic_launch
+// turned it on.
+bool programmatic_launch_enabled();
+
+// Launch configuration with the programmatic-dependent-launch attribute
+// when it is enabled; attr must have room for it (numAttrs 0 or 1 on return,
+// more may be appended by the caller).
+inline cudaLaunchConfig_t launch_config(dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                                        cudaLaunchAttribute* attr) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 0;
+    if (programmatic_launch_enabled()) {
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.numAttrs = 1;
+    }
+    return cfg;
+}
+
 // Per-device status word (a __device__ int defined in api.cu); kernels get
 // its address as an argument and set it to an MMQ_ERR_* code on failure.
 int* status_word_ptr();   // nullptr on failure (sets no error)
@@ -33,6 +58,10 @@ cudaError_t launch_gemm_tc2(mmq_q8_1_t aq, const uint8_t* w, float* C,
 cudaError_t launch_gemm_small_m(mmq_q8_1_t aq, const uint8_t* w, float* C,
                                 int64_t M, int64_t N, int64_t K, int* status,
                                 cudaStream_t s);
+// The dp4a GEMV (M <= 4) that also writes its result as q8_1 (N % 32 == 0;
+// C may be null).
+cudaError_t launch_gemv_q8_1(mmq_q8_1_t aq, const uint8_t* w, float* C, mmq_q8_1_t out, int64_t M, int64_t N,
+                             int64_t K, cudaStream_t s);
 // tcgen05 kernel for few tokens: 128 weight rows x 16/32/64 tokens per CTA.
 cudaError_t launch_gemm_tc_small(mmq_q8_1_t aq, const uint8_t* w, float* C,
                                  int64_t M, int64_t N, int64_t K, int* status,

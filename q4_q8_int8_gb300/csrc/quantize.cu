@@ -14,6 +14,7 @@
 // quant1), so the bits match IEEE division followed by roundf.
 #include "mmq_internal.h"
 #include "q8_round.cuh"
+#include "sm103_ptx.cuh"
 
 namespace {
 
@@ -35,6 +36,10 @@ quantize_q8_1_kernel(const float* __restrict__ x, int8_t* __restrict__ qs,
     const int64_t ngroups = (nblocks + 3) / 4;
     const int64_t warp = (int64_t(blockIdx.x) * kThreads + threadIdx.x) >> 5;
     const int64_t nwarps = (int64_t(gridDim.x) * kThreads) >> 5;
+    // programmatic dependent launch: x may be the previous kernel's output,
+    // and the q8_1 planes may still be read by it
+    mmq::ptx::griddep_launch_dependents();
+    mmq::ptx::griddep_wait();
 
     for (int64_t g0 = warp * kUnroll; g0 < ngroups; g0 += nwarps * kUnroll) {
         float4 v[kUnroll];
@@ -124,8 +129,9 @@ cudaError_t launch_quantize_q8_1(const float* x, int64_t M, int64_t K, mmq_q8_1_
     int64_t ctas = (warps_needed + (kThreads / 32) - 1) / (kThreads / 32);
     if (ctas > max_ctas) ctas = max_ctas;
     if (ctas < 1) ctas = 1;
-    quantize_q8_1_kernel<<<unsigned(ctas), kThreads, 0, s>>>(x, aq.qs, aq.da, aq.sa, nblocks);
-    return cudaGetLastError();
+    cudaLaunchAttribute attr[1];
+    cudaLaunchConfig_t cfg = launch_config(dim3(unsigned(ctas)), dim3(kThreads), 0, s, attr);
+    return cudaLaunchKernelEx(&cfg, quantize_q8_1_kernel, x, aq.qs, aq.da, aq.sa, nblocks);
 }
 
 }  // namespace mmq

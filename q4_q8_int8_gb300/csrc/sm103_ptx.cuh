@@ -23,6 +23,17 @@ __device__ __forceinline__ uint64_t globaltimer() {
     return t;
 }
 
+// ------------------------------------------------ programmatic dependent launch
+// With the launch attribute set, a kernel may start before the previous one on
+// its stream has finished.  griddep_wait blocks until every prerequisite grid
+// has completed and its memory is visible (a no-op for ordinary launches);
+// griddep_launch_dependents lets the next kernel on the stream be scheduled
+// (it still waits for this one before it touches anything this one writes).
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
