@@ -413,8 +413,6 @@ __device__ __forceinline__ uint32_t quantize_group8(float4 v, float& d, int& sum
            ((uint32_t(q3) & 0xFFu) << 24);
 }
 
-constexpr int kQC = 8;   // CTAs (of 4 weight rows) per cluster: one q8_1 block of outputs
-
 __device__ __forceinline__ void st_dsmem_f32(uint32_t addr, float v) {
     asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
 }
@@ -423,24 +421,29 @@ __device__ __forceinline__ void st_dsmem_f32(uint32_t addr, float v) {
 // 64 quants of a chunk pair, its two da and sa) serves R rows, so the
 // activation traffic through L1 is 1/R of one row per warp.  R rows x the
 // lane's pair of weights (48 bytes each) are all requested before any is
-// used.  Per (row, token) the arithmetic is the same for every R: the same
-// fmaf sequence per pair in the lane, the same xor-shuffle tree.
+// used.  K is split over KS warps of the CTA (pair blocks of 32 dealt
+// round-robin), so that a long row takes fewer dependent load rounds per
+// warp and more warps have loads in flight; the KS partial sums are added
+// in slice order through shared memory.
 //
 // kQ8: the result is also written as q8_1 (the next GEMM's activations,
-// with the bits of a prepass over C): launched in clusters of 8 / R CTAs,
-// whose 32 consecutive output rows form one q8_1 block per token; each warp
-// pushes its rows' sums into rank 0's shared memory and rank 0 quantizes
-// the block.  C may then be null.
-template <int MT, int R, bool kQ8>
+// with the bits of a prepass over C): launched in clusters of CTAs whose 32
+// consecutive output rows form one q8_1 block per token; each row's sum is
+// pushed into rank 0's shared memory and rank 0 quantizes the block.  C may
+// then be null.
+template <int MT, int R, int KS, bool kQ8>
 __global__ void __launch_bounds__(128)
 gemv_dp4a_kernel(mmq_q8_1_t aq, const uint8_t* __restrict__ w, float* __restrict__ C, mmq_q8_1_t out,
                  int M, int N, int K) {
-    constexpr int kCluster = 8 / R;   // kQ8: CTAs per 32 output rows
+    constexpr int kGroups = 4 / KS;                 // row groups (of R rows) per CTA
+    constexpr int kCluster = 32 / (kGroups * R);    // kQ8: CTAs per 32 output rows
     __shared__ __align__(16) float red[kQ8 ? MT : 1][32];   // kQ8, rank 0: the cluster's outputs [t][row]
+    __shared__ float part[KS > 1 ? 4 : 1][MT][R];          // KS > 1: each warp's partial sums
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int row0 = (blockIdx.x * 4 + warp) * R;   // this warp's rows row0 .. row0 + R - 1
+    const int slice = warp % KS, grp = warp / KS;
+    const int row0 = (blockIdx.x * kGroups + grp) * R;   // this warp's rows row0 .. row0 + R - 1
     griddep_launch_dependents();
-    if (!kQ8 && row0 >= N) return;   // (with kQ8 every row exists: N % 32 == 0)
+    if (KS == 1 && !kQ8 && row0 >= N) return;   // (with kQ8 every row exists: N % 32 == 0)
     if (kQ8) asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");   // this CTA has started
     const int nsb = K / 256, npairs = K / 64, nb = K / 32;
     float acc[MT][R];
@@ -448,7 +451,7 @@ gemv_dp4a_kernel(mmq_q8_1_t aq, const uint8_t* __restrict__ w, float* __restrict
     for (int t = 0; t < MT; ++t)
 #pragma unroll
         for (int r = 0; r < R; ++r) acc[t][r] = 0.0f;
-    for (int base = 0; base < npairs; base += 32) {
+    for (int base = 32 * slice; base < npairs; base += 32 * KS) {
         const int pr = base + lane;
         const int p = pr & 3;
         uint4 hdr[R], q0[R], q1[R];
@@ -465,7 +468,7 @@ gemv_dp4a_kernel(mmq_q8_1_t aq, const uint8_t* __restrict__ w, float* __restrict
         }
         // weights stream in while the previous kernel (programmatic dependent
         // launch) finishes; activations and C only after it has
-        if (base == 0) griddep_wait();
+        if (base == 32 * slice) griddep_wait();
         if (pr >= npairs) continue;
         float dsv[R][2], dmv[R][2];
 #pragma unroll
@@ -527,20 +530,47 @@ gemv_dp4a_kernel(mmq_q8_1_t aq, const uint8_t* __restrict__ w, float* __restrict
             float a = acc[t][r];
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
-            if (lane == 0 && t < M && row0 + r < N && C) C[int64_t(t) * N + row0 + r] = a;
             acc[t][r] = a;
         }
+    }
+    if constexpr (KS > 1) {   // add the K slices' partials in slice order (slice 0 keeps the sum)
+        if (lane == 0) {
+#pragma unroll
+            for (int t = 0; t < MT; ++t)
+#pragma unroll
+                for (int r = 0; r < R; ++r) part[warp][t][r] = acc[t][r];
+        }
+        __syncthreads();
+        if (slice == 0) {
+#pragma unroll
+            for (int t = 0; t < MT; ++t)
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    float a = part[warp][t][r];
+#pragma unroll
+                    for (int q = 1; q < KS; ++q) a += part[warp + q][t][r];
+                    acc[t][r] = a;
+                }
+        }
+    }
+    if (slice == 0 && lane == 0 && C) {
+#pragma unroll
+        for (int t = 0; t < MT; ++t)
+#pragma unroll
+            for (int r = 0; r < R; ++r)
+                if (t < M && row0 + r < N) C[int64_t(t) * N + row0 + r] = acc[t][r];
     }
     if constexpr (kQ8) {
         const uint32_t rank = cluster_ctarank();
         asm volatile("barrier.cluster.wait.aligned;" ::: "memory");   // every CTA of the cluster has started
-        if (lane == 0) {
+        if (slice == 0 && lane == 0) {
 #pragma unroll
             for (int t = 0; t < MT; ++t)
 #pragma unroll
                 for (int r = 0; r < R; ++r)
                     if (t < M)
-                        st_dsmem_f32(map_shared_rank(smem_u32(&red[t][(rank * 4 + warp) * R + r]), 0), acc[t][r]);
+                        st_dsmem_f32(map_shared_rank(smem_u32(&red[t][(rank * kGroups + grp) * R + r]), 0),
+                                     acc[t][r]);
         }
         cluster_sync();   // the 32 rows' sums are in rank 0
         if (rank == 0 && warp == 0) {
@@ -567,21 +597,32 @@ gemv_dp4a_kernel(mmq_q8_1_t aq, const uint8_t* __restrict__ w, float* __restrict
 // token) 8 for 1, 2 and 4 tokens.
 constexpr int kGemvRows = 4;
 
-template <int MT, bool kQ8>
-cudaError_t launch_gemv(mmq_q8_1_t aq, const uint8_t* w, float* C, mmq_q8_1_t out, int64_t M, int64_t N, int64_t K,
-                        cudaStream_t s) {
-    constexpr int R = kGemvRows;
+template <int MT, int KS, bool kQ8>
+cudaError_t launch_gemv_ks(mmq_q8_1_t aq, const uint8_t* w, float* C, mmq_q8_1_t out, int64_t M, int64_t N,
+                           int64_t K, cudaStream_t s) {
+    constexpr int R = kGemvRows, rows = 4 / KS * R;   // rows per CTA
     cudaLaunchAttribute attr[2];
-    const unsigned grid = unsigned((N + 4 * R - 1) / (4 * R));
+    const unsigned grid = unsigned((N + rows - 1) / rows);
     cudaLaunchConfig_t cfg = mmq::launch_config(dim3(grid), dim3(128), 0, s, attr);
-    if (kQ8) {   // grid = N / (4R) is a multiple of 8 / R when N % 32 == 0
+    if (kQ8) {   // grid = N / rows is a multiple of 32 / rows when N % 32 == 0
         attr[cfg.numAttrs].id = cudaLaunchAttributeClusterDimension;
-        attr[cfg.numAttrs].val.clusterDim.x = 8 / R;
+        attr[cfg.numAttrs].val.clusterDim.x = 32 / rows;
         attr[cfg.numAttrs].val.clusterDim.y = 1;
         attr[cfg.numAttrs].val.clusterDim.z = 1;
         ++cfg.numAttrs;
     }
-    return cudaLaunchKernelEx(&cfg, gemv_dp4a_kernel<MT, R, kQ8>, aq, w, C, out, int(M), int(N), int(K));
+    return cudaLaunchKernelEx(&cfg, gemv_dp4a_kernel<MT, R, KS, kQ8>, aq, w, C, out, int(M), int(N), int(K));
+}
+
+// K split by the number of 32-pair rounds a row takes: 1 round -> 1 warp,
+// 2-3 -> 2 warps, 4 or more -> 4 warps per row group.
+template <int MT, bool kQ8>
+cudaError_t launch_gemv(mmq_q8_1_t aq, const uint8_t* w, float* C, mmq_q8_1_t out, int64_t M, int64_t N, int64_t K,
+                        cudaStream_t s) {
+    const int64_t rounds = (K / 64 + 31) / 32;
+    if (rounds >= 4) return launch_gemv_ks<MT, 4, kQ8>(aq, w, C, out, M, N, K, s);
+    if (rounds >= 2) return launch_gemv_ks<MT, 2, kQ8>(aq, w, C, out, M, N, K, s);
+    return launch_gemv_ks<MT, 1, kQ8>(aq, w, C, out, M, N, K, s);
 }
 
 }  // namespace

@@ -10,6 +10,9 @@ the plain stream-launch time is reported beside it.
 The path "q6k" times the q6_K x q8_1 GEMM (mmq_q6K_gemm) on q6_K weights
 of the same shapes, repacked once to the device layout before timing.
 
+Extra shapes: --shapes M:K:N,... (named shape_MxKxN); --pdl launches with
+programmatic dependent launch (mmq_set_programmatic_launch).
+
   python -m q4_q8_int8_gb300.tools.sweep [--reps 50] [--paths auto,tc,mma_s8,small_m,q6k]
 """
 from __future__ import annotations
@@ -29,7 +32,9 @@ PATHS = {"auto": mmq.MMQ_PATH_AUTO, "tc": mmq.MMQ_PATH_TC, "mma_s8": mmq.MMQ_PAT
          "q6k": "q6k"}
 
 
-def shapes():
+def shapes(extra=()):
+    for M, K, N in extra:
+        yield f"shape_{M}x{K}x{N}", M, K, N
     for name in ("q_proj", "gate_up", "down"):
         M, K, N = synthetic.SHAPES[name]
         yield name, M, K, N
@@ -120,14 +125,18 @@ def main():
     ap.add_argument("--paths", default="auto")
     ap.add_argument("--workloads", default="", help="comma-separated subset, e.g. q_proj,sweep_M1")
     ap.add_argument("--no-graph", action="store_true", help="skip the CUDA-graph timing (for profilers)")
+    ap.add_argument("--shapes", default="", help="extra M:K:N shapes, comma-separated")
+    ap.add_argument("--pdl", action="store_true")
     args = ap.parse_args()
     build.build()
     mmq.load_library()
+    mmq.mmq_set_programmatic_launch(args.pdl)
+    extra = [tuple(int(v) for v in sh.split(":")) for sh in args.shapes.split(",") if sh]
     dev = torch.device("cuda", 0)
     hbm = 6785.2
     only = set(w for w in args.workloads.split(",") if w)
-    for name, M, K, N in shapes():
-        if only and name not in only:
+    for name, M, K, N in shapes(extra):
+        if (only or extra) and name not in only and not name.startswith("shape_"):
             continue
         for pname in args.paths.split(","):
             path = PATHS[pname]
