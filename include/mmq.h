@@ -285,7 +285,9 @@ const char* mmq_strerror(int code);
  * kernel so launched issues only its weight loads before it waits for the
  * previous grid to complete; it reads activations and writes its outputs
  * only after that wait, so results are the same either way.  Hides most of
- * the per-kernel start cost in a decode-style sequence of small GEMMs. */
+ * the per-kernel start cost in a decode-style sequence of small GEMMs.
+ * While enabled, a GEMM's weights must not be written by the kernel
+ * launched just before it on the same stream. */
 void mmq_set_programmatic_launch(int enable);
 
 /* Test hook: when nonzero, the next tensor-core GEMM launch on this host
