@@ -211,6 +211,8 @@ int mmq_q4K_gemm_swiglu_q8_1(mmq_q8_1_t aq, const uint8_t* bq4k_gu, float* hf, m
     if (F < 32 || (F % 32) != 0 || F > (int64_t(1) << 30)) return MMQ_ERR_ARG;
     if ((rc = check_gemm_args(aq, bq4k_gu, out.qs, M, 2 * F, K))) return rc;
     if (hf && !aligned16(hf)) return MMQ_ERR_ALIGN;
+    if (M <= 4)   // one dot-product kernel, SwiGLU and q8_1 in a cluster epilogue
+        return from_cuda(mmq::launch_gemv_swiglu_q8_1(aq, bq4k_gu, hf, out, M, F, K, static_cast<cudaStream_t>(stream)));
     if ((rc = mmq::tc_gemm_check_resources())) return rc;
     int* status = mmq::status_word_ptr();
     if (!status) return MMQ_ERR_CUDA;

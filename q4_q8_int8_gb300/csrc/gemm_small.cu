@@ -426,25 +426,34 @@ __device__ __forceinline__ void st_dsmem_f32(uint32_t addr, float v) {
 // warp and more warps have loads in flight; the KS partial sums are added
 // in slice order through shared memory.
 //
-// kQ8: the result is also written as q8_1 (the next GEMM's activations,
-// with the bits of a prepass over C): launched in clusters of CTAs whose 32
-// consecutive output rows form one q8_1 block per token; each row's sum is
-// pushed into rank 0's shared memory and rank 0 quantizes the block.  C may
-// then be null.
-template <int MT, int R, int KS, bool kQ8>
+// kOut selects the epilogue:
+//  kF32    C only;
+//  kQ8     the result also as q8_1 (the next GEMM's activations, with the
+//          bits of a prepass over C): launched in clusters of CTAs whose 32
+//          consecutive output rows form one q8_1 block per token; each row's
+//          sum is pushed into rank 0's shared memory and rank 0 quantizes the
+//          block.  C may be null;
+//  kSwiGLU gate and up rows interleaved (row 2f = gate f, 2f + 1 = up f):
+//          clusters cover 64 rows = 32 features, rank 0 forms
+//          h = silu(g) * u = g / (1 + exp(-g)) * u in f32 and quantizes it
+//          to q8_1 ([M][N/2]); C, if not null, receives h as f32 [M][N/2].
+constexpr int kF32 = 0, kQ8 = 1, kSwiGLU = 2;
+
+template <int MT, int R, int KS, int kOut>
 __global__ void __launch_bounds__(128)
 gemv_dp4a_kernel(mmq_q8_1_t aq, const uint8_t* __restrict__ w, float* __restrict__ C, mmq_q8_1_t out,
                  int M, int N, int K) {
-    constexpr int kGroups = 4 / KS;                 // row groups (of R rows) per CTA
-    constexpr int kCluster = 32 / (kGroups * R);    // kQ8: CTAs per 32 output rows
-    __shared__ __align__(16) float red[kQ8 ? MT : 1][32];   // kQ8, rank 0: the cluster's outputs [t][row]
+    constexpr int kGroups = 4 / KS;                        // row groups (of R rows) per CTA
+    constexpr int kBlockRows = kOut == kSwiGLU ? 64 : 32;  // rows behind one q8_1 output block
+    constexpr int kCluster = kBlockRows / (kGroups * R);   // CTAs per output block
+    __shared__ __align__(16) float red[kOut != kF32 ? MT : 1][kBlockRows];   // rank 0: the cluster's rows [t][row]
     __shared__ float part[KS > 1 ? 4 : 1][MT][R];          // KS > 1: each warp's partial sums
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int slice = warp % KS, grp = warp / KS;
     const int row0 = (blockIdx.x * kGroups + grp) * R;   // this warp's rows row0 .. row0 + R - 1
     griddep_launch_dependents();
-    if (KS == 1 && !kQ8 && row0 >= N) return;   // (with kQ8 every row exists: N % 32 == 0)
-    if (kQ8) asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");   // this CTA has started
+    if (KS == 1 && kOut == kF32 && row0 >= N) return;   // (with q8_1 output every row exists)
+    if (kOut != kF32) asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");   // this CTA has started
     const int nsb = K / 256, npairs = K / 64, nb = K / 32;
     float acc[MT][R];
 #pragma unroll
@@ -553,14 +562,14 @@ gemv_dp4a_kernel(mmq_q8_1_t aq, const uint8_t* __restrict__ w, float* __restrict
                 }
         }
     }
-    if (slice == 0 && lane == 0 && C) {
+    if (kOut != kSwiGLU && slice == 0 && lane == 0 && C) {
 #pragma unroll
         for (int t = 0; t < MT; ++t)
 #pragma unroll
             for (int r = 0; r < R; ++r)
                 if (t < M && row0 + r < N) C[int64_t(t) * N + row0 + r] = acc[t][r];
     }
-    if constexpr (kQ8) {
+    if constexpr (kOut != kF32) {
         const uint32_t rank = cluster_ctarank();
         asm volatile("barrier.cluster.wait.aligned;" ::: "memory");   // every CTA of the cluster has started
         if (slice == 0 && lane == 0) {
@@ -572,20 +581,35 @@ gemv_dp4a_kernel(mmq_q8_1_t aq, const uint8_t* __restrict__ w, float* __restrict
                         st_dsmem_f32(map_shared_rank(smem_u32(&red[t][(rank * kGroups + grp) * R + r]), 0),
                                      acc[t][r]);
         }
-        cluster_sync();   // the 32 rows' sums are in rank 0
+        cluster_sync();   // the block's rows are in rank 0
         if (rank == 0 && warp == 0) {
-            const int t = lane >> 3, part = lane & 7;   // 8 lanes per token
-            const float4 v = t < M ? *reinterpret_cast<const float4*>(&red[t < MT ? t : 0][part * 4])
-                                   : make_float4(0.f, 0.f, 0.f, 0.f);
+            const int t = lane >> 3, part = lane & 7;   // 8 lanes per token, 4 outputs per lane
+            const int tt = t < MT ? t : 0;
+            const int width = kOut == kSwiGLU ? N / 2 : N;   // output columns
+            const int blk = int(blockIdx.x / kCluster);     // output columns 32 blk .. 32 blk + 31
+            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (t < M) {
+                if constexpr (kOut == kSwiGLU) {
+                    float h[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const float g = red[tt][2 * (part * 4 + i)], u = red[tt][2 * (part * 4 + i) + 1];
+                        h[i] = __fmul_rn(__fdiv_rn(g, __fadd_rn(1.0f, expf(-g))), u);
+                    }
+                    v = make_float4(h[0], h[1], h[2], h[3]);
+                    if (C) *reinterpret_cast<float4*>(C + int64_t(t) * width + 32 * blk + part * 4) = v;
+                } else {
+                    v = *reinterpret_cast<const float4*>(&red[tt][part * 4]);
+                }
+            }
             float d;
             int sum;
             const uint32_t word = quantize_group8(v, d, sum);
-            const int blk = int(blockIdx.x / kCluster);   // output columns 32 blk .. 32 blk + 31
             if (t < M) {
-                *reinterpret_cast<uint32_t*>(out.qs + int64_t(t) * N + 32 * blk + part * 4) = word;
+                *reinterpret_cast<uint32_t*>(out.qs + int64_t(t) * width + 32 * blk + part * 4) = word;
                 if (part == 0) {
-                    out.da[int64_t(t) * (N / 32) + blk] = d;
-                    out.sa[int64_t(t) * (N / 32) + blk] = sum;
+                    out.da[int64_t(t) * (width / 32) + blk] = d;
+                    out.sa[int64_t(t) * (width / 32) + blk] = sum;
                 }
             }
         }
@@ -597,32 +621,37 @@ gemv_dp4a_kernel(mmq_q8_1_t aq, const uint8_t* __restrict__ w, float* __restrict
 // token) 8 for 1, 2 and 4 tokens.
 constexpr int kGemvRows = 4;
 
-template <int MT, int KS, bool kQ8>
+template <int MT, int KS, int kOut>
 cudaError_t launch_gemv_ks(mmq_q8_1_t aq, const uint8_t* w, float* C, mmq_q8_1_t out, int64_t M, int64_t N,
                            int64_t K, cudaStream_t s) {
     constexpr int R = kGemvRows, rows = 4 / KS * R;   // rows per CTA
+    constexpr int cluster = (kOut == kSwiGLU ? 64 : 32) / rows;
+    static_assert(kOut == kF32 || (cluster >= 1 && cluster <= 8), "portable cluster size");
     cudaLaunchAttribute attr[2];
     const unsigned grid = unsigned((N + rows - 1) / rows);
     cudaLaunchConfig_t cfg = mmq::launch_config(dim3(grid), dim3(128), 0, s, attr);
-    if (kQ8) {   // grid = N / rows is a multiple of 32 / rows when N % 32 == 0
+    if (kOut != kF32) {   // grid = N / rows is a multiple of the cluster (N % 32 or N % 64 == 0)
         attr[cfg.numAttrs].id = cudaLaunchAttributeClusterDimension;
-        attr[cfg.numAttrs].val.clusterDim.x = 32 / rows;
+        attr[cfg.numAttrs].val.clusterDim.x = cluster;
         attr[cfg.numAttrs].val.clusterDim.y = 1;
         attr[cfg.numAttrs].val.clusterDim.z = 1;
         ++cfg.numAttrs;
     }
-    return cudaLaunchKernelEx(&cfg, gemv_dp4a_kernel<MT, R, KS, kQ8>, aq, w, C, out, int(M), int(N), int(K));
+    return cudaLaunchKernelEx(&cfg, gemv_dp4a_kernel<MT, R, KS, kOut>, aq, w, C, out, int(M), int(N), int(K));
 }
 
 // K split by the number of 32-pair rounds a row takes: 1 round -> 1 warp,
-// 2-3 -> 2 warps, 4 or more -> 4 warps per row group.
-template <int MT, bool kQ8>
+// 2-3 -> 2 warps, 4 or more -> 4 warps per row group (2 at most for the
+// SwiGLU epilogue, whose 64-row blocks would otherwise need clusters of 16).
+template <int MT, int kOut>
 cudaError_t launch_gemv(mmq_q8_1_t aq, const uint8_t* w, float* C, mmq_q8_1_t out, int64_t M, int64_t N, int64_t K,
                         cudaStream_t s) {
     const int64_t rounds = (K / 64 + 31) / 32;
-    if (rounds >= 4) return launch_gemv_ks<MT, 4, kQ8>(aq, w, C, out, M, N, K, s);
-    if (rounds >= 2) return launch_gemv_ks<MT, 2, kQ8>(aq, w, C, out, M, N, K, s);
-    return launch_gemv_ks<MT, 1, kQ8>(aq, w, C, out, M, N, K, s);
+    if constexpr (kOut != kSwiGLU) {
+        if (rounds >= 4) return launch_gemv_ks<MT, 4, kOut>(aq, w, C, out, M, N, K, s);
+    }
+    if (rounds >= 2) return launch_gemv_ks<MT, 2, kOut>(aq, w, C, out, M, N, K, s);
+    return launch_gemv_ks<MT, 1, kOut>(aq, w, C, out, M, N, K, s);
 }
 
 }  // namespace
@@ -633,9 +662,19 @@ cudaError_t launch_gemv_q8_1(mmq_q8_1_t aq, const uint8_t* w, float* C, mmq_q8_1
                              int64_t K, cudaStream_t s) {
     if (M < 1 || M > 4 || N % 32 != 0) return cudaErrorInvalidValue;
     switch (M) {
-        case 1: return launch_gemv<1, true>(aq, w, C, out, M, N, K, s);
-        case 2: return launch_gemv<2, true>(aq, w, C, out, M, N, K, s);
-        default: return launch_gemv<4, true>(aq, w, C, out, M, N, K, s);
+        case 1: return launch_gemv<1, kQ8>(aq, w, C, out, M, N, K, s);
+        case 2: return launch_gemv<2, kQ8>(aq, w, C, out, M, N, K, s);
+        default: return launch_gemv<4, kQ8>(aq, w, C, out, M, N, K, s);
+    }
+}
+
+cudaError_t launch_gemv_swiglu_q8_1(mmq_q8_1_t aq, const uint8_t* w_gu, float* hf, mmq_q8_1_t out, int64_t M,
+                                    int64_t F, int64_t K, cudaStream_t s) {
+    if (M < 1 || M > 4 || F % 32 != 0) return cudaErrorInvalidValue;
+    switch (M) {
+        case 1: return launch_gemv<1, kSwiGLU>(aq, w_gu, hf, out, M, 2 * F, K, s);
+        case 2: return launch_gemv<2, kSwiGLU>(aq, w_gu, hf, out, M, 2 * F, K, s);
+        default: return launch_gemv<4, kSwiGLU>(aq, w_gu, hf, out, M, 2 * F, K, s);
     }
 }
 
@@ -717,9 +756,9 @@ cudaError_t launch_gemm_small_m(mmq_q8_1_t aq, const uint8_t* w, float* C, int64
     if (M <= 4) {   // a few tokens: streaming dot products on dp4a
         const mmq_q8_1_t none = {nullptr, nullptr, nullptr};
         switch (M) {
-            case 1: return launch_gemv<1, false>(aq, w, C, none, M, N, K, s);
-            case 2: return launch_gemv<2, false>(aq, w, C, none, M, N, K, s);
-            default: return launch_gemv<4, false>(aq, w, C, none, M, N, K, s);
+            case 1: return launch_gemv<1, kF32>(aq, w, C, none, M, N, K, s);
+            case 2: return launch_gemv<2, kF32>(aq, w, C, none, M, N, K, s);
+            default: return launch_gemv<4, kF32>(aq, w, C, none, M, N, K, s);
         }
     }
     const int nf = int((M + 7) / 8);

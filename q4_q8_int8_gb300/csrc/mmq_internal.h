@@ -62,6 +62,10 @@ cudaError_t launch_gemm_small_m(mmq_q8_1_t aq, const uint8_t* w, float* C,
 // C may be null).
 cudaError_t launch_gemv_q8_1(mmq_q8_1_t aq, const uint8_t* w, float* C, mmq_q8_1_t out, int64_t M, int64_t N,
                              int64_t K, cudaStream_t s);
+// The same kernel with the SwiGLU epilogue: rows interleaved gate/up (N = 2F,
+// F % 32 == 0), q8_1 of silu(g)*u into out [M][F], h as f32 into hf if not null.
+cudaError_t launch_gemv_swiglu_q8_1(mmq_q8_1_t aq, const uint8_t* w_gu, float* hf, mmq_q8_1_t out, int64_t M,
+                                    int64_t F, int64_t K, cudaStream_t s);
 // tcgen05 kernel for few tokens: 128 weight rows x 16/32/64 tokens per CTA.
 cudaError_t launch_gemm_tc_small(mmq_q8_1_t aq, const uint8_t* w, float* C,
                                  int64_t M, int64_t N, int64_t K, int* status,

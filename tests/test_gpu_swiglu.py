@@ -43,7 +43,8 @@ def _run(M, F, K, seed, with_h=True):
 
 
 @pytest.mark.parametrize("M,F,K", [(200, 256, 512), (130, 512, 1024), (37, 96, 512), (1, 32, 256),
-                                   (300, 160, 2816)])
+                                   (300, 160, 2816), (2, 96, 768), (3, 160, 4096), (4, 256, 2816),
+                                   (1, 4096, 4096)])
 def test_swiglu_full(M, F, K):
     mmq, x, blk_gu, aq, w_gu, h, (qs, da, sa) = _run(M, F, K, 400 + M)
     h = h.cpu().numpy()
@@ -57,8 +58,9 @@ def test_swiglu_full(M, F, K):
     assert (qs == rq).all() and (da.view(np.uint32) == rda.view(np.uint32)).all() and (sa == rsa).all()
 
 
-def test_swiglu_without_h_same_bits():
-    mmq, x, blk_gu, aq, w_gu, h, o1 = _run(130, 256, 1024, 77, with_h=True)
+@pytest.mark.parametrize("M", [130, 1, 4])
+def test_swiglu_without_h_same_bits(M):
+    mmq, x, blk_gu, aq, w_gu, h, o1 = _run(M, 256, 1024, 77, with_h=True)
     _, o2 = mmq.q4K_gemm_swiglu_q8_1(aq, w_gu, 256, with_h=False)
     assert mmq.status() == 0
     for a, b in zip(o1, o2):
@@ -94,3 +96,20 @@ def test_swiglu_argument_errors():
     assert mmq.mmq_q4K_gemm_swiglu_q8_1(good, P(w), None, out, 4, 64, 250, None) == mmq.MMQ_ERR_ARG  # K % 256
     assert mmq.mmq_interleave_rows_q4K(P(w), None, P(w), 4, 256, None) == mmq.MMQ_ERR_ARG
     assert mmq.status() == 0
+
+
+@pytest.mark.parametrize("M", [1, 4])
+def test_swiglu_gate_up_decode_full_size(M):
+    # the 7B FFN at a few tokens (the dot-product kernel's cluster epilogue)
+    M_, F, K = M, 11008, 4096
+    mmq, x, blk_gu, aq, w_gu, h, (qs, da, sa) = _run(M_, F, K, 510 + M)
+    h = h.cpu().numpy()
+    q, dq, sq = oracle.quantize_q8_1(x)
+    rows, fcols = sample_points(M_, F, 3000, 10)
+    Cg, Cg64, Tg = oracle.gemm_sampled(q, dq, sq, blk_gu, 2 * F, rows, 2 * fcols)
+    Cu, Cu64, Tu = oracle.gemm_sampled(q, dq, sq, blk_gu, 2 * F, rows, 2 * fcols + 1)
+    bound = ffn.swiglu_bound(Cg64, Cu64, RTOL * Tg + ATOL, RTOL * Tu + ATOL)
+    err = np.abs(h[rows, fcols].astype(np.float64) - ffn.swiglu(Cg64, Cu64))
+    assert (err <= bound).all()
+    rq, rda, rsa = oracle.quantize_q8_1(h)
+    assert (qs == rq).all() and (da.view(np.uint32) == rda.view(np.uint32)).all() and (sa == rsa).all()
