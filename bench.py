@@ -352,21 +352,21 @@ def run_mine(args, rank, world, local_rank):
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
     step_ms, q_ms, g_ms = t.tolist()
 
-    # ---- end to end through the C ABI with pinned host buffers
+    # ---- end to end through the C ABI with pinned host buffers: mmq_q4K_gemm_host
+    # (x in from host memory, C out to host memory, chunked so that the copies
+    # overlap the prepass and GEMM)
     xh = torch.empty((M, K), dtype=torch.float32, pin_memory=True)
     xh.copy_(xs[0].cpu())
     Ch = torch.empty((M, N), dtype=torch.float32, pin_memory=True)
-    xd = torch.empty_like(xs[0])
+    ws_bytes = mmq.mmq_q4K_gemm_host_workspace(M, N, K)
+    ws_t = torch.empty(ws_bytes + 256, dtype=torch.uint8, device=dev)
+    ws_base = (ws_t.data_ptr() + 255) // 256 * 256
 
     def e2e_step(i):
-        r = i % R
-        (qs, da, sa), C, w = aqs[r], Cs[r], ws[r]
-        xd.copy_(xh, non_blocking=True)
-        aq = mmq.q8_1_struct(qs, da, sa)
-        rc = mmq.mmq_quantize_q8_1(ctypes.c_void_p(xd.data_ptr()), M, K, aq, sp)
-        rc |= mmq.mmq_q4K_gemm_path(aq, ctypes.c_void_p(w.data_ptr()), ctypes.c_void_p(C.data_ptr()),
-                                    M, N, K, path, sp)
-        Ch.copy_(C, non_blocking=True)
+        w = ws[i % R]
+        rc = mmq.mmq_q4K_gemm_host(ctypes.c_void_p(xh.data_ptr()), ctypes.c_void_p(w.data_ptr()),
+                                   ctypes.c_void_p(Ch.data_ptr()), M, N, K, ctypes.c_void_p(ws_base),
+                                   ws_bytes, sp)
         if rc:
             raise RuntimeError(f"MMQ call failed: {rc}")
 

@@ -111,6 +111,33 @@ int mmq_q4K_gemm(mmq_q8_1_t aq, const uint8_t* bq4k, float* C, int64_t M,
                  int64_t N, int64_t K, void* stream);
 
 
+/* Device workspace bytes for mmq_q4K_gemm_host on an M x K by N x K problem
+ * (0 for shapes mmq_q4K_gemm refuses).  It holds two chunks of x, one chunk
+ * of q8_1 planes and two chunks of C, a chunk being up to a quarter of the
+ * rows rounded up to 128 (all rows when M <= 256). */
+size_t mmq_q4K_gemm_host_workspace(int64_t M, int64_t N, int64_t K);
+
+/* The prepass and the GEMM (page r15 section 2.1, as mmq_quantize_q8_1 then
+ * mmq_q4K_gemm) with the activations and the result in HOST memory:
+ * x_host float [M][K] and C_host float [M][N] row-major, weights bq4k on the
+ * device.  The rows are processed in chunks.  Chunk i+1's host-to-device
+ * copy, chunk i's prepass and GEMM (on `stream`) and chunk i-1's
+ * device-to-host copy run concurrently, on two copy streams the library
+ * keeps per device, ordered by events.  Page-locked host memory
+ * (cudaHostAlloc) lets the copies overlap; pageable memory works but does
+ * not overlap.  The copies start after the work already queued on `stream`,
+ * and work queued on `stream` afterwards runs after the last copy, so
+ * synchronizing `stream` makes C_host valid.  workspace: device memory of
+ * mmq_q4K_gemm_host_workspace(M, N, K) bytes or more, 256-byte aligned,
+ * caller-owned, not used by anything else until `stream` passes this call.
+ * Per chunk the kernel is the one mmq_q4K_gemm picks for the chunk's rows,
+ * so C equals mmq_q4K_gemm applied chunk by chunk, within the GEMM's
+ * tolerance of the whole.  Errors: MMQ_ERR_ARG (null pointer, shape, small
+ * workspace), MMQ_ERR_ALIGN, MMQ_ERR_DEVICE, MMQ_ERR_CUDA. */
+int mmq_q4K_gemm_host(const float* x_host, const uint8_t* bq4k, float* C_host,
+                      int64_t M, int64_t N, int64_t K, void* workspace,
+                      size_t workspace_bytes, void* stream);
+
 /* Kernel selection for mmq_q4K_gemm_path (testing and A/B timing). */
 #define MMQ_PATH_AUTO 0
 #define MMQ_PATH_MMA_S8 1   /* warp-level mma.sync s8 x s8 -> s32 kernel    */

@@ -36,7 +36,7 @@ MMQ_GGUF_F32, MMQ_GGUF_F16, MMQ_GGUF_Q4_K, MMQ_GGUF_Q6_K = 0, 1, 12, 14
 # Every symbol include/mmq.h declares.
 EXPORTS = (
     "mmq_q8_1_bytes", "mmq_q8_1_view", "mmq_quantize_q8_1", "mmq_q4K_bytes",
-    "mmq_pack_q4K", "mmq_q4K_gemm", "mmq_q4K_gemm_path", "mmq_q4K_gemm_q8_1", "mmq_q4K_block_dots",
+    "mmq_pack_q4K", "mmq_q4K_gemm", "mmq_q4K_gemm_host_workspace", "mmq_q4K_gemm_host", "mmq_q4K_gemm_path", "mmq_q4K_gemm_q8_1", "mmq_q4K_block_dots",
     "mmq_dequantize_q4K_f16", "mmq_convert_f32_f16", "mmq_gemm_f16",
     "mmq_q4K_gemm_swiglu_q8_1", "mmq_interleave_rows_q4K",
     "mmq_q6K_bytes", "mmq_pack_q6K", "mmq_q6K_dev_bytes", "mmq_repack_q6K", "mmq_q6K_gemm",
@@ -78,6 +78,8 @@ def load_library(path: str = LIB_PATH):
                 "mmq_q4K_bytes": ([I, I], S),
                 "mmq_pack_q4K": ([P, P, P, P, P, I, I, P], ctypes.c_int),
                 "mmq_q4K_gemm": ([Q, P, P, I, I, I, P], ctypes.c_int),
+                "mmq_q4K_gemm_host_workspace": ([I, I, I], S),
+                "mmq_q4K_gemm_host": ([P, P, P, I, I, I, P, S, P], ctypes.c_int),
                 "mmq_q4K_gemm_path": ([Q, P, P, I, I, I, ctypes.c_int, P], ctypes.c_int),
                 "mmq_q4K_gemm_q8_1": ([Q, P, P, Q, I, I, I, P], ctypes.c_int),
                 "mmq_q4K_block_dots": ([Q, P, P, I, I, I, ctypes.c_int, P], ctypes.c_int),
@@ -139,6 +141,14 @@ def mmq_pack_q4K(v, sc, m, d, dmin, N, K, out):
 
 def mmq_q4K_gemm(aq, bq4k, C, M, N, K, stream):
     return load_library().mmq_q4K_gemm(aq, bq4k, C, M, N, K, stream)
+
+
+def mmq_q4K_gemm_host_workspace(M, N, K):
+    return load_library().mmq_q4K_gemm_host_workspace(M, N, K)
+
+
+def mmq_q4K_gemm_host(x_host, bq4k, C_host, M, N, K, ws, ws_bytes, stream):
+    return load_library().mmq_q4K_gemm_host(x_host, bq4k, C_host, M, N, K, ws, ws_bytes, stream)
 
 
 def mmq_q4K_gemm_path(aq, bq4k, C, M, N, K, path, stream):
@@ -215,6 +225,31 @@ def q4K_gemm(aq, w, N: int, path: int = MMQ_PATH_AUTO, out=None, stream=None):
     _check(mmq_q4K_gemm_path(q8_1_struct(qs, da, sa), ctypes.c_void_p(w.data_ptr()),
                              ctypes.c_void_p(C.data_ptr()), M, N, K, path, _stream_ptr(stream)),
            "mmq_q4K_gemm")
+    return C
+
+
+def q4K_gemm_host(x_host, w, N: int, out=None, workspace=None, stream=None):
+    """x_host float32 [M][K] CPU tensor (pinned for overlap) -> C float32 [M][N]
+    CPU tensor, through mmq_q4K_gemm_host (chunked copies overlapped with the
+    kernels).  Returns after the call is queued; synchronize the stream before
+    reading the result.  Without a caller-owned `workspace` (a CUDA uint8
+    tensor) one is allocated here and the call synchronizes the stream before
+    returning, since the allocator cannot see the library's copy streams."""
+    import torch
+    M, K = x_host.shape
+    C = out if out is not None else torch.empty((M, N), dtype=torch.float32, pin_memory=True)
+    need = mmq_q4K_gemm_host_workspace(M, N, K)
+    own = workspace is None
+    if own:
+        workspace = torch.empty(need + 256, dtype=torch.uint8, device=w.device)
+    base = (workspace.data_ptr() + 255) // 256 * 256
+    avail = workspace.numel() - (base - workspace.data_ptr())
+    sp = _stream_ptr(stream)
+    _check(mmq_q4K_gemm_host(ctypes.c_void_p(x_host.data_ptr()), ctypes.c_void_p(w.data_ptr()),
+                             ctypes.c_void_p(C.data_ptr()), M, N, K, ctypes.c_void_p(base), avail, sp),
+           "mmq_q4K_gemm_host")
+    if own:
+        (stream if stream is not None else torch.cuda.current_stream()).synchronize()
     return C
 
 

@@ -177,6 +177,28 @@ int mmq_q4K_gemm(mmq_q8_1_t aq, const uint8_t* bq4k, float* C, int64_t M, int64_
     return mmq_q4K_gemm_path(aq, bq4k, C, M, N, K, MMQ_PATH_AUTO, stream);
 }
 
+static int gemm_auto(mmq_q8_1_t aq, const uint8_t* w, float* C, int64_t M, int64_t N, int64_t K,
+                     cudaStream_t s) {
+    return run_gemm(aq, w, C, nullptr, M, N, K, MMQ_PATH_AUTO, s);
+}
+
+size_t mmq_q4K_gemm_host_workspace(int64_t M, int64_t N, int64_t K) {
+    if (M < 1 || N < 1 || K < 256 || (K % 256) != 0 || (N % 4) != 0) return 0;
+    if (M > (int64_t(1) << 31) - 1 || N > (int64_t(1) << 31) - 1 || K > (int64_t(1) << 31) - 1) return 0;
+    return mmq::host_workspace_bytes(M, N, K);
+}
+
+int mmq_q4K_gemm_host(const float* x_host, const uint8_t* bq4k, float* C_host, int64_t M, int64_t N, int64_t K,
+                      void* workspace, size_t workspace_bytes, void* stream) {
+    if (!x_host || !bq4k || !C_host || !workspace) return MMQ_ERR_ARG;
+    const size_t need = mmq_q4K_gemm_host_workspace(M, N, K);
+    if (need == 0 || workspace_bytes < need) return MMQ_ERR_ARG;
+    if (!aligned16(bq4k) || (reinterpret_cast<uintptr_t>(workspace) & 255)) return MMQ_ERR_ALIGN;
+    int rc = check_device();
+    if (rc) return rc;
+    return mmq::gemm_host(x_host, bq4k, C_host, M, N, K, workspace, static_cast<cudaStream_t>(stream), gemm_auto);
+}
+
 int mmq_q4K_gemm_path(mmq_q8_1_t aq, const uint8_t* bq4k, float* C, int64_t M, int64_t N,
                       int64_t K, int path, void* stream) {
     if (path < MMQ_PATH_AUTO || path > MMQ_PATH_TC_SMALL) return MMQ_ERR_ARG;

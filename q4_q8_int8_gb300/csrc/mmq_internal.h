@@ -58,6 +58,15 @@ cudaError_t launch_gemm_tc2(mmq_q8_1_t aq, const uint8_t* w, float* C,
 cudaError_t launch_gemm_small_m(mmq_q8_1_t aq, const uint8_t* w, float* C,
                                 int64_t M, int64_t N, int64_t K, int* status,
                                 cudaStream_t s);
+// Host-buffer pipeline (host_pipeline.cu): rows per chunk, workspace bytes,
+// and the chunked copy-in / prepass + GEMM / copy-out, with `gemm` the GEMM
+// to run on each chunk's q8_1 planes (MMQ_* code).
+using GemmFn = int (*)(mmq_q8_1_t aq, const uint8_t* w, float* C, int64_t M, int64_t N, int64_t K,
+                       cudaStream_t s);
+int64_t host_chunk_rows(int64_t M);
+size_t host_workspace_bytes(int64_t M, int64_t N, int64_t K);
+int gemm_host(const float* x_host, const uint8_t* w, float* C_host, int64_t M, int64_t N, int64_t K, void* ws,
+              cudaStream_t s, GemmFn gemm);
 // The dp4a GEMV (M <= 4) that also writes its result as q8_1 (N % 32 == 0;
 // C may be null).
 cudaError_t launch_gemv_q8_1(mmq_q8_1_t aq, const uint8_t* w, float* C, mmq_q8_1_t out, int64_t M, int64_t N,
