@@ -271,6 +271,148 @@ gemm_q6k_kernel(mmq_q8_1_t aq, const uint8_t* __restrict__ w, float* __restrict_
     }
 }
 
+// ---------------------------------------------------------------------------
+// M <= 4 tokens: a streaming dot product on dp4a, one warp per kGvR weight
+// rows.  Lane l takes chunks l, l+32, ... of each row (chunk c = 4n + r of a
+// super-block: its 32 quants are nibble r/2 of ql[64n + 32(r%2) + l] and
+// bit pair r of qh[32n + l], l = 0..31); the 6-bit u becomes the int8 q = u -
+// 32 per byte, two dp4a chains give the exact dots of the chunk's two
+// 16-element sub-blocks, and acc += da * (d * sc) * S per sub-block.  Every
+// activation load serves the warp's kGvR rows.  A row taking r rounds of 32
+// chunks is shared by min(4, r) warps of the CTA, whose partial sums are
+// added in slice order through shared memory.
+// ---------------------------------------------------------------------------
+constexpr int kGvR = 4;
+
+template <int MT, int KS>
+__global__ void __launch_bounds__(128)
+gemv_q6k_kernel(mmq_q8_1_t aq, const uint8_t* __restrict__ w, float* __restrict__ C, int M, int N, int K) {
+    constexpr int kGroups = 4 / KS;   // row groups (of kGvR rows) per CTA
+    __shared__ float part[KS > 1 ? 4 : 1][MT][kGvR];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int slice = warp % KS, grp = warp / KS;
+    const int row0 = (blockIdx.x * kGroups + grp) * kGvR;
+    if (KS == 1 && row0 >= N) return;
+    const int nsb = K / 256, nch = K / 32;
+    float acc[MT][kGvR];
+#pragma unroll
+    for (int t = 0; t < MT; ++t)
+#pragma unroll
+        for (int r = 0; r < kGvR; ++r) acc[t][r] = 0.0f;
+    for (int base = 32 * slice; base < nch; base += 32 * KS) {
+        const int ci = base + lane;   // this lane's chunk of the row
+        const int c = ci & 7, n = c >> 2, rr = c & 3;
+        uint4 ql[kGvR][2], qh[kGvR][2];
+        uint32_t scw[kGvR], dw[kGvR];
+#pragma unroll
+        for (int r = 0; r < kGvR; ++r) {
+            if (ci < nch && row0 + r < N) {
+                const uint8_t* blk = w + (int64_t(row0 + r) * nsb + (ci >> 3)) * 224;
+                ql[r][0] = __ldcs(reinterpret_cast<const uint4*>(blk + 64 * n + 32 * (rr & 1)));
+                ql[r][1] = __ldcs(reinterpret_cast<const uint4*>(blk + 64 * n + 32 * (rr & 1) + 16));
+                qh[r][0] = __ldcs(reinterpret_cast<const uint4*>(blk + 128 + 32 * n));
+                qh[r][1] = __ldcs(reinterpret_cast<const uint4*>(blk + 128 + 32 * n + 16));
+                scw[r] = __ldg(reinterpret_cast<const uint16_t*>(blk + 192 + 2 * c));
+                dw[r] = __ldg(reinterpret_cast<const uint16_t*>(blk + 208));
+            } else {
+                ql[r][0] = ql[r][1] = qh[r][0] = qh[r][1] = make_uint4(0u, 0u, 0u, 0u);
+                scw[r] = dw[r] = 0u;
+            }
+        }
+        if (ci >= nch) continue;
+        float ds[kGvR][2];   // d * sc of the chunk's two sub-blocks (exact in f32)
+#pragma unroll
+        for (int r = 0; r < kGvR; ++r) {
+            const float d = __half2float(__ushort_as_half(uint16_t(dw[r])));
+            ds[r][0] = d * float(int8_t(scw[r] & 0xFFu));
+            ds[r][1] = d * float(int8_t(scw[r] >> 8));
+        }
+#pragma unroll
+        for (int t = 0; t < MT; ++t) {
+            if (t < M) {
+                const int8_t* qt = aq.qs + int64_t(t) * K + 32 * ci;
+                const uint4 a0 = __ldg(reinterpret_cast<const uint4*>(qt));
+                const uint4 a1 = __ldg(reinterpret_cast<const uint4*>(qt + 16));
+                const float da = __ldg(aq.da + int64_t(t) * nch + ci);
+                const uint32_t av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+#pragma unroll
+                for (int r = 0; r < kGvR; ++r) {
+                    const uint32_t lw[8] = {ql[r][0].x, ql[r][0].y, ql[r][0].z, ql[r][0].w,
+                                            ql[r][1].x, ql[r][1].y, ql[r][1].z, ql[r][1].w};
+                    const uint32_t hw[8] = {qh[r][0].x, qh[r][0].y, qh[r][0].z, qh[r][0].w,
+                                            qh[r][1].x, qh[r][1].y, qh[r][1].z, qh[r][1].w};
+                    int s0 = 0, s1 = 0;
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const uint32_t u = ((lw[e] >> (4 * (rr >> 1))) & 0x0F0F0F0Fu) |
+                                           (((hw[e] >> (2 * rr)) & 0x03030303u) << 4);
+                        const int q = int(__vsub4(u, 0x20202020u));   // u - 32 per byte: int8 quants
+                        if (e < 4) s0 = __dp4a(q, int(av[e]), s0);
+                        else s1 = __dp4a(q, int(av[e]), s1);
+                    }
+                    float a = acc[t][r];
+                    a = fmaf(da * ds[r][0], float(s0), a);
+                    a = fmaf(da * ds[r][1], float(s1), a);
+                    acc[t][r] = a;
+                }
+            }
+        }
+    }
+#pragma unroll
+    for (int t = 0; t < MT; ++t)
+#pragma unroll
+        for (int r = 0; r < kGvR; ++r) {
+            float a = acc[t][r];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
+            acc[t][r] = a;
+        }
+    if constexpr (KS > 1) {
+        if (lane == 0) {
+#pragma unroll
+            for (int t = 0; t < MT; ++t)
+#pragma unroll
+                for (int r = 0; r < kGvR; ++r) part[warp][t][r] = acc[t][r];
+        }
+        __syncthreads();
+        if (slice == 0) {
+#pragma unroll
+            for (int t = 0; t < MT; ++t)
+#pragma unroll
+                for (int r = 0; r < kGvR; ++r) {
+                    float a = part[warp][t][r];
+#pragma unroll
+                    for (int q = 1; q < KS; ++q) a += part[warp + q][t][r];
+                    acc[t][r] = a;
+                }
+        }
+    }
+    if (slice == 0 && lane == 0) {
+#pragma unroll
+        for (int t = 0; t < MT; ++t)
+#pragma unroll
+            for (int r = 0; r < kGvR; ++r)
+                if (t < M && row0 + r < N) C[int64_t(t) * N + row0 + r] = acc[t][r];
+    }
+}
+
+template <int MT, int KS>
+cudaError_t launch_gemv_q6k_ks(mmq_q8_1_t aq, const uint8_t* w, float* C, int64_t M, int64_t N, int64_t K,
+                               cudaStream_t s) {
+    constexpr int rows = 4 / KS * kGvR;   // rows per CTA
+    gemv_q6k_kernel<MT, KS><<<unsigned((N + rows - 1) / rows), 128, 0, s>>>(aq, w, C, int(M), int(N), int(K));
+    return cudaGetLastError();
+}
+
+template <int MT>
+cudaError_t launch_gemv_q6k(mmq_q8_1_t aq, const uint8_t* w, float* C, int64_t M, int64_t N, int64_t K,
+                            cudaStream_t s) {
+    const int64_t rounds = (K / 32 + 31) / 32;
+    if (rounds >= 4) return launch_gemv_q6k_ks<MT, 4>(aq, w, C, M, N, K, s);
+    if (rounds >= 2) return launch_gemv_q6k_ks<MT, 2>(aq, w, C, M, N, K, s);
+    return launch_gemv_q6k_ks<MT, 1>(aq, w, C, M, N, K, s);
+}
+
 }  // namespace
 
 namespace mmq {
@@ -284,6 +426,11 @@ cudaError_t launch_repack_q6K(const uint8_t* src, uint8_t* dst, int64_t N, int64
 
 cudaError_t launch_gemm_q6k(mmq_q8_1_t aq, const uint8_t* w, float* C, int32_t* S, int64_t M, int64_t N,
                             int64_t K, cudaStream_t s) {
+    if (!S && M <= 4) {   // a few tokens: the dot-product kernel
+        if (M == 1) return launch_gemv_q6k<1>(aq, w, C, M, N, K, s);
+        if (M == 2) return launch_gemv_q6k<2>(aq, w, C, M, N, K, s);
+        return launch_gemv_q6k<4>(aq, w, C, M, N, K, s);
+    }
     const dim3 grid(unsigned((N + BN - 1) / BN), unsigned((M + BM - 1) / BM));
     if (grid.y > 65535u) return cudaErrorInvalidConfiguration;
     auto k = S ? gemm_q6k_kernel<true> : gemm_q6k_kernel<false>;

@@ -59,7 +59,8 @@ def test_q6k_block_dots_extremes(sign):
 
 
 @pytest.mark.parametrize("M,N,K", [(128, 256, 512), (77, 132, 768), (300, 388, 1280), (1, 4, 256),
-                                   (64, 128, 2816)])
+                                   (64, 128, 2816), (2, 132, 768), (3, 260, 4096), (4, 68, 11008),
+                                   (1, 36, 1280)])
 def test_q6k_gemm_full(M, N, K):
     x = synthetic.activations(M, K, 630 + M, 0.01)
     blk = synthetic.q6K_weights(N, K, 640 + N)
@@ -83,6 +84,20 @@ def test_q6k_gemm_full_size_sampled(name):
     assert np.isfinite(C).all()
     q, da, _ = oracle.quantize_q8_1(x)
     rows, cols = sample_points(M, N, 2000, 11)
+    _, C64, T = q6k.gemm(q, da, blk, N, rows=rows, cols=cols)
+    assert (np.abs(C[rows, cols].astype(np.float64) - C64) <= RTOL * T + ATOL).all()
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 11008, 4096), (4, 4096, 11008)])
+def test_q6k_gemm_decode_size_sampled(M, N, K):
+    # decode shapes: the dot-product kernel (M <= 4)
+    x = synthetic.activations(M, K, 655 + M, 0.01)
+    blk = synthetic.q6K_weights(N, K, 665 + M)
+    mmq, w_dev = _dev(blk, N, K)
+    C = mmq.q6K_gemm(mmq.quantize_q8_1(to_dev(x)), w_dev, N).cpu().numpy()
+    assert mmq.status() == 0
+    q, da, _ = oracle.quantize_q8_1(x)
+    rows, cols = sample_points(M, N, 3000, 12)
     _, C64, T = q6k.gemm(q, da, blk, N, rows=rows, cols=cols)
     assert (np.abs(C[rows, cols].astype(np.float64) - C64) <= RTOL * T + ATOL).all()
 
