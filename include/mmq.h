@@ -258,7 +258,8 @@ int mmq_repack_q6K(const uint8_t* src, uint8_t* dst, int64_t N, int64_t K, void*
 /* C = A . W^T for q8_1 activations and q6_K weights in the device layout:
  * per 16-weight sub-block s of the 32-element q8_1 block c,
  * C_ij += da_ic * d_j * sc_js * S_ijs with S the exact int32 dot (warp-level
- * int8 tensor MMAs; for M <= 4 dp4a dot products streaming the weights).
+ * int8 tensor MMAs, K split over a cluster when tiles are few; for M <= 16
+ * dp4a dot products streaming the weights).
  * Shape rules and tolerance as mmq_q4K_gemm. */
 int mmq_q6K_gemm(mmq_q8_1_t aq, const uint8_t* bq6k_dev, float* C, int64_t M,
                  int64_t N, int64_t K, void* stream);

@@ -113,10 +113,28 @@ __device__ __forceinline__ void load_stage(uint32_t st, const mmq_q8_1_t& aq, co
     }
 }
 
+__device__ __forceinline__ void q6_cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ float4 q6_ld_peer_v4(uint32_t saddr, uint32_t rank) {
+    uint32_t a;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(saddr), "r"(rank));
+    float4 v;
+    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(a)
+                 : "memory");
+    return v;
+}
+
+// split > 1 (few tiles): a cluster of `split` CTAs along z shares one tile,
+// rank r taking super-blocks [nsb*r/split, nsb*(r+1)/split); each rank leaves
+// its partial tile in its own (then idle) stage memory and rank 0 adds them
+// in rank order, so the sum is the same on every run.
 template <bool kDump>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_q6k_kernel(mmq_q8_1_t aq, const uint8_t* __restrict__ w, float* __restrict__ C, int32_t* __restrict__ S,
-                int64_t M, int64_t N, int64_t K) {
+                int64_t M, int64_t N, int64_t K, int split) {
     extern __shared__ __align__(128) uint8_t smem[];
     const uint32_t sbase = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
     float* colsc = reinterpret_cast<float*>(smem + kStages * kStageBytes);   // d * sc [16][128]
@@ -127,6 +145,8 @@ gemm_q6k_kernel(mmq_q8_1_t aq, const uint8_t* __restrict__ w, float* __restrict_
     const int64_t m0 = int64_t(blockIdx.y) * BM, n0 = int64_t(blockIdx.x) * BN;
     const int64_t nsb = K / 256;
     const int64_t ns16 = K / 16;
+    const int rank = split > 1 ? int(blockIdx.z) : 0;
+    const int64_t sb_lo = nsb * rank / split, cnt = nsb * (rank + 1) / split - sb_lo;
 
     float acc[4][4][4];
 #pragma unroll
@@ -138,19 +158,20 @@ gemm_q6k_kernel(mmq_q8_1_t aq, const uint8_t* __restrict__ w, float* __restrict_
 
 #pragma unroll
     for (int s = 0; s < kStages - 1; ++s) {
-        if (s < nsb) load_stage(sbase + s * kStageBytes, aq, w, M, N, K, m0, n0, s);
+        if (s < cnt) load_stage(sbase + s * kStageBytes, aq, w, M, N, K, m0, n0, sb_lo + s);
         cp_async_commit();
     }
 
-    for (int64_t sb = 0; sb < nsb; ++sb) {
+    for (int64_t i = 0; i < cnt; ++i) {
+        const int64_t sb = sb_lo + i;
         cp_async_wait<kStages - 2>();
-        __syncthreads();   // stage sb visible; everyone is done with sb-1
+        __syncthreads();   // stage i visible; everyone is done with i-1
         {
-            const int64_t nx = sb + kStages - 1;
-            if (nx < nsb) load_stage(sbase + (nx % kStages) * kStageBytes, aq, w, M, N, K, m0, n0, nx);
+            const int64_t nx = i + kStages - 1;
+            if (nx < cnt) load_stage(sbase + (nx % kStages) * kStageBytes, aq, w, M, N, K, m0, n0, sb_lo + nx);
             cp_async_commit();
         }
-        const int st = int(sb % kStages);
+        const int st = int(i % kStages);
         const uint8_t* sA = smem + st * kStageBytes;
         const uint8_t* sW = sA + kAStage;
         const float* sDa = reinterpret_cast<const float*>(sW + kWStage);
@@ -255,6 +276,31 @@ gemm_q6k_kernel(mmq_q8_1_t aq, const uint8_t* __restrict__ w, float* __restrict_
     }
     cp_async_wait<0>();
 
+    if (!kDump && split > 1) {
+        __syncthreads();   // every warp is done with the stages: reuse them for the partial tile
+        float4* mine = reinterpret_cast<float4*>(smem) + t * 16;
+#pragma unroll
+        for (int fm = 0; fm < 4; ++fm)
+#pragma unroll
+            for (int fn = 0; fn < 4; ++fn)
+                mine[fm * 4 + fn] = make_float4(acc[fm][fn][0], acc[fm][fn][1], acc[fm][fn][2], acc[fm][fn][3]);
+        q6_cluster_sync();   // every rank's partial is in its shared memory
+        if (rank == 0) {
+            for (int r = 1; r < split; ++r)
+#pragma unroll
+                for (int fm = 0; fm < 4; ++fm)
+#pragma unroll
+                    for (int fn = 0; fn < 4; ++fn) {
+                        const float4 v = q6_ld_peer_v4(sbase + uint32_t(t * 256 + (fm * 4 + fn) * 16), uint32_t(r));
+                        acc[fm][fn][0] += v.x;
+                        acc[fm][fn][1] += v.y;
+                        acc[fm][fn][2] += v.z;
+                        acc[fm][fn][3] += v.w;
+                    }
+        }
+        q6_cluster_sync();   // the peers' memory stays alive until rank 0 has read it
+        if (rank != 0) return;
+    }
     if (!kDump) {
 #pragma unroll
         for (int fm = 0; fm < 4; ++fm)
@@ -321,11 +367,21 @@ gemv_q6k_kernel(mmq_q8_1_t aq, const uint8_t* __restrict__ w, float* __restrict_
         }
         if (ci >= nch) continue;
         float ds[kGvR][2];   // d * sc of the chunk's two sub-blocks (exact in f32)
+        uint32_t qw[kGvR][8];   // the chunk's 32 quants as int8, once for all tokens
 #pragma unroll
         for (int r = 0; r < kGvR; ++r) {
             const float d = __half2float(__ushort_as_half(uint16_t(dw[r])));
             ds[r][0] = d * float(int8_t(scw[r] & 0xFFu));
             ds[r][1] = d * float(int8_t(scw[r] >> 8));
+            const uint32_t lw[8] = {ql[r][0].x, ql[r][0].y, ql[r][0].z, ql[r][0].w,
+                                    ql[r][1].x, ql[r][1].y, ql[r][1].z, ql[r][1].w};
+            const uint32_t hw[8] = {qh[r][0].x, qh[r][0].y, qh[r][0].z, qh[r][0].w,
+                                    qh[r][1].x, qh[r][1].y, qh[r][1].z, qh[r][1].w};
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const uint32_t u = ((lw[e] >> (4 * (rr >> 1))) & 0x0F0F0F0Fu) | (((hw[e] >> (2 * rr)) & 0x03030303u) << 4);
+                qw[r][e] = __vsub4(u, 0x20202020u);   // u - 32 per byte: int8 quants
+            }
         }
 #pragma unroll
         for (int t = 0; t < MT; ++t) {
@@ -337,18 +393,11 @@ gemv_q6k_kernel(mmq_q8_1_t aq, const uint8_t* __restrict__ w, float* __restrict_
                 const uint32_t av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
 #pragma unroll
                 for (int r = 0; r < kGvR; ++r) {
-                    const uint32_t lw[8] = {ql[r][0].x, ql[r][0].y, ql[r][0].z, ql[r][0].w,
-                                            ql[r][1].x, ql[r][1].y, ql[r][1].z, ql[r][1].w};
-                    const uint32_t hw[8] = {qh[r][0].x, qh[r][0].y, qh[r][0].z, qh[r][0].w,
-                                            qh[r][1].x, qh[r][1].y, qh[r][1].z, qh[r][1].w};
                     int s0 = 0, s1 = 0;
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        const uint32_t u = ((lw[e] >> (4 * (rr >> 1))) & 0x0F0F0F0Fu) |
-                                           (((hw[e] >> (2 * rr)) & 0x03030303u) << 4);
-                        const int q = int(__vsub4(u, 0x20202020u));   // u - 32 per byte: int8 quants
-                        if (e < 4) s0 = __dp4a(q, int(av[e]), s0);
-                        else s1 = __dp4a(q, int(av[e]), s1);
+                    for (int e = 0; e < 4; ++e) {
+                        s0 = __dp4a(int(qw[r][e]), int(av[e]), s0);
+                        s1 = __dp4a(int(qw[r][4 + e]), int(av[4 + e]), s1);
                     }
                     float a = acc[t][r];
                     a = fmaf(da * ds[r][0], float(s0), a);
@@ -426,18 +475,38 @@ cudaError_t launch_repack_q6K(const uint8_t* src, uint8_t* dst, int64_t N, int64
 
 cudaError_t launch_gemm_q6k(mmq_q8_1_t aq, const uint8_t* w, float* C, int32_t* S, int64_t M, int64_t N,
                             int64_t K, cudaStream_t s) {
-    if (!S && M <= 4) {   // a few tokens: the dot-product kernel
+    if (!S && M <= 16) {   // a few tokens: the dot-product kernel
         if (M == 1) return launch_gemv_q6k<1>(aq, w, C, M, N, K, s);
         if (M == 2) return launch_gemv_q6k<2>(aq, w, C, M, N, K, s);
-        return launch_gemv_q6k<4>(aq, w, C, M, N, K, s);
+        if (M <= 4) return launch_gemv_q6k<4>(aq, w, C, M, N, K, s);
+        if (M <= 8) return launch_gemv_q6k<8>(aq, w, C, M, N, K, s);
+        return launch_gemv_q6k<16>(aq, w, C, M, N, K, s);
     }
-    const dim3 grid(unsigned((N + BN - 1) / BN), unsigned((M + BM - 1) / BM));
-    if (grid.y > 65535u) return cudaErrorInvalidConfiguration;
+    const int64_t tiles_n = (N + BN - 1) / BN, tiles_m = (M + BM - 1) / BM;
+    if (tiles_m > 65535) return cudaErrorInvalidConfiguration;
+    // few tiles: split K over a cluster so that more SMs stream the weights
+    int dev = 0, nsm = 152;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
+    const int64_t nsb = K / 256;
+    int split = 1;
+    while (!S && split < 8 && 2 * split <= nsb && tiles_m * tiles_n * 2 * split <= nsm) split *= 2;
     auto k = S ? gemm_q6k_kernel<true> : gemm_q6k_kernel<false>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
-    k<<<grid, kThreads, kSmemBytes, s>>>(aq, w, C, S, M, N, K);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(unsigned(tiles_n), unsigned(tiles_m), unsigned(split));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = size_t(kSmemBytes);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 1;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = unsigned(split);
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, k, aq, w, C, S, M, N, K, split);
 }
 
 }  // namespace mmq

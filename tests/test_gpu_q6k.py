@@ -60,7 +60,7 @@ def test_q6k_block_dots_extremes(sign):
 
 @pytest.mark.parametrize("M,N,K", [(128, 256, 512), (77, 132, 768), (300, 388, 1280), (1, 4, 256),
                                    (64, 128, 2816), (2, 132, 768), (3, 260, 4096), (4, 68, 11008),
-                                   (1, 36, 1280)])
+                                   (1, 36, 1280), (7, 132, 1024), (16, 260, 2816), (12, 4, 256)])
 def test_q6k_gemm_full(M, N, K):
     x = synthetic.activations(M, K, 630 + M, 0.01)
     blk = synthetic.q6K_weights(N, K, 640 + N)
@@ -88,7 +88,7 @@ def test_q6k_gemm_full_size_sampled(name):
     assert (np.abs(C[rows, cols].astype(np.float64) - C64) <= RTOL * T + ATOL).all()
 
 
-@pytest.mark.parametrize("M,N,K", [(1, 11008, 4096), (4, 4096, 11008)])
+@pytest.mark.parametrize("M,N,K", [(1, 11008, 4096), (4, 4096, 11008), (16, 4096, 4096)])
 def test_q6k_gemm_decode_size_sampled(M, N, K):
     # decode shapes: the dot-product kernel (M <= 4)
     x = synthetic.activations(M, K, 655 + M, 0.01)
