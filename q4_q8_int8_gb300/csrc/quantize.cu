@@ -6,12 +6,15 @@
 // in-block integer sum sa, both produced by the quantize prepass.
 //
 // Bandwidth kernel: x is read once (5/4 bytes written per 4 read).  A group
-// of 8 lanes owns one 32-element block (one float4 per lane), so a warp
-// covers four consecutive blocks = 512 contiguous bytes per load; amax and
-// the sum are reduced with three xor-shuffles inside the 8-lane group.
-// Each warp keeps kUnroll groups of four blocks in flight.  The quotient
-// x / da is formed from the block's reciprocal with an exactness check (see
-// quant1), so the bits match IEEE division followed by roundf.
+// of 4 lanes owns one 32-element block, each lane two float4 (elements 4p..
+// 4p+3 and 16+4p..16+4p+3 for lane p of the group), so one load instruction
+// of the warp covers 8 blocks in fully used 32-byte sectors; amax and the
+// sum are reduced with two xor-shuffles inside the group, and the per-block
+// work (the scale's division and reciprocal, the reductions, the scale and
+// sum stores) is shared by 8 elements per lane.  Each warp keeps kUnroll
+// groups of eight blocks in flight.  The quotient x / da is formed from the
+// block's reciprocal with an exactness check (see quant_fast), so the bits
+// match IEEE division followed by roundf.
 #include "mmq_internal.h"
 #include "q8_round.cuh"
 #include "sm103_ptx.cuh"
@@ -21,92 +24,92 @@ namespace {
 using namespace mmq::q8;
 
 constexpr int kThreads = 256;
-constexpr int kUnroll = 4;
+constexpr int kUnroll = 2;
+constexpr int kBlocksPerWarp = 8;   // blocks covered by one warp instruction
 
 __device__ __forceinline__ float4 load_stream(const float* p) {
     return __ldcs(reinterpret_cast<const float4*>(p));
+}
+
+__device__ __forceinline__ uint32_t pack4(int q0, int q1, int q2, int q3) {
+    return (uint32_t(q0) & 0xFFu) | ((uint32_t(q1) & 0xFFu) << 8) | ((uint32_t(q2) & 0xFFu) << 16) |
+           ((uint32_t(q3) & 0xFFu) << 24);
 }
 
 __global__ void __launch_bounds__(kThreads)
 quantize_q8_1_kernel(const float* __restrict__ x, int8_t* __restrict__ qs,
                      float* __restrict__ da, int32_t* __restrict__ sa, int64_t nblocks) {
     const int lane = threadIdx.x & 31;
-    const int sub = lane >> 3;          // which of the warp's 4 blocks
-    const int part = lane & 7;          // which float4 of the block
-    const int64_t ngroups = (nblocks + 3) / 4;
+    const int sub = lane >> 2;          // which of the warp's 8 blocks
+    const int part = lane & 3;          // which pair of float4 of the block
+    const int64_t ngroups = (nblocks + kBlocksPerWarp - 1) / kBlocksPerWarp;
     const int64_t warp = (int64_t(blockIdx.x) * kThreads + threadIdx.x) >> 5;
     const int64_t nwarps = (int64_t(gridDim.x) * kThreads) >> 5;
     // programmatic dependent launch: x may be the previous kernel's output,
     // and the q8_1 planes may still be read by it
     mmq::ptx::griddep_launch_dependents();
     mmq::ptx::griddep_wait();
-
     for (int64_t g0 = warp * kUnroll; g0 < ngroups; g0 += nwarps * kUnroll) {
-        float4 v[kUnroll];
+        float4 v[kUnroll][2];
 #pragma unroll
         for (int u = 0; u < kUnroll; ++u) {
-            const int64_t blk = (g0 + u) * 4 + sub;
-            v[u] = (blk < nblocks) ? load_stream(x + blk * 32 + part * 4)
-                                   : make_float4(0.f, 0.f, 0.f, 0.f);
+            const int64_t blk = (g0 + u) * kBlocksPerWarp + sub;
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+                v[u][h] = (blk < nblocks) ? load_stream(x + blk * 32 + 16 * h + part * 4)
+                                          : make_float4(0.f, 0.f, 0.f, 0.f);
         }
 #pragma unroll
         for (int u = 0; u < kUnroll; ++u) {
-            const int64_t g = g0 + u;
-            const int64_t blk = g * 4 + sub;
-            float amax = fmaxf(fmaxf(fabsf(v[u].x), fabsf(v[u].y)),
-                               fmaxf(fabsf(v[u].z), fabsf(v[u].w)));
+            const int64_t blk = (g0 + u) * kBlocksPerWarp + sub;
+            const float4 a = v[u][0], b = v[u][1];
+            float amax = fmaxf(fmaxf(fmaxf(fabsf(a.x), fabsf(a.y)), fmaxf(fabsf(a.z), fabsf(a.w))),
+                               fmaxf(fmaxf(fabsf(b.x), fabsf(b.y)), fmaxf(fabsf(b.z), fabsf(b.w))));
             amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
             amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
             const float d = __fdiv_rn(amax, 127.0f);
-            int q0 = 0, q1 = 0, q2 = 0, q3 = 0;   // a zero scale gives zero quants
+            int q[8] = {0, 0, 0, 0, 0, 0, 0, 0};   // a zero scale gives zero quants
             bool redo = false;
             if (d != 0.0f) {
                 redo = d < 0x1p-126f;   // d below the smallest normal float: always divide
                 const float r = __frcp_rn(d);
-                q0 = quant_fast(v[u].x, r, redo);
-                q1 = quant_fast(v[u].y, r, redo);
-                q2 = quant_fast(v[u].z, r, redo);
-                q3 = quant_fast(v[u].w, r, redo);
+                q[0] = quant_fast(a.x, r, redo);
+                q[1] = quant_fast(a.y, r, redo);
+                q[2] = quant_fast(a.z, r, redo);
+                q[3] = quant_fast(a.w, r, redo);
+                q[4] = quant_fast(b.x, r, redo);
+                q[5] = quant_fast(b.y, r, redo);
+                q[6] = quant_fast(b.z, r, redo);
+                q[7] = quant_fast(b.w, r, redo);
             }
             // Rare: some lane needs IEEE division.  The vote runs on all 32
             // lanes (outside the per-block branch above).
             if (__any_sync(0xffffffffu, redo)) {
                 if (redo) {
-                    q0 = quant_exact(v[u].x, d);
-                    q1 = quant_exact(v[u].y, d);
-                    q2 = quant_exact(v[u].z, d);
-                    q3 = quant_exact(v[u].w, d);
+                    q[0] = quant_exact(a.x, d);
+                    q[1] = quant_exact(a.y, d);
+                    q[2] = quant_exact(a.z, d);
+                    q[3] = quant_exact(a.w, d);
+                    q[4] = quant_exact(b.x, d);
+                    q[5] = quant_exact(b.y, d);
+                    q[6] = quant_exact(b.z, d);
+                    q[7] = quant_exact(b.w, d);
                 }
             }
-            q0 = clamp127(q0);
-            q1 = clamp127(q1);
-            q2 = clamp127(q2);
-            q3 = clamp127(q3);
-            int s = q0 + q1 + q2 + q3;
-            s += __shfl_xor_sync(0xffffffffu, s, 1);
-            s += __shfl_xor_sync(0xffffffffu, s, 2);
-            s += __shfl_xor_sync(0xffffffffu, s, 4);
-            const uint32_t packed = (uint32_t(q0) & 0xFFu) | ((uint32_t(q1) & 0xFFu) << 8) |
-                                    ((uint32_t(q2) & 0xFFu) << 16) | ((uint32_t(q3) & 0xFFu) << 24);
-            if (blk < nblocks)
-                *reinterpret_cast<uint32_t*>(qs + blk * 32 + part * 4) = packed;
-            // Gather the four blocks' (d, s) into lane 0 for one 16-byte store each.
-            const float d1 = __shfl_sync(0xffffffffu, d, 8), d2 = __shfl_sync(0xffffffffu, d, 16),
-                        d3 = __shfl_sync(0xffffffffu, d, 24);
-            const int s1 = __shfl_sync(0xffffffffu, s, 8), s2 = __shfl_sync(0xffffffffu, s, 16),
-                      s3 = __shfl_sync(0xffffffffu, s, 24);
-            if (lane == 0 && g < ngroups) {
-                if (g * 4 + 3 < nblocks) {
-                    *reinterpret_cast<float4*>(da + g * 4) = make_float4(d, d1, d2, d3);
-                    *reinterpret_cast<int4*>(sa + g * 4) = make_int4(s, s1, s2, s3);
-                } else {
-                    const float dd[4] = {d, d1, d2, d3};
-                    const int ss[4] = {s, s1, s2, s3};
-                    for (int t = 0; t < 4 && g * 4 + t < nblocks; ++t) {
-                        da[g * 4 + t] = dd[t];
-                        sa[g * 4 + t] = ss[t];
-                    }
+            int sum = 0;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                q[i] = clamp127(q[i]);
+                sum += q[i];
+            }
+            sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+            sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+            if (blk < nblocks) {
+                *reinterpret_cast<uint32_t*>(qs + blk * 32 + part * 4) = pack4(q[0], q[1], q[2], q[3]);
+                *reinterpret_cast<uint32_t*>(qs + blk * 32 + 16 + part * 4) = pack4(q[4], q[5], q[6], q[7]);
+                if (part == 0) {
+                    da[blk] = d;
+                    sa[blk] = sum;
                 }
             }
         }
@@ -120,7 +123,7 @@ namespace mmq {
 cudaError_t launch_quantize_q8_1(const float* x, int64_t M, int64_t K, mmq_q8_1_t aq,
                                  cudaStream_t s) {
     const int64_t nblocks = M * (K / 32);
-    const int64_t ngroups = (nblocks + 3) / 4;
+    const int64_t ngroups = (nblocks + kBlocksPerWarp - 1) / kBlocksPerWarp;
     const int64_t warps_needed = (ngroups + kUnroll - 1) / kUnroll;
     int dev = 0, nsm = 152;
     cudaGetDevice(&dev);
