@@ -237,9 +237,11 @@ def run_reference(args, rank, world):
     import oracle
     oracle.build()
     cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
-    # each step: quantize + GEMM over a bounded row sample (sized from one probe step)
-    per_step_budget = max(0.5, 150.0 / max(1, args.steps + args.warmup))
-    _, m, _, _ = cpu_oracle_sample(M, K, N, per_step_budget, x, blk)
+    # each step: quantize + GEMM over a bounded row sample, sized from a probe
+    # so that the whole run (warm-up and timed steps) takes about two minutes
+    per_step_budget = 120.0 / max(1, args.steps + args.warmup)
+    _, m, dt_probe, _ = cpu_oracle_sample(M, K, N, min(per_step_budget, 2.0), x, blk)
+    m = max(1, min(M, int(m * per_step_budget / max(dt_probe, 1e-6))))
     xs = x[:m]
     for _ in range(args.warmup):
         q, da, sa = oracle.quantize_q8_1(xs)
