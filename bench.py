@@ -47,12 +47,30 @@ def parse():
     ap.add_argument("--no-control", action="store_true", help="skip the dequantize-then-dense control timing")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="target seconds of oracle work for the CPU baseline sample")
+    ap.add_argument("--ref-seconds", type=float, default=120.0,
+                    help="target seconds for the whole --impl reference run")
     return ap.parse_args()
 
 
 def dist_env():
     return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
             int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def max_over_ranks(vals, world, device=None):
+    """Each value's maximum over all ranks (the slowest rank sets the job
+    time); the values themselves when world == 1."""
+    import torch
+    t = torch.tensor([float(v) for v in vals], dtype=torch.float64, device=device)
+    if world > 1:
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return t.tolist()
+
+
+def whole_job_tmacs(macs_per_rank, world, max_ms):
+    """Whole-job throughput: every rank's independent problem, over the
+    slowest rank's time."""
+    return macs_per_rank * world / (max_ms * 1e-3) / 1e12
 
 
 # --------------------------------------------------------------------- clocks
@@ -239,7 +257,7 @@ def run_reference(args, rank, world):
     cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
     # each step: quantize + GEMM over a bounded row sample, sized from a probe
     # so that the whole run (warm-up and timed steps) takes about two minutes
-    per_step_budget = 120.0 / max(1, args.steps + args.warmup)
+    per_step_budget = args.ref_seconds / max(1, args.steps + args.warmup)
     _, m, dt_probe, _ = cpu_oracle_sample(M, K, N, min(per_step_budget, 2.0), x, blk)
     m = max(1, min(M, int(m * per_step_budget / max(dt_probe, 1e-6))))
     xs = x[:m]
@@ -349,10 +367,7 @@ def run_mine(args, rank, world, local_rank):
     g_all = np.array([e[1].elapsed_time(e[2]) for e in evs])
     g_ms = float(np.mean(g_all))
     g_dist = {"median": float(np.median(g_all)), "min": float(g_all.min()), "max": float(g_all.max())}
-    t = torch.tensor([step_ms, q_ms, g_ms], device=dev)
-    if world > 1:
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-    step_ms, q_ms, g_ms = t.tolist()
+    step_ms, q_ms, g_ms = max_over_ranks([step_ms, q_ms, g_ms], world, dev)
 
     # ---- end to end through the C ABI with pinned host buffers: mmq_q4K_gemm_host
     # (x in from host memory, C out to host memory, chunked so that the copies
@@ -383,10 +398,7 @@ def run_mine(args, rank, world, local_rank):
     eb.record(stream)
     torch.cuda.synchronize(dev)
     e2e_ms = ea.elapsed_time(eb) / e2e_steps
-    te = torch.tensor([e2e_ms], device=dev)
-    if world > 1:
-        torch.distributed.all_reduce(te, op=torch.distributed.ReduceOp.MAX)
-    e2e_ms = te.item()
+    e2e_ms = max_over_ranks([e2e_ms], world, dev)[0]
 
     # ---- the dequantize-then-dense control path on the same inputs (rank 0)
     control = None
@@ -440,7 +452,7 @@ def run_mine(args, rank, world, local_rank):
         return
 
     macs = M * N * K
-    value = macs * world / (step_ms * 1e-3) / 1e12
+    value = whole_job_tmacs(macs, world, step_ms)
     gemm_tmacs = macs / (g_ms * 1e-3) / 1e12
     peaks = measured_peaks()
     micro = microbench_peaks()
@@ -524,7 +536,7 @@ def run_mine(args, rank, world, local_rank):
         "prepass": {"ms": q_ms, "gbs": (M * K * 4 + M * K * 1.25) / (q_ms * 1e-3) / 1e9},
         "roofline": roof,
         "cpu_baseline": cpu,
-        "e2e": {"value": macs * world / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
+        "e2e": {"value": whole_job_tmacs(macs, world, e2e_ms), "unit": UNIT,
                 "h2d_bytes_per_step": M * K * 4, "d2h_bytes_per_step": M * N * 4,
                 "ms_per_step": e2e_ms},
         "gpu_launches": 2 * args.steps,
