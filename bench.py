@@ -49,6 +49,9 @@ def parse():
                     help="target seconds of oracle work for the CPU baseline sample")
     ap.add_argument("--ref-seconds", type=float, default=120.0,
                     help="target seconds for the whole --impl reference run")
+    ap.add_argument("--oracle-table", action="store_true",
+                    help="with --impl reference: time the oracle's prepass and GEMM per configuration "
+                         "(bounded row samples, extrapolated per row) instead of the contract line")
     return ap.parse_args()
 
 
@@ -246,9 +249,60 @@ def cpu_oracle_sample(M, K, N, target_s, x, blk):
     return m * N * K / dt / 1e12, m, dt, cores
 
 
+def _oracle_rows_timed(fn, M, target_s):
+    """Time fn(m) on growing row counts m until it takes target_s or m == M;
+    returns (seconds for m rows, m)."""
+    m = 1
+    while True:
+        t0 = time.perf_counter()
+        fn(m)
+        dt = time.perf_counter() - t0
+        if dt >= target_s or m >= M:
+            return dt, m
+        m = min(M, m * max(2, int(target_s / max(dt, 1e-3) * 0.9)))
+
+
+def run_oracle_table(args):
+    """The oracle's prepass and GEMM per configuration on this host's cores,
+    on row samples of about args.cpu_seconds each; a sample smaller than the
+    configuration is scaled per row and labelled extrapolated.  The 7B stack
+    (32 layers x q, k, v, o, gate, up, down, a prepass per GEMM) is the sum
+    of its GEMMs' timings x 32, labelled extrapolated."""
+    from q4_q8_int8_gb300 import synthetic
+    import oracle
+    oracle.build()
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    items = [("tiny", None), ("q_proj", None), ("gate_up", None), ("down", None)]
+    items += [("sweep", m) for m in synthetic.SWEEP_M]
+    per = {}
+    for name, msweep in items:
+        x, blk, N = synthetic.config_inputs(name, msweep)
+        M, K = x.shape
+        tq, mq = _oracle_rows_timed(lambda m: oracle.quantize_q8_1(x[:m]), M, args.cpu_seconds / 4)
+        q, da, sa = oracle.quantize_q8_1(x)
+        tg, mg = _oracle_rows_timed(lambda m: oracle.gemm(q[:m], da[:m], sa[:m], blk, N, want_bound=False),
+                                    M, args.cpu_seconds)
+        prep_s, gemm_s = tq * M / mq, tg * M / mg
+        label = name if msweep is None else f"sweep_M{msweep}"
+        per[label] = (prep_s, gemm_s)
+        print(json.dumps({"impl": "reference-table", "config": label, "M": M, "K": K, "N": N,
+                          "prepass_s": prep_s, "gemm_s": gemm_s,
+                          "gemm_tmacs": M * N * K / gemm_s / 1e12, "rows_timed": {"prepass": mq, "gemm": mg},
+                          "extrapolated": bool(mq < M or mg < M), "cores": cores}), flush=True)
+    layer = 4 * sum(per["q_proj"]) + 2 * sum(per["gate_up"]) + sum(per["down"])
+    total = 32 * layer
+    macs = 32 * (4 * 2048 * 4096 * 4096 + 3 * 2048 * 4096 * 11008)
+    print(json.dumps({"impl": "reference-table", "config": "stack_7B_32_layers", "seconds": total,
+                      "equivalent_tokens_per_s": 2048 / total, "tmacs": macs / total / 1e12,
+                      "extrapolated": True, "from": "q_proj x 4 + gate_up x 2 + down, x 32 layers",
+                      "cores": cores}), flush=True)
+
+
 def run_reference(args, rank, world):
     if rank != 0:
         return
+    if args.oracle_table:
+        return run_oracle_table(args)
     M, K, N = WORKLOADS[args.workload]
     from q4_q8_int8_gb300 import synthetic
     x, blk, _ = synthetic.config_inputs(args.workload)
