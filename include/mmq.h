@@ -162,11 +162,10 @@ int mmq_q4K_gemm_path(mmq_q8_1_t aq, const uint8_t* bq4k, float* C, int64_t M,
  * (mmq_q8_1_bytes(M, N); N % 32 == 0) and receives exactly what
  * mmq_quantize_q8_1 would produce from the f32 result (per 32 output
  * columns: da = amax/127, q = roundf(c/da) clamped to +-127, sa = sum q).
- * For M > 64 the tcgen05 kernel quantizes in its epilogue and C may be NULL
- * (then no f32 result is stored).  For M <= 4 the dot-product kernel runs in
- * clusters of 8 CTAs (32 output columns) and quantizes in its epilogue; C
- * may be NULL.  For 4 < M <= 64 C is required: the small-M kernel writes C
- * and a quantize pass over it follows on the same stream.
+ * Every kernel quantizes in its epilogue and C may be NULL (then no f32
+ * result is stored): the tcgen05 kernel for M > 64; for M <= 64 the
+ * few-token kernels, whose CTA (or cluster of CTAs, for the dot-product
+ * kernel at M <= 4) covers whole 32-column output blocks.
  * Otherwise as mmq_q4K_gemm (same argument rules and error codes). */
 int mmq_q4K_gemm_q8_1(mmq_q8_1_t aq, const uint8_t* bq4k, float* C, mmq_q8_1_t out,
                       int64_t M, int64_t N, int64_t K, void* stream);
@@ -182,7 +181,8 @@ int mmq_q4K_gemm_q8_1(mmq_q8_1_t aq, const uint8_t* bq4k, float* C, mmq_q8_1_t o
  * quantized to q8_1 exactly as mmq_quantize_q8_1 would quantize h: `out`
  * describes an [M][F] q8_1 buffer.  hf (may be NULL) receives h, f32
  * [M][F].  F % 32 == 0; other rules as mmq_q4K_gemm (N = 2F).  Runs the
- * tcgen05 kernel for every M. */
+ * tcgen05 kernel for M > 64 and the few-token kernels (dot-product for
+ * M <= 4, mma.sync for M <= 64) below, each with the SwiGLU epilogue. */
 int mmq_q4K_gemm_swiglu_q8_1(mmq_q8_1_t aq, const uint8_t* bq4k_gu, float* hf,
                              mmq_q8_1_t out, int64_t M, int64_t F, int64_t K,
                              void* stream);

@@ -214,14 +214,13 @@ int mmq_q4K_gemm_q8_1(mmq_q8_1_t aq, const uint8_t* bq4k, float* C, mmq_q8_1_t o
     if (rc) return rc;
     if (N % 32 != 0) return MMQ_ERR_ARG;
     const bool small = M <= mmq::kSmallMMax;
-    if (small && M > 4 && !C) return MMQ_ERR_ARG;   // the mma.sync kernel writes C, then it is quantized
     rc = check_gemm_args(aq, bq4k, C ? static_cast<const void*>(C) : static_cast<const void*>(out.qs), M, N, K);
     if (rc) return rc;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (M <= 4) return from_cuda(mmq::launch_gemv_q8_1(aq, bq4k, C, out, M, N, K, s));   // one kernel
-    if (small) {
-        if ((rc = run_gemm(aq, bq4k, C, nullptr, M, N, K, MMQ_PATH_SMALL_M, s))) return rc;
-        return from_cuda(mmq::launch_quantize_q8_1(C, M, N, out, s));
+    if (small) {   // one few-token kernel with the quantizing epilogue
+        int* status = mmq::status_word_ptr();
+        if (!status) return MMQ_ERR_CUDA;
+        return from_cuda(mmq::launch_gemm_small_m(aq, bq4k, C, M, N, K, status, s, out, 1));
     }
     return run_gemm(aq, bq4k, C, nullptr, M, N, K, MMQ_PATH_TC, s, out);
 }
@@ -233,8 +232,12 @@ int mmq_q4K_gemm_swiglu_q8_1(mmq_q8_1_t aq, const uint8_t* bq4k_gu, float* hf, m
     if (F < 32 || (F % 32) != 0 || F > (int64_t(1) << 30)) return MMQ_ERR_ARG;
     if ((rc = check_gemm_args(aq, bq4k_gu, out.qs, M, 2 * F, K))) return rc;
     if (hf && !aligned16(hf)) return MMQ_ERR_ALIGN;
-    if (M <= 4)   // one dot-product kernel, SwiGLU and q8_1 in a cluster epilogue
-        return from_cuda(mmq::launch_gemv_swiglu_q8_1(aq, bq4k_gu, hf, out, M, F, K, static_cast<cudaStream_t>(stream)));
+    if (M <= mmq::kSmallMMax) {   // one few-token kernel, SwiGLU and q8_1 in its epilogue
+        int* status = mmq::status_word_ptr();
+        if (!status) return MMQ_ERR_CUDA;
+        return from_cuda(mmq::launch_gemm_small_m(aq, bq4k_gu, hf, M, 2 * F, K, status,
+                                                  static_cast<cudaStream_t>(stream), out, 2));
+    }
     if ((rc = mmq::tc_gemm_check_resources())) return rc;
     int* status = mmq::status_word_ptr();
     if (!status) return MMQ_ERR_CUDA;

@@ -129,9 +129,59 @@ __device__ __forceinline__ void group_sync(int group) {   // the 4 warps (128 th
     asm volatile("bar.sync %0, 128;" ::"r"(group + 1) : "memory");
 }
 
-template <int NF, int G, int D>
+// q8_1 of one 32-element block held by 8 lanes (one float4 each; the
+// group's lanes xor-reduce amax and the sum): the rounding of the prepass
+// (reciprocal with an exactness check, IEEE division where a quotient lies
+// too close to a half-integer), so the bits equal quantize-after-store.
+__device__ __forceinline__ uint32_t quantize_group8(float4 v, float& d, int& sum) {
+    using namespace mmq::q8;
+    float amax = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
+    d = __fdiv_rn(amax, 127.0f);
+    int q0 = 0, q1 = 0, q2 = 0, q3 = 0;   // a zero scale gives zero quants
+    if (d != 0.0f) {
+        bool redo = d < 0x1p-126f;
+        const float r = __frcp_rn(d);
+        q0 = quant_fast(v.x, r, redo);
+        q1 = quant_fast(v.y, r, redo);
+        q2 = quant_fast(v.z, r, redo);
+        q3 = quant_fast(v.w, r, redo);
+        if (redo) {
+            q0 = quant_exact(v.x, d);
+            q1 = quant_exact(v.y, d);
+            q2 = quant_exact(v.z, d);
+            q3 = quant_exact(v.w, d);
+        }
+    }
+    q0 = clamp127(q0);
+    q1 = clamp127(q1);
+    q2 = clamp127(q2);
+    q3 = clamp127(q3);
+    sum = q0 + q1 + q2 + q3;
+    sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+    sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+    sum += __shfl_xor_sync(0xffffffffu, sum, 4);
+    return (uint32_t(q0) & 0xFFu) | ((uint32_t(q1) & 0xFFu) << 8) | ((uint32_t(q2) & 0xFFu) << 16) |
+           ((uint32_t(q3) & 0xFFu) << 24);
+}
+
+// Epilogue modes of the few-token kernels (kOut):
+//  kF32    C only;
+//  kQ8     the result also as q8_1 (the next GEMM's activations, with the
+//          bits of a prepass over C); C may be null;
+//  kSwiGLU gate and up rows interleaved (row 2f = gate f, 2f + 1 = up f):
+//          h = silu(g) * u = g / (1 + exp(-g)) * u in f32, quantized to q8_1
+//          ([M][N/2]); C, if not null, receives h as f32 [M][N/2].
+constexpr int kF32 = 0, kQ8 = 1, kSwiGLU = 2;
+
+// kOut != kF32: rank 0's first group stages the CTA's finished [tokens][64
+// rows] tile in shared memory and quantizes it: two q8_1 blocks of 32 output
+// columns per token (kQ8), or one block of 32 SwiGLU features (kSwiGLU).
+template <int NF, int G, int D, int kOut>
 __global__ void __launch_bounds__(G * 128)
-gemm_small_kernel(const __grid_constant__ SmallMaps maps, float* __restrict__ C, int M, int N,
+gemm_small_kernel(const __grid_constant__ SmallMaps maps, float* __restrict__ C, mmq_q8_1_t out, int M, int N,
                   int K, int split, int* status) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -346,15 +396,65 @@ gemm_small_kernel(const __grid_constant__ SmallMaps maps, float* __restrict__ C,
                 acc[f][0] = pack2(lo_f(acc[f][0]) + o.x, hi_f(acc[f][0]) + o.y);
                 acc[f][1] = pack2(lo_f(acc[f][1]) + o.z, hi_f(acc[f][1]) + o.w);
             }
+        if (kOut == kF32 || (kOut == kQ8 && C)) {
 #pragma unroll
-        for (int f = 0; f < NF; ++f) {
-            const int t0 = 8 * f + 2 * j;
+            for (int f = 0; f < NF; ++f) {
+                const int t0 = 8 * f + 2 * j;
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const int row = n0 + r0 + 8 * h;
-                if (row < N) {
-                    if (t0 < M) C[int64_t(t0) * N + row] = lo_f(acc[f][h]);
-                    if (t0 + 1 < M) C[int64_t(t0 + 1) * N + row] = hi_f(acc[f][h]);
+                for (int h = 0; h < 2; ++h) {
+                    const int row = n0 + r0 + 8 * h;
+                    if (row < N) {
+                        if (t0 < M) C[int64_t(t0) * N + row] = lo_f(acc[f][h]);
+                        if (t0 + 1 < M) C[int64_t(t0 + 1) * N + row] = hi_f(acc[f][h]);
+                    }
+                }
+            }
+        }
+        if constexpr (kOut != kF32) {
+            // the tile [8 NF tokens][64 rows] after the groups' partials (stage memory is idle)
+            float* tile = reinterpret_cast<float*>(smem + L.stages_off + G * 128 * NF * 16);
+#pragma unroll
+            for (int f = 0; f < NF; ++f)
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    tile[(8 * f + 2 * j) * kRows + r0 + 8 * h] = lo_f(acc[f][h]);
+                    tile[(8 * f + 2 * j + 1) * kRows + r0 + 8 * h] = hi_f(acc[f][h]);
+                }
+            group_sync(0);
+            const int part8 = gt & 7;   // 8 lanes per output block, 4 values each
+            constexpr int kBlocksPerToken = kOut == kSwiGLU ? 1 : 2;
+            for (int b0 = 0; b0 < M * kBlocksPerToken; b0 += 16) {   // 16 groups of 8 lanes
+                const int b = b0 + (gt >> 3);
+                const int t = b / kBlocksPerToken, half = b % kBlocksPerToken;
+                const bool ok = b < M * kBlocksPerToken;
+                float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (ok) {
+                    if constexpr (kOut == kSwiGLU) {
+                        float hv[4];
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const float g = tile[t * kRows + 2 * (4 * part8 + i)];
+                            const float u = tile[t * kRows + 2 * (4 * part8 + i) + 1];
+                            hv[i] = __fmul_rn(__fdiv_rn(g, __fadd_rn(1.0f, expf(-g))), u);
+                        }
+                        v = make_float4(hv[0], hv[1], hv[2], hv[3]);
+                    } else {
+                        v = *reinterpret_cast<const float4*>(&tile[t * kRows + 32 * half + 4 * part8]);
+                    }
+                }
+                float d;
+                int sum;
+                const uint32_t word = quantize_group8(v, d, sum);   // all 32 lanes take part
+                const int width = kOut == kSwiGLU ? N / 2 : N;       // output columns
+                const int col0 = (kOut == kSwiGLU ? n0 / 2 : n0) + 32 * half;
+                if (ok && col0 < width) {
+                    *reinterpret_cast<uint32_t*>(out.qs + int64_t(t) * width + col0 + 4 * part8) = word;
+                    if (kOut == kSwiGLU && C)
+                        *reinterpret_cast<float4*>(C + int64_t(t) * width + col0 + 4 * part8) = v;
+                    if (part8 == 0) {
+                        out.da[int64_t(t) * (width / 32) + col0 / 32] = d;
+                        out.sa[int64_t(t) * (width / 32) + col0 / 32] = sum;
+                    }
                 }
             }
         }
@@ -375,43 +475,6 @@ __device__ __forceinline__ int dp4a_us(uint32_t a_u8, uint32_t b_s8, int c) {
     return d;
 }
 
-// q8_1 of one 32-element block held by 8 lanes (one float4 each; the
-// group's lanes xor-reduce amax and the sum): the rounding of the prepass
-// (reciprocal with an exactness check, IEEE division where a quotient lies
-// too close to a half-integer), so the bits equal quantize-after-store.
-__device__ __forceinline__ uint32_t quantize_group8(float4 v, float& d, int& sum) {
-    using namespace mmq::q8;
-    float amax = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
-    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
-    d = __fdiv_rn(amax, 127.0f);
-    int q0 = 0, q1 = 0, q2 = 0, q3 = 0;   // a zero scale gives zero quants
-    if (d != 0.0f) {
-        bool redo = d < 0x1p-126f;
-        const float r = __frcp_rn(d);
-        q0 = quant_fast(v.x, r, redo);
-        q1 = quant_fast(v.y, r, redo);
-        q2 = quant_fast(v.z, r, redo);
-        q3 = quant_fast(v.w, r, redo);
-        if (redo) {
-            q0 = quant_exact(v.x, d);
-            q1 = quant_exact(v.y, d);
-            q2 = quant_exact(v.z, d);
-            q3 = quant_exact(v.w, d);
-        }
-    }
-    q0 = clamp127(q0);
-    q1 = clamp127(q1);
-    q2 = clamp127(q2);
-    q3 = clamp127(q3);
-    sum = q0 + q1 + q2 + q3;
-    sum += __shfl_xor_sync(0xffffffffu, sum, 1);
-    sum += __shfl_xor_sync(0xffffffffu, sum, 2);
-    sum += __shfl_xor_sync(0xffffffffu, sum, 4);
-    return (uint32_t(q0) & 0xFFu) | ((uint32_t(q1) & 0xFFu) << 8) | ((uint32_t(q2) & 0xFFu) << 16) |
-           ((uint32_t(q3) & 0xFFu) << 24);
-}
 
 __device__ __forceinline__ void st_dsmem_f32(uint32_t addr, float v) {
     asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
@@ -426,19 +489,10 @@ __device__ __forceinline__ void st_dsmem_f32(uint32_t addr, float v) {
 // warp and more warps have loads in flight; the KS partial sums are added
 // in slice order through shared memory.
 //
-// kOut selects the epilogue:
-//  kF32    C only;
-//  kQ8     the result also as q8_1 (the next GEMM's activations, with the
-//          bits of a prepass over C): launched in clusters of CTAs whose 32
-//          consecutive output rows form one q8_1 block per token; each row's
-//          sum is pushed into rank 0's shared memory and rank 0 quantizes the
-//          block.  C may be null;
-//  kSwiGLU gate and up rows interleaved (row 2f = gate f, 2f + 1 = up f):
-//          clusters cover 64 rows = 32 features, rank 0 forms
-//          h = silu(g) * u = g / (1 + exp(-g)) * u in f32 and quantizes it
-//          to q8_1 ([M][N/2]); C, if not null, receives h as f32 [M][N/2].
-constexpr int kF32 = 0, kQ8 = 1, kSwiGLU = 2;
-
+// With a q8_1 output (kQ8, kSwiGLU) the kernel runs in clusters of CTAs
+// covering one output block's rows (32, or 64 interleaved rows for
+// SwiGLU); each row's sum goes into rank 0's shared memory and rank 0
+// quantizes the block.
 template <int MT, int R, int KS, int kOut>
 __global__ void __launch_bounds__(128)
 gemv_dp4a_kernel(mmq_q8_1_t aq, const uint8_t* __restrict__ w, float* __restrict__ C, mmq_q8_1_t out,
@@ -711,9 +765,9 @@ bool encode(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t i
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int NF, int G, int D>
-cudaError_t launch_nf(const SmallMaps& maps, float* C, int64_t M, int64_t N, int64_t K, int* status,
-                      cudaStream_t s) {
+template <int NF, int G, int D, int kOut>
+cudaError_t launch_nf(const SmallMaps& maps, float* C, mmq_q8_1_t out, int64_t M, int64_t N, int64_t K,
+                      int* status, cudaStream_t s) {
     int dev = 0, nsm = 0, optin = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
@@ -730,9 +784,12 @@ cudaError_t launch_nf(const SmallMaps& maps, float* C, int64_t M, int64_t N, int
     while (split < kMaxSplit && row_tiles * split * 2 <= per_sm * int64_t(nsm) && split * 2 <= nsb &&
            Layout::make(NF, G, D, split * 2).total + 1024 <= optin)
         split *= 2;
-    const int smem = Layout::make(NF, G, D, split).total + 1024;   // + alignment slack
+    const Layout L = Layout::make(NF, G, D, split);
+    const int smem = L.total + 1024;   // + alignment slack
     if (smem > optin) return cudaErrorInvalidConfiguration;
-    auto k = gemm_small_kernel<NF, G, D>;
+    // the quantizing epilogue stages its tile behind the groups' partials in stage memory
+    if (kOut != kF32 && G * 128 * NF * 16 + 8 * NF * kRows * 4 > L.work_off) return cudaErrorInvalidConfiguration;
+    auto k = gemm_small_kernel<NF, G, D, kOut>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     cudaLaunchAttribute attr[2];
@@ -743,7 +800,22 @@ cudaError_t launch_nf(const SmallMaps& maps, float* C, int64_t M, int64_t N, int
     attr[cfg.numAttrs].val.clusterDim.y = 1;
     attr[cfg.numAttrs].val.clusterDim.z = 1;
     cfg.numAttrs += 1;
-    return cudaLaunchKernelEx(&cfg, k, maps, C, int(M), int(N), int(K), split, status);
+    return cudaLaunchKernelEx(&cfg, k, maps, C, out, int(M), int(N), int(K), split, status);
+}
+
+template <int kOut>
+cudaError_t launch_nf_any(int nf, const SmallMaps& maps, float* C, mmq_q8_1_t out, int64_t M, int64_t N,
+                          int64_t K, int* status, cudaStream_t s) {
+    switch (nf) {
+        case 1: return launch_nf<1, 4, 1, kOut>(maps, C, out, M, N, K, status, s);
+        case 2: return launch_nf<2, 4, 2, kOut>(maps, C, out, M, N, K, status, s);
+        case 3: return launch_nf<3, 4, 2, kOut>(maps, C, out, M, N, K, status, s);
+        case 4: return launch_nf<4, 4, 1, kOut>(maps, C, out, M, N, K, status, s);
+        case 5: return launch_nf<5, 2, 2, kOut>(maps, C, out, M, N, K, status, s);
+        case 6: return launch_nf<6, 2, 2, kOut>(maps, C, out, M, N, K, status, s);
+        case 7: return launch_nf<7, 2, 2, kOut>(maps, C, out, M, N, K, status, s);
+        default: return launch_nf<8, 2, 2, kOut>(maps, C, out, M, N, K, status, s);
+    }
 }
 
 }  // namespace
@@ -751,9 +823,12 @@ cudaError_t launch_nf(const SmallMaps& maps, float* C, int64_t M, int64_t N, int
 namespace mmq {
 
 cudaError_t launch_gemm_small_m(mmq_q8_1_t aq, const uint8_t* w, float* C, int64_t M, int64_t N,
-                                int64_t K, int* status, cudaStream_t s) {
-    if (M > kMaxTok) return cudaErrorInvalidValue;
+                                int64_t K, int* status, cudaStream_t s, mmq_q8_1_t out, int mode) {
+    if (M > kMaxTok || mode < kF32 || mode > kSwiGLU) return cudaErrorInvalidValue;
+    if (mode != kF32 && (out.qs == nullptr || N % (mode == kSwiGLU ? 64 : 32) != 0)) return cudaErrorInvalidValue;
     if (M <= 4) {   // a few tokens: streaming dot products on dp4a
+        if (mode == kQ8) return launch_gemv_q8_1(aq, w, C, out, M, N, K, s);
+        if (mode == kSwiGLU) return launch_gemv_swiglu_q8_1(aq, w, C, out, M, N / 2, K, s);
         const mmq_q8_1_t none = {nullptr, nullptr, nullptr};
         switch (M) {
             case 1: return launch_gemv<1, kF32>(aq, w, C, none, M, N, K, s);
@@ -774,16 +849,9 @@ cudaError_t launch_gemm_small_m(mmq_q8_1_t aq, const uint8_t* w, float* C, int64
         !encode(&maps.sa, CU_TENSOR_MAP_DATA_TYPE_INT32, aq.sa, nb, uint64_t(M), nb * 4, 8, mp,
                 CU_TENSOR_MAP_SWIZZLE_NONE))
         return cudaErrorInvalidValue;
-    switch (nf) {
-        case 1: return launch_nf<1, 4, 1>(maps, C, M, N, K, status, s);
-        case 2: return launch_nf<2, 4, 2>(maps, C, M, N, K, status, s);
-        case 3: return launch_nf<3, 4, 2>(maps, C, M, N, K, status, s);
-        case 4: return launch_nf<4, 4, 1>(maps, C, M, N, K, status, s);
-        case 5: return launch_nf<5, 2, 2>(maps, C, M, N, K, status, s);
-        case 6: return launch_nf<6, 2, 2>(maps, C, M, N, K, status, s);
-        case 7: return launch_nf<7, 2, 2>(maps, C, M, N, K, status, s);
-        default: return launch_nf<8, 2, 2>(maps, C, M, N, K, status, s);
-    }
+    if (mode == kQ8) return launch_nf_any<kQ8>(nf, maps, C, out, M, N, K, status, s);
+    if (mode == kSwiGLU) return launch_nf_any<kSwiGLU>(nf, maps, C, out, M, N, K, status, s);
+    return launch_nf_any<kF32>(nf, maps, C, out, M, N, K, status, s);
 }
 
 }  // namespace mmq

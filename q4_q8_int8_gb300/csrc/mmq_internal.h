@@ -55,9 +55,13 @@ int64_t tc2_pair_tiles(int64_t M, int64_t N);
 cudaError_t launch_gemm_tc2(mmq_q8_1_t aq, const uint8_t* w, float* C,
                             int32_t* S, int64_t M, int64_t N, int64_t K,
                             int* status, int inject_timeout, cudaStream_t s);
+// mode 0: C only; 1: also q8_1 into `out` (C may be null); 2: gate/up rows
+// interleaved, q8_1 of silu(g)*u into `out` [M][N/2] and, if C is not null,
+// h as f32 [M][N/2] into C.
 cudaError_t launch_gemm_small_m(mmq_q8_1_t aq, const uint8_t* w, float* C,
                                 int64_t M, int64_t N, int64_t K, int* status,
-                                cudaStream_t s);
+                                cudaStream_t s, mmq_q8_1_t out = mmq_q8_1_t{nullptr, nullptr, nullptr},
+                                int mode = 0);
 // Host-buffer pipeline (host_pipeline.cu): rows per chunk, workspace bytes,
 // and the chunked copy-in / prepass + GEMM / copy-out, with `gemm` the GEMM
 // to run on each chunk's q8_1 planes (MMQ_* code).

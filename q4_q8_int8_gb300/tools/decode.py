@@ -10,8 +10,8 @@ prepass and GEMM kernels are launched with programmatic dependent launch
 (mmq_set_programmatic_launch), so each starts streaming its weights while
 the previous kernel finishes.  With --fused every GEMM writes its result as
 q8_1 (mmq_q4K_gemm_q8_1) and the next GEMM reads it with no prepass between
-them: one kernel per GEMM for 1 to 4 tokens (q8_1 out of the dot-product
-kernel's epilogue), a GEMM and a quantize pass for more.  Prints one JSON line: step time, tokens/s,
+them: one kernel per GEMM up to 64 tokens (q8_1 out of the few-token
+kernels' epilogues).  Prints one JSON line: step time, tokens/s,
 and the weight stream's rate against the measured HBM copy bandwidth.
 
 With --model the step has a transformer layer's structure instead: q, k
@@ -103,10 +103,10 @@ def main():
             x = prev if (prev is not None and prev.shape[1] == K) else pool[K]
             if args.fused:
                 # q8_1 in: the previous GEMM's q8_1 output where the widths chain, else
-                # a prequantized pool entry; q8_1 out (and no f32 result for M <= 4)
+                # a prequantized pool entry; q8_1 out (and no f32 result up to 64 tokens)
                 src = qprev if (qprev is not None and N_prev == K) else qpool[K]
                 rc = mmq.mmq_q4K_gemm_q8_1(src, ctypes.c_void_p(w.data_ptr()),
-                                           ctypes.c_void_p(0 if M <= 4 else outs[i].data_ptr()),
+                                           ctypes.c_void_p(0 if M <= 64 else outs[i].data_ptr()),
                                            qout[i % 2][N], M, N, K, sp)
                 qprev, N_prev = qout[i % 2][N], N
             else:
@@ -140,7 +140,7 @@ def main():
                      "MEASURED_PEAKS.json")
     if os.path.exists(p):
         hbm = json.load(open(p))["hbm_gbs"]
-    nk = 7 * args.layers if args.model else (1 if args.fused and M <= 4 else 2) * len(gemms)
+    nk = 7 * args.layers if args.model else (1 if args.fused and M <= 64 else 2) * len(gemms)
     print(json.dumps({
         "workload": (f"7B decode step, layer structure: {args.layers} x (qkv, o, gate|up + SwiGLU, down), "
                      f"{M} token(s)") if args.model else

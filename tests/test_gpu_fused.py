@@ -23,7 +23,8 @@ def _check_q8_of(C, o):
 
 @pytest.mark.parametrize("M,N,K", [(200, 256, 512), (130, 4096, 1024), (256, 160, 2816), (37, 96, 512),
                                    (1, 32, 256), (2, 288, 768), (3, 4096, 4096), (4, 11008, 4096),
-                                   (4, 4096, 11008)])
+                                   (4, 4096, 11008), (5, 96, 256), (16, 4096, 4096), (31, 160, 2816),
+                                   (64, 11008, 4096), (9, 4096, 11008)])
 def test_fused_q8_1_output(M, N, K):
     mmq = require_gpu()
     x = synthetic.activations(M, K, 300 + M, 0.01)
@@ -36,11 +37,11 @@ def test_fused_q8_1_output(M, N, K):
     q, da, sa = oracle.quantize_q8_1(x)
     C_ref, _, T = oracle.gemm(q, da, sa, blk, N)
     assert oracle.within_tolerance(Ch, C_ref, T, RTOL, ATOL).all()
-    if M > 64 or M <= 4:   # without the f32 result: the same q8_1 bits
-        _, o2 = mmq.q4K_gemm_q8_1(aq, to_dev(blk.reshape(-1)), N, with_c=False)
-        assert mmq.status() == 0
-        for a, b in zip(o, o2):
-            assert np.array_equal(a.cpu().numpy(), b.cpu().numpy())
+    # without the f32 result: the same q8_1 bits
+    _, o2 = mmq.q4K_gemm_q8_1(aq, to_dev(blk.reshape(-1)), N, with_c=False)
+    assert mmq.status() == 0
+    for a, b in zip(o, o2):
+        assert np.array_equal(a.cpu().numpy(), b.cpu().numpy())
 
 
 def test_fused_q8_1_output_full_size():

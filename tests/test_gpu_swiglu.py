@@ -44,7 +44,8 @@ def _run(M, F, K, seed, with_h=True):
 
 @pytest.mark.parametrize("M,F,K", [(200, 256, 512), (130, 512, 1024), (37, 96, 512), (1, 32, 256),
                                    (300, 160, 2816), (2, 96, 768), (3, 160, 4096), (4, 256, 2816),
-                                   (1, 4096, 4096)])
+                                   (1, 4096, 4096), (5, 96, 512), (16, 256, 4096), (33, 160, 2816),
+                                   (64, 512, 1024)])
 def test_swiglu_full(M, F, K):
     mmq, x, blk_gu, aq, w_gu, h, (qs, da, sa) = _run(M, F, K, 400 + M)
     h = h.cpu().numpy()
@@ -58,7 +59,7 @@ def test_swiglu_full(M, F, K):
     assert (qs == rq).all() and (da.view(np.uint32) == rda.view(np.uint32)).all() and (sa == rsa).all()
 
 
-@pytest.mark.parametrize("M", [130, 1, 4])
+@pytest.mark.parametrize("M", [130, 1, 4, 16, 64])
 def test_swiglu_without_h_same_bits(M):
     mmq, x, blk_gu, aq, w_gu, h, o1 = _run(M, 256, 1024, 77, with_h=True)
     _, o2 = mmq.q4K_gemm_swiglu_q8_1(aq, w_gu, 256, with_h=False)
@@ -98,7 +99,7 @@ def test_swiglu_argument_errors():
     assert mmq.status() == 0
 
 
-@pytest.mark.parametrize("M", [1, 4])
+@pytest.mark.parametrize("M", [1, 4, 16])
 def test_swiglu_gate_up_decode_full_size(M):
     # the 7B FFN at a few tokens (the dot-product kernel's cluster epilogue)
     M_, F, K = M, 11008, 4096
