@@ -99,3 +99,33 @@ def test_host_pipeline_argument_errors():
     torch.cuda.synchronize()
     assert (Ch == 0).all()   # zero weights and zero activations
     assert mmq.status() == 0
+
+
+def test_host_pipeline_in_cuda_graph():
+    # the three-stream pipeline captured into a CUDA graph (its copy streams
+    # join the capture through the caller stream's start event) and replayed
+    import torch
+    mmq = require_gpu()
+    M, N, K = 1100, 516, 1024
+    blk = synthetic.q4K_weights(N, K, 721)
+    w = to_dev(blk.reshape(-1))
+    xh = torch.from_numpy(synthetic.activations(M, K, 722, 0.01)).pin_memory()
+    ref = mmq.q4K_gemm_host(xh, w, N)
+    need = mmq.mmq_q4K_gemm_host_workspace(M, N, K)
+    ws = torch.empty(need + 256, dtype=torch.uint8, device="cuda")
+    out = torch.zeros((M, N), dtype=torch.float32, pin_memory=True)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        mmq.q4K_gemm_host(xh, w, N, out=out, workspace=ws, stream=s)   # warm-up outside capture
+        s.synchronize()
+        out.zero_()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            mmq.q4K_gemm_host(xh, w, N, out=out, workspace=ws, stream=s)
+        for _ in range(2):
+            out.zero_()
+            g.replay()
+            s.synchronize()
+            assert torch.equal(out.view(torch.int32), ref.view(torch.int32))
+    assert mmq.status() == 0
