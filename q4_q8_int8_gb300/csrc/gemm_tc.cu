@@ -141,7 +141,8 @@ struct Bars {
 template <bool kDump, bool kQ8, bool kGlu = false>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_tc_kernel(const __grid_constant__ TmaMaps maps, float* __restrict__ C, mmq_q8_1_t q8out,
-               int32_t* __restrict__ S, int M, int N, int K, int split, int* status, int inject_timeout) {
+               int32_t* __restrict__ S, int M, int N, int K, int split, int* status, int inject_timeout,
+               int tile_lo, int num_tiles) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~uintptr_t(1023));
@@ -152,14 +153,15 @@ gemm_tc_kernel(const __grid_constant__ TmaMaps maps, float* __restrict__ C, mmq_
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nsb = K / 256;
-    const int tiles_m = (M + BM - 1) / BM, tiles_n = (N + BN - 1) / BN;
-    const int num_tiles = tiles_m * tiles_n;
-    // Persistent mode (split == 1): CTAs stride over all tiles and K.  Split
-    // mode: a cluster of `split` CTAs shares one tile, rank r takes
-    // super-blocks [nsb*r/split, nsb*(r+1)/split), and rank 0 adds the
-    // partial sums in rank order.
+    const int tiles_n = (N + BN - 1) / BN;
+    // This launch covers tiles [tile_lo, num_tiles) (a launch may take only
+    // the last, partial round of a larger GEMM).  Persistent mode (split ==
+    // 1): CTAs stride over those tiles with all of K.  Split mode: a cluster
+    // of `split` CTAs shares one tile, rank r takes super-blocks
+    // [nsb*r/split, nsb*(r+1)/split), and rank 0 adds the partial sums in
+    // rank order.
     const int rank = split > 1 ? int(blockIdx.x % unsigned(split)) : 0;
-    const int tile_first = split > 1 ? int(blockIdx.x / unsigned(split)) : int(blockIdx.x);
+    const int tile_first = tile_lo + (split > 1 ? int(blockIdx.x / unsigned(split)) : int(blockIdx.x));
     const int tile_step = split > 1 ? num_tiles : int(gridDim.x);
     const int sb_lo = (nsb * rank) / split, sb_hi = (nsb * (rank + 1)) / split;
 
@@ -656,31 +658,49 @@ cudaError_t launch_gemm_tc(mmq_q8_1_t aq, const uint8_t* w, float* C, mmq_q8_1_t
         if (fa.numRegs != int(kRegsLaunch)) return cudaErrorInvalidConfiguration;
     }
     const int64_t tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
-    // Few tiles: split K over a cluster so that most SMs get work.
-    int split = 1;
-    if (tiles * 2 <= nsm)
-        while (split < 8 && tiles * split * 2 <= nsm && split * 2 <= int64_t(nsb)) split *= 2;
     auto k = S ? gemm_tc_kernel<true, false>
                : swiglu ? gemm_tc_kernel<false, true, true>
                : (q8out.qs ? gemm_tc_kernel<false, true> : gemm_tc_kernel<false, false>);
     cudaError_t e;
     if ((e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes)))
         return e;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(unsigned(split > 1 ? tiles * split : (tiles < nsm ? tiles : nsm)));
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = size_t(kSmemBytes);
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = unsigned(split);
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, k, maps, C, q8out, S, int(M), int(N), int(K), split, status, inject_timeout);
-    if (e != cudaSuccess) return e;
-    return cudaGetLastError();
+    // One launch over tiles [lo, hi): persistent with one CTA per SM, or K
+    // split over clusters of `split` CTAs, one tile per cluster.
+    auto launch = [&](int64_t lo, int64_t hi, int split, int inject) -> cudaError_t {
+        const int64_t n = hi - lo;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(unsigned(split > 1 ? n * split : (n < nsm ? n : nsm)));
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = size_t(kSmemBytes);
+        cfg.stream = s;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = unsigned(split);
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        const cudaError_t le = cudaLaunchKernelEx(&cfg, k, maps, C, q8out, S, int(M), int(N), int(K), split, status,
+                                                  inject, int(lo), int(hi));
+        return le != cudaSuccess ? le : cudaGetLastError();
+    };
+    // the largest power-of-two split (<= 8, <= the super-blocks) that keeps
+    // n tiles x split CTAs within one round of the SMs
+    auto split_for = [&](int64_t n) {
+        int sp = 1;
+        while (sp < 8 && n * sp * 2 <= nsm && sp * 2 <= int64_t(nsb)) sp *= 2;
+        return sp;
+    };
+    // Few tiles: split K over a cluster so that most SMs get work.
+    if (tiles * 2 <= nsm) return launch(0, tiles, split_for(tiles), inject_timeout);
+    // Many tiles: whole persistent rounds, then the partial last round's tiles
+    // (at most half the SMs' worth) with K split, so that the idle SMs share it.
+    const int64_t rem = tiles % nsm;
+    if (!S && tiles > nsm && rem > 0 && split_for(rem) > 1) {
+        if ((e = launch(0, tiles - rem, 1, inject_timeout)) != cudaSuccess) return e;
+        return launch(tiles - rem, tiles, split_for(rem), 0);
+    }
+    return launch(0, tiles, 1, inject_timeout);
 }
 
 }  // namespace mmq
