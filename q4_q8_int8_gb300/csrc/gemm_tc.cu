@@ -698,7 +698,11 @@ cudaError_t launch_gemm_tc(mmq_q8_1_t aq, const uint8_t* w, float* C, mmq_q8_1_t
     const int64_t rem = tiles % nsm;
     if (!S && tiles > nsm && rem > 0 && split_for(rem) > 1) {
         if ((e = launch(0, tiles - rem, 1, inject_timeout)) != cudaSuccess) return e;
-        return launch(tiles - rem, tiles, split_for(rem), 0);
+        // at least 4 super-blocks per rank: a rank's fixed start-up and
+        // reduction cost is not worth fewer (gate/up's 8 tail tiles: split 4)
+        int sp = split_for(rem);
+        while (sp > 2 && int64_t(nsb) / sp < 4) sp /= 2;
+        return launch(tiles - rem, tiles, sp, 0);
     }
     return launch(0, tiles, 1, inject_timeout);
 }
