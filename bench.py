@@ -45,6 +45,8 @@ def parse():
     ap.add_argument("--path", default="auto", choices=["auto", "mma_s8", "tc", "tc_pair", "small_m", "tc_small"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-control", action="store_true", help="skip the dequantize-then-dense control timing")
+    ap.add_argument("--no-pdl", action="store_true",
+                    help="launch without programmatic dependent launch (mmq_set_programmatic_launch(0))")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="target seconds of oracle work for the CPU baseline sample")
     ap.add_argument("--ref-seconds", type=float, default=120.0,
@@ -350,6 +352,7 @@ def run_mine(args, rank, world, local_rank):
         dist.init_process_group("nccl", device_id=dev)
     mmq_build.build()
     mmq.load_library()
+    mmq.mmq_set_programmatic_launch(0 if args.no_pdl else 1)
     path = {"auto": mmq.MMQ_PATH_AUTO, "mma_s8": mmq.MMQ_PATH_MMA_S8, "tc": mmq.MMQ_PATH_TC,
             "tc_pair": mmq.MMQ_PATH_TC_PAIR, "small_m": mmq.MMQ_PATH_SMALL_M,
             "tc_small": mmq.MMQ_PATH_TC_SMALL}[args.path]
@@ -580,7 +583,7 @@ def run_mine(args, rank, world, local_rank):
         "config": {"workload": f"{args.workload} M={M} K={K} N={N}", "global_batch_tokens": M * world,
                    "parallelism": f"independent problem per GPU x{world}",
                    "l2": f"{R} rotating input sets ({R * set_bytes / 1e6:.0f} MB > 2x L2)",
-                   "path": args.path},
+                   "path": args.path, "programmatic_launch": not args.no_pdl},
         "us_per_gmac": step_ms * 1e3 / (macs / 1e9),
         "gemm_only": {"tmacs": gemm_tmacs, "us_per_gmac": g_ms * 1e3 / (macs / 1e9), "ms": g_ms,
                       "ms_over_steps": g_dist,

@@ -309,11 +309,12 @@ int mmq_status(void* stream);
 const char* mmq_strerror(int code);
 
 /* Programmatic dependent launch (process-wide, default off): when enabled,
- * the q8_1 prepass and the few-token GEMM kernels (M <= 64) are launched so
- * that each may start while the previous kernel on its stream finishes.  A
- * kernel so launched issues only its weight loads before it waits for the
- * previous grid to complete; it reads activations and writes its outputs
- * only after that wait, so results are the same either way.  Hides most of
+ * the q8_1 prepass and the GEMM kernels (few-token and tcgen05) are launched
+ * so that each may start while the previous kernel on its stream finishes.
+ * A kernel so launched issues only its weight loads (or, for the tcgen05
+ * kernel, only its set-up) before it waits for the previous grid to
+ * complete; it reads activations and writes its outputs only after that
+ * wait, so results are the same either way.  Hides most of
  * the per-kernel start cost in a decode-style sequence of small GEMMs.
  * While enabled, a GEMM's weights must not be written by the kernel
  * launched just before it on the same stream. */

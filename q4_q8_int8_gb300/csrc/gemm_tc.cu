@@ -148,6 +148,7 @@ gemm_tc_kernel(const __grid_constant__ TmaMaps maps, float* __restrict__ C, mmq_
                                                ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
     const Bars bars{sbase + kOffBar};
+    griddep_launch_dependents();
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
     const AbortFlag abort_flag{sbase + kOffMisc + 4};
 
@@ -207,6 +208,12 @@ gemm_tc_kernel(const __grid_constant__ TmaMaps maps, float* __restrict__ C, mmq_
     if (warp == 0) {
         // ------------------------------------------------------ TMA producer
         if (lane == 0) {
+            // programmatic dependent launch: everything before this point (the
+            // tensor-memory allocation, barriers, tensor-map prefetch) may overlap
+            // the previous kernel; its outputs (the activations) are read only
+            // after it has completed.  Every later global access of this kernel
+            // depends on these copies through the mbarriers.
+            griddep_wait();
             Ring<kNumRaw> rr;
             int raw_issued[kNumRaw] = {};
             uint32_t raw_par[kNumRaw] = {};
@@ -673,13 +680,18 @@ cudaError_t launch_gemm_tc(mmq_q8_1_t aq, const uint8_t* w, float* C, mmq_q8_1_t
         cfg.blockDim = dim3(kThreads);
         cfg.dynamicSmemBytes = size_t(kSmemBytes);
         cfg.stream = s;
-        cudaLaunchAttribute attr[1];
+        cudaLaunchAttribute attr[2];
         attr[0].id = cudaLaunchAttributeClusterDimension;
         attr[0].val.clusterDim.x = unsigned(split);
         attr[0].val.clusterDim.y = 1;
         attr[0].val.clusterDim.z = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
+        if (mmq::programmatic_launch_enabled()) {
+            attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+            attr[1].val.programmaticStreamSerializationAllowed = 1;
+            cfg.numAttrs = 2;
+        }
         const cudaError_t le = cudaLaunchKernelEx(&cfg, k, maps, C, q8out, S, int(M), int(N), int(K), split, status,
                                                   inject, int(lo), int(hi));
         return le != cudaSuccess ? le : cudaGetLastError();

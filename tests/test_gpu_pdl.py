@@ -1,7 +1,8 @@
 """Programmatic dependent launch changes when kernels start, not what they
 compute: a chain quantize -> GEMM -> quantize(its output) -> GEMM gives the
 same bits with the launch mode on and off, launched directly and from a
-CUDA graph, on the dp4a (M <= 4) and mma.sync (M <= 64) few-token paths;
+CUDA graph, on the dp4a (M <= 4), mma.sync (M <= 64) and tcgen05 paths
+(M = 700: K split over clusters for few tiles);
 and the second GEMM matches the oracle on the first GEMM's output."""
 import numpy as np
 import pytest
@@ -21,7 +22,7 @@ def _chain(mmq, x, w1, w2, K, N1, N2):
     return c1, aq2, c2
 
 
-@pytest.mark.parametrize("M", [1, 4, 9, 64])
+@pytest.mark.parametrize("M", [1, 4, 9, 64, 200, 700])
 def test_pdl_chain_same_bits_and_oracle(M):
     import torch
     mmq = require_gpu()
@@ -59,3 +60,33 @@ def test_pdl_chain_same_bits_and_oracle(M):
     q, da, sa = oracle.quantize_q8_1(c1)
     C_ref, _, T = oracle.gemm(q, da, sa, b2, N2)
     assert oracle.within_tolerance(ref[2].cpu().numpy(), C_ref, T).all()
+
+
+def test_pdl_split_tail_same_bits():
+    # more tiles than SMs: the GEMM runs as two launches (whole rounds, then
+    # the last partial round with K split); with the launch mode on, each
+    # starts while the previous kernel finishes.  Same bits either way, and
+    # sampled outputs within the tolerance of the oracle.
+    import torch
+    from tests.gpu_util import sample_points
+    mmq = require_gpu()
+    M, K, N = 2048, 512, 4096
+    x = synthetic.activations(M, K, 830, 0.01)
+    blk = synthetic.q4K_weights(N, K, 831)
+    xd, w = to_dev(x), to_dev(blk.reshape(-1))
+    try:
+        mmq.mmq_set_programmatic_launch(False)
+        ref = mmq.q4K_gemm(mmq.quantize_q8_1(xd), w, N)
+        torch.cuda.synchronize()
+        mmq.mmq_set_programmatic_launch(True)
+        for _ in range(2):
+            got = mmq.q4K_gemm(mmq.quantize_q8_1(xd), w, N)
+            torch.cuda.synchronize()
+            assert torch.equal(got.view(torch.int32), ref.view(torch.int32))
+        assert mmq.status() == 0
+    finally:
+        mmq.mmq_set_programmatic_launch(False)
+    q, da, sa = oracle.quantize_q8_1(x)
+    rows, cols = sample_points(M, N, 3000, 31)
+    C_ref, _, T = oracle.gemm_sampled(q, da, sa, blk, N, rows, cols)
+    assert oracle.within_tolerance(ref.cpu().numpy()[rows, cols], C_ref, T).all()
