@@ -43,11 +43,13 @@ def main():
     ap.add_argument("--layers", type=int, default=synthetic.STACK_LAYERS)
     ap.add_argument("--fused", action="store_true")
     ap.add_argument("--swiglu", action="store_true")
+    ap.add_argument("--pdl", action="store_true", help="programmatic dependent launch (mmq_set_programmatic_launch)")
     args = ap.parse_args()
     if args.swiglu:
         args.fused = True
     build.build()
     mmq.load_library()
+    mmq.mmq_set_programmatic_launch(args.pdl)
     dev = torch.device("cuda", 0)
     M = synthetic.STACK_TOKENS
     path = PATHS[args.path]
@@ -138,6 +140,7 @@ def main():
         "workload": f"7B prefill stack: {args.layers} layers x (q,k,v,o 4096x4096; gate,up 4096->11008; "
                     f"down 11008->4096), M={M}",
         "path": args.path, "passes": args.passes, "fused_requantize": args.fused, "fused_swiglu": args.swiglu,
+        "programmatic_launch": args.pdl,
         "stack_ms": {"min": best, "median": sorted(t_stack)[len(t_stack) // 2], "max": max(t_stack)},
         "equivalent_tok_s": M / (best * 1e-3),
         "tmacs_with_prepass": macs / (best * 1e-3) / 1e12,
