@@ -549,6 +549,12 @@ def run_mine(args, rank, world, local_rank):
                 "frac": achieved / peak, "traffic": traffic,
                 "peak_source": "measured int8 mma.sync peak (profiles/peaks.json)"}
     roof["kernel"] = kname[0]
+    # One GEMM call may be two kernels (the tcgen05 kernel's split-K tail
+    # launch); "per launch" figures here are per call, both kernels together.
+    gemm_launches = mmq.mmq_q4K_gemm_launches(M, N, K, used_path)
+    if gemm_launches < 1:
+        raise RuntimeError(f"mmq_q4K_gemm_launches failed: {gemm_launches}")
+    roof["kernels_per_call"] = gemm_launches
     # The epilogue's FP32 ceiling, reported beside the tensor roofline: per
     # output and 32-k chunk the tcgen05 kernel does one FMA (2 flops), plus
     # per super-block one FMA for d and one add of the second term (0.5 flop
@@ -596,7 +602,7 @@ def run_mine(args, rank, world, local_rank):
         "e2e": {"value": whole_job_tmacs(macs, world, e2e_ms), "unit": UNIT,
                 "h2d_bytes_per_step": M * K * 4, "d2h_bytes_per_step": M * N * 4,
                 "ms_per_step": e2e_ms},
-        "gpu_launches": 2 * args.steps,
+        "gpu_launches": args.steps * (1 + gemm_launches),
         "control": control,
         "clocks": clk,
         "clocks_window": "from warm-up start to timed-region end",

@@ -150,6 +150,13 @@ int mmq_q4K_gemm_host(const float* x_host, const uint8_t* bq4k, float* C_host,
                             /* rows on the MMA's M side, 16/32/64 tokens on */
                             /* its N side; accepts any M (token tiles of 64) */
 
+/* Number of kernels mmq_q4K_gemm_path(…, path, …) enqueues for this shape
+ * on the current device: 1, or 2 when the tcgen05 kernel splits off its
+ * last partial round of tiles into a second, split-K launch.  For counting
+ * launches (e.g. in a timed region); MMQ_ERR_ARG for a shape or path the
+ * GEMM refuses, MMQ_ERR_DEVICE / MMQ_ERR_CUDA as the GEMM would. */
+int mmq_q4K_gemm_launches(int64_t M, int64_t N, int64_t K, int path);
+
 /* Same as mmq_q4K_gemm with an explicit kernel.  MMQ_ERR_ARG if `path` is
  * unknown or the kernel does not accept the shape (the small-M kernel takes
  * M <= 64).  The automatic choice: M <= 64 -> small-M, else the one-CTA

@@ -199,6 +199,20 @@ int mmq_q4K_gemm_host(const float* x_host, const uint8_t* bq4k, float* C_host, i
     return mmq::gemm_host(x_host, bq4k, C_host, M, N, K, workspace, static_cast<cudaStream_t>(stream), gemm_auto);
 }
 
+int mmq_q4K_gemm_launches(int64_t M, int64_t N, int64_t K, int path) {
+    if (path < MMQ_PATH_AUTO || path > MMQ_PATH_TC_SMALL) return MMQ_ERR_ARG;
+    if (M < 1 || N < 1 || K < 256 || (K % 256) != 0 || (N % 4) != 0) return MMQ_ERR_ARG;
+    if (M > (int64_t(1) << 31) - 1 || N > (int64_t(1) << 31) - 1 || K > (int64_t(1) << 31) - 1)
+        return MMQ_ERR_ARG;
+    if (path == MMQ_PATH_SMALL_M && M > mmq::kSmallMMax) return MMQ_ERR_ARG;
+    int rc = check_device();
+    if (rc) return rc;
+    if (path == MMQ_PATH_AUTO) path = auto_path(M, N, false);
+    if (path != MMQ_PATH_TC) return 1;
+    const int n = mmq::tc_gemm_launch_count(M, N, K);
+    return n < 0 ? MMQ_ERR_CUDA : n;
+}
+
 int mmq_q4K_gemm_path(mmq_q8_1_t aq, const uint8_t* bq4k, float* C, int64_t M, int64_t N,
                       int64_t K, int path, void* stream) {
     if (path < MMQ_PATH_AUTO || path > MMQ_PATH_TC_SMALL) return MMQ_ERR_ARG;

@@ -637,6 +637,52 @@ int tc_gemm_check_resources() {
     return optin >= kSmemBytes ? MMQ_OK : MMQ_ERR_RESOURCE;
 }
 
+// The launches of one call: [0, tail_lo) persistent (or K split over
+// clusters of first_split CTAs when the tiles are few), then, if tail_lo <
+// tiles, the tiles [tail_lo, tiles) of the last partial round with K split
+// over clusters of tail_split CTAs.
+TcPlan tc_plan(int64_t M, int64_t N, int64_t K, int nsm, bool allow_tail) {
+    TcPlan p;
+    const int64_t nsb = K / 256;
+    p.tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
+    p.tail_lo = p.tiles;
+    // the largest power-of-two split (<= 8, <= the super-blocks) that keeps
+    // n tiles x split CTAs within one round of the SMs
+    auto split_for = [&](int64_t n) {
+        int sp = 1;
+        while (sp < 8 && n * sp * 2 <= nsm && sp * 2 <= nsb) sp *= 2;
+        return sp;
+    };
+    // Few tiles: split K over a cluster so that most SMs get work.
+    if (p.tiles * 2 <= nsm) {
+        p.first_split = split_for(p.tiles);
+        return p;
+    }
+    // Many tiles: whole persistent rounds, then the partial last round's tiles
+    // (at most half the SMs' worth) with K split, so that the idle SMs share it.
+    const int64_t rem = p.tiles % nsm;
+    if (allow_tail && p.tiles > nsm && rem > 0 && split_for(rem) > 1) {
+        // at least 4 super-blocks per rank: a rank's fixed start-up and
+        // reduction cost is not worth fewer (gate/up's 8 tail tiles: split 4)
+        int sp = split_for(rem);
+        while (sp > 2 && nsb / sp < 4) sp /= 2;
+        p.tail_lo = p.tiles - rem;
+        p.tail_split = sp;
+    }
+    return p;
+}
+
+int tc_gemm_launch_count(int64_t M, int64_t N, int64_t K) {
+    int dev = 0, nsm = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+        cudaGetLastError();
+        return -1;
+    }
+    const TcPlan p = tc_plan(M, N, K, nsm, true);
+    return p.tail_lo < p.tiles ? 2 : 1;
+}
+
 cudaError_t launch_gemm_tc(mmq_q8_1_t aq, const uint8_t* w, float* C, mmq_q8_1_t q8out, int32_t* S, int64_t M,
                            int64_t N, int64_t K, int* status, int inject_timeout, cudaStream_t s, bool swiglu) {
     TmaMaps maps;
@@ -664,7 +710,6 @@ cudaError_t launch_gemm_tc(mmq_q8_1_t aq, const uint8_t* w, float* C, mmq_q8_1_t
         if (e != cudaSuccess) return e;
         if (fa.numRegs != int(kRegsLaunch)) return cudaErrorInvalidConfiguration;
     }
-    const int64_t tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
     auto k = S ? gemm_tc_kernel<true, false>
                : swiglu ? gemm_tc_kernel<false, true, true>
                : (q8out.qs ? gemm_tc_kernel<false, true> : gemm_tc_kernel<false, false>);
@@ -696,27 +741,12 @@ cudaError_t launch_gemm_tc(mmq_q8_1_t aq, const uint8_t* w, float* C, mmq_q8_1_t
                                                   inject, int(lo), int(hi));
         return le != cudaSuccess ? le : cudaGetLastError();
     };
-    // the largest power-of-two split (<= 8, <= the super-blocks) that keeps
-    // n tiles x split CTAs within one round of the SMs
-    auto split_for = [&](int64_t n) {
-        int sp = 1;
-        while (sp < 8 && n * sp * 2 <= nsm && sp * 2 <= int64_t(nsb)) sp *= 2;
-        return sp;
-    };
-    // Few tiles: split K over a cluster so that most SMs get work.
-    if (tiles * 2 <= nsm) return launch(0, tiles, split_for(tiles), inject_timeout);
-    // Many tiles: whole persistent rounds, then the partial last round's tiles
-    // (at most half the SMs' worth) with K split, so that the idle SMs share it.
-    const int64_t rem = tiles % nsm;
-    if (!S && tiles > nsm && rem > 0 && split_for(rem) > 1) {
-        if ((e = launch(0, tiles - rem, 1, inject_timeout)) != cudaSuccess) return e;
-        // at least 4 super-blocks per rank: a rank's fixed start-up and
-        // reduction cost is not worth fewer (gate/up's 8 tail tiles: split 4)
-        int sp = split_for(rem);
-        while (sp > 2 && int64_t(nsb) / sp < 4) sp /= 2;
-        return launch(tiles - rem, tiles, sp, 0);
-    }
-    return launch(0, tiles, 1, inject_timeout);
+    const TcPlan p = tc_plan(M, N, K, nsm, S == nullptr);
+    // tile indices (and a tile plus the stride over tiles) stay in int
+    if (p.tiles > (int64_t(1) << 30)) return cudaErrorInvalidValue;
+    if (p.tail_lo == p.tiles) return launch(0, p.tiles, p.first_split, inject_timeout);
+    if ((e = launch(0, p.tail_lo, 1, inject_timeout)) != cudaSuccess) return e;
+    return launch(p.tail_lo, p.tiles, p.tail_split, 0);
 }
 
 }  // namespace mmq

@@ -50,6 +50,18 @@ int tc_gemm_check_resources();   // MMQ_OK or MMQ_ERR_RESOURCE
 cudaError_t launch_gemm_tc(mmq_q8_1_t aq, const uint8_t* w, float* C, mmq_q8_1_t q8out,
                            int32_t* S, int64_t M, int64_t N, int64_t K,
                            int* status, int inject_timeout, cudaStream_t s, bool swiglu = false);
+// The tcgen05 kernel's launch plan for one call (gemm_tc.cu): tiles
+// [0, tail_lo) in the first launch (persistent, or K split over clusters of
+// first_split CTAs), tiles [tail_lo, tiles) in a second launch with K split
+// over clusters of tail_split CTAs.
+struct TcPlan {
+    int64_t tiles = 0;
+    int first_split = 1;
+    int64_t tail_lo = 0;
+    int tail_split = 1;
+};
+TcPlan tc_plan(int64_t M, int64_t N, int64_t K, int nsm, bool allow_tail);
+int tc_gemm_launch_count(int64_t M, int64_t N, int64_t K);   // kernels per call, -1 on a CUDA error
 int tc2_gemm_check_resources();  // MMQ_OK or MMQ_ERR_RESOURCE
 int64_t tc2_pair_tiles(int64_t M, int64_t N);
 cudaError_t launch_gemm_tc2(mmq_q8_1_t aq, const uint8_t* w, float* C,

@@ -117,6 +117,12 @@ def test_argument_errors_before_device(lib):
     assert mmq.mmq_q4K_gemm(good, w, C, 1, 6, 256, None) == mmq.MMQ_ERR_ARG
     assert mmq.mmq_q4K_gemm_path(good, w, C, 65, 4, 256, mmq.MMQ_PATH_SMALL_M, None) == mmq.MMQ_ERR_ARG
     assert mmq.mmq_q4K_gemm_path(good, w, C, 1, 4, 256, 9, None) == mmq.MMQ_ERR_ARG
+    # the launch-count query refuses what the GEMM refuses, before the device
+    assert mmq.mmq_q4K_gemm_launches(0, 4, 256, mmq.MMQ_PATH_AUTO) == mmq.MMQ_ERR_ARG
+    assert mmq.mmq_q4K_gemm_launches(1, 6, 256, mmq.MMQ_PATH_AUTO) == mmq.MMQ_ERR_ARG
+    assert mmq.mmq_q4K_gemm_launches(1, 4, 300, mmq.MMQ_PATH_AUTO) == mmq.MMQ_ERR_ARG
+    assert mmq.mmq_q4K_gemm_launches(65, 4, 256, mmq.MMQ_PATH_SMALL_M) == mmq.MMQ_ERR_ARG
+    assert mmq.mmq_q4K_gemm_launches(1, 4, 256, 9) == mmq.MMQ_ERR_ARG
     assert mmq.mmq_q4K_block_dots(good, w, C, 1, 4, 256, mmq.MMQ_PATH_SMALL_M, None) == mmq.MMQ_ERR_ARG
     assert mmq.mmq_q4K_block_dots(good, w, C, 1, 4, 256, mmq.MMQ_PATH_TC_SMALL, None) == mmq.MMQ_ERR_ARG
     # alignment

@@ -74,6 +74,10 @@ def test_pdl_split_tail_same_bits():
     x = synthetic.activations(M, K, 830, 0.01)
     blk = synthetic.q4K_weights(N, K, 831)
     xd, w = to_dev(x), to_dev(blk.reshape(-1))
+    # 512 tiles on 152 SMs: three whole rounds, then 56 tiles split-K
+    assert mmq.mmq_q4K_gemm_launches(M, N, K, mmq.MMQ_PATH_AUTO) == 2
+    assert mmq.mmq_q4K_gemm_launches(700, 512, 1024, mmq.MMQ_PATH_AUTO) == 1   # 24 tiles, one split launch
+    assert mmq.mmq_q4K_gemm_launches(64, N, K, mmq.MMQ_PATH_AUTO) == 1         # few tokens
     try:
         mmq.mmq_set_programmatic_launch(False)
         ref = mmq.q4K_gemm(mmq.quantize_q8_1(xd), w, N)
