@@ -36,6 +36,8 @@
 #include <cudaTypedefs.h>
 #include <cuda_fp16.h>
 
+#include <atomic>
+#include <cstdint>
 #include <mutex>
 
 #include "mmq_internal.h"
@@ -694,18 +696,56 @@ cudaError_t launch_gemv_ks(mmq_q8_1_t aq, const uint8_t* w, float* C, mmq_q8_1_t
     return cudaLaunchKernelEx(&cfg, gemv_dp4a_kernel<MT, R, KS, kOut>, aq, w, C, out, int(M), int(N), int(K));
 }
 
-// K split by the number of 32-pair rounds a row takes: 1 round -> 1 warp,
-// 2-3 -> 2 warps, 4 or more -> 4 warps per row group (2 at most for the
-// SwiGLU epilogue, whose 64-row blocks would otherwise need clusters of 16).
+// CTAs of one kernel instance that fit on the GPU at once (register-bound),
+// found once per instance.
+template <int MT, int KS, int kOut>
+int64_t gemv_resident_ctas() {
+    static std::atomic<int64_t> cached{0};
+    int64_t v = cached.load(std::memory_order_relaxed);
+    if (v == 0) {
+        int dev = 0, nsm = 0, per_sm = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gemv_dp4a_kernel<MT, kGemvRows, KS, kOut>, 128,
+                                                          0) != cudaSuccess || per_sm < 1) {
+            cudaGetLastError();
+            per_sm = 1;
+        }
+        v = int64_t(per_sm) * (nsm > 0 ? nsm : 1);
+        cached.store(v, std::memory_order_relaxed);
+    }
+    return v;
+}
+
+// The K split (KS warps per row group) with the lowest modelled cost:
+// waves of CTAs x (dependent load rounds per warp + 1/2), the half standing
+// for a wave's own start-up and drain.  More warps per row take fewer rounds
+// each but make more CTAs, and a wave that is only just started costs almost
+// a whole one.  Fitted to one and four tokens on the 7B shapes (4096 ->
+// 4096, 11008, 12288, 22016 and 11008 -> 4096), where it picks the fastest
+// of 1, 2 and 4 every time.  The SwiGLU epilogue takes KS <= 2 (its 64-row
+// blocks would otherwise need clusters of 16).
 template <int MT, int kOut>
 cudaError_t launch_gemv(mmq_q8_1_t aq, const uint8_t* w, float* C, mmq_q8_1_t out, int64_t M, int64_t N, int64_t K,
                         cudaStream_t s) {
-    const int64_t rounds = (K / 64 + 31) / 32;
+    const int64_t npairs = K / 64;
+    auto cost2 = [&](int ks, int64_t resident) {   // twice the modelled cost
+        const int64_t rows = 16 / ks;                 // (4 / ks) row groups x kGemvRows rows per CTA
+        const int64_t ctas = (N + rows - 1) / rows;
+        const int64_t waves = (ctas + resident - 1) / resident;
+        const int64_t rounds = (npairs + 32 * ks - 1) / (32 * ks);
+        return waves * (2 * rounds + 1);
+    };
+    static_assert(kGemvRows == 4, "the cost model counts 4 rows per warp");
+    const int64_t c1 = cost2(1, gemv_resident_ctas<MT, 1, kOut>());
+    const int64_t c2 = cost2(2, gemv_resident_ctas<MT, 2, kOut>());
+    int64_t c4 = INT64_MAX;
+    if constexpr (kOut != kSwiGLU) c4 = cost2(4, gemv_resident_ctas<MT, 4, kOut>());
+    if (c1 <= c2 && c1 <= c4) return launch_gemv_ks<MT, 1, kOut>(aq, w, C, out, M, N, K, s);
     if constexpr (kOut != kSwiGLU) {
-        if (rounds >= 4) return launch_gemv_ks<MT, 4, kOut>(aq, w, C, out, M, N, K, s);
+        if (c4 < c2) return launch_gemv_ks<MT, 4, kOut>(aq, w, C, out, M, N, K, s);
     }
-    if (rounds >= 2) return launch_gemv_ks<MT, 2, kOut>(aq, w, C, out, M, N, K, s);
-    return launch_gemv_ks<MT, 1, kOut>(aq, w, C, out, M, N, K, s);
+    return launch_gemv_ks<MT, 2, kOut>(aq, w, C, out, M, N, K, s);
 }
 
 }  // namespace
