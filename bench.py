@@ -13,6 +13,18 @@ Under torchrun each rank runs its own independent problem on its own GPU
 (weak scaling, no data-path collective); rank 0 prints one JSON line with
 the max time over ranks.  `--impl reference` times the CPU oracle on a
 bounded sample of the same workload.
+
+After the contract line's timed region, and outside it, rank 0 adds:
+  "sweep"  kernel-only GEMM times of the other configurations (the FFN
+           GEMMs at 2K tokens, the token-count sweep at 4096 x 4096 and the
+           few-token decode shapes), each replayed from a CUDA graph over
+           rotating inputs larger than twice the L2, with t_roof / t;
+  "stack"  the 32-layer 7B prefill linear stack (224 GEMMs, a prepass each)
+           as equivalent tokens per second;
+  "clocks" sampled from the warm-up to the end of a ~1 s soak of the same
+           step loop, so that it holds many samples under load.
+`--measure-peaks` compiles bench_peaks.cu (under _build/) and prints the
+instruction-rate peaks recorded in profiles/peaks.json.
 """
 from __future__ import annotations
 
@@ -31,6 +43,11 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 WORKLOADS = {"q_proj": (2048, 4096, 4096)}
+PATH_NAMES = ("auto", "mma_s8", "tc", "small_m")
+# A timed region shorter than this is held to the burst tensor peak, a longer
+# one to the sustained peak (the GPU settles at its power cap within seconds).
+SUSTAINED_AFTER_S = 1.0
+L2_BYTES = 129e6
 METRIC = "q4_K x q8_1 GEMM TMAC/s at 7B@2K (q-proj 2048x4096x4096), prepass included"
 UNIT = "TMAC/s"
 
@@ -42,7 +59,7 @@ def parse():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="mine", choices=["mine", "reference"])
     ap.add_argument("--workload", default="q_proj", choices=sorted(WORKLOADS))
-    ap.add_argument("--path", default="auto", choices=["auto", "mma_s8", "tc", "tc_pair", "small_m", "tc_small"])
+    ap.add_argument("--path", default="auto", choices=sorted(PATH_NAMES))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-control", action="store_true", help="skip the dequantize-then-dense control timing")
     ap.add_argument("--no-pdl", action="store_true",
@@ -51,6 +68,12 @@ def parse():
                     help="target seconds of oracle work for the CPU baseline sample")
     ap.add_argument("--ref-seconds", type=float, default=120.0,
                     help="target seconds for the whole --impl reference run")
+    ap.add_argument("--no-sweep", action="store_true", help="skip the extra configurations' kernel sweep")
+    ap.add_argument("--no-stack", action="store_true", help="skip the 32-layer stack")
+    ap.add_argument("--soak-seconds", type=float, default=1.0,
+                    help="seconds of the step loop run after the timed region for the clock record")
+    ap.add_argument("--measure-peaks", action="store_true",
+                    help="compile and run bench_peaks.cu (instruction-rate peaks) and exit")
     ap.add_argument("--oracle-table", action="store_true",
                     help="with --impl reference: time the oracle's prepass and GEMM per configuration "
                          "(bounded row samples, extrapolated per row) instead of the contract line")
@@ -340,6 +363,161 @@ def run_reference(args, rank, world):
 
 
 # ----------------------------------------------------------------- GPU leg
+def path_code(mmq, name):
+    return {"auto": mmq.MMQ_PATH_AUTO, "mma_s8": mmq.MMQ_PATH_MMA_S8, "tc": mmq.MMQ_PATH_TC,
+            "small_m": mmq.MMQ_PATH_SMALL_M}[name]
+
+
+def resolved_path(mmq, path, M):
+    """The kernel family mmq_q4K_gemm runs for `path` at M tokens."""
+    if path == mmq.MMQ_PATH_AUTO:
+        return mmq.MMQ_PATH_SMALL_M if M <= mmq.SMALL_M_MAX else mmq.MMQ_PATH_TC
+    return path
+
+
+def roofline_seconds(M, K, N, peaks, burst=True):
+    """(t_roof, bound): the larger of the algorithmic HBM bytes at the measured
+    copy bandwidth and the contraction's f16 tensor flops at the measured bf16
+    (= f16) peak."""
+    alg_bytes = 0.5625 * N * K + 1.25 * M * K + 4 * M * N
+    t_hbm = alg_bytes / (peaks["hbm_gbs"] * 1e9)
+    tpk = peaks["bf16_tflops"] if burst else (peaks["bf16_tflops_sustained"] or peaks["bf16_tflops"])
+    t_tc = 2.0 * M * N * K / (tpk * 1e12)
+    return (t_hbm, "hbm") if t_hbm >= t_tc else (t_tc, "tensor")
+
+
+def graph_time_ms(fn, reps, dev):
+    """Mean device ms of fn(i) for i < reps, replayed from a CUDA graph after a
+    warm-up replay (no host launch cost inside the measurement)."""
+    import torch
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream(device=dev)
+    s.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            for i in range(reps):
+                fn(i, s)
+    torch.cuda.synchronize(dev)
+    g.replay()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    cur = torch.cuda.current_stream(dev)
+    e0.record(cur)
+    g.replay()
+    e1.record(cur)
+    torch.cuda.synchronize(dev)
+    return e0.elapsed_time(e1) / reps
+
+
+def sweep_shapes():
+    """(label, M, K, N): the FFN GEMMs at 2K tokens, the token-count sweep on
+    4096 x 4096, and few-token decode shapes of the 7B layer."""
+    from q4_q8_int8_gb300 import synthetic
+    out = [(name, *synthetic.SHAPES[name]) for name in ("gate_up", "down")]
+    out += [(f"sweep_M{m}", m, 4096, 4096) for m in synthetic.SWEEP_M]
+    out += [("decode_M1_4096x11008", 1, 4096, 11008), ("decode_M1_11008x4096", 1, 11008, 4096),
+            ("decode_M1_4096x12288", 1, 4096, 12288), ("decode_M4_4096x4096", 4, 4096, 4096),
+            ("decode_M16_4096x11008", 16, 4096, 11008)]
+    return out
+
+
+def run_sweep(mmq, dev, peaks, path_name):
+    """Kernel-only GEMM time per shape, graph-replayed over rotating inputs
+    whose sets together exceed twice the L2."""
+    import ctypes
+    import torch
+    from q4_q8_int8_gb300 import synthetic
+    res = {}
+    for label, M, K, N in sweep_shapes():
+        path = path_code(mmq, path_name)
+        if path == mmq.MMQ_PATH_SMALL_M and M > mmq.SMALL_M_MAX:
+            continue
+        set_bytes = 0.5625 * N * K + 1.25 * M * K + 4 * M * N
+        R = min(64, max(2, int(np.ceil(2 * L2_BYTES / set_bytes)) + 1))
+        ws = [synthetic.torch_q4K_weights(N, K, 9100 + r, dev).view(-1) for r in range(R)]
+        aqs = [mmq.quantize_q8_1(synthetic.torch_activations(M, K, 9200 + r, dev, 0.01)) for r in range(R)]
+        Cs = [torch.empty((M, N), dtype=torch.float32, device=dev) for _ in range(R)]
+        structs = [mmq.q8_1_struct(*aq) for aq in aqs]
+
+        def call(i, stream):
+            r = i % R
+            rc = mmq.mmq_q4K_gemm_path(structs[r], ctypes.c_void_p(ws[r].data_ptr()),
+                                       ctypes.c_void_p(Cs[r].data_ptr()), M, N, K, path, mmq._stream_ptr(stream))
+            if rc:
+                raise mmq.MMQError(rc, "mmq_q4K_gemm_path")
+
+        reps = int(max(2 * R, min(400, 20e-3 / max(set_bytes / 6e12, 2e-6))))
+        ms = graph_time_ms(call, reps, dev)
+        if mmq.status() != 0:
+            raise RuntimeError(f"device status error in sweep {label}")
+        t_roof, bound = roofline_seconds(M, K, N, peaks)
+        macs = M * N * K
+        res[label] = {"M": M, "K": K, "N": N, "us": ms * 1e3, "tmacs": macs / (ms * 1e-3) / 1e12,
+                      "us_per_gmac": ms * 1e3 / (macs / 1e9),
+                      "gbs": set_bytes / (ms * 1e-3) / 1e9, "bound": bound,
+                      "t_roof_us": t_roof * 1e6, "roof_frac": t_roof / (ms * 1e-3),
+                      "kernels_per_call": mmq.mmq_q4K_gemm_launches(M, N, K, path),
+                      "rotating_sets": R, "reps": reps}
+        del ws, aqs, Cs, structs
+        torch.cuda.empty_cache()
+    return res
+
+
+def run_stack(mmq, dev, path_name, passes=2):
+    """The 7B prefill linear stack: 32 layers x {q, k, v, o 4096->4096; gate,
+    up 4096->11008; down 11008->4096} at 2048 tokens, every GEMM with its own
+    seeded q4_K weights (3.64 GB resident) and a q8_1 prepass of its own
+    activations (eight seeded sets per input width, used in turn)."""
+    import ctypes
+    import torch
+    from q4_q8_int8_gb300 import synthetic
+    T = synthetic.STACK_TOKENS
+    path = path_code(mmq, path_name)
+    weights = []
+    for layer in range(synthetic.STACK_LAYERS):
+        for g, (_, K, N) in enumerate(synthetic.STACK_GEMMS):
+            ws, _ = synthetic.stack_seeds(layer, g)
+            weights.append((K, N, synthetic.torch_q4K_weights(N, K, ws, dev).view(-1)))
+    xs = {K: [synthetic.torch_activations(T, K, 9300 + K + r, dev, 0.01) for r in range(8)] for K in (4096, 11008)}
+    q8 = {K: mmq.empty_q8_1(T, K, dev) for K in (4096, 11008)}
+    C = torch.empty((T, 11008), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sp = mmq._stream_ptr(stream)
+
+    def one_pass():
+        for i, (K, N, w) in enumerate(weights):
+            x = xs[K][i % 8]
+            aq = mmq.q8_1_struct(*q8[K])
+            rc = mmq.mmq_quantize_q8_1(ctypes.c_void_p(x.data_ptr()), T, K, aq, sp)
+            rc |= mmq.mmq_q4K_gemm_path(aq, ctypes.c_void_p(w.data_ptr()), ctypes.c_void_p(C.data_ptr()),
+                                        T, N, K, path, sp)
+            if rc:
+                raise RuntimeError(f"stack call failed: {rc}")
+
+    one_pass()
+    torch.cuda.synchronize(dev)
+    times = []
+    for _ in range(passes):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        one_pass()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        times.append(e0.elapsed_time(e1))
+    if mmq.status(stream) != 0:
+        raise RuntimeError("device status error in the stack")
+    ms = float(np.median(times))
+    macs = synthetic.STACK_LAYERS * sum(T * K * N for _, K, N in synthetic.STACK_GEMMS)
+    out = {"ms_per_pass": ms, "passes": passes, "equivalent_tokens_per_s": T / (ms * 1e-3),
+           "tmacs": macs / (ms * 1e-3) / 1e12, "gemms": len(weights),
+           "weights_gb": sum(w.numel() for _, _, w in weights) / 1e9,
+           "what": "32 layers x (q, k, v, o, gate, up, down) at 2048 tokens, a q8_1 prepass per GEMM, "
+                   "224 independent weight matrices resident"}
+    del weights, xs, q8, C
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_mine(args, rank, world, local_rank):
     import torch
     import q4_q8_int8_gb300 as mmq
@@ -353,15 +531,13 @@ def run_mine(args, rank, world, local_rank):
     mmq_build.build()
     mmq.load_library()
     mmq.mmq_set_programmatic_launch(0 if args.no_pdl else 1)
-    path = {"auto": mmq.MMQ_PATH_AUTO, "mma_s8": mmq.MMQ_PATH_MMA_S8, "tc": mmq.MMQ_PATH_TC,
-            "tc_pair": mmq.MMQ_PATH_TC_PAIR, "small_m": mmq.MMQ_PATH_SMALL_M,
-            "tc_small": mmq.MMQ_PATH_TC_SMALL}[args.path]
+    path = path_code(mmq, args.path)
 
     M, K, N = WORKLOADS[args.workload]
     # Inputs: R independent sets rotated step by step so that every step reads
     # its inputs from HBM (R sets together exceed twice the 129 MB L2).
     set_bytes = M * K * 4 + M * K * 1.25 + N * K * 0.5625 + M * N * 4
-    R = max(2, int(np.ceil(2 * 129e6 / set_bytes)) + 1)
+    R = max(2, int(np.ceil(2 * L2_BYTES / set_bytes)) + 1)
     xs, ws, aqs, Cs = [], [], [], []
     for r in range(R):
         xs.append(synthetic.torch_activations(M, K, 7000 + 97 * rank + r, dev, 0.01))
@@ -388,7 +564,7 @@ def run_mine(args, rank, world, local_rank):
         if rc:
             raise RuntimeError(f"MMQ call failed: {rc}")
 
-    # clocks are sampled from the start of warm-up to the end of the timed region
+    # clocks are sampled from the start of warm-up to the end of the soak below
     pci = None
     try:
         pr = torch.cuda.get_device_properties(dev)
@@ -430,12 +606,23 @@ def run_mine(args, rank, world, local_rank):
     for i in range(args.steps):
         step(args.warmup + args.steps + i, evs[i])
     torch.cuda.synchronize(dev)
+    step_ms = ev_t0.elapsed_time(ev_t1) / args.steps
+    # Soak: the same step loop for about --soak-seconds more, so that the
+    # clock record holds many samples taken under load (the timed region of
+    # a default run is only a few milliseconds).
+    soak_steps = int(args.soak_seconds / max(step_ms * 1e-3, 1e-6)) if clocks else 0
+    ts0 = time.perf_counter()
+    for i in range(soak_steps):
+        step(i)
+        if i % 256 == 255:
+            torch.cuda.synchronize(dev)
+    torch.cuda.synchronize(dev)
+    soak_s = time.perf_counter() - ts0
     clk = clocks.stop() if clocks else None
     rc = mmq.status(stream)
     if rc != 0:
         raise RuntimeError(f"device status {rc} after timed region")
 
-    step_ms = ev_t0.elapsed_time(ev_t1) / args.steps
     split_step_ms = evs[0][0].elapsed_time(evs[-1][2]) / args.steps
     q_ms = float(np.mean([e[0].elapsed_time(e[1]) for e in evs]))
     g_all = np.array([e[1].elapsed_time(e[2]) for e in evs])
@@ -519,52 +706,63 @@ def run_mine(args, rank, world, local_rank):
             "mmq_step_over_control": step_ms / (c_conv + c_deq + c_gemm),
             "gpu_launches": 3 * cn,
         }
+        del xh16, wh16
 
     if rank != 0:
         if world > 1:
             torch.distributed.destroy_process_group()
         return
 
+    peaks = measured_peaks()
+    sweep = None
+    stack = None
+    if not args.no_sweep or not args.no_stack:
+        del xs, ws, aqs, Cs, ws_t
+        torch.cuda.empty_cache()
+    if not args.no_sweep:
+        sweep = run_sweep(mmq, dev, peaks, args.path)
+    if not args.no_stack:
+        stack = run_stack(mmq, dev, args.path)
+
     macs = M * N * K
     value = whole_job_tmacs(macs, world, step_ms)
     gemm_tmacs = macs / (g_ms * 1e-3) / 1e12
-    peaks = measured_peaks()
     micro = microbench_peaks()
-    used_path = path
-    if used_path == mmq.MMQ_PATH_AUTO:
-        used_path = mmq.MMQ_PATH_SMALL_M if M <= mmq.SMALL_M_MAX else mmq.MMQ_PATH_TC
+    used_path = resolved_path(mmq, path, M)
     kname = {mmq.MMQ_PATH_MMA_S8: ("gemm_mma_s8", "gemm_mma.cu"),
              mmq.MMQ_PATH_TC: ("gemm_tc", "gemm_tc.cu"),
-             mmq.MMQ_PATH_TC_PAIR: ("gemm_tc2", "gemm_tc2.cu"),
-             mmq.MMQ_PATH_SMALL_M: ("gemm_small_m", "gemm_small.cu"),
-             mmq.MMQ_PATH_TC_SMALL: ("gemm_tc_small", "gemm_tc_small.cu")}[used_path]
+             mmq.MMQ_PATH_SMALL_M: ("gemm_small_m", "gemm_small.cu")}[used_path]
     src_hash = kernel_source_hash([kname[1], "sm103_ptx.cuh", "tc_common.cuh", "q8_round.cuh"])
     traffic = recorded_traffic(kname[0], src_hash)
     alg_bytes = 0.5625 * N * K + 1.25 * M * K + 4 * M * N
     sm_mhz = (clk or {}).get("sm_mhz") or micro["sm_max_mhz"]
+    timed_s = step_ms * 1e-3 * args.steps
+    burst = timed_s < SUSTAINED_AFTER_S
     if used_path == mmq.MMQ_PATH_SMALL_M:
         achieved = alg_bytes / (g_ms * 1e-3) / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
                 "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json hbm copy)"}
-    elif used_path in (mmq.MMQ_PATH_TC, mmq.MMQ_PATH_TC_PAIR, mmq.MMQ_PATH_TC_SMALL):
+    elif used_path == mmq.MMQ_PATH_TC:
         # The exact integer contraction runs on the tensor pipe as kind::f16
-        # MMAs (2 flops per MAC); the kernel is timed inside a long loop, so
-        # the denominator is the sustained measured bf16 (= f16 rate) peak.
+        # MMAs (2 flops per MAC).  A timed region of milliseconds is held to
+        # the burst bf16 (= f16 rate) peak; the sustained fraction is beside it.
         flops = 2.0 * macs
         achieved = flops / (g_ms * 1e-3) / 1e12
-        peak = peaks["bf16_tflops_sustained"] or peaks["bf16_tflops"]
+        sus = peaks["bf16_tflops_sustained"] or peaks["bf16_tflops"]
+        peak = peaks["bf16_tflops"] if burst else sus
         roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": achieved / peak, "traffic": traffic,
-                "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json bf16 sustained; "
-                               "f16 runs at the bf16 rate)",
-                "frac_of_burst": achieved / peaks["bf16_tflops"]}
+                "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json bf16 "
+                               f"{'burst' if burst else 'sustained'}; f16 runs at the bf16 rate; "
+                               f"timed region {timed_s * 1e3:.1f} ms)",
+                "frac_of_sustained": achieved / sus, "frac_of_burst": achieved / peaks["bf16_tflops"]}
     else:
         achieved = 2 * macs / (g_ms * 1e-3) / 1e12
         peak = micro["int8_mma_sync_tops"]
         roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TOP/s",
                 "frac": achieved / peak, "traffic": traffic,
-                "peak_source": "measured int8 mma.sync peak (profiles/peaks.json)"}
+                "peak_source": "measured int8 mma.sync peak (profiles/peaks.json, bench_peaks.cu)"}
     roof["kernel"] = kname[0]
     # One GEMM call may be two kernels (the tcgen05 kernel's split-K tail
     # launch); "per launch" figures here are per call, both kernels together.
@@ -576,16 +774,13 @@ def run_mine(args, rank, world, local_rank):
     # output and 32-k chunk the tcgen05 kernel does one FMA (2 flops), plus
     # per super-block one FMA for d and one add of the second term (0.5 flop
     # per chunk); the other kernels do the pages' 1 FMUL + 2 FFMA (5 flops).
-    alu_flops = (2.5 if used_path in (mmq.MMQ_PATH_TC, mmq.MMQ_PATH_TC_PAIR) else 5.0) * macs / 32
-    if used_path == mmq.MMQ_PATH_TC_SMALL:
-        alu_flops = 4.0 * macs / 32   # one FMA with da and one with dma * dmv per output and chunk
+    alu_flops = (2.5 if used_path == mmq.MMQ_PATH_TC else 5.0) * macs / 32
     alu_peak = micro["sms"] * 128 * 2 * sm_mhz * 1e6 / 1e12
     alu = {"flops_per_launch": alu_flops, "achieved_tflops": alu_flops / (g_ms * 1e-3) / 1e12,
            "peak_tflops": alu_peak, "frac": alu_flops / (g_ms * 1e-3) / 1e12 / alu_peak,
            "peak_source": f"derived: {micro['sms']} SMs x 128 FP32 lanes x 2 x {sm_mhz:.0f} MHz"}
     roof["algorithmic_bytes_per_launch"] = alg_bytes
     roof["algorithmic_macs_per_launch"] = macs
-    int8_frac = 2 * gemm_tmacs / micro["int8_mma_sync_tops"]
 
     cpu = None
     if not args.no_cpu_baseline:
@@ -600,8 +795,7 @@ def run_mine(args, rank, world, local_rank):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "int8xu4->f32 (fp16-exact ints on tensor cores)"
-        if used_path in (mmq.MMQ_PATH_TC, mmq.MMQ_PATH_TC_PAIR, mmq.MMQ_PATH_TC_SMALL)
-        else "s8xs8->s32, f32 rescale",
+        if used_path == mmq.MMQ_PATH_TC else "s8xs8->s32, f32 rescale",
         "data": "synthetic",
         "config": {"workload": f"{args.workload} M={M} K={K} N={N}", "global_batch_tokens": M * world,
                    "parallelism": f"independent problem per GPU x{world}",
@@ -610,10 +804,14 @@ def run_mine(args, rank, world, local_rank):
         "us_per_gmac": step_ms * 1e3 / (macs / 1e9),
         "gemm_only": {"tmacs": gemm_tmacs, "us_per_gmac": g_ms * 1e3 / (macs / 1e9), "ms": g_ms,
                       "ms_over_steps": g_dist,
-                      "frac_of_int8_peak": int8_frac,
-                      "int8_peak_source": "measured mma.sync s8 peak, profiles/peaks.json"},
+                      "x_int8_mma_sync_rate": 2 * gemm_tmacs / micro["int8_mma_sync_tops"],
+                      "int8_note": "a multiple of the measured legacy mma.sync s8 rate "
+                                   f"({micro['int8_mma_sync_tops']} TOP/s, bench_peaks.cu); sm_103a has "
+                                   "no tcgen05 integer MMA, and this kernel runs on the f16 tensor pipe, "
+                                   "so the roofline fraction is the one in 'roofline'"},
         "epilogue_alu": alu,
-        "prepass": {"ms": q_ms, "gbs": (M * K * 4 + M * K * 1.25) / (q_ms * 1e-3) / 1e9},
+        "prepass": {"ms": q_ms, "gbs": (M * K * 4 + M * K * 1.25) / (q_ms * 1e-3) / 1e9,
+                    "frac_of_hbm": (M * K * 4 + M * K * 1.25) / (q_ms * 1e-3) / 1e9 / peaks["hbm_gbs"]},
         "roofline": roof,
         "cpu_baseline": cpu,
         "e2e": {"value": whole_job_tmacs(macs, world, e2e_ms), "unit": UNIT,
@@ -622,19 +820,38 @@ def run_mine(args, rank, world, local_rank):
         "gpu_launches": args.steps * (1 + gemm_launches),
         "control": control,
         "clocks": clk,
-        "clocks_window": "from warm-up start to the end of the per-kernel split pass",
+        "clocks_window": f"from warm-up start through the timed region, the per-kernel split pass and "
+                         f"a {soak_s:.2f} s soak of {soak_steps} more steps of the same loop",
         "split_pass": {"ms_per_step": split_step_ms,
                        "what": "the same K steps again with an event before and after each kernel; "
                                "prepass, gemm_only and roofline come from this pass"},
         "wall_s_timed": wall,
+        "sweep": sweep,
+        "sweep_note": "kernel-only GEMM per configuration (outside the timed region), CUDA-graph replay over "
+                      "rotating inputs > 2x L2; roof_frac = t_roof / t with t_roof = max(algorithmic bytes / "
+                      "measured HBM, 2MNK / measured burst bf16)",
+        "stack": stack,
     }
     print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
 
 
+def measure_peaks():
+    """Compile bench_peaks.cu under _build/ and run it (prints one JSON line)."""
+    out_dir = os.path.join(ROOT, "_build")
+    os.makedirs(out_dir, exist_ok=True)
+    exe = os.path.join(out_dir, "bench_peaks")
+    nvcc = os.environ.get("NVCC", "nvcc")
+    subprocess.run([nvcc, "-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-o", exe,
+                    os.path.join(ROOT, "bench_peaks.cu")], check=True)
+    subprocess.run([exe], check=True)
+
+
 def main():
     args = parse()
+    if args.measure_peaks:
+        return measure_peaks()
     rank, world, local_rank = dist_env()
     if args.impl == "reference":
         run_reference(args, rank, world)

@@ -106,7 +106,10 @@ int mmq_pack_q4K(const uint8_t* v_host, const uint8_t* sc_host,
  * Picks the kernel for the shape (small-M weight-streaming kernel or the
  * large-M tensor-core kernel).  Results agree with the CPU reference within
  * |C - C_ref| <= 1e-4 * sum_k |a_k w_k| + 1e-6 and are bitwise
- * deterministic run to run. */
+ * deterministic run to run on one device and build.  The grouping of the
+ * f32 partial sums (K split, clusters) is chosen from the shape and the
+ * device's SM count and occupancy, so the last bits of C may differ between
+ * devices or builds; the tolerance is the contract across them. */
 int mmq_q4K_gemm(mmq_q8_1_t aq, const uint8_t* bq4k, float* C, int64_t M,
                  int64_t N, int64_t K, void* stream);
 
@@ -138,17 +141,16 @@ int mmq_q4K_gemm_host(const float* x_host, const uint8_t* bq4k, float* C_host,
                       int64_t M, int64_t N, int64_t K, void* workspace,
                       size_t workspace_bytes, void* stream);
 
-/* Kernel selection for mmq_q4K_gemm_path (testing and A/B timing). */
+/* Kernel selection for mmq_q4K_gemm_path (testing and A/B timing).  The
+ * values 4 and 5 are retired (two tensor-core variants that no shape ever
+ * selected) and are refused like any unknown value. */
 #define MMQ_PATH_AUTO 0
 #define MMQ_PATH_MMA_S8 1   /* warp-level mma.sync s8 x s8 -> s32 kernel    */
 #define MMQ_PATH_TC 2       /* tcgen05 kernel (exact integers in fp16, f32   */
                             /* accumulation in tensor memory)               */
-#define MMQ_PATH_SMALL_M 3  /* weight-streaming kernel for few tokens       */
-#define MMQ_PATH_TC_PAIR 4  /* tcgen05 kernel on CTA pairs (one M=256 MMA    */
-                            /* over two SMs; 256 x 128 output tiles)        */
-#define MMQ_PATH_TC_SMALL 5 /* tcgen05 kernel for few tokens: 128 weight     */
-                            /* rows on the MMA's M side, 16/32/64 tokens on */
-                            /* its N side; accepts any M (token tiles of 64) */
+#define MMQ_PATH_SMALL_M 3  /* weight-streaming kernels for few tokens:     */
+                            /* dp4a dot products for M <= 4, mma.sync f16   */
+                            /* with cluster split-K for 4 < M <= 64         */
 
 /* Number of kernels mmq_q4K_gemm_path(…, path, …) enqueues for this shape
  * on the current device: 1, or 2 when the tcgen05 kernel splits off its
@@ -203,11 +205,22 @@ int mmq_interleave_rows_q4K(const uint8_t* gate, const uint8_t* up, uint8_t* out
 
 /* Debug/test dump of the exact per-chunk integer dots (page r15 section 2.1:
  * S_ij = sum_k a_int[i,k] * v[j,k]; section 2.3: |S| <= 32*127*15) computed
- * by the same unpack and MMA code as the GEMM kernel selected by `path`
- * (MMQ_PATH_MMA_S8, MMQ_PATH_TC or MMQ_PATH_TC_PAIR).  S int32 [M][N][K/32].  Same shape
- * rules as the GEMM. */
+ * by the same unpack and MMA (or dp4a) code as the GEMM kernel selected by
+ * `path`: MMQ_PATH_MMA_S8, MMQ_PATH_TC, MMQ_PATH_SMALL_M (M <= 64: the
+ * dot-product kernel for M <= 4, the mma.sync kernel above) or
+ * MMQ_PATH_AUTO (the kernel mmq_q4K_gemm picks for M).  S int32
+ * [M][N][K/32].  Same shape rules as the GEMM. */
 int mmq_q4K_block_dots(mmq_q8_1_t aq, const uint8_t* bq4k, int32_t* S,
                        int64_t M, int64_t N, int64_t K, int path, void* stream);
+
+/* The tcgen05 kernel (MMQ_PATH_TC) folds the 6-bit sub-block scale into its
+ * weight operand, so its tensor cores form S'_ijc = sc_jc * S_ijc exactly
+ * (|S'| <= 32*127*63*15 < 2^22; page r15 section 2.1 for S and sc).  This
+ * dump returns S' int32 [M][N][K/32] from that kernel run on its product
+ * operand, unchanged except that the epilogue writes S' instead of
+ * rescaling it.  Shape rules as the GEMM. */
+int mmq_q4K_scaled_block_dots(mmq_q8_1_t aq, const uint8_t* bq4k, int32_t* S,
+                              int64_t M, int64_t N, int64_t K, void* stream);
 
 /* ---- The dequantize-then-dense control path (the f16 GEMM path the pages
  * measure MMQ against: page r12, the landing note comparing MMQ with the f16
@@ -326,6 +339,15 @@ const char* mmq_strerror(int code);
  * While enabled, a GEMM's weights must not be written by the kernel
  * launched just before it on the same stream. */
 void mmq_set_programmatic_launch(int enable);
+
+/* Test hook: force the K split of the dot-product kernel (M <= 4) for
+ * later calls on this host thread: ks = 1, 2 or 4 warps per row group
+ * (the SwiGLU epilogue takes 1 or 2; a forced 4 makes its calls fail with
+ * MMQ_ERR_CUDA), 0 restores the automatic choice.  Returns MMQ_ERR_ARG for
+ * any other value.  The split changes how the row's partial sums are
+ * grouped, so f32 results may differ in the last bits between splits; the
+ * integer dots and the tolerance do not. */
+int mmq_debug_force_gemv_split(int ks);
 
 /* Test hook: when nonzero, the next tensor-core GEMM launch on this host
  * thread withholds one producer arrival so that its consumers' bounded

@@ -17,7 +17,7 @@
  *  [r16]  "21 . r16 -- Narrow kernel gets the rank-1 fold", section 2.1
  *          (the fold dma = da*sa; a re-association only).
  *
- * Readings where the pages are silent (each also listed in the design doc):
+ * Readings where the pages are silent:
  *  - q8_1 scale da is f32 (the pages store f16); da = amax/127 with IEEE
  *    round-to-nearest division; q = clamp(roundf(x/da), -127, 127) with
  *    roundf = round half away from zero; when da == 0 every q is 0 and sa = 0.

@@ -28,22 +28,21 @@ MMQ_PATH_AUTO = 0
 MMQ_PATH_MMA_S8 = 1
 MMQ_PATH_TC = 2
 MMQ_PATH_SMALL_M = 3
-MMQ_PATH_TC_PAIR = 4
-MMQ_PATH_TC_SMALL = 5
 SMALL_M_MAX = 64
 MMQ_GGUF_F32, MMQ_GGUF_F16, MMQ_GGUF_Q4_K, MMQ_GGUF_Q6_K = 0, 1, 12, 14
 
 # Every symbol include/mmq.h declares.
 EXPORTS = (
     "mmq_q8_1_bytes", "mmq_q8_1_view", "mmq_quantize_q8_1", "mmq_q4K_bytes",
-    "mmq_pack_q4K", "mmq_q4K_gemm", "mmq_q4K_gemm_host_workspace", "mmq_q4K_gemm_host", "mmq_q4K_gemm_launches", "mmq_q4K_gemm_path", "mmq_q4K_gemm_q8_1", "mmq_q4K_block_dots",
+    "mmq_pack_q4K", "mmq_q4K_gemm", "mmq_q4K_gemm_host_workspace", "mmq_q4K_gemm_host", "mmq_q4K_gemm_launches", "mmq_q4K_gemm_path", "mmq_q4K_gemm_q8_1", "mmq_q4K_block_dots", "mmq_q4K_scaled_block_dots",
     "mmq_dequantize_q4K_f16", "mmq_convert_f32_f16", "mmq_gemm_f16",
     "mmq_q4K_gemm_swiglu_q8_1", "mmq_interleave_rows_q4K",
     "mmq_q6K_bytes", "mmq_pack_q6K", "mmq_q6K_dev_bytes", "mmq_repack_q6K", "mmq_q6K_gemm",
     "mmq_q6K_block_dots",
     "mmq_gguf_open", "mmq_gguf_close", "mmq_gguf_tensor_count", "mmq_gguf_find", "mmq_gguf_tensor_info",
     "mmq_gguf_read", "mmq_gguf_write",
-    "mmq_status", "mmq_strerror", "mmq_debug_inject_timeout", "mmq_set_programmatic_launch",
+    "mmq_status", "mmq_strerror", "mmq_debug_inject_timeout", "mmq_debug_force_gemv_split",
+    "mmq_set_programmatic_launch",
 )
 
 
@@ -84,6 +83,7 @@ def load_library(path: str = LIB_PATH):
                 "mmq_q4K_gemm_path": ([Q, P, P, I, I, I, ctypes.c_int, P], ctypes.c_int),
                 "mmq_q4K_gemm_q8_1": ([Q, P, P, Q, I, I, I, P], ctypes.c_int),
                 "mmq_q4K_block_dots": ([Q, P, P, I, I, I, ctypes.c_int, P], ctypes.c_int),
+                "mmq_q4K_scaled_block_dots": ([Q, P, P, I, I, I, P], ctypes.c_int),
                 "mmq_dequantize_q4K_f16": ([P, P, I, I, P], ctypes.c_int),
                 "mmq_convert_f32_f16": ([P, P, I, P], ctypes.c_int),
                 "mmq_gemm_f16": ([P, P, P, I, I, I, P], ctypes.c_int),
@@ -109,6 +109,7 @@ def load_library(path: str = LIB_PATH):
                 "mmq_status": ([P], ctypes.c_int),
                 "mmq_strerror": ([ctypes.c_int], ctypes.c_char_p),
                 "mmq_debug_inject_timeout": ([ctypes.c_int], None),
+                "mmq_debug_force_gemv_split": ([ctypes.c_int], ctypes.c_int),
                 "mmq_set_programmatic_launch": ([ctypes.c_int], None),
             }
             for name, (args, res) in sigs.items():
@@ -168,6 +169,10 @@ def mmq_q4K_block_dots(aq, bq4k, S, M, N, K, path, stream):
     return load_library().mmq_q4K_block_dots(aq, bq4k, S, M, N, K, path, stream)
 
 
+def mmq_q4K_scaled_block_dots(aq, bq4k, S, M, N, K, stream):
+    return load_library().mmq_q4K_scaled_block_dots(aq, bq4k, S, M, N, K, stream)
+
+
 def mmq_status(stream):
     return load_library().mmq_status(stream)
 
@@ -178,6 +183,10 @@ def mmq_strerror(code):
 
 def mmq_debug_inject_timeout(enable):
     load_library().mmq_debug_inject_timeout(1 if enable else 0)
+
+
+def mmq_debug_force_gemv_split(ks):
+    return load_library().mmq_debug_force_gemv_split(ks)
 
 
 def mmq_set_programmatic_launch(enable):
@@ -273,8 +282,8 @@ def q4K_gemm_q8_1(aq, w, N: int, with_c: bool = True, out=None, stream=None):
     return C, o
 
 
-def q4K_block_dots(aq, w, N: int, path: int = MMQ_PATH_MMA_S8, out=None, stream=None):
-    """Exact per-chunk int32 dots S [M][N][K/32] from the selected kernel's MMA path."""
+def q4K_block_dots(aq, w, N: int, path: int = MMQ_PATH_AUTO, out=None, stream=None):
+    """Exact per-chunk int32 dots S [M][N][K/32] from the selected kernel's dot-product code."""
     import torch
     qs, da, sa = aq
     M, K = qs.shape
@@ -283,6 +292,23 @@ def q4K_block_dots(aq, w, N: int, path: int = MMQ_PATH_MMA_S8, out=None, stream=
                               ctypes.c_void_p(S.data_ptr()), M, N, K, path, _stream_ptr(stream)),
            "mmq_q4K_block_dots")
     return S
+
+
+def q4K_scaled_block_dots(aq, w, N: int, out=None, stream=None):
+    """sc * S int32 [M][N][K/32] from the tcgen05 kernel's own weight operand."""
+    import torch
+    qs, da, sa = aq
+    M, K = qs.shape
+    S = out if out is not None else torch.empty((M, N, K // 32), dtype=torch.int32, device=qs.device)
+    _check(mmq_q4K_scaled_block_dots(q8_1_struct(qs, da, sa), ctypes.c_void_p(w.data_ptr()),
+                                     ctypes.c_void_p(S.data_ptr()), M, N, K, _stream_ptr(stream)),
+           "mmq_q4K_scaled_block_dots")
+    return S
+
+
+def force_gemv_split(ks: int):
+    """Test hook: force the dot-product kernel's K split (1, 2, 4; 0 = automatic)."""
+    _check(mmq_debug_force_gemv_split(ks), "mmq_debug_force_gemv_split")
 
 
 def mmq_dequantize_q4K_f16(bq4k, wh, N, K, stream):

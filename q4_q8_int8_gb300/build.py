@@ -37,7 +37,8 @@ def sources():
 
 def _digest():
     h = hashlib.sha256()
-    for p in sources() + [os.path.join(CSRC, f) for f in sorted(os.listdir(CSRC)) if f.endswith(".h")]:
+    headers = [os.path.join(CSRC, f) for f in sorted(os.listdir(CSRC)) if f.endswith((".h", ".cuh"))]
+    for p in sources() + headers:
         h.update(p.encode())
         with open(p, "rb") as f:
             h.update(f.read())

@@ -128,19 +128,22 @@ size_t mmq_q4K_bytes(int64_t N, int64_t K) {
 }
 
 // The automatic kernel choice (shape only): few tokens -> weight streaming,
-// else the one-CTA tcgen05 kernel. (The CTA-pair kernel is measured slower
-// on every shape tried so far and is only taken on request.)
-static int auto_path(int64_t M, int64_t N, bool dump) {
+// else the tcgen05 kernel.
+static int auto_path(int64_t M, int64_t N) {
     (void)N;
-    return (M <= mmq::kSmallMMax && !dump) ? MMQ_PATH_SMALL_M : MMQ_PATH_TC;
+    return M <= mmq::kSmallMMax ? MMQ_PATH_SMALL_M : MMQ_PATH_TC;
+}
+
+static bool known_path(int path) {
+    return path == MMQ_PATH_AUTO || path == MMQ_PATH_MMA_S8 || path == MMQ_PATH_TC || path == MMQ_PATH_SMALL_M;
 }
 
 static int run_gemm(mmq_q8_1_t aq, const uint8_t* w, float* C, int32_t* S, int64_t M,
                     int64_t N, int64_t K, int path, cudaStream_t s,
-                    mmq_q8_1_t q8out = mmq_q8_1_t{nullptr, nullptr, nullptr}) {
+                    mmq_q8_1_t q8out = mmq_q8_1_t{nullptr, nullptr, nullptr}, bool dump_scaled = false) {
     int* status = mmq::status_word_ptr();
     if (!status) return MMQ_ERR_CUDA;
-    if (path == MMQ_PATH_AUTO) path = auto_path(M, N, S != nullptr);
+    if (path == MMQ_PATH_AUTO) path = auto_path(M, N);
     switch (path) {
         case MMQ_PATH_MMA_S8:
             return from_cuda(mmq::launch_gemm_mma_s8(aq, w, C, S, M, N, K, status, s));
@@ -149,24 +152,15 @@ static int run_gemm(mmq_q8_1_t aq, const uint8_t* w, float* C, int32_t* S, int64
             if (rc) return rc;
             const int inject = t_inject_timeout;
             t_inject_timeout = 0;
-            return from_cuda(mmq::launch_gemm_tc(aq, w, C, q8out, S, M, N, K, status, inject, s));
-        }
-        case MMQ_PATH_TC_PAIR: {
-            int rc = mmq::tc2_gemm_check_resources();
-            if (rc) return rc;
-            const int inject = t_inject_timeout;
-            t_inject_timeout = 0;
-            return from_cuda(mmq::launch_gemm_tc2(aq, w, C, S, M, N, K, status, inject, s));
+            return from_cuda(mmq::launch_gemm_tc(aq, w, C, q8out, S, M, N, K, status, inject, s, false,
+                                                 dump_scaled));
         }
         case MMQ_PATH_SMALL_M:
-            if (S || M > mmq::kSmallMMax) return MMQ_ERR_ARG;
+            if (M > mmq::kSmallMMax) return MMQ_ERR_ARG;
+            if (S)
+                return from_cuda(mmq::launch_gemm_small_m(aq, w, nullptr, M, N, K, status, s,
+                                                          mmq_q8_1_t{nullptr, nullptr, nullptr}, mmq::kSmallDump, S));
             return from_cuda(mmq::launch_gemm_small_m(aq, w, C, M, N, K, status, s));
-        case MMQ_PATH_TC_SMALL: {
-            if (S) return MMQ_ERR_ARG;
-            const int inject = t_inject_timeout;
-            t_inject_timeout = 0;
-            return from_cuda(mmq::launch_gemm_tc_small(aq, w, C, M, N, K, status, inject, s));
-        }
         default:
             return MMQ_ERR_ARG;
     }
@@ -200,14 +194,14 @@ int mmq_q4K_gemm_host(const float* x_host, const uint8_t* bq4k, float* C_host, i
 }
 
 int mmq_q4K_gemm_launches(int64_t M, int64_t N, int64_t K, int path) {
-    if (path < MMQ_PATH_AUTO || path > MMQ_PATH_TC_SMALL) return MMQ_ERR_ARG;
+    if (!known_path(path)) return MMQ_ERR_ARG;
     if (M < 1 || N < 1 || K < 256 || (K % 256) != 0 || (N % 4) != 0) return MMQ_ERR_ARG;
     if (M > (int64_t(1) << 31) - 1 || N > (int64_t(1) << 31) - 1 || K > (int64_t(1) << 31) - 1)
         return MMQ_ERR_ARG;
     if (path == MMQ_PATH_SMALL_M && M > mmq::kSmallMMax) return MMQ_ERR_ARG;
     int rc = check_device();
     if (rc) return rc;
-    if (path == MMQ_PATH_AUTO) path = auto_path(M, N, false);
+    if (path == MMQ_PATH_AUTO) path = auto_path(M, N);
     if (path != MMQ_PATH_TC) return 1;
     const int n = mmq::tc_gemm_launch_count(M, N, K);
     return n < 0 ? MMQ_ERR_CUDA : n;
@@ -215,7 +209,7 @@ int mmq_q4K_gemm_launches(int64_t M, int64_t N, int64_t K, int path) {
 
 int mmq_q4K_gemm_path(mmq_q8_1_t aq, const uint8_t* bq4k, float* C, int64_t M, int64_t N,
                       int64_t K, int path, void* stream) {
-    if (path < MMQ_PATH_AUTO || path > MMQ_PATH_TC_SMALL) return MMQ_ERR_ARG;
+    if (!known_path(path)) return MMQ_ERR_ARG;
     if (path == MMQ_PATH_SMALL_M && M > mmq::kSmallMMax) return MMQ_ERR_ARG;
     int rc = check_gemm_args(aq, bq4k, C, M, N, K);
     if (rc) return rc;
@@ -278,10 +272,19 @@ int mmq_interleave_rows_q4K(const uint8_t* gate, const uint8_t* up, uint8_t* out
 
 int mmq_q4K_block_dots(mmq_q8_1_t aq, const uint8_t* bq4k, int32_t* S, int64_t M, int64_t N,
                        int64_t K, int path, void* stream) {
-    if (path != MMQ_PATH_MMA_S8 && path != MMQ_PATH_TC && path != MMQ_PATH_TC_PAIR) return MMQ_ERR_ARG;
+    if (!known_path(path)) return MMQ_ERR_ARG;
+    if (path == MMQ_PATH_SMALL_M && M > mmq::kSmallMMax) return MMQ_ERR_ARG;
     int rc = check_gemm_args(aq, bq4k, S, M, N, K);
     if (rc) return rc;
     return run_gemm(aq, bq4k, nullptr, S, M, N, K, path, static_cast<cudaStream_t>(stream));
+}
+
+int mmq_q4K_scaled_block_dots(mmq_q8_1_t aq, const uint8_t* bq4k, int32_t* S, int64_t M, int64_t N,
+                              int64_t K, void* stream) {
+    int rc = check_gemm_args(aq, bq4k, S, M, N, K);
+    if (rc) return rc;
+    return run_gemm(aq, bq4k, nullptr, S, M, N, K, MMQ_PATH_TC, static_cast<cudaStream_t>(stream),
+                    mmq_q8_1_t{nullptr, nullptr, nullptr}, true);
 }
 
 int mmq_dequantize_q4K_f16(const uint8_t* bq4k, uint16_t* wh, int64_t N, int64_t K, void* stream) {
@@ -377,6 +380,8 @@ const char* mmq_strerror(int code) {
 }
 
 void mmq_debug_inject_timeout(int enable) { t_inject_timeout = enable ? 1 : 0; }
+
+int mmq_debug_force_gemv_split(int ks) { return mmq::set_force_gemv_split(ks); }
 
 void mmq_set_programmatic_launch(int enable) { g_programmatic_launch.store(enable ? 1 : 0); }
 

@@ -175,16 +175,19 @@ __device__ __forceinline__ uint32_t quantize_group8(float4 v, float& d, int& sum
 //          bits of a prepass over C); C may be null;
 //  kSwiGLU gate and up rows interleaved (row 2f = gate f, 2f + 1 = up f):
 //          h = silu(g) * u = g / (1 + exp(-g)) * u in f32, quantized to q8_1
-//          ([M][N/2]); C, if not null, receives h as f32 [M][N/2].
-constexpr int kF32 = 0, kQ8 = 1, kSwiGLU = 2;
+//          ([M][N/2]); C, if not null, receives h as f32 [M][N/2];
+//  kDump   no rescale: the exact per-chunk dots S go to S int32 [M][N][K/32]
+//          straight from the same unpack and dot-product code.
+constexpr int kF32 = 0, kQ8 = 1, kSwiGLU = 2, kDump = 3;
+__host__ __device__ constexpr bool quant_out(int mode) { return mode == kQ8 || mode == kSwiGLU; }
 
 // kOut != kF32: rank 0's first group stages the CTA's finished [tokens][64
 // rows] tile in shared memory and quantizes it: two q8_1 blocks of 32 output
 // columns per token (kQ8), or one block of 32 SwiGLU features (kSwiGLU).
 template <int NF, int G, int D, int kOut>
 __global__ void __launch_bounds__(G * 128)
-gemm_small_kernel(const __grid_constant__ SmallMaps maps, float* __restrict__ C, mmq_q8_1_t out, int M, int N,
-                  int K, int split, int* status) {
+gemm_small_kernel(const __grid_constant__ SmallMaps maps, float* __restrict__ C, mmq_q8_1_t out,
+                  int32_t* __restrict__ S, int M, int N, int K, int split, int* status) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~uintptr_t(1023));
@@ -340,10 +343,25 @@ gemm_small_kernel(const __grid_constant__ SmallMaps maps, float* __restrict__ C,
                     hmma(sc4, a[0][0], a[0][1], a[0][2], a[0][3], fr.x, fr.y);
                     hmma(sc4, a[1][0], a[1][1], a[1][2], a[1][3], fr.z, fr.w);
                     // C fragment: (row g, tokens 8f + 2j, +1) and (row g + 8, same tokens)
-                    const uint64_t da2 = pack2(ts.x, ts.y), dma2 = pack2(ts.z, ts.w);
-                    const uint64_t s01 = pack2(sc4[0], sc4[1]), s23 = pack2(sc4[2], sc4[3]);
-                    acc[f][0] = ffma2(dma2, dmv0, ffma2(fmul2(da2, dsv0), s01, acc[f][0]));
-                    acc[f][1] = ffma2(dma2, dmv1, ffma2(fmul2(da2, dsv1), s23, acc[f][1]));
+                    if constexpr (kOut == kDump) {
+                        // the fragment holds S * 2^-24 exactly (|S| < 2^16)
+                        const int64_t kb = int64_t(sb_begin + i) * 8 + c, nb = K / 32;
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            const int row = n0 + r0 + 8 * h;
+#pragma unroll
+                            for (int e = 0; e < 2; ++e) {
+                                const int t = 8 * f + 2 * j + e;
+                                if (row < N && t < M)
+                                    S[(int64_t(t) * N + row) * nb + kb] = int32_t(sc4[2 * h + e] * kDsvScale);
+                            }
+                        }
+                    } else {
+                        const uint64_t da2 = pack2(ts.x, ts.y), dma2 = pack2(ts.z, ts.w);
+                        const uint64_t s01 = pack2(sc4[0], sc4[1]), s23 = pack2(sc4[2], sc4[3]);
+                        acc[f][0] = ffma2(dma2, dmv0, ffma2(fmul2(da2, dsv0), s01, acc[f][0]));
+                        acc[f][1] = ffma2(dma2, dmv1, ffma2(fmul2(da2, dsv1), s23, acc[f][1]));
+                    }
                 }
             }
         }
@@ -362,6 +380,7 @@ gemm_small_kernel(const __grid_constant__ SmallMaps maps, float* __restrict__ C,
                 wait_drain(stage_bar(q), uint32_t((last_issued[q] / D) & 1), status);
     }
     __syncthreads();
+    if constexpr (kOut == kDump) return;   // S is written; nothing to add up
 
     // ---- add the groups' partials (super-blocks were dealt round-robin)
     float4* part = reinterpret_cast<float4*>(smem + L.stages_off);   // [G][128][NF]
@@ -412,7 +431,7 @@ gemm_small_kernel(const __grid_constant__ SmallMaps maps, float* __restrict__ C,
                 }
             }
         }
-        if constexpr (kOut != kF32) {
+        if constexpr (quant_out(kOut)) {
             // the tile [8 NF tokens][64 rows] after the groups' partials (stage memory is idle)
             float* tile = reinterpret_cast<float*>(smem + L.stages_off + G * 128 * NF * 16);
 #pragma unroll
@@ -498,18 +517,18 @@ __device__ __forceinline__ void st_dsmem_f32(uint32_t addr, float v) {
 template <int MT, int R, int KS, int kOut>
 __global__ void __launch_bounds__(128)
 gemv_dp4a_kernel(mmq_q8_1_t aq, const uint8_t* __restrict__ w, float* __restrict__ C, mmq_q8_1_t out,
-                 int M, int N, int K) {
+                 int32_t* __restrict__ S, int M, int N, int K) {
     constexpr int kGroups = 4 / KS;                        // row groups (of R rows) per CTA
     constexpr int kBlockRows = kOut == kSwiGLU ? 64 : 32;  // rows behind one q8_1 output block
     constexpr int kCluster = kBlockRows / (kGroups * R);   // CTAs per output block
-    __shared__ __align__(16) float red[kOut != kF32 ? MT : 1][kBlockRows];   // rank 0: the cluster's rows [t][row]
+    __shared__ __align__(16) float red[quant_out(kOut) ? MT : 1][kBlockRows];   // rank 0: the cluster's rows [t][row]
     __shared__ float part[KS > 1 ? 4 : 1][MT][R];          // KS > 1: each warp's partial sums
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int slice = warp % KS, grp = warp / KS;
     const int row0 = (blockIdx.x * kGroups + grp) * R;   // this warp's rows row0 .. row0 + R - 1
     griddep_launch_dependents();
-    if (KS == 1 && kOut == kF32 && row0 >= N) return;   // (with q8_1 output every row exists)
-    if (kOut != kF32) asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");   // this CTA has started
+    if (KS == 1 && !quant_out(kOut) && row0 >= N) return;   // (with q8_1 output every row exists)
+    if (quant_out(kOut)) asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");   // this CTA has started
     const int nsb = K / 256, npairs = K / 64, nb = K / 32;
     float acc[MT][R];
 #pragma unroll
@@ -578,6 +597,14 @@ gemv_dp4a_kernel(mmq_q8_1_t aq, const uint8_t* __restrict__ w, float* __restrict
                         s0 = dp4a_us(wv[e] & 0x0F0F0F0Fu, av[e], s0);
                         s1 = dp4a_us((wv[e] >> 4) & 0x0F0F0F0Fu, bv[e], s1);
                     }
+                    if constexpr (kOut == kDump) {   // the exact dots of chunks 2pr, 2pr + 1
+                        if (row0 + r < N) {
+                            int32_t* sp = S + (int64_t(t) * N + row0 + r) * nb + 2 * pr;
+                            sp[0] = s0;
+                            sp[1] = s1;
+                        }
+                        continue;
+                    }
                     float a = acc[t][r];
                     a = fmaf(da.x * dsv[r][0], float(s0), a);
                     a = fmaf(da.x * float(sa.x), dmv[r][0], a);   // rank-1 fold: dma = da*sa
@@ -588,6 +615,7 @@ gemv_dp4a_kernel(mmq_q8_1_t aq, const uint8_t* __restrict__ w, float* __restrict
             }
         }
     }
+    if constexpr (kOut == kDump) return;   // S is written; nothing to add up
 #pragma unroll
     for (int t = 0; t < MT; ++t) {
 #pragma unroll
@@ -625,7 +653,7 @@ gemv_dp4a_kernel(mmq_q8_1_t aq, const uint8_t* __restrict__ w, float* __restrict
             for (int r = 0; r < R; ++r)
                 if (t < M && row0 + r < N) C[int64_t(t) * N + row0 + r] = acc[t][r];
     }
-    if constexpr (kOut != kF32) {
+    if constexpr (quant_out(kOut)) {
         const uint32_t rank = cluster_ctarank();
         asm volatile("barrier.cluster.wait.aligned;" ::: "memory");   // every CTA of the cluster has started
         if (slice == 0 && lane == 0) {
@@ -678,44 +706,55 @@ gemv_dp4a_kernel(mmq_q8_1_t aq, const uint8_t* __restrict__ w, float* __restrict
 constexpr int kGemvRows = 4;
 
 template <int MT, int KS, int kOut>
-cudaError_t launch_gemv_ks(mmq_q8_1_t aq, const uint8_t* w, float* C, mmq_q8_1_t out, int64_t M, int64_t N,
-                           int64_t K, cudaStream_t s) {
+cudaError_t launch_gemv_ks(mmq_q8_1_t aq, const uint8_t* w, float* C, mmq_q8_1_t out, int32_t* S, int64_t M,
+                           int64_t N, int64_t K, cudaStream_t s) {
     constexpr int R = kGemvRows, rows = 4 / KS * R;   // rows per CTA
     constexpr int cluster = (kOut == kSwiGLU ? 64 : 32) / rows;
-    static_assert(kOut == kF32 || (cluster >= 1 && cluster <= 8), "portable cluster size");
+    static_assert(!quant_out(kOut) || (cluster >= 1 && cluster <= 8), "portable cluster size");
     cudaLaunchAttribute attr[2];
     const unsigned grid = unsigned((N + rows - 1) / rows);
     cudaLaunchConfig_t cfg = mmq::launch_config(dim3(grid), dim3(128), 0, s, attr);
-    if (kOut != kF32) {   // grid = N / rows is a multiple of the cluster (N % 32 or N % 64 == 0)
+    if (quant_out(kOut)) {   // grid = N / rows is a multiple of the cluster (N % 32 or N % 64 == 0)
         attr[cfg.numAttrs].id = cudaLaunchAttributeClusterDimension;
         attr[cfg.numAttrs].val.clusterDim.x = cluster;
         attr[cfg.numAttrs].val.clusterDim.y = 1;
         attr[cfg.numAttrs].val.clusterDim.z = 1;
         ++cfg.numAttrs;
     }
-    return cudaLaunchKernelEx(&cfg, gemv_dp4a_kernel<MT, R, KS, kOut>, aq, w, C, out, int(M), int(N), int(K));
+    return cudaLaunchKernelEx(&cfg, gemv_dp4a_kernel<MT, R, KS, kOut>, aq, w, C, out, S, int(M), int(N), int(K));
 }
 
-// CTAs of one kernel instance that fit on the GPU at once (register-bound),
-// found once per instance.
+// CTAs of one kernel instance that fit on a device at once (register-bound),
+// found once per instance and device.
+constexpr int kMaxDevices = 64;
 template <int MT, int KS, int kOut>
 int64_t gemv_resident_ctas() {
-    static std::atomic<int64_t> cached{0};
-    int64_t v = cached.load(std::memory_order_relaxed);
+    static std::atomic<int64_t> cached[kMaxDevices];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        cudaGetLastError();
+        dev = -1;
+    }
+    int64_t v = dev >= 0 ? cached[dev].load(std::memory_order_relaxed) : 0;
     if (v == 0) {
-        int dev = 0, nsm = 0, per_sm = 0;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
+        int nsm = 0, per_sm = 0;
+        if (dev < 0 || cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+            cudaGetLastError();
+            nsm = 1;
+        }
         if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gemv_dp4a_kernel<MT, kGemvRows, KS, kOut>, 128,
                                                           0) != cudaSuccess || per_sm < 1) {
             cudaGetLastError();
             per_sm = 1;
         }
         v = int64_t(per_sm) * (nsm > 0 ? nsm : 1);
-        cached.store(v, std::memory_order_relaxed);
+        if (dev >= 0) cached[dev].store(v, std::memory_order_relaxed);
     }
     return v;
 }
+
+// Test hook: a K split forced for this host thread (0: the cost model's).
+thread_local int t_force_ks = 0;
 
 // The K split (KS warps per row group) with the lowest modelled cost:
 // waves of CTAs x (dependent load rounds per warp + 1/2), the half standing
@@ -726,26 +765,31 @@ int64_t gemv_resident_ctas() {
 // of 1, 2 and 4 every time.  The SwiGLU epilogue takes KS <= 2 (its 64-row
 // blocks would otherwise need clusters of 16).
 template <int MT, int kOut>
-cudaError_t launch_gemv(mmq_q8_1_t aq, const uint8_t* w, float* C, mmq_q8_1_t out, int64_t M, int64_t N, int64_t K,
-                        cudaStream_t s) {
-    const int64_t npairs = K / 64;
-    auto cost2 = [&](int ks, int64_t resident) {   // twice the modelled cost
-        const int64_t rows = 16 / ks;                 // (4 / ks) row groups x kGemvRows rows per CTA
-        const int64_t ctas = (N + rows - 1) / rows;
-        const int64_t waves = (ctas + resident - 1) / resident;
-        const int64_t rounds = (npairs + 32 * ks - 1) / (32 * ks);
-        return waves * (2 * rounds + 1);
-    };
-    static_assert(kGemvRows == 4, "the cost model counts 4 rows per warp");
-    const int64_t c1 = cost2(1, gemv_resident_ctas<MT, 1, kOut>());
-    const int64_t c2 = cost2(2, gemv_resident_ctas<MT, 2, kOut>());
-    int64_t c4 = INT64_MAX;
-    if constexpr (kOut != kSwiGLU) c4 = cost2(4, gemv_resident_ctas<MT, 4, kOut>());
-    if (c1 <= c2 && c1 <= c4) return launch_gemv_ks<MT, 1, kOut>(aq, w, C, out, M, N, K, s);
-    if constexpr (kOut != kSwiGLU) {
-        if (c4 < c2) return launch_gemv_ks<MT, 4, kOut>(aq, w, C, out, M, N, K, s);
+cudaError_t launch_gemv(mmq_q8_1_t aq, const uint8_t* w, float* C, mmq_q8_1_t out, int32_t* S, int64_t M,
+                        int64_t N, int64_t K, cudaStream_t s) {
+    int ks = t_force_ks;
+    if (ks == 0) {
+        const int64_t npairs = K / 64;
+        auto cost2 = [&](int k, int64_t resident) {   // twice the modelled cost
+            const int64_t rows = 16 / k;                 // (4 / k) row groups x kGemvRows rows per CTA
+            const int64_t ctas = (N + rows - 1) / rows;
+            const int64_t waves = (ctas + resident - 1) / resident;
+            const int64_t rounds = (npairs + 32 * k - 1) / (32 * k);
+            return waves * (2 * rounds + 1);
+        };
+        static_assert(kGemvRows == 4, "the cost model counts 4 rows per warp");
+        const int64_t c1 = cost2(1, gemv_resident_ctas<MT, 1, kOut>());
+        const int64_t c2 = cost2(2, gemv_resident_ctas<MT, 2, kOut>());
+        int64_t c4 = INT64_MAX;
+        if constexpr (kOut != kSwiGLU) c4 = cost2(4, gemv_resident_ctas<MT, 4, kOut>());
+        ks = (c1 <= c2 && c1 <= c4) ? 1 : (c4 < c2 ? 4 : 2);
     }
-    return launch_gemv_ks<MT, 2, kOut>(aq, w, C, out, M, N, K, s);
+    if (ks == 1) return launch_gemv_ks<MT, 1, kOut>(aq, w, C, out, S, M, N, K, s);
+    if (ks == 2) return launch_gemv_ks<MT, 2, kOut>(aq, w, C, out, S, M, N, K, s);
+    if constexpr (kOut != kSwiGLU) {
+        if (ks == 4) return launch_gemv_ks<MT, 4, kOut>(aq, w, C, out, S, M, N, K, s);
+    }
+    return cudaErrorInvalidValue;
 }
 
 }  // namespace
@@ -756,9 +800,9 @@ cudaError_t launch_gemv_q8_1(mmq_q8_1_t aq, const uint8_t* w, float* C, mmq_q8_1
                              int64_t K, cudaStream_t s) {
     if (M < 1 || M > 4 || N % 32 != 0) return cudaErrorInvalidValue;
     switch (M) {
-        case 1: return launch_gemv<1, kQ8>(aq, w, C, out, M, N, K, s);
-        case 2: return launch_gemv<2, kQ8>(aq, w, C, out, M, N, K, s);
-        default: return launch_gemv<4, kQ8>(aq, w, C, out, M, N, K, s);
+        case 1: return launch_gemv<1, kQ8>(aq, w, C, out, nullptr, M, N, K, s);
+        case 2: return launch_gemv<2, kQ8>(aq, w, C, out, nullptr, M, N, K, s);
+        default: return launch_gemv<4, kQ8>(aq, w, C, out, nullptr, M, N, K, s);
     }
 }
 
@@ -766,9 +810,9 @@ cudaError_t launch_gemv_swiglu_q8_1(mmq_q8_1_t aq, const uint8_t* w_gu, float* h
                                     int64_t F, int64_t K, cudaStream_t s) {
     if (M < 1 || M > 4 || F % 32 != 0) return cudaErrorInvalidValue;
     switch (M) {
-        case 1: return launch_gemv<1, kSwiGLU>(aq, w_gu, hf, out, M, 2 * F, K, s);
-        case 2: return launch_gemv<2, kSwiGLU>(aq, w_gu, hf, out, M, 2 * F, K, s);
-        default: return launch_gemv<4, kSwiGLU>(aq, w_gu, hf, out, M, 2 * F, K, s);
+        case 1: return launch_gemv<1, kSwiGLU>(aq, w_gu, hf, out, nullptr, M, 2 * F, K, s);
+        case 2: return launch_gemv<2, kSwiGLU>(aq, w_gu, hf, out, nullptr, M, 2 * F, K, s);
+        default: return launch_gemv<4, kSwiGLU>(aq, w_gu, hf, out, nullptr, M, 2 * F, K, s);
     }
 }
 
@@ -806,8 +850,8 @@ bool encode(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t i
 }
 
 template <int NF, int G, int D, int kOut>
-cudaError_t launch_nf(const SmallMaps& maps, float* C, mmq_q8_1_t out, int64_t M, int64_t N, int64_t K,
-                      int* status, cudaStream_t s) {
+cudaError_t launch_nf(const SmallMaps& maps, float* C, mmq_q8_1_t out, int32_t* S, int64_t M, int64_t N,
+                      int64_t K, int* status, cudaStream_t s) {
     int dev = 0, nsm = 0, optin = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
@@ -828,7 +872,7 @@ cudaError_t launch_nf(const SmallMaps& maps, float* C, mmq_q8_1_t out, int64_t M
     const int smem = L.total + 1024;   // + alignment slack
     if (smem > optin) return cudaErrorInvalidConfiguration;
     // the quantizing epilogue stages its tile behind the groups' partials in stage memory
-    if (kOut != kF32 && G * 128 * NF * 16 + 8 * NF * kRows * 4 > L.work_off) return cudaErrorInvalidConfiguration;
+    if (quant_out(kOut) && G * 128 * NF * 16 + 8 * NF * kRows * 4 > L.work_off) return cudaErrorInvalidConfiguration;
     auto k = gemm_small_kernel<NF, G, D, kOut>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
@@ -840,21 +884,21 @@ cudaError_t launch_nf(const SmallMaps& maps, float* C, mmq_q8_1_t out, int64_t M
     attr[cfg.numAttrs].val.clusterDim.y = 1;
     attr[cfg.numAttrs].val.clusterDim.z = 1;
     cfg.numAttrs += 1;
-    return cudaLaunchKernelEx(&cfg, k, maps, C, out, int(M), int(N), int(K), split, status);
+    return cudaLaunchKernelEx(&cfg, k, maps, C, out, S, int(M), int(N), int(K), split, status);
 }
 
 template <int kOut>
-cudaError_t launch_nf_any(int nf, const SmallMaps& maps, float* C, mmq_q8_1_t out, int64_t M, int64_t N,
-                          int64_t K, int* status, cudaStream_t s) {
+cudaError_t launch_nf_any(int nf, const SmallMaps& maps, float* C, mmq_q8_1_t out, int32_t* S, int64_t M,
+                          int64_t N, int64_t K, int* status, cudaStream_t s) {
     switch (nf) {
-        case 1: return launch_nf<1, 4, 1, kOut>(maps, C, out, M, N, K, status, s);
-        case 2: return launch_nf<2, 4, 2, kOut>(maps, C, out, M, N, K, status, s);
-        case 3: return launch_nf<3, 4, 2, kOut>(maps, C, out, M, N, K, status, s);
-        case 4: return launch_nf<4, 4, 1, kOut>(maps, C, out, M, N, K, status, s);
-        case 5: return launch_nf<5, 2, 2, kOut>(maps, C, out, M, N, K, status, s);
-        case 6: return launch_nf<6, 2, 2, kOut>(maps, C, out, M, N, K, status, s);
-        case 7: return launch_nf<7, 2, 2, kOut>(maps, C, out, M, N, K, status, s);
-        default: return launch_nf<8, 2, 2, kOut>(maps, C, out, M, N, K, status, s);
+        case 1: return launch_nf<1, 4, 1, kOut>(maps, C, out, S, M, N, K, status, s);
+        case 2: return launch_nf<2, 4, 2, kOut>(maps, C, out, S, M, N, K, status, s);
+        case 3: return launch_nf<3, 4, 2, kOut>(maps, C, out, S, M, N, K, status, s);
+        case 4: return launch_nf<4, 4, 1, kOut>(maps, C, out, S, M, N, K, status, s);
+        case 5: return launch_nf<5, 2, 2, kOut>(maps, C, out, S, M, N, K, status, s);
+        case 6: return launch_nf<6, 2, 2, kOut>(maps, C, out, S, M, N, K, status, s);
+        case 7: return launch_nf<7, 2, 2, kOut>(maps, C, out, S, M, N, K, status, s);
+        default: return launch_nf<8, 2, 2, kOut>(maps, C, out, S, M, N, K, status, s);
     }
 }
 
@@ -863,17 +907,25 @@ cudaError_t launch_nf_any(int nf, const SmallMaps& maps, float* C, mmq_q8_1_t ou
 namespace mmq {
 
 cudaError_t launch_gemm_small_m(mmq_q8_1_t aq, const uint8_t* w, float* C, int64_t M, int64_t N,
-                                int64_t K, int* status, cudaStream_t s, mmq_q8_1_t out, int mode) {
-    if (M > kMaxTok || mode < kF32 || mode > kSwiGLU) return cudaErrorInvalidValue;
-    if (mode != kF32 && (out.qs == nullptr || N % (mode == kSwiGLU ? 64 : 32) != 0)) return cudaErrorInvalidValue;
+                                int64_t K, int* status, cudaStream_t s, mmq_q8_1_t out, int mode, int32_t* S) {
+    if (M > kMaxTok || mode < kF32 || mode > kDump) return cudaErrorInvalidValue;
+    if (quant_out(mode) && (out.qs == nullptr || N % (mode == kSwiGLU ? 64 : 32) != 0)) return cudaErrorInvalidValue;
+    if ((mode == kDump) != (S != nullptr)) return cudaErrorInvalidValue;
+    const mmq_q8_1_t none = {nullptr, nullptr, nullptr};
     if (M <= 4) {   // a few tokens: streaming dot products on dp4a
         if (mode == kQ8) return launch_gemv_q8_1(aq, w, C, out, M, N, K, s);
         if (mode == kSwiGLU) return launch_gemv_swiglu_q8_1(aq, w, C, out, M, N / 2, K, s);
-        const mmq_q8_1_t none = {nullptr, nullptr, nullptr};
+        if (mode == kDump) {
+            switch (M) {
+                case 1: return launch_gemv<1, kDump>(aq, w, nullptr, none, S, M, N, K, s);
+                case 2: return launch_gemv<2, kDump>(aq, w, nullptr, none, S, M, N, K, s);
+                default: return launch_gemv<4, kDump>(aq, w, nullptr, none, S, M, N, K, s);
+            }
+        }
         switch (M) {
-            case 1: return launch_gemv<1, kF32>(aq, w, C, none, M, N, K, s);
-            case 2: return launch_gemv<2, kF32>(aq, w, C, none, M, N, K, s);
-            default: return launch_gemv<4, kF32>(aq, w, C, none, M, N, K, s);
+            case 1: return launch_gemv<1, kF32>(aq, w, C, none, nullptr, M, N, K, s);
+            case 2: return launch_gemv<2, kF32>(aq, w, C, none, nullptr, M, N, K, s);
+            default: return launch_gemv<4, kF32>(aq, w, C, none, nullptr, M, N, K, s);
         }
     }
     const int nf = int((M + 7) / 8);
@@ -889,9 +941,16 @@ cudaError_t launch_gemm_small_m(mmq_q8_1_t aq, const uint8_t* w, float* C, int64
         !encode(&maps.sa, CU_TENSOR_MAP_DATA_TYPE_INT32, aq.sa, nb, uint64_t(M), nb * 4, 8, mp,
                 CU_TENSOR_MAP_SWIZZLE_NONE))
         return cudaErrorInvalidValue;
-    if (mode == kQ8) return launch_nf_any<kQ8>(nf, maps, C, out, M, N, K, status, s);
-    if (mode == kSwiGLU) return launch_nf_any<kSwiGLU>(nf, maps, C, out, M, N, K, status, s);
-    return launch_nf_any<kF32>(nf, maps, C, out, M, N, K, status, s);
+    if (mode == kQ8) return launch_nf_any<kQ8>(nf, maps, C, out, nullptr, M, N, K, status, s);
+    if (mode == kSwiGLU) return launch_nf_any<kSwiGLU>(nf, maps, C, out, nullptr, M, N, K, status, s);
+    if (mode == kDump) return launch_nf_any<kDump>(nf, maps, nullptr, none, S, M, N, K, status, s);
+    return launch_nf_any<kF32>(nf, maps, C, out, nullptr, M, N, K, status, s);
+}
+
+int set_force_gemv_split(int ks) {
+    if (ks != 0 && ks != 1 && ks != 2 && ks != 4) return MMQ_ERR_ARG;
+    t_force_ks = ks;
+    return MMQ_OK;
 }
 
 }  // namespace mmq

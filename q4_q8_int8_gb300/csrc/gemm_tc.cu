@@ -23,8 +23,10 @@
 // weight factor sc*v <= 945 is written as the fp16 subnormal sc*v * 2^-24
 // (just the integer in the mantissa bits); every product and partial sum is
 // an integer multiple of 2^-24 below 2^-2, so the f32 accumulator holds
-// S' * 2^-24 exactly.  The 2^24 is folded into d.  The S dump (kDump) leaves
-// sc out and returns S itself, bit for bit.
+// S' * 2^-24 exactly.  The 2^24 is folded into d.  Two dumps write the
+// accumulator per chunk instead of rescaling it: kDumpS leaves sc out of the
+// weight operand and returns S itself, kDumpScaled keeps the product's
+// operand and returns S' = sc * S, both bit for bit.
 //
 // One CTA per SM, persistent over 128 (tokens) x 128 (weight rows) tiles,
 // warp-specialised (16 warps; setmaxnreg moves registers to the epilogue):
@@ -136,9 +138,12 @@ struct Bars {
 
 // kGlu: the weight rows alternate gate / up rows; write SwiGLU(gate, up)
 // quantized to q8_1 (and, if C is not null, as f32 [M][N/2] into C).
-// kDump: write the exact block dots S instead of C; kQ8: also (or only, C
-// == nullptr) write the result quantized to q8_1.
-template <bool kDump, bool kQ8, bool kGlu = false>
+// kDump: kNoDump, or write the exact block dots instead of C (kDumpS: S with
+// sc left out of the weight operand; kDumpScaled: S' = sc * S from the
+// product's own operand); kQ8: also (or only, C == nullptr) write the result
+// quantized to q8_1.
+constexpr int kNoDump = 0, kDumpS = 1, kDumpScaled = 2;
+template <int kDump, bool kQ8, bool kGlu = false>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_tc_kernel(const __grid_constant__ TmaMaps maps, float* __restrict__ C, mmq_q8_1_t q8out,
                int32_t* __restrict__ S, int M, int N, int K, int split, int* status, int inject_timeout,
@@ -400,7 +405,7 @@ gemm_tc_kernel(const __grid_constant__ TmaMaps maps, float* __restrict__ C, mmq_
                 const uint32_t raw = sbase + kOffRaw + rr.slot * kRawStage;
                 const uint32_t rawB = raw + kOffRawB + t * 144 + 16;
                 uint32_t scw_lo = 0x01010101u, scw_hi = 0x01010101u;   // the S dump keeps sc out
-                if (!kDump) {
+                if (kDump != kDumpS) {
                     const uint4 hdr = ld_shared_v4(raw + kOffRawB + t * 144);
                     scw_lo = sc_lo4(hdr.y);
                     scw_hi = sc_hi4(hdr.y, hdr.w);
@@ -684,7 +689,8 @@ int tc_gemm_launch_count(int64_t M, int64_t N, int64_t K) {
 }
 
 cudaError_t launch_gemm_tc(mmq_q8_1_t aq, const uint8_t* w, float* C, mmq_q8_1_t q8out, int32_t* S, int64_t M,
-                           int64_t N, int64_t K, int* status, int inject_timeout, cudaStream_t s, bool swiglu) {
+                           int64_t N, int64_t K, int* status, int inject_timeout, cudaStream_t s, bool swiglu,
+                           bool dump_scaled) {
     TmaMaps maps;
     const uint64_t nb = uint64_t(K / 32), nsb = uint64_t(K / 256);
     if (!encode_2d(&maps.a, CU_TENSOR_MAP_DATA_TYPE_UINT8, aq.qs, uint64_t(K), uint64_t(M),
@@ -701,18 +707,15 @@ cudaError_t launch_gemm_tc(mmq_q8_1_t aq, const uint8_t* w, float* C, mmq_q8_1_t
     cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
     // The register split (setmaxnreg) needs the block launched with exactly
     // kRegsLaunch registers per thread; refuse anything else.
+    cudaFuncAttributes fa;
+    auto k = S ? (dump_scaled ? gemm_tc_kernel<kDumpScaled, false> : gemm_tc_kernel<kDumpS, false>)
+               : swiglu ? gemm_tc_kernel<kNoDump, true, true>
+               : (q8out.qs ? gemm_tc_kernel<kNoDump, true> : gemm_tc_kernel<kNoDump, false>);
     {
-        cudaFuncAttributes fa;
-        cudaError_t e = cudaFuncGetAttributes(&fa, S ? gemm_tc_kernel<true, false>
-                                                   : swiglu ? gemm_tc_kernel<false, true, true>
-                                                   : (q8out.qs ? gemm_tc_kernel<false, true>
-                                                               : gemm_tc_kernel<false, false>));
+        cudaError_t e = cudaFuncGetAttributes(&fa, k);
         if (e != cudaSuccess) return e;
         if (fa.numRegs != int(kRegsLaunch)) return cudaErrorInvalidConfiguration;
     }
-    auto k = S ? gemm_tc_kernel<true, false>
-               : swiglu ? gemm_tc_kernel<false, true, true>
-               : (q8out.qs ? gemm_tc_kernel<false, true> : gemm_tc_kernel<false, false>);
     cudaError_t e;
     if ((e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes)))
         return e;

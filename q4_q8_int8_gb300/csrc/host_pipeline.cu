@@ -112,6 +112,12 @@ int gemm_host(const float* x_host, const uint8_t* w, float* C_host, int64_t M, i
         const int rc = gemm(q8, w, cb[b], mc, N, K, s0);
         if (rc != MMQ_OK) {
             cudaGetLastError();
+            // join both copy streams back into the caller's stream, so that
+            // work queued there later (or a graph capture) stays ordered
+            // after the copies already issued
+            for (cudaStream_t cs : {hp->in, hp->out})
+                if (cudaEventRecord(hp->start, cs) == cudaSuccess) cudaStreamWaitEvent(s0, hp->start, 0);
+            cudaGetLastError();
             return rc;
         }
         ck(cudaEventRecord(hp->comp_done[b], s0));
@@ -123,6 +129,9 @@ int gemm_host(const float* x_host, const uint8_t* w, float* C_host, int64_t M, i
     // the caller's stream is ordered after the last copies of both buffers
     for (int b = 0; b < 2 && b < nchunks && e == cudaSuccess; ++b) ck(cudaStreamWaitEvent(s0, hp->out_done[b], 0));
     if (e != cudaSuccess) {
+        cudaGetLastError();
+        for (cudaStream_t cs : {hp->in, hp->out})   // best effort: keep the caller's stream joined
+            if (cudaEventRecord(hp->start, cs) == cudaSuccess) cudaStreamWaitEvent(s0, hp->start, 0);
         cudaGetLastError();
         return MMQ_ERR_CUDA;
     }

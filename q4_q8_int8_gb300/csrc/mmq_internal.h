@@ -47,9 +47,12 @@ int tc_gemm_check_resources();   // MMQ_OK or MMQ_ERR_RESOURCE
 // q8out.qs == nullptr: no q8_1 output; C == nullptr: no f32 output.
 // swiglu: the N weight rows alternate gate / up; q8out receives the [M][N/2]
 // q8_1 of silu(gate) * up and C (may be null) the same values in f32.
+// S != nullptr: write the per-chunk dots instead of C (dump_scaled: S' = sc*S
+// from the product's weight operand; otherwise S with sc left out).
 cudaError_t launch_gemm_tc(mmq_q8_1_t aq, const uint8_t* w, float* C, mmq_q8_1_t q8out,
                            int32_t* S, int64_t M, int64_t N, int64_t K,
-                           int* status, int inject_timeout, cudaStream_t s, bool swiglu = false);
+                           int* status, int inject_timeout, cudaStream_t s, bool swiglu = false,
+                           bool dump_scaled = false);
 // The tcgen05 kernel's launch plan for one call (gemm_tc.cu): tiles
 // [0, tail_lo) in the first launch (persistent, or K split over clusters of
 // first_split CTAs), tiles [tail_lo, tiles) in a second launch with K split
@@ -62,18 +65,18 @@ struct TcPlan {
 };
 TcPlan tc_plan(int64_t M, int64_t N, int64_t K, int nsm, bool allow_tail);
 int tc_gemm_launch_count(int64_t M, int64_t N, int64_t K);   // kernels per call, -1 on a CUDA error
-int tc2_gemm_check_resources();  // MMQ_OK or MMQ_ERR_RESOURCE
-int64_t tc2_pair_tiles(int64_t M, int64_t N);
-cudaError_t launch_gemm_tc2(mmq_q8_1_t aq, const uint8_t* w, float* C,
-                            int32_t* S, int64_t M, int64_t N, int64_t K,
-                            int* status, int inject_timeout, cudaStream_t s);
 // mode 0: C only; 1: also q8_1 into `out` (C may be null); 2: gate/up rows
 // interleaved, q8_1 of silu(g)*u into `out` [M][N/2] and, if C is not null,
-// h as f32 [M][N/2] into C.
+// h as f32 [M][N/2] into C; 3: the exact per-chunk dots into S [M][N][K/32]
+// (C and out unused) from the same kernel the shape selects.
 cudaError_t launch_gemm_small_m(mmq_q8_1_t aq, const uint8_t* w, float* C,
                                 int64_t M, int64_t N, int64_t K, int* status,
                                 cudaStream_t s, mmq_q8_1_t out = mmq_q8_1_t{nullptr, nullptr, nullptr},
-                                int mode = 0);
+                                int mode = 0, int32_t* S = nullptr);
+constexpr int kSmallDump = 3;
+// Test hook of the dot-product kernel: force its K split (0, 1, 2, 4) for the
+// calling host thread; MMQ_ERR_ARG for other values.
+int set_force_gemv_split(int ks);
 // Host-buffer pipeline (host_pipeline.cu): rows per chunk, workspace bytes,
 // and the chunked copy-in / prepass + GEMM / copy-out, with `gemm` the GEMM
 // to run on each chunk's q8_1 planes (MMQ_* code).
@@ -91,10 +94,6 @@ cudaError_t launch_gemv_q8_1(mmq_q8_1_t aq, const uint8_t* w, float* C, mmq_q8_1
 // F % 32 == 0), q8_1 of silu(g)*u into out [M][F], h as f32 into hf if not null.
 cudaError_t launch_gemv_swiglu_q8_1(mmq_q8_1_t aq, const uint8_t* w_gu, float* hf, mmq_q8_1_t out, int64_t M,
                                     int64_t F, int64_t K, cudaStream_t s);
-// tcgen05 kernel for few tokens: 128 weight rows x 16/32/64 tokens per CTA.
-cudaError_t launch_gemm_tc_small(mmq_q8_1_t aq, const uint8_t* w, float* C,
-                                 int64_t M, int64_t N, int64_t K, int* status,
-                                 int inject_timeout, cudaStream_t s);
 // The dequantize-then-dense control path (dense.cu).
 cudaError_t launch_dequantize_q4K_f16(const uint8_t* w, uint16_t* out, int64_t N, int64_t K,
                                       cudaStream_t s);

@@ -123,8 +123,16 @@ def test_argument_errors_before_device(lib):
     assert mmq.mmq_q4K_gemm_launches(1, 4, 300, mmq.MMQ_PATH_AUTO) == mmq.MMQ_ERR_ARG
     assert mmq.mmq_q4K_gemm_launches(65, 4, 256, mmq.MMQ_PATH_SMALL_M) == mmq.MMQ_ERR_ARG
     assert mmq.mmq_q4K_gemm_launches(1, 4, 256, 9) == mmq.MMQ_ERR_ARG
-    assert mmq.mmq_q4K_block_dots(good, w, C, 1, 4, 256, mmq.MMQ_PATH_SMALL_M, None) == mmq.MMQ_ERR_ARG
-    assert mmq.mmq_q4K_block_dots(good, w, C, 1, 4, 256, mmq.MMQ_PATH_TC_SMALL, None) == mmq.MMQ_ERR_ARG
+    assert mmq.mmq_q4K_block_dots(good, w, C, 65, 4, 256, mmq.MMQ_PATH_SMALL_M, None) == mmq.MMQ_ERR_ARG
+    for retired in (4, 5):   # two retired tensor-core paths are refused like unknown values
+        assert mmq.mmq_q4K_block_dots(good, w, C, 1, 4, 256, retired, None) == mmq.MMQ_ERR_ARG
+        assert mmq.mmq_q4K_gemm_path(good, w, C, 128, 4, 256, retired, None) == mmq.MMQ_ERR_ARG
+    assert mmq.mmq_q4K_scaled_block_dots(good, w, None, 1, 4, 256, None) == mmq.MMQ_ERR_ARG
+    assert mmq.mmq_q4K_scaled_block_dots(good, w, C, 1, 6, 256, None) == mmq.MMQ_ERR_ARG
+    # the split hook takes 0, 1, 2, 4 only
+    for bad in (-1, 3, 8):
+        assert mmq.mmq_debug_force_gemv_split(bad) == mmq.MMQ_ERR_ARG
+    assert mmq.mmq_debug_force_gemv_split(0) == mmq.MMQ_OK
     # alignment
     assert mmq.mmq_q4K_gemm(Q(0x10004, 0x20000, 0x30000), w, C, 1, 4, 256, None) == mmq.MMQ_ERR_ALIGN
     assert mmq.mmq_q4K_gemm(good, ctypes.c_void_p(0x40008), C, 1, 4, 256, None) == mmq.MMQ_ERR_ALIGN

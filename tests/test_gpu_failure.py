@@ -11,8 +11,7 @@ from tests.gpu_util import require_gpu, to_dev
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("path_name,M", [("MMQ_PATH_TC", 128), ("MMQ_PATH_TC_PAIR", 128),
-                                         ("MMQ_PATH_TC_SMALL", 16), ("MMQ_PATH_TC_SMALL", 128)])
+@pytest.mark.parametrize("path_name,M", [("MMQ_PATH_TC", 128), ("MMQ_PATH_TC", 77), ("MMQ_PATH_TC", 2048)])
 def test_injected_timeout_is_reported_and_context_survives(path_name, M):
     mmq = require_gpu()
     path = getattr(mmq, path_name)
