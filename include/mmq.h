@@ -141,6 +141,42 @@ int mmq_q4K_gemm_host(const float* x_host, const uint8_t* bq4k, float* C_host,
                       int64_t M, int64_t N, int64_t K, void* workspace,
                       size_t workspace_bytes, void* stream);
 
+/* Size of the fixed device array behind mmq_q4K_gemm_host_noalloc: 64 MiB. */
+#define MMQ_HOST_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
+
+/* mmq_q4K_gemm_host without a workspace argument.  The pages have no
+ * counterpart: this entry point serves callers that hold the activations in
+ * host memory but cannot hand the library device memory, for example code
+ * that reaches the GPU only through this C ABI (a foreign-function caller
+ * with no CUDA bindings, so no way to obtain a device pointer), or a plug-in
+ * in a process whose memory pool has reserved the device's memory, where a
+ * cudaMalloc of its own would fail or break that reservation (and could
+ * synchronize the device on the way).
+ *
+ * The workspace is a file-scope device array of MMQ_HOST_NOALLOC_SCRATCH_BYTES
+ * inside the library; every device on which the library's code is loaded
+ * holds it until the process exits.  The call allocates no device memory
+ * (no cudaMalloc or cudaFree, no allocating library routine).  The first
+ * call on a device looks up the array's device address (and, as
+ * mmq_q4K_gemm_host does, creates the library's two copy streams for that
+ * device); make that first call before any stream capture on the device.
+ *
+ * Arguments, results and errors are those of mmq_q4K_gemm_host (the same
+ * chunked copies and kernels, so C is what mmq_q4K_gemm_host gives),
+ * except: a shape whose mmq_q4K_gemm_host_workspace(M, N, K) exceeds
+ * MMQ_HOST_NOALLOC_SCRATCH_BYTES is refused with MMQ_ERR_ARG before any
+ * device work (e.g. M = 2048, K = N = 4096 needs 36 MB and fits; the
+ * 2048 x 11008 -> 4096 down projection needs 69 MB and does not).
+ *
+ * Every call uses the same array, and it keeps whatever the last call left
+ * there; each call overwrites every byte it reads (nothing in it has to
+ * start at zero).  Calls on one stream run one after another; calls whose
+ * device work can overlap (different streams not ordered by events, or
+ * several host threads) race on the array and give wrong results. */
+int mmq_q4K_gemm_host_noalloc(const float* x_host, const uint8_t* bq4k,
+                              float* C_host, int64_t M, int64_t N, int64_t K,
+                              void* stream);
+
 /* Kernel selection for mmq_q4K_gemm_path (testing and A/B timing).  The
  * values 4 and 5 are retired (two tensor-core variants that no shape ever
  * selected) and are refused like any unknown value. */

@@ -28,13 +28,14 @@ MMQ_PATH_AUTO = 0
 MMQ_PATH_MMA_S8 = 1
 MMQ_PATH_TC = 2
 MMQ_PATH_SMALL_M = 3
+MMQ_HOST_NOALLOC_SCRATCH_BYTES = 64 << 20
 SMALL_M_MAX = 64
 MMQ_GGUF_F32, MMQ_GGUF_F16, MMQ_GGUF_Q4_K, MMQ_GGUF_Q6_K = 0, 1, 12, 14
 
 # Every symbol include/mmq.h declares.
 EXPORTS = (
     "mmq_q8_1_bytes", "mmq_q8_1_view", "mmq_quantize_q8_1", "mmq_q4K_bytes",
-    "mmq_pack_q4K", "mmq_q4K_gemm", "mmq_q4K_gemm_host_workspace", "mmq_q4K_gemm_host", "mmq_q4K_gemm_launches", "mmq_q4K_gemm_path", "mmq_q4K_gemm_q8_1", "mmq_q4K_block_dots", "mmq_q4K_scaled_block_dots",
+    "mmq_pack_q4K", "mmq_q4K_gemm", "mmq_q4K_gemm_host_workspace", "mmq_q4K_gemm_host", "mmq_q4K_gemm_host_noalloc", "mmq_q4K_gemm_launches", "mmq_q4K_gemm_path", "mmq_q4K_gemm_q8_1", "mmq_q4K_block_dots", "mmq_q4K_scaled_block_dots",
     "mmq_dequantize_q4K_f16", "mmq_convert_f32_f16", "mmq_gemm_f16",
     "mmq_q4K_gemm_swiglu_q8_1", "mmq_interleave_rows_q4K",
     "mmq_q6K_bytes", "mmq_pack_q6K", "mmq_q6K_dev_bytes", "mmq_repack_q6K", "mmq_q6K_gemm",
@@ -79,6 +80,7 @@ def load_library(path: str = LIB_PATH):
                 "mmq_q4K_gemm": ([Q, P, P, I, I, I, P], ctypes.c_int),
                 "mmq_q4K_gemm_host_workspace": ([I, I, I], S),
                 "mmq_q4K_gemm_host": ([P, P, P, I, I, I, P, S, P], ctypes.c_int),
+                "mmq_q4K_gemm_host_noalloc": ([P, P, P, I, I, I, P], ctypes.c_int),
                 "mmq_q4K_gemm_launches": ([I, I, I, ctypes.c_int], ctypes.c_int),
                 "mmq_q4K_gemm_path": ([Q, P, P, I, I, I, ctypes.c_int, P], ctypes.c_int),
                 "mmq_q4K_gemm_q8_1": ([Q, P, P, Q, I, I, I, P], ctypes.c_int),
@@ -151,6 +153,10 @@ def mmq_q4K_gemm_host_workspace(M, N, K):
 
 def mmq_q4K_gemm_host(x_host, bq4k, C_host, M, N, K, ws, ws_bytes, stream):
     return load_library().mmq_q4K_gemm_host(x_host, bq4k, C_host, M, N, K, ws, ws_bytes, stream)
+
+
+def mmq_q4K_gemm_host_noalloc(x_host, bq4k, C_host, M, N, K, stream):
+    return load_library().mmq_q4K_gemm_host_noalloc(x_host, bq4k, C_host, M, N, K, stream)
 
 
 def mmq_q4K_gemm_launches(M, N, K, path):

@@ -193,6 +193,19 @@ int mmq_q4K_gemm_host(const float* x_host, const uint8_t* bq4k, float* C_host, i
     return mmq::gemm_host(x_host, bq4k, C_host, M, N, K, workspace, static_cast<cudaStream_t>(stream), gemm_auto);
 }
 
+int mmq_q4K_gemm_host_noalloc(const float* x_host, const uint8_t* bq4k, float* C_host, int64_t M, int64_t N,
+                              int64_t K, void* stream) {
+    if (!x_host || !bq4k || !C_host) return MMQ_ERR_ARG;
+    const size_t need = mmq_q4K_gemm_host_workspace(M, N, K);
+    if (need == 0 || need > MMQ_HOST_NOALLOC_SCRATCH_BYTES) return MMQ_ERR_ARG;
+    if (!aligned16(bq4k)) return MMQ_ERR_ALIGN;
+    int rc = check_device();
+    if (rc) return rc;
+    void* scratch = nullptr;
+    if ((rc = mmq::host_noalloc_scratch(&scratch))) return rc;
+    return mmq::gemm_host(x_host, bq4k, C_host, M, N, K, scratch, static_cast<cudaStream_t>(stream), gemm_auto);
+}
+
 int mmq_q4K_gemm_launches(int64_t M, int64_t N, int64_t K, int path) {
     if (!known_path(path)) return MMQ_ERR_ARG;
     if (M < 1 || N < 1 || K < 256 || (K % 256) != 0 || (N % 4) != 0) return MMQ_ERR_ARG;

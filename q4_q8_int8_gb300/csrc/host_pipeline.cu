@@ -42,9 +42,36 @@ cudaError_t pipe_for(int dev, HostPipe** out) {
 
 size_t up256(size_t b) { return (b + 255) & ~size_t(255); }
 
+// The fixed device workspace of mmq_q4K_gemm_host_noalloc.  Every device on
+// which the library's code is loaded holds it until the process exits.  In
+// host code the name is only a host-side stand-in for the array; its device
+// address comes from cudaGetSymbolAddress, looked up once per device.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[MMQ_HOST_NOALLOC_SCRATCH_BYTES];
+std::mutex g_noalloc_mu;
+void* g_noalloc_addr[kMaxDevices];
+
 }  // namespace
 
 namespace mmq {
+
+int host_noalloc_scratch(void** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        cudaGetLastError();
+        return MMQ_ERR_DEVICE;
+    }
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    if (!g_noalloc_addr[dev]) {   // first call on this device (it is the current one)
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) {
+            cudaGetLastError();
+            return MMQ_ERR_CUDA;
+        }
+        g_noalloc_addr[dev] = p;
+    }
+    *out = g_noalloc_addr[dev];
+    return MMQ_OK;
+}
 
 int64_t host_chunk_rows(int64_t M) {
     if (M <= 256) return M;

@@ -86,6 +86,11 @@ int64_t host_chunk_rows(int64_t M);
 size_t host_workspace_bytes(int64_t M, int64_t N, int64_t K);
 int gemm_host(const float* x_host, const uint8_t* w, float* C_host, int64_t M, int64_t N, int64_t K, void* ws,
               cudaStream_t s, GemmFn gemm);
+// Device address of the fixed workspace behind mmq_q4K_gemm_host_noalloc
+// (MMQ_HOST_NOALLOC_SCRATCH_BYTES, 256-byte aligned) on the current device,
+// looked up on the first call per device: MMQ_OK, MMQ_ERR_DEVICE or
+// MMQ_ERR_CUDA.
+int host_noalloc_scratch(void** out);
 // The dp4a GEMV (M <= 4) that also writes its result as q8_1 (N % 32 == 0;
 // C may be null).
 cudaError_t launch_gemv_q8_1(mmq_q8_1_t aq, const uint8_t* w, float* C, mmq_q8_1_t out, int64_t M, int64_t N,
