@@ -188,6 +188,47 @@ int mmq_q4K_gemm_host_noalloc(const float* x_host, const uint8_t* bq4k,
                             /* dp4a dot products for M <= 4, mma.sync f16   */
                             /* with cluster split-K for 4 < M <= 64         */
 
+/* ---- the tensor-core operand plane (GB300 fast path for many tokens) ----
+ *
+ * The pages' rescale multiplies each 32-k chunk's integer dot by its own
+ * activation scale da (page r15 section 2.1), which on the tensor cores
+ * means a round trip through tensor memory per chunk.  The operand plane
+ * carries that scale inside the activation operand instead, so that one
+ * accumulator can hold a whole 256-k super-block:
+ *   per token row i and super-block b, g_ib = 2^E (E from the largest da of
+ *   the block's eight chunks) and s = da * 2^-E (exact); per element
+ *   hi = q * s_hi with s_hi = s rounded to 4 significant bits (an exact
+ *   fp16 product) and lo = fp16(q * fp16(s - s_hi)), so hi + lo is within
+ *   2^-14 of q * s; and the second term's factors dma * 2^-E (dma = da *
+ *   sa, page r16 section 2.1) split into tf32 hi + lo.
+ * The plane is a device-only encoding of the q8_1 values (its bytes are
+ * defined by the prepass below and read only by mmq_q4K_gemm_tcop): a
+ * single caller-owned buffer of mmq_q8_1_tcop_bytes(M, K) bytes, 256-byte
+ * aligned. */
+
+/* Bytes of the operand plane of M x K activations (K % 256 == 0); 0 for an
+ * invalid shape. */
+size_t mmq_q8_1_tcop_bytes(int64_t M, int64_t K);
+
+/* The q8_1 prepass (exactly as mmq_quantize_q8_1: `aq` receives the same
+ * bits) that also writes the operand plane `tcop` (device memory,
+ * mmq_q8_1_tcop_bytes(M, K) bytes, 256-byte aligned).  K % 256 == 0.
+ * MMQ_ERR_ARG / MMQ_ERR_ALIGN / MMQ_ERR_DEVICE / MMQ_ERR_CUDA as
+ * mmq_quantize_q8_1. */
+int mmq_quantize_q8_1_tcop(const float* x, int64_t M, int64_t K, mmq_q8_1_t aq,
+                           void* tcop, void* stream);
+
+/* C[M][N] (f32, overwritten) = the q4_K x q8_1 GEMM of the activations whose
+ * operand plane `tcop` mmq_quantize_q8_1_tcop wrote, on the tcgen05 kernel
+ * that accumulates whole super-blocks (128 x 256 tiles, one CTA per SM).
+ * The result meets the GEMM's tolerance |C - C_ref| <= 1e-4 sum|a w| + 1e-6
+ * (the plane's 2^-14 and f32 accumulation stay far inside it) but the
+ * per-chunk integer dots S are never formed: mmq_q4K_block_dots covers the
+ * other kernels.  Shape and alignment rules as mmq_q4K_gemm; the result
+ * does not depend on the stream or on earlier calls (deterministic). */
+int mmq_q4K_gemm_tcop(const void* tcop, const uint8_t* bq4k, float* C, int64_t M,
+                      int64_t N, int64_t K, void* stream);
+
 /* Number of kernels mmq_q4K_gemm_path(…, path, …) enqueues for this shape
  * on the current device: 1, or 2 when the tcgen05 kernel splits off its
  * last partial round of tiles into a second, split-K launch.  For counting

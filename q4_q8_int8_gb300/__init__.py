@@ -35,7 +35,7 @@ MMQ_GGUF_F32, MMQ_GGUF_F16, MMQ_GGUF_Q4_K, MMQ_GGUF_Q6_K = 0, 1, 12, 14
 # Every symbol include/mmq.h declares.
 EXPORTS = (
     "mmq_q8_1_bytes", "mmq_q8_1_view", "mmq_quantize_q8_1", "mmq_q4K_bytes",
-    "mmq_pack_q4K", "mmq_q4K_gemm", "mmq_q4K_gemm_host_workspace", "mmq_q4K_gemm_host", "mmq_q4K_gemm_host_noalloc", "mmq_q4K_gemm_launches", "mmq_q4K_gemm_path", "mmq_q4K_gemm_q8_1", "mmq_q4K_block_dots", "mmq_q4K_scaled_block_dots",
+    "mmq_pack_q4K", "mmq_q4K_gemm", "mmq_q8_1_tcop_bytes", "mmq_quantize_q8_1_tcop", "mmq_q4K_gemm_tcop", "mmq_q4K_gemm_host_workspace", "mmq_q4K_gemm_host", "mmq_q4K_gemm_host_noalloc", "mmq_q4K_gemm_launches", "mmq_q4K_gemm_path", "mmq_q4K_gemm_q8_1", "mmq_q4K_block_dots", "mmq_q4K_scaled_block_dots",
     "mmq_dequantize_q4K_f16", "mmq_convert_f32_f16", "mmq_gemm_f16",
     "mmq_q4K_gemm_swiglu_q8_1", "mmq_interleave_rows_q4K",
     "mmq_q6K_bytes", "mmq_pack_q6K", "mmq_q6K_dev_bytes", "mmq_repack_q6K", "mmq_q6K_gemm",
@@ -76,6 +76,9 @@ def load_library(path: str = LIB_PATH):
                 "mmq_q8_1_view": ([P, I, I, ctypes.POINTER(Q)], ctypes.c_int),
                 "mmq_quantize_q8_1": ([P, I, I, Q, P], ctypes.c_int),
                 "mmq_q4K_bytes": ([I, I], S),
+                "mmq_q8_1_tcop_bytes": ([I, I], S),
+                "mmq_quantize_q8_1_tcop": ([P, I, I, Q, P, P], ctypes.c_int),
+                "mmq_q4K_gemm_tcop": ([P, P, P, I, I, I, P], ctypes.c_int),
                 "mmq_pack_q4K": ([P, P, P, P, P, I, I, P], ctypes.c_int),
                 "mmq_q4K_gemm": ([Q, P, P, I, I, I, P], ctypes.c_int),
                 "mmq_q4K_gemm_host_workspace": ([I, I, I], S),
@@ -137,6 +140,18 @@ def mmq_quantize_q8_1(x, M, K, aq, stream):
 
 def mmq_q4K_bytes(N, K):
     return load_library().mmq_q4K_bytes(N, K)
+
+
+def mmq_q8_1_tcop_bytes(M, K):
+    return load_library().mmq_q8_1_tcop_bytes(M, K)
+
+
+def mmq_quantize_q8_1_tcop(x, M, K, aq, tcop, stream):
+    return load_library().mmq_quantize_q8_1_tcop(x, M, K, aq, tcop, stream)
+
+
+def mmq_q4K_gemm_tcop(tcop, bq4k, C, M, N, K, stream):
+    return load_library().mmq_q4K_gemm_tcop(tcop, bq4k, C, M, N, K, stream)
 
 
 def mmq_pack_q4K(v, sc, m, d, dmin, N, K, out):
@@ -234,6 +249,39 @@ def quantize_q8_1(x, out=None, stream=None):
     _check(mmq_quantize_q8_1(ctypes.c_void_p(x.data_ptr()), M, K, q8_1_struct(qs, da, sa),
                              _stream_ptr(stream)), "mmq_quantize_q8_1")
     return qs, da, sa
+
+
+def empty_tcop(M: int, K: int, device="cuda"):
+    """Allocate the tensor-core operand plane of M x K activations (uint8,
+    mmq_q8_1_tcop_bytes(M, K) bytes; the caching allocator's blocks are
+    256-byte aligned, which the call checks)."""
+    import torch
+    n = mmq_q8_1_tcop_bytes(M, K)
+    if n == 0:
+        raise MMQError(MMQ_ERR_ARG, "mmq_q8_1_tcop_bytes")
+    return torch.empty((n,), dtype=torch.uint8, device=device)
+
+
+def quantize_q8_1_tcop(x, out=None, tcop=None, stream=None):
+    """x float32 [M][K] (CUDA) -> ((qs, da, sa), tcop): the q8_1 prepass that
+    also writes the operand plane for q4K_gemm_tcop."""
+    M, K = x.shape
+    qs, da, sa = out if out is not None else empty_q8_1(M, K, x.device)
+    tcop = tcop if tcop is not None else empty_tcop(M, K, x.device)
+    _check(mmq_quantize_q8_1_tcop(ctypes.c_void_p(x.data_ptr()), M, K, q8_1_struct(qs, da, sa),
+                                  ctypes.c_void_p(tcop.data_ptr()), _stream_ptr(stream)),
+           "mmq_quantize_q8_1_tcop")
+    return (qs, da, sa), tcop
+
+
+def q4K_gemm_tcop(tcop, w, M: int, N: int, K: int, out=None, stream=None):
+    """The super-block tcgen05 GEMM on an operand plane -> C float32 [M][N]."""
+    import torch
+    C = out if out is not None else torch.empty((M, N), dtype=torch.float32, device=w.device)
+    _check(mmq_q4K_gemm_tcop(ctypes.c_void_p(tcop.data_ptr()), ctypes.c_void_p(w.data_ptr()),
+                             ctypes.c_void_p(C.data_ptr()), M, N, K, _stream_ptr(stream)),
+           "mmq_q4K_gemm_tcop")
+    return C
 
 
 def q4K_gemm(aq, w, N: int, path: int = MMQ_PATH_AUTO, out=None, stream=None):

@@ -122,6 +122,23 @@ int mmq_quantize_q8_1(const float* x, int64_t M, int64_t K, mmq_q8_1_t aq, void*
     return from_cuda(mmq::launch_quantize_q8_1(x, M, K, aq, static_cast<cudaStream_t>(stream)));
 }
 
+size_t mmq_q8_1_tcop_bytes(int64_t M, int64_t K) {
+    if (M < 1 || K < 256 || (K % 256) != 0) return 0;
+    if (M > (int64_t(1) << 31) - 1 || K > (int64_t(1) << 31) - 1) return 0;
+    return mmq::tcop_layout(M, K).bytes;
+}
+
+int mmq_quantize_q8_1_tcop(const float* x, int64_t M, int64_t K, mmq_q8_1_t aq, void* tcop, void* stream) {
+    if (!x || !tcop) return MMQ_ERR_ARG;
+    int rc = check_q8(aq);
+    if (rc) return rc;
+    if (mmq_q8_1_tcop_bytes(M, K) == 0) return MMQ_ERR_ARG;
+    if (!aligned16(x)) return MMQ_ERR_ALIGN;
+    if (reinterpret_cast<uintptr_t>(tcop) & 255) return MMQ_ERR_ALIGN;
+    if ((rc = check_device())) return rc;
+    return from_cuda(mmq::launch_quantize_q8_1_tcop(x, M, K, aq, tcop, static_cast<cudaStream_t>(stream)));
+}
+
 size_t mmq_q4K_bytes(int64_t N, int64_t K) {
     if (N < 1 || K < 256 || (K % 256) != 0) return 0;
     return size_t(N) * size_t(K / 256) * 144;
@@ -227,6 +244,21 @@ int mmq_q4K_gemm_path(mmq_q8_1_t aq, const uint8_t* bq4k, float* C, int64_t M, i
     int rc = check_gemm_args(aq, bq4k, C, M, N, K);
     if (rc) return rc;
     return run_gemm(aq, bq4k, C, nullptr, M, N, K, path, static_cast<cudaStream_t>(stream));
+}
+
+int mmq_q4K_gemm_tcop(const void* tcop, const uint8_t* bq4k, float* C, int64_t M, int64_t N, int64_t K,
+                      void* stream) {
+    if (!tcop || !bq4k || !C) return MMQ_ERR_ARG;
+    if (mmq_q8_1_tcop_bytes(M, K) == 0 || N < 1 || (N % 4) != 0 || N > (int64_t(1) << 31) - 1) return MMQ_ERR_ARG;
+    if ((reinterpret_cast<uintptr_t>(tcop) & 255) || !aligned16(bq4k) || !aligned16(C)) return MMQ_ERR_ALIGN;
+    int rc = check_device();
+    if (rc) return rc;
+    if ((rc = mmq::sb_gemm_check_resources())) return rc;
+    int* status = mmq::status_word_ptr();
+    if (!status) return MMQ_ERR_CUDA;
+    const int inject = t_inject_timeout;
+    t_inject_timeout = 0;
+    return from_cuda(mmq::launch_gemm_sb(tcop, bq4k, C, M, N, K, status, inject, static_cast<cudaStream_t>(stream)));
 }
 
 int mmq_q4K_gemm_q8_1(mmq_q8_1_t aq, const uint8_t* bq4k, float* C, mmq_q8_1_t out, int64_t M,

@@ -53,6 +53,33 @@ cudaError_t launch_gemm_tc(mmq_q8_1_t aq, const uint8_t* w, float* C, mmq_q8_1_t
                            int32_t* S, int64_t M, int64_t N, int64_t K,
                            int* status, int inject_timeout, cudaStream_t s, bool swiglu = false,
                            bool dump_scaled = false);
+// The tensor-core operand plane of M x K activations (written by the
+// prepass's tensor-core form, read by the super-block GEMM): byte offsets of
+// its three parts, each 256-byte aligned.
+//   a   fp16 [M][K/32][64]  per 32-k chunk 32 values q * s_hi, then 32 values
+//       fp16(q * s_lo), each in k order 0,2,1,3 per group of four (one
+//       128-byte line per token row and chunk)
+//   t2  f32 [M][K/256][32]  second-term factors [hi x8 | hi x8 | lo x8 | 0 x8]
+//   g   f32 [M][K/256]  2^E of each token row and super-block
+struct TcopLayout {
+    size_t a, t2, g, bytes;
+};
+inline TcopLayout tcop_layout(int64_t M, int64_t K) {
+    auto up = [](size_t b) { return (b + 255) & ~size_t(255); };
+    TcopLayout L;
+    const size_t n = size_t(M) * size_t(K), nsb = size_t(M) * size_t(K / 256);
+    L.a = 0;
+    L.t2 = up(4 * n);
+    L.g = L.t2 + up(nsb * 128);
+    L.bytes = L.g + up(nsb * 4);
+    return L;
+}
+cudaError_t launch_quantize_q8_1_tcop(const float* x, int64_t M, int64_t K, mmq_q8_1_t aq, void* tcop,
+                                      cudaStream_t s);
+// The super-block-accumulating GEMM on the operand plane (gemm_sb.cu): C only.
+int sb_gemm_check_resources();   // MMQ_OK or MMQ_ERR_RESOURCE
+cudaError_t launch_gemm_sb(const void* tcop, const uint8_t* w, float* C, int64_t M, int64_t N, int64_t K,
+                           int* status, int inject_timeout, cudaStream_t s);
 // The tcgen05 kernel's launch plan for one call (gemm_tc.cu): tiles
 // [0, tail_lo) in the first launch (persistent, or K split over clusters of
 // first_split CTAs), tiles [tail_lo, tiles) in a second launch with K split

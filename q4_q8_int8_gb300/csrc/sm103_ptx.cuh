@@ -169,6 +169,15 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
         : "memory");
 }
 
+// Prefetch a tile of the tensor map's box shape into L2 (no shared memory,
+// no completion signal).
+__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int32_t x, int32_t y) {
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(x), "r"(y)
+                 : "memory");
+}
+
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
@@ -417,6 +426,19 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
     d |= uint64_t(1024 >> 4) << 32;                   // stride byte offset: 8-row group pitch
     d |= uint64_t(1) << 46;                           // descriptor version for sm_100 family
     d |= uint64_t(2) << 61;                           // swizzle mode: 128B
+    return d;
+}
+
+// The same for a K-major tile stored with the 64-byte swizzle: rows of 64
+// bytes (32 fp16), 8-row groups 512 bytes apart; 16-byte granule g of row r
+// sits at granule g ^ ((r >> 1) & 3) of its row.
+__device__ __forceinline__ uint64_t smem_desc_sw64(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= uint64_t((saddr & 0x3FFFFu) >> 4);          // start address
+    d |= uint64_t(1) << 16;                           // leading byte offset (unused here)
+    d |= uint64_t(512 >> 4) << 32;                    // stride byte offset: 8-row group pitch
+    d |= uint64_t(1) << 46;                           // descriptor version for sm_100 family
+    d |= uint64_t(4) << 61;                           // swizzle mode: 64B
     return d;
 }
 
