@@ -94,7 +94,7 @@ constexpr int kOffT2 = kOffWH + kNumWH * kWHStage;
 constexpr int kOffTab = kOffT2 + kT2A + kT2B;
 constexpr int kOffBar = kOffTab + kNumTab * kTabStage;
 constexpr int kNumBars = 2 * kNumA + 2 * kNumB + 2 * kNumWH + 2 * kNumWN + 3 + 2 * kNumTm + 2 * kNumTab;
-constexpr int kOffMisc = kOffBar + kNumBars * 8;   // tmem slot, abort flag
+constexpr int kOffMisc = kOffBar + kNumBars * 8;   // tmem slot, abort flag, scratch word
 constexpr int kSmemBytes = kOffMisc + 16 + 1024;   // + alignment slack
 static_assert(kOffB % 1024 == 0 && kOffWN % 1024 == 0 && kOffT2 % 1024 == 0, "operand tiles need 1024-byte alignment");
 static_assert(kSmemBytes <= 232448, "shared memory budget");
@@ -416,6 +416,7 @@ gemm_sb_kernel(const __grid_constant__ TmaMaps maps, const float* __restrict__ g
                     scl[1] = z1 ? 0u : sc_lo4(h1.y);
                     sch[1] = z1 ? 0u : sc_hi4(h1.y, h1.w);
                 }
+                loads_done(sbase + kOffMisc + 8, scl[0] ^ sch[0] ^ scl[1] ^ sch[1]);
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bars.wh_empty(hr.slot));
                 hr.next();
@@ -430,6 +431,10 @@ gemm_sb_kernel(const __grid_constant__ TmaMaps maps, const float* __restrict__ g
                         nq[0][1] = ld_shared_v4(nb + uint32_t(t) * 32u + 16u);
                         nq[1][0] = ld_shared_v4(nb + uint32_t(t + 128) * 32u);
                         nq[1][1] = ld_shared_v4(nb + uint32_t(t + 128) * 32u + 16u);
+                        loads_done(sbase + kOffMisc + 8,
+                                   nq[0][0].x ^ nq[0][0].y ^ nq[0][0].z ^ nq[0][0].w ^ nq[0][1].x ^ nq[0][1].y ^
+                                       nq[0][1].z ^ nq[0][1].w ^ nq[1][0].x ^ nq[1][0].y ^ nq[1][0].z ^ nq[1][0].w ^
+                                       nq[1][1].x ^ nq[1][1].y ^ nq[1][1].z ^ nq[1][1].w);
                         __syncwarp();
                         if (lane == 0) mbar_arrive(bars.wn_empty(nr.slot));
                         nr.next();

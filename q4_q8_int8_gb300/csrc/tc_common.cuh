@@ -87,6 +87,14 @@ __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
     return v;
 }
 
+// Completes this thread's shared-memory loads that produced v before what
+// follows, through a store that depends on them (to a scratch word).  A
+// release arrival that frees a ring slot for its next TMA copy goes after it:
+// the arrival alone does not wait for a load still queued behind other
+// shared-memory traffic, and the copy could land under it.
+__device__ __forceinline__ void loads_done(uint32_t scratch, uint32_t v) {
+    asm volatile("st.shared.u32 [%0], %1;" ::"r"(scratch), "r"(v) : "memory");
+}
 __device__ __forceinline__ void st_shared_u32(uint32_t addr, uint32_t v) {
     asm volatile("st.shared.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
