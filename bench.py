@@ -43,7 +43,10 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 WORKLOADS = {"q_proj": (2048, 4096, 4096)}
-PATH_NAMES = ("auto", "mma_s8", "tc", "small_m")
+PATH_NAMES = ("auto", "mma_s8", "tc", "small_m", "sb")
+# "sb": the step runs the tensor-core prepass (q8_1 plus the operand plane) and
+# the super-block GEMM on it (mmq_quantize_q8_1_tcop + mmq_q4K_gemm_tcop).
+SB = "sb"
 # A timed region shorter than this is held to the burst tensor peak, a longer
 # one to the sustained peak (the GPU settles at its power cap within seconds).
 SUSTAINED_AFTER_S = 1.0
@@ -364,12 +367,16 @@ def run_reference(args, rank, world):
 
 # ----------------------------------------------------------------- GPU leg
 def path_code(mmq, name):
+    """The mmq_q4K_gemm_path code of a path name; SB for the super-block GEMM,
+    which has its own entry point."""
     return {"auto": mmq.MMQ_PATH_AUTO, "mma_s8": mmq.MMQ_PATH_MMA_S8, "tc": mmq.MMQ_PATH_TC,
-            "small_m": mmq.MMQ_PATH_SMALL_M}[name]
+            "small_m": mmq.MMQ_PATH_SMALL_M, SB: SB}[name]
 
 
 def resolved_path(mmq, path, M):
     """The kernel family mmq_q4K_gemm runs for `path` at M tokens."""
+    if path == SB:
+        return SB
     if path == mmq.MMQ_PATH_AUTO:
         return mmq.MMQ_PATH_SMALL_M if M <= mmq.SMALL_M_MAX else mmq.MMQ_PATH_TC
     return path
@@ -432,17 +439,29 @@ def run_sweep(mmq, dev, peaks, path_name):
         path = path_code(mmq, path_name)
         if path == mmq.MMQ_PATH_SMALL_M and M > mmq.SMALL_M_MAX:
             continue
-        set_bytes = 0.5625 * N * K + 1.25 * M * K + 4 * M * N
+        # the super-block GEMM reads the operand plane (4 B per activation) instead of the int8 quants
+        set_bytes = 0.5625 * N * K + (4.0 if path == SB else 1.25) * M * K + 4 * M * N
         R = min(64, max(2, int(np.ceil(2 * L2_BYTES / set_bytes)) + 1))
         ws = [synthetic.torch_q4K_weights(N, K, 9100 + r, dev).view(-1) for r in range(R)]
-        aqs = [mmq.quantize_q8_1(synthetic.torch_activations(M, K, 9200 + r, dev, 0.01)) for r in range(R)]
+        xs_ = [synthetic.torch_activations(M, K, 9200 + r, dev, 0.01) for r in range(R)]
+        if path == SB:
+            pre = [mmq.quantize_q8_1_tcop(x) for x in xs_]
+            tcops = [t for _, t in pre]
+            aqs = [aq for aq, _ in pre]
+        else:
+            aqs = [mmq.quantize_q8_1(x) for x in xs_]
+        del xs_
         Cs = [torch.empty((M, N), dtype=torch.float32, device=dev) for _ in range(R)]
         structs = [mmq.q8_1_struct(*aq) for aq in aqs]
 
         def call(i, stream):
             r = i % R
-            rc = mmq.mmq_q4K_gemm_path(structs[r], ctypes.c_void_p(ws[r].data_ptr()),
-                                       ctypes.c_void_p(Cs[r].data_ptr()), M, N, K, path, mmq._stream_ptr(stream))
+            if path == SB:
+                rc = mmq.mmq_q4K_gemm_tcop(ctypes.c_void_p(tcops[r].data_ptr()), ctypes.c_void_p(ws[r].data_ptr()),
+                                           ctypes.c_void_p(Cs[r].data_ptr()), M, N, K, mmq._stream_ptr(stream))
+            else:
+                rc = mmq.mmq_q4K_gemm_path(structs[r], ctypes.c_void_p(ws[r].data_ptr()),
+                                           ctypes.c_void_p(Cs[r].data_ptr()), M, N, K, path, mmq._stream_ptr(stream))
             if rc:
                 raise mmq.MMQError(rc, "mmq_q4K_gemm_path")
 
@@ -456,9 +475,11 @@ def run_sweep(mmq, dev, peaks, path_name):
                       "us_per_gmac": ms * 1e3 / (macs / 1e9),
                       "gbs": set_bytes / (ms * 1e-3) / 1e9, "bound": bound,
                       "t_roof_us": t_roof * 1e6, "roof_frac": t_roof / (ms * 1e-3),
-                      "kernels_per_call": mmq.mmq_q4K_gemm_launches(M, N, K, path),
+                      "kernels_per_call": 1 if path == SB else mmq.mmq_q4K_gemm_launches(M, N, K, path),
                       "rotating_sets": R, "reps": reps}
         del ws, aqs, Cs, structs
+        if path == SB:
+            del pre, tcops
         torch.cuda.empty_cache()
     return res
 
@@ -480,6 +501,7 @@ def run_stack(mmq, dev, path_name, passes=2):
             weights.append((K, N, synthetic.torch_q4K_weights(N, K, ws, dev).view(-1)))
     xs = {K: [synthetic.torch_activations(T, K, 9300 + K + r, dev, 0.01) for r in range(8)] for K in (4096, 11008)}
     q8 = {K: mmq.empty_q8_1(T, K, dev) for K in (4096, 11008)}
+    tcop = {K: mmq.empty_tcop(T, K, dev) for K in (4096, 11008)} if path == SB else None
     C = torch.empty((T, 11008), dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
     sp = mmq._stream_ptr(stream)
@@ -488,9 +510,15 @@ def run_stack(mmq, dev, path_name, passes=2):
         for i, (K, N, w) in enumerate(weights):
             x = xs[K][i % 8]
             aq = mmq.q8_1_struct(*q8[K])
-            rc = mmq.mmq_quantize_q8_1(ctypes.c_void_p(x.data_ptr()), T, K, aq, sp)
-            rc |= mmq.mmq_q4K_gemm_path(aq, ctypes.c_void_p(w.data_ptr()), ctypes.c_void_p(C.data_ptr()),
-                                        T, N, K, path, sp)
+            if path == SB:
+                tp = ctypes.c_void_p(tcop[K].data_ptr())
+                rc = mmq.mmq_quantize_q8_1_tcop(ctypes.c_void_p(x.data_ptr()), T, K, aq, tp, sp)
+                rc |= mmq.mmq_q4K_gemm_tcop(tp, ctypes.c_void_p(w.data_ptr()), ctypes.c_void_p(C.data_ptr()),
+                                            T, N, K, sp)
+            else:
+                rc = mmq.mmq_quantize_q8_1(ctypes.c_void_p(x.data_ptr()), T, K, aq, sp)
+                rc |= mmq.mmq_q4K_gemm_path(aq, ctypes.c_void_p(w.data_ptr()), ctypes.c_void_p(C.data_ptr()),
+                                            T, N, K, path, sp)
             if rc:
                 raise RuntimeError(f"stack call failed: {rc}")
 
@@ -513,7 +541,7 @@ def run_stack(mmq, dev, path_name, passes=2):
            "weights_gb": sum(w.numel() for _, _, w in weights) / 1e9,
            "what": "32 layers x (q, k, v, o, gate, up, down) at 2048 tokens, a q8_1 prepass per GEMM, "
                    "224 independent weight matrices resident"}
-    del weights, xs, q8, C
+    del weights, xs, q8, tcop, C
     torch.cuda.empty_cache()
     return out
 
@@ -536,14 +564,18 @@ def run_mine(args, rank, world, local_rank):
     M, K, N = WORKLOADS[args.workload]
     # Inputs: R independent sets rotated step by step so that every step reads
     # its inputs from HBM (R sets together exceed twice the 129 MB L2).
-    set_bytes = M * K * 4 + M * K * 1.25 + N * K * 0.5625 + M * N * 4
+    sb = path == SB
+    plane = 4.0 * M * K if sb else 0.0   # the super-block path's operand plane (written, then read)
+    set_bytes = M * K * 4 + M * K * 1.25 + plane + N * K * 0.5625 + M * N * 4
     R = max(2, int(np.ceil(2 * L2_BYTES / set_bytes)) + 1)
-    xs, ws, aqs, Cs = [], [], [], []
+    xs, ws, aqs, Cs, tcops = [], [], [], [], []
     for r in range(R):
         xs.append(synthetic.torch_activations(M, K, 7000 + 97 * rank + r, dev, 0.01))
         ws.append(synthetic.torch_q4K_weights(N, K, 8000 + 97 * rank + r, dev).view(-1))
         aqs.append(mmq.empty_q8_1(M, K, dev))
         Cs.append(torch.empty((M, N), dtype=torch.float32, device=dev))
+        if sb:
+            tcops.append(mmq.empty_tcop(M, K, dev))
     stream = torch.cuda.current_stream(dev)
     sp = mmq._stream_ptr(stream)
     import ctypes
@@ -554,11 +586,19 @@ def run_mine(args, rank, world, local_rank):
         aq = mmq.q8_1_struct(qs, da, sa)
         if evs is not None:
             evs[0].record(stream)
-        rc = mmq.mmq_quantize_q8_1(ctypes.c_void_p(x.data_ptr()), M, K, aq, sp)
+        if sb:
+            tp = ctypes.c_void_p(tcops[r].data_ptr())
+            rc = mmq.mmq_quantize_q8_1_tcop(ctypes.c_void_p(x.data_ptr()), M, K, aq, tp, sp)
+        else:
+            rc = mmq.mmq_quantize_q8_1(ctypes.c_void_p(x.data_ptr()), M, K, aq, sp)
         if evs is not None:
             evs[1].record(stream)
-        rc |= mmq.mmq_q4K_gemm_path(aq, ctypes.c_void_p(w.data_ptr()), ctypes.c_void_p(C.data_ptr()),
-                                    M, N, K, path, sp)
+        if sb:
+            rc |= mmq.mmq_q4K_gemm_tcop(tp, ctypes.c_void_p(w.data_ptr()), ctypes.c_void_p(C.data_ptr()),
+                                        M, N, K, sp)
+        else:
+            rc |= mmq.mmq_q4K_gemm_path(aq, ctypes.c_void_p(w.data_ptr()), ctypes.c_void_p(C.data_ptr()),
+                                        M, N, K, path, sp)
         if evs is not None:
             evs[2].record(stream)
         if rc:
@@ -717,7 +757,7 @@ def run_mine(args, rank, world, local_rank):
     sweep = None
     stack = None
     if not args.no_sweep or not args.no_stack:
-        del xs, ws, aqs, Cs, ws_t
+        del xs, ws, aqs, Cs, ws_t, tcops
         torch.cuda.empty_cache()
     if not args.no_sweep:
         sweep = run_sweep(mmq, dev, peaks, args.path)
@@ -731,7 +771,8 @@ def run_mine(args, rank, world, local_rank):
     used_path = resolved_path(mmq, path, M)
     kname = {mmq.MMQ_PATH_MMA_S8: ("gemm_mma_s8", "gemm_mma.cu"),
              mmq.MMQ_PATH_TC: ("gemm_tc", "gemm_tc.cu"),
-             mmq.MMQ_PATH_SMALL_M: ("gemm_small_m", "gemm_small.cu")}[used_path]
+             mmq.MMQ_PATH_SMALL_M: ("gemm_small_m", "gemm_small.cu"),
+             SB: ("gemm_sb", "gemm_sb.cu")}[used_path]
     src_hash = kernel_source_hash([kname[1], "sm103_ptx.cuh", "tc_common.cuh", "q8_round.cuh"])
     traffic = recorded_traffic(kname[0], src_hash)
     alg_bytes = 0.5625 * N * K + 1.25 * M * K + 4 * M * N
@@ -743,7 +784,7 @@ def run_mine(args, rank, world, local_rank):
         roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
                 "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json hbm copy)"}
-    elif used_path == mmq.MMQ_PATH_TC:
+    elif used_path in (mmq.MMQ_PATH_TC, SB):
         # The exact integer contraction runs on the tensor pipe as kind::f16
         # MMAs (2 flops per MAC).  A timed region of milliseconds is held to
         # the burst bf16 (= f16 rate) peak; the sustained fraction is beside it.
@@ -766,7 +807,7 @@ def run_mine(args, rank, world, local_rank):
     roof["kernel"] = kname[0]
     # One GEMM call may be two kernels (the tcgen05 kernel's split-K tail
     # launch); "per launch" figures here are per call, both kernels together.
-    gemm_launches = mmq.mmq_q4K_gemm_launches(M, N, K, used_path)
+    gemm_launches = 1 if used_path == SB else mmq.mmq_q4K_gemm_launches(M, N, K, used_path)
     if gemm_launches < 1:
         raise RuntimeError(f"mmq_q4K_gemm_launches failed: {gemm_launches}")
     roof["kernels_per_call"] = gemm_launches
@@ -774,7 +815,9 @@ def run_mine(args, rank, world, local_rank):
     # output and 32-k chunk the tcgen05 kernel does one FMA (2 flops), plus
     # per super-block one FMA for d and one add of the second term (0.5 flop
     # per chunk); the other kernels do the pages' 1 FMUL + 2 FFMA (5 flops).
-    alu_flops = (2.5 if used_path == mmq.MMQ_PATH_TC else 5.0) * macs / 32
+    # (the super-block kernel: per output and super-block a multiply, an FMA
+    # and the second term's FMA: 6 flops per 256 k, under 0.75 per chunk)
+    alu_flops = {mmq.MMQ_PATH_TC: 2.5, SB: 0.75}.get(used_path, 5.0) * macs / 32
     alu_peak = micro["sms"] * 128 * 2 * sm_mhz * 1e6 / 1e12
     alu = {"flops_per_launch": alu_flops, "achieved_tflops": alu_flops / (g_ms * 1e-3) / 1e12,
            "peak_tflops": alu_peak, "frac": alu_flops / (g_ms * 1e-3) / 1e12 / alu_peak,
@@ -794,8 +837,10 @@ def run_mine(args, rank, world, local_rank):
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "int8xu4->f32 (fp16-exact ints on tensor cores)"
-        if used_path == mmq.MMQ_PATH_TC else "s8xs8->s32, f32 rescale",
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": {mmq.MMQ_PATH_TC: "int8xu4->f32 (fp16-exact ints on tensor cores)",
+                  SB: "fp16 hi+lo activations x fp16-exact sc*v -> f32 (tensor cores)"}.get(
+                      used_path, "s8xs8->s32, f32 rescale"),
         "data": "synthetic",
         "config": {"workload": f"{args.workload} M={M} K={K} N={N}", "global_batch_tokens": M * world,
                    "parallelism": f"independent problem per GPU x{world}",
@@ -810,8 +855,9 @@ def run_mine(args, rank, world, local_rank):
                                    "no tcgen05 integer MMA, and this kernel runs on the f16 tensor pipe, "
                                    "so the roofline fraction is the one in 'roofline'"},
         "epilogue_alu": alu,
-        "prepass": {"ms": q_ms, "gbs": (M * K * 4 + M * K * 1.25) / (q_ms * 1e-3) / 1e9,
-                    "frac_of_hbm": (M * K * 4 + M * K * 1.25) / (q_ms * 1e-3) / 1e9 / peaks["hbm_gbs"]},
+        "prepass": {"ms": q_ms, "gbs": (M * K * 5.25 + plane) / (q_ms * 1e-3) / 1e9,
+                    "frac_of_hbm": (M * K * 5.25 + plane) / (q_ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                    "bytes": M * K * 5.25 + plane},
         "roofline": roof,
         "cpu_baseline": cpu,
         "e2e": {"value": whole_job_tmacs(macs, world, e2e_ms), "unit": UNIT,
