@@ -587,7 +587,60 @@ gemm_tc_kernel(const __grid_constant__ TmaMaps maps, float* __restrict__ C, mmq_
             }
         }
     epi_done:;
-        if (split > 1) {
+        if (split > 1 && !kDump && !kQ8 && !kGlu) {
+            // Reduce-scatter over the cluster: rank r owns the tile's columns
+            // [r*W, (r+1)*W), W = BN / split.  Every thread pushes the columns
+            // it holds for another rank into that rank's (idle) staging memory,
+            // landing[src][row][W] f32; then each rank's owners add the split
+            // partials in rank order (the same additions, in the same order,
+            // as one rank pulling them all) and store their W columns.  Stores
+            // to a peer need no round trip, and the ranks reduce in parallel.
+            const int W = BN / split;                        // 64, 32 or 16
+            const int lw = W == 64 ? 6 : (W == 32 ? 5 : 4);   // log2 W
+            const int tile_m0 = (tile_first / tiles_n) * BM, tile_n0 = (tile_first % tiles_n) * BN;
+            const int64_t gr = int64_t(tile_m0) + row;
+            cluster_sync_all();   // every CTA of the cluster is done with its staging memory
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const int c = colhalf * 64 + 4 * i;   // first of this float4's columns in the tile
+                const int d = c >> lw;
+                if (d != rank) {
+                    const uint32_t off = uint32_t(((rank * BM + row) << lw) + (c - (d << lw))) * 4u;
+                    st_dsmem_v4(map_shared_rank(sbase + kOffRaw + off, uint32_t(d)),
+                                make_float4(lo_f(acc[2 * i]), hi_f(acc[2 * i]), lo_f(acc[2 * i + 1]),
+                                            hi_f(acc[2 * i + 1])));
+                }
+            }
+            cluster_sync_all();   // the pushed partials are visible
+            if (gr < M) {
+                float* crow = C + gr * N;
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const int c = colhalf * 64 + 4 * i;
+                    const int gc = tile_n0 + c;   // N % 4 == 0: all four columns or none
+                    if ((c >> lw) == rank && gc < N) {
+                        const float4 own = make_float4(lo_f(acc[2 * i]), hi_f(acc[2 * i]), lo_f(acc[2 * i + 1]),
+                                                       hi_f(acc[2 * i + 1]));
+                        float4 sum = own;
+                        for (int r = 0; r < split; ++r) {
+                            const float4 p =
+                                r == rank ? own
+                                          : ld_shared_v4f(sbase + kOffRaw +
+                                                          uint32_t(((r * BM + row) << lw) + (c - (rank << lw))) * 4u);
+                            if (r == 0) {
+                                sum = p;
+                            } else {
+                                sum.x += p.x;
+                                sum.y += p.y;
+                                sum.z += p.z;
+                                sum.w += p.w;
+                            }
+                        }
+                        *reinterpret_cast<float4*>(crow + gc) = sum;
+                    }
+                }
+            }
+        } else if (split > 1) {
             // Each rank leaves its partial tile in its own (now idle) staging
             // memory; rank 0 pulls ranks 1..split-1 in order and stores C.
             const int e = threadIdx.x - kEpiWarp0 * 32;   // 0..255

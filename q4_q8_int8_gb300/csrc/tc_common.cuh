@@ -86,6 +86,10 @@ __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
                  : "memory");
     return v;
 }
+__device__ __forceinline__ float4 ld_shared_v4f(uint32_t addr) {
+    const uint4 v = ld_shared_v4(addr);
+    return make_float4(__uint_as_float(v.x), __uint_as_float(v.y), __uint_as_float(v.z), __uint_as_float(v.w));
+}
 
 // Completes this thread's shared-memory loads that produced v before what
 // follows, through a store that depends on them (to a scratch word).  A
@@ -111,6 +115,13 @@ __device__ __forceinline__ uint32_t map_shared_rank(uint32_t saddr, uint32_t ran
     uint32_t d;
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(d) : "r"(saddr), "r"(rank));
     return d;
+}
+// Store to a peer CTA's shared memory (an address from map_shared_rank); no
+// round trip: the issuing thread does not wait for it.
+__device__ __forceinline__ void st_dsmem_v4(uint32_t addr, float4 v) {
+    asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(v.x), "f"(v.y), "f"(v.z),
+                 "f"(v.w)
+                 : "memory");
 }
 __device__ __forceinline__ float4 ld_dsmem_v4(uint32_t addr) {
     float4 v;
