@@ -354,14 +354,34 @@ int mmq_repack_q6K(const uint8_t* src, uint8_t* dst, int64_t N, int64_t K, void*
 
 /* C = A . W^T for q8_1 activations and q6_K weights in the device layout:
  * per 16-weight sub-block s of the 32-element q8_1 block c,
- * C_ij += da_ic * d_j * sc_js * S_ijs with S the exact int32 dot (warp-level
- * int8 tensor MMAs, K split over a cluster when tiles are few; for M <= 16
- * dp4a dot products streaming the weights).
- * Shape rules and tolerance as mmq_q4K_gemm. */
+ * C_ij += da_ic * d_j * sc_js * S_ijs with S the exact int32 dot.  M <= 16:
+ * dp4a dot products streaming the weights; above that the tcgen05 kernel
+ * (MMQ_PATH_TC below).  Shape rules and tolerance as mmq_q4K_gemm. */
 int mmq_q6K_gemm(mmq_q8_1_t aq, const uint8_t* bq6k_dev, float* C, int64_t M,
                  int64_t N, int64_t K, void* stream);
 
-/* The exact per-16 dots S int32 [M][N][K/16] of the same kernel. */
+/* The same with an explicit kernel family, for tests and A/B timing:
+ *   MMQ_PATH_SMALL_M  the dp4a dot-product kernel (M <= 16, else MMQ_ERR_ARG);
+ *   MMQ_PATH_MMA_S8   warp-level int8 mma.sync on 128 x 128 tiles, K split
+ *                     over a cluster when the tiles are few;
+ *   MMQ_PATH_TC       tcgen05: per 32-k chunk the exact S' = sum a * sc * q
+ *                     in f32 tensor memory from fp16 operands (sc * q split
+ *                     into an fp16 hi part and an exact lo part, both MMA'd),
+ *                     then C += da * d * S' (page r15, "Proof of pattern
+ *                     portability", for the family); persistent 128 x 128
+ *                     tiles as the q4_K kernel, up to two kernels per call;
+ *                     MMQ_ERR_RESOURCE if the shared-memory budget is missing;
+ *   MMQ_PATH_AUTO     what mmq_q6K_gemm runs.
+ * Errors as mmq_q4K_gemm_path. */
+int mmq_q6K_gemm_path(mmq_q8_1_t aq, const uint8_t* bq6k_dev, float* C, int64_t M,
+                      int64_t N, int64_t K, int path, void* stream);
+
+/* Kernels one mmq_q6K_gemm_path call enqueues for this shape: 1 or 2;
+ * MMQ_ERR_ARG / MMQ_ERR_CUDA as mmq_q4K_gemm_launches. */
+int mmq_q6K_gemm_launches(int64_t M, int64_t N, int64_t K, int path);
+
+/* The exact per-16 dots S int32 [M][N][K/16] from the mma.sync tile kernel's
+ * unpack and MMA code. */
 int mmq_q6K_block_dots(mmq_q8_1_t aq, const uint8_t* bq6k_dev, int32_t* S,
                        int64_t M, int64_t N, int64_t K, void* stream);
 

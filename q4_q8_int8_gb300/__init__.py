@@ -35,7 +35,7 @@ MMQ_GGUF_F32, MMQ_GGUF_F16, MMQ_GGUF_Q4_K, MMQ_GGUF_Q6_K = 0, 1, 12, 14
 # Every symbol include/mmq.h declares.
 EXPORTS = (
     "mmq_q8_1_bytes", "mmq_q8_1_view", "mmq_quantize_q8_1", "mmq_q4K_bytes",
-    "mmq_pack_q4K", "mmq_q4K_gemm", "mmq_q8_1_tcop_bytes", "mmq_quantize_q8_1_tcop", "mmq_q4K_gemm_tcop", "mmq_q4K_gemm_host_workspace", "mmq_q4K_gemm_host", "mmq_q4K_gemm_host_noalloc", "mmq_q4K_gemm_launches", "mmq_q4K_gemm_path", "mmq_q4K_gemm_q8_1", "mmq_q4K_block_dots", "mmq_q4K_scaled_block_dots",
+    "mmq_pack_q4K", "mmq_q4K_gemm", "mmq_q8_1_tcop_bytes", "mmq_quantize_q8_1_tcop", "mmq_q4K_gemm_tcop", "mmq_q6K_gemm_path", "mmq_q6K_gemm_launches", "mmq_q4K_gemm_host_workspace", "mmq_q4K_gemm_host", "mmq_q4K_gemm_host_noalloc", "mmq_q4K_gemm_launches", "mmq_q4K_gemm_path", "mmq_q4K_gemm_q8_1", "mmq_q4K_block_dots", "mmq_q4K_scaled_block_dots",
     "mmq_dequantize_q4K_f16", "mmq_convert_f32_f16", "mmq_gemm_f16",
     "mmq_q4K_gemm_swiglu_q8_1", "mmq_interleave_rows_q4K",
     "mmq_q6K_bytes", "mmq_pack_q6K", "mmq_q6K_dev_bytes", "mmq_repack_q6K", "mmq_q6K_gemm",
@@ -99,6 +99,8 @@ def load_library(path: str = LIB_PATH):
                 "mmq_q6K_dev_bytes": ([I, I], S),
                 "mmq_repack_q6K": ([P, P, I, I, P], ctypes.c_int),
                 "mmq_q6K_gemm": ([Q, P, P, I, I, I, P], ctypes.c_int),
+                "mmq_q6K_gemm_path": ([Q, P, P, I, I, I, ctypes.c_int, P], ctypes.c_int),
+                "mmq_q6K_gemm_launches": ([I, I, I, ctypes.c_int], ctypes.c_int),
                 "mmq_q6K_block_dots": ([Q, P, P, I, I, I, P], ctypes.c_int),
                 "mmq_gguf_open": ([ctypes.c_char_p, ctypes.POINTER(P)], ctypes.c_int),
                 "mmq_gguf_close": ([P], None),
@@ -430,6 +432,14 @@ def mmq_q6K_gemm(aq, w, C, M, N, K, stream):
     return load_library().mmq_q6K_gemm(aq, w, C, M, N, K, stream)
 
 
+def mmq_q6K_gemm_path(aq, w, C, M, N, K, path, stream):
+    return load_library().mmq_q6K_gemm_path(aq, w, C, M, N, K, path, stream)
+
+
+def mmq_q6K_gemm_launches(M, N, K, path):
+    return load_library().mmq_q6K_gemm_launches(M, N, K, path)
+
+
 def mmq_q6K_block_dots(aq, w, S, M, N, K, stream):
     return load_library().mmq_q6K_block_dots(aq, w, S, M, N, K, stream)
 
@@ -456,14 +466,14 @@ def repack_q6K(w, N: int, K: int, out=None, stream=None):
     return o
 
 
-def q6K_gemm(aq, w_dev, N: int, out=None, stream=None):
+def q6K_gemm(aq, w_dev, N: int, path: int = MMQ_PATH_AUTO, out=None, stream=None):
     """aq = (qs, da, sa); w_dev q6_K bytes in the device layout -> C float32 [M][N]."""
     import torch
     qs, da, sa = aq
     M, K = qs.shape
     C = out if out is not None else torch.empty((M, N), dtype=torch.float32, device=qs.device)
-    _check(mmq_q6K_gemm(q8_1_struct(qs, da, sa), ctypes.c_void_p(w_dev.data_ptr()), ctypes.c_void_p(C.data_ptr()),
-                        M, N, K, _stream_ptr(stream)), "mmq_q6K_gemm")
+    _check(mmq_q6K_gemm_path(q8_1_struct(qs, da, sa), ctypes.c_void_p(w_dev.data_ptr()),
+                             ctypes.c_void_p(C.data_ptr()), M, N, K, path, _stream_ptr(stream)), "mmq_q6K_gemm")
     return C
 
 

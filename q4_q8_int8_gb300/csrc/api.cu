@@ -381,11 +381,46 @@ int mmq_repack_q6K(const uint8_t* src, uint8_t* dst, int64_t N, int64_t K, void*
     return from_cuda(mmq::launch_repack_q6K(src, dst, N, K, static_cast<cudaStream_t>(stream)));
 }
 
-int mmq_q6K_gemm(mmq_q8_1_t aq, const uint8_t* bq6k_dev, float* C, int64_t M, int64_t N, int64_t K,
-                 void* stream) {
+// The q6_K kernel family for M tokens: the dot-product kernel for a few,
+// the tcgen05 kernel above that.
+static int q6k_auto_path(int64_t M) { return M <= mmq::kQ6GemvMax ? MMQ_PATH_SMALL_M : MMQ_PATH_TC; }
+
+int mmq_q6K_gemm_path(mmq_q8_1_t aq, const uint8_t* bq6k_dev, float* C, int64_t M, int64_t N, int64_t K,
+                      int path, void* stream) {
+    if (!known_path(path)) return MMQ_ERR_ARG;
     int rc = check_gemm_args(aq, bq6k_dev, C, M, N, K);
     if (rc) return rc;
-    return from_cuda(mmq::launch_gemm_q6k(aq, bq6k_dev, C, nullptr, M, N, K, static_cast<cudaStream_t>(stream)));
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (path == MMQ_PATH_AUTO) path = q6k_auto_path(M);
+    switch (path) {
+        case MMQ_PATH_SMALL_M:
+            if (M > mmq::kQ6GemvMax) return MMQ_ERR_ARG;
+            return from_cuda(mmq::launch_gemm_q6k(aq, bq6k_dev, C, nullptr, M, N, K, s));
+        case MMQ_PATH_MMA_S8:
+            return from_cuda(mmq::launch_gemm_q6k(aq, bq6k_dev, C, nullptr, M, N, K, s, false));
+        default: {   // MMQ_PATH_TC
+            if ((rc = mmq::q6k_tc_check_resources())) return rc;
+            int* status = mmq::status_word_ptr();
+            if (!status) return MMQ_ERR_CUDA;
+            const int inject = t_inject_timeout;
+            t_inject_timeout = 0;
+            return from_cuda(mmq::launch_gemm_q6k_tc(aq, bq6k_dev, C, M, N, K, status, inject, s));
+        }
+    }
+}
+
+int mmq_q6K_gemm(mmq_q8_1_t aq, const uint8_t* bq6k_dev, float* C, int64_t M, int64_t N, int64_t K,
+                 void* stream) {
+    return mmq_q6K_gemm_path(aq, bq6k_dev, C, M, N, K, MMQ_PATH_AUTO, stream);
+}
+
+int mmq_q6K_gemm_launches(int64_t M, int64_t N, int64_t K, int path) {
+    if (!known_path(path) || M < 1 || N < 1 || K < 256 || (K % 256) != 0) return MMQ_ERR_ARG;
+    if (path == MMQ_PATH_AUTO) path = q6k_auto_path(M);
+    if (path == MMQ_PATH_SMALL_M && M > mmq::kQ6GemvMax) return MMQ_ERR_ARG;
+    if (path != MMQ_PATH_TC) return 1;
+    const int n = mmq::q6k_tc_launch_count(M, N, K);
+    return n < 0 ? MMQ_ERR_CUDA : n;
 }
 
 int mmq_q6K_block_dots(mmq_q8_1_t aq, const uint8_t* bq6k_dev, int32_t* S, int64_t M, int64_t N, int64_t K,

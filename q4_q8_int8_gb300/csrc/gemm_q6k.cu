@@ -474,8 +474,8 @@ cudaError_t launch_repack_q6K(const uint8_t* src, uint8_t* dst, int64_t N, int64
 }
 
 cudaError_t launch_gemm_q6k(mmq_q8_1_t aq, const uint8_t* w, float* C, int32_t* S, int64_t M, int64_t N,
-                            int64_t K, cudaStream_t s) {
-    if (!S && M <= 16) {   // a few tokens: the dot-product kernel
+                            int64_t K, cudaStream_t s, bool allow_gemv) {
+    if (!S && allow_gemv && M <= kQ6GemvMax) {   // a few tokens: the dot-product kernel
         if (M == 1) return launch_gemv_q6k<1>(aq, w, C, M, N, K, s);
         if (M == 2) return launch_gemv_q6k<2>(aq, w, C, M, N, K, s);
         if (M <= 4) return launch_gemv_q6k<4>(aq, w, C, M, N, K, s);

@@ -135,8 +135,17 @@ cudaError_t launch_gemm_f16(const uint16_t* A, const uint16_t* B, float* C, int6
                             int64_t K, int* status, cudaStream_t s);
 // q6_K x q8_1 (gemm_q6k.cu): S != nullptr dumps the per-16 dots instead of C.
 cudaError_t launch_repack_q6K(const uint8_t* src, uint8_t* dst, int64_t N, int64_t K, cudaStream_t s);
+// allow_gemv: M <= 16 (C only) takes the dp4a dot-product kernel; false forces
+// the mma.sync tile kernel.
 cudaError_t launch_gemm_q6k(mmq_q8_1_t aq, const uint8_t* w, float* C, int32_t* S, int64_t M,
-                            int64_t N, int64_t K, cudaStream_t s);
+                            int64_t N, int64_t K, cudaStream_t s, bool allow_gemv = true);
+constexpr int64_t kQ6GemvMax = 16;
+// q6_K on tcgen05 (gemm_q6k_tc.cu): C only, the same 128 x 128 tile plan as
+// the q4_K kernel (tc_plan), one or two kernels per call.
+int q6k_tc_check_resources();   // MMQ_OK or MMQ_ERR_RESOURCE
+int q6k_tc_launch_count(int64_t M, int64_t N, int64_t K);
+cudaError_t launch_gemm_q6k_tc(mmq_q8_1_t aq, const uint8_t* w, float* C, int64_t M, int64_t N, int64_t K,
+                               int* status, int inject_timeout, cudaStream_t s);
 constexpr int64_t kSmallMMax = 64;
 
 }  // namespace mmq
