@@ -19,6 +19,7 @@ After the contract line's timed region, and outside it, rank 0 adds:
            GEMMs at 2K tokens, the token-count sweep at 4096 x 4096 and the
            few-token decode shapes), each replayed from a CUDA graph over
            rotating inputs larger than twice the L2, with t_roof / t;
+           "sweep_q6k" the same for q6_K weights;
   "stack"  the 32-layer 7B prefill linear stack (224 GEMMs, a prepass each)
            as equivalent tokens per second;
   "clocks" sampled from the warm-up to the end of a ~1 s soak of the same
@@ -75,6 +76,11 @@ def parse():
     ap.add_argument("--no-stack", action="store_true", help="skip the 32-layer stack")
     ap.add_argument("--soak-seconds", type=float, default=1.0,
                     help="seconds of the step loop run after the timed region for the clock record")
+    ap.add_argument("--shape", default=None, metavar="M:K:N",
+                    help="profiling mode: run one GEMM shape --launches times on --path (or the q6_K kernels "
+                         "with --weights q6k) and exit; no timing line (a target for ncu captures)")
+    ap.add_argument("--weights", default="q4k", choices=["q4k", "q6k"])
+    ap.add_argument("--launches", type=int, default=5)
     ap.add_argument("--measure-peaks", action="store_true",
                     help="compile and run bench_peaks.cu (instruction-rate peaks) and exit")
     ap.add_argument("--oracle-table", action="store_true",
@@ -484,6 +490,55 @@ def run_sweep(mmq, dev, peaks, path_name):
     return res
 
 
+def run_sweep_q6k(mmq, dev, peaks):
+    """Kernel-only q6_K GEMM times (mmq_q6K_gemm, the automatic kernel: dp4a up
+    to 16 tokens, tcgen05 above), graph-replayed over rotating inputs."""
+    import ctypes
+    import torch
+    from q4_q8_int8_gb300 import synthetic
+    res = {}
+    for label, M, K, N in (("q6k_M1", 1, 4096, 4096), ("q6k_M128", 128, 4096, 4096),
+                           ("q6k_q_proj", 2048, 4096, 4096), ("q6k_down", 2048, 11008, 4096)):
+        wbytes = 210.0 / 256.0 * N * K
+        set_bytes = wbytes + 1.25 * M * K + 4 * M * N
+        R = min(64, max(2, int(np.ceil(2 * L2_BYTES / set_bytes)) + 1))
+        ws = []
+        for r in range(R):
+            g = torch.Generator(device=dev)
+            g.manual_seed(9700 + r)
+            raw = torch.randint(0, 256, (N, K // 256, 210), dtype=torch.uint8, device=dev, generator=g)
+            raw[:, :, 208] = 0x00
+            raw[:, :, 209] = 0x1c   # d = 2^-8 (fp16 0x1c00)
+            ws.append(mmq.repack_q6K(raw.view(-1), N, K))
+            del raw
+        aqs = [mmq.quantize_q8_1(synthetic.torch_activations(M, K, 9800 + r, dev, 0.01)) for r in range(R)]
+        Cs = [torch.empty((M, N), dtype=torch.float32, device=dev) for _ in range(R)]
+        structs = [mmq.q8_1_struct(*aq) for aq in aqs]
+
+        def call(i, stream):
+            r = i % R
+            rc = mmq.mmq_q6K_gemm(structs[r], ctypes.c_void_p(ws[r].data_ptr()), ctypes.c_void_p(Cs[r].data_ptr()),
+                                  M, N, K, mmq._stream_ptr(stream))
+            if rc:
+                raise mmq.MMQError(rc, "mmq_q6K_gemm")
+
+        reps = int(max(2 * R, min(400, 20e-3 / max(set_bytes / 6e12, 2e-6))))
+        ms = graph_time_ms(call, reps, dev)
+        if mmq.status() != 0:
+            raise RuntimeError(f"device status error in sweep {label}")
+        t_hbm = set_bytes / (peaks["hbm_gbs"] * 1e9)
+        t_tc = 2.0 * M * N * K / (peaks["bf16_tflops"] * 1e12)
+        macs = M * N * K
+        res[label] = {"M": M, "K": K, "N": N, "us": ms * 1e3, "tmacs": macs / (ms * 1e-3) / 1e12,
+                      "bound": "hbm" if t_hbm >= t_tc else "tensor", "t_roof_us": max(t_hbm, t_tc) * 1e6,
+                      "roof_frac": max(t_hbm, t_tc) / (ms * 1e-3),
+                      "kernels_per_call": mmq.mmq_q6K_gemm_launches(M, N, K, mmq.MMQ_PATH_AUTO),
+                      "rotating_sets": R, "reps": reps}
+        del ws, aqs, Cs, structs
+        torch.cuda.empty_cache()
+    return res
+
+
 def run_stack(mmq, dev, path_name, passes=2):
     """The 7B prefill linear stack: 32 layers x {q, k, v, o 4096->4096; gate,
     up 4096->11008; down 11008->4096} at 2048 tokens, every GEMM with its own
@@ -759,8 +814,10 @@ def run_mine(args, rank, world, local_rank):
     if not args.no_sweep or not args.no_stack:
         del xs, ws, aqs, Cs, ws_t, tcops
         torch.cuda.empty_cache()
+    sweep_q6k = None
     if not args.no_sweep:
         sweep = run_sweep(mmq, dev, peaks, args.path)
+        sweep_q6k = run_sweep_q6k(mmq, dev, peaks)
     if not args.no_stack:
         stack = run_stack(mmq, dev, args.path)
 
@@ -877,6 +934,9 @@ def run_mine(args, rank, world, local_rank):
                       "rotating inputs > 2x L2; roof_frac = t_roof / t with t_roof = max(algorithmic bytes / "
                       "measured HBM, 2MNK / measured burst bf16)",
         "stack": stack,
+        "sweep_q6k": sweep_q6k,
+        "sweep_q6k_note": "q6_K weights (the pages' next family): kernel-only mmq_q6K_gemm, graph replay over rotating "
+                          "inputs > 2x L2; roof_frac as in sweep with 210 / 256 bytes per weight",
     }
     print(json.dumps(line), flush=True)
     if world > 1:
@@ -894,10 +954,62 @@ def measure_peaks():
     subprocess.run([exe], check=True)
 
 
+def run_shape(args):
+    """Profiling mode: prepass + GEMM of one seeded shape, --launches times,
+    then the device status (a command line for ncu -k ... -s ... -c ...)."""
+    import ctypes
+    import torch
+    import q4_q8_int8_gb300 as mmq
+    from q4_q8_int8_gb300 import build as mmq_build, synthetic
+    M, K, N = (int(v) for v in args.shape.split(":"))
+    dev = torch.device("cuda", 0)
+    mmq_build.build()
+    mmq.load_library()
+    mmq.mmq_set_programmatic_launch(0 if args.no_pdl else 1)
+    x = synthetic.torch_activations(M, K, 9500, dev, 0.01)
+    C = torch.empty((M, N), dtype=torch.float32, device=dev)
+    sp = mmq._stream_ptr()
+    if args.weights == "q6k":
+        g = torch.Generator(device=dev)
+        g.manual_seed(9600)
+        raw = torch.randint(0, 256, (N, K // 256, 210), dtype=torch.uint8, device=dev, generator=g)
+        raw[:, :, 208] = 0x00
+        raw[:, :, 209] = 0x1c   # d = 2^-8 (fp16 0x1c00)
+        w = mmq.repack_q6K(raw.view(-1), N, K)
+        path = path_code(mmq, args.path if args.path != SB else "auto")
+        gemm = lambda aq: mmq.mmq_q6K_gemm_path(mmq.q8_1_struct(*aq), ctypes.c_void_p(w.data_ptr()),
+                                                ctypes.c_void_p(C.data_ptr()), M, N, K, path, sp)
+        prep = lambda: (mmq.quantize_q8_1(x), None)
+    else:
+        w = synthetic.torch_q4K_weights(N, K, 9600, dev).view(-1)
+        path = path_code(mmq, args.path)
+        if path == SB:
+            prep = lambda: mmq.quantize_q8_1_tcop(x)
+            gemm = lambda aq, t=None: mmq.mmq_q4K_gemm_tcop(ctypes.c_void_p(t.data_ptr()), ctypes.c_void_p(w.data_ptr()),
+                                                            ctypes.c_void_p(C.data_ptr()), M, N, K, sp)
+        else:
+            prep = lambda: (mmq.quantize_q8_1(x), None)
+            gemm = lambda aq, t=None: mmq.mmq_q4K_gemm_path(mmq.q8_1_struct(*aq), ctypes.c_void_p(w.data_ptr()),
+                                                            ctypes.c_void_p(C.data_ptr()), M, N, K, path, sp)
+    for _ in range(args.launches):
+        aq, t = prep()
+        rc = gemm(aq) if args.weights == "q6k" else gemm(aq, t)
+        if rc:
+            raise RuntimeError(f"GEMM call failed: {rc}")
+    torch.cuda.synchronize()
+    st = mmq.status()
+    print(json.dumps({"shape": args.shape, "weights": args.weights, "path": args.path, "launches": args.launches,
+                      "status": st}), flush=True)
+    if st != 0:
+        raise SystemExit(1)
+
+
 def main():
     args = parse()
     if args.measure_peaks:
         return measure_peaks()
+    if args.shape:
+        return run_shape(args)
     rank, world, local_rank = dist_env()
     if args.impl == "reference":
         run_reference(args, rank, world)
