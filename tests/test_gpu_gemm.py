@@ -199,6 +199,20 @@ def test_gemm_full_size_sampled(path_name, name):
     assert np.isfinite(C).all()
 
 
+def test_q_proj_every_element():
+    # the headline workload, every one of its 8.4 M outputs against the oracle
+    # (the oracle's full C and bound take a few seconds on the host's cores)
+    mmq = require_gpu()
+    x, blk, N = synthetic.config_inputs("q_proj")
+    _, aq, w = _dev_inputs(x, blk)
+    C = mmq.q4K_gemm(aq, w, N).cpu().numpy()
+    assert mmq.status() == 0
+    q, da, sa = oracle.quantize_q8_1(x)
+    C_ref, _, T = oracle.gemm(q, da, sa, blk, N)
+    ok = oracle.within_tolerance(C, C_ref, T, RTOL, ATOL)
+    assert ok.all(), f"{(~ok).sum()} of {ok.size} outputs outside tolerance"
+
+
 @pytest.mark.parametrize("M", synthetic.SWEEP_M)
 def test_gemm_sweep_auto_sampled(M):
     mmq = require_gpu()

@@ -102,6 +102,24 @@ def test_q6k_tc_full_size_sampled(name):
     assert ok.all(), f"{(~ok).sum()} sampled outputs outside tolerance"
 
 
+def test_q6k_tc_q_proj_every_element():
+    # every output at q-proj against the oracle's brute-force dequantized dot
+    # (float64 BLAS over the same a = da * q and w = d * sc * q; pinned to the
+    # blockwise form in the oracle tests), with T = |a| . |w|^T
+    M, K, N = synthetic.SHAPES["q_proj"]
+    x = synthetic.activations(M, K, 731, 0.01)
+    blk = synthetic.q6K_weights(N, K, 741)
+    mmq, w_dev, aq = _setup(blk, N, K, x)
+    C = mmq.q6K_gemm(aq, w_dev, N, path=mmq.MMQ_PATH_TC).cpu().numpy()
+    assert mmq.status() == 0
+    q, da, _ = oracle.quantize_q8_1(x)
+    D = q6k.dequant_dot(q, da, blk, N)
+    a = np.repeat(da.astype(np.float64), 32, axis=1) * q.astype(np.float64)
+    T = np.abs(a) @ np.abs(q6k.dequant_q6K(blk, N, K)).T
+    ok = np.abs(C.astype(np.float64) - D) <= RTOL * T + ATOL
+    assert ok.all(), f"{(~ok).sum()} of {ok.size} outputs outside tolerance"
+
+
 def test_q6k_tc_every_output_written_and_deterministic():
     import torch
     M, N, K = 300, 516, 1024

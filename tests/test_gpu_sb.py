@@ -187,6 +187,20 @@ def test_full_size_sampled(name):
     assert np.isfinite(C).all()
 
 
+def test_q_proj_every_element():
+    # every output of the headline workload through the operand plane
+    mmq = require_gpu()
+    x, blk, N = synthetic.config_inputs("q_proj")
+    M, K = x.shape
+    _, tcop = mmq.quantize_q8_1_tcop(to_dev(x))
+    C = mmq.q4K_gemm_tcop(tcop, to_dev(blk.reshape(-1)), M, N, K).cpu().numpy()
+    assert mmq.status() == 0
+    q, da, sa = oracle.quantize_q8_1(x)
+    C_ref, _, T = oracle.gemm(q, da, sa, blk, N)
+    ok = oracle.within_tolerance(C, C_ref, T, RTOL, ATOL)
+    assert ok.all(), f"{(~ok).sum()} of {ok.size} outputs outside tolerance"
+
+
 def test_argument_errors():
     import torch
     mmq = require_gpu()

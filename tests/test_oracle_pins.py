@@ -361,6 +361,63 @@ def test_ffn_silu_closed_forms():
     assert np.allclose(ffn.swiglu(g, u), [3.0 / (1 + np.exp(-1.0)), 0.5 * -2.0 / (1 + np.exp(2.0))])
 
 
+def test_ffn_swiglu_bound_lipschitz_constant():
+    # the bound uses |silu'| <= 1.1: silu'(g) = s(g) (1 + g (1 - s(g))), s the
+    # logistic function, peaks at 1.0998... near g = 2.40 and tends to 1 and 0
+    from oracle import ffn
+    g = np.linspace(-60.0, 60.0, 1_200_001)
+    sg = 1.0 / (1.0 + np.exp(-g))
+    d = sg * (1.0 + g * (1.0 - sg))
+    assert d.max() < 1.1 and d.max() > 1.099
+    assert d.min() > -0.1 - 1e-12 and d.min() < -0.099   # the negative lobe near g = -2.40
+    # the closed-form derivative agrees with a difference quotient of ffn.silu
+    h = 1e-6
+    gs = np.linspace(-30.0, 30.0, 6001)
+    fd = (ffn.silu(gs + h) - ffn.silu(gs - h)) / (2 * h)
+    sgs = 1.0 / (1.0 + np.exp(-gs))
+    assert np.allclose(fd, sgs * (1.0 + gs * (1.0 - sgs)), rtol=0, atol=1e-8)
+
+
+def test_ffn_swiglu_bound_holds_for_perturbed_inputs():
+    # |h(g', u') - h(g, u)| <= bound for every |g' - g| <= Eg, |u' - u| <= Eu
+    # (the corners of the box and random points inside it), without the
+    # rounding allowance: the Lipschitz part of the bound alone must hold
+    from oracle import ffn
+    rng = np.random.default_rng(901)
+    n = 200_000
+    g = rng.normal(0, 4, n) * np.where(rng.random(n) < 0.1, 10.0, 1.0)
+    u = rng.normal(0, 4, n)
+    Eg = np.abs(g) * 10.0 ** rng.uniform(-6, -1, n) + 1e-6
+    Eu = np.abs(u) * 10.0 ** rng.uniform(-6, -1, n) + 1e-6
+    h = ffn.swiglu(g, u)
+    lip = 1.1 * np.abs(u) * Eg + (np.abs(ffn.silu(g)) + 1.1 * Eg) * Eu
+    assert (ffn.swiglu_bound(g, u, Eg, Eu) >= lip).all()
+    for sgn_g, sgn_u in ((1, 1), (1, -1), (-1, 1), (-1, -1)):
+        dh = np.abs(ffn.swiglu(g + sgn_g * Eg, u + sgn_u * Eu) - h)
+        assert (dh <= lip * (1 + 1e-12) + 1e-300).all()
+    tg, tu = rng.uniform(-1, 1, n), rng.uniform(-1, 1, n)
+    dh = np.abs(ffn.swiglu(g + tg * Eg, u + tu * Eu) - h)
+    assert (dh <= lip * (1 + 1e-12) + 1e-300).all()
+    # the constant is needed: with |silu'| taken as 1 the bound fails somewhere
+    lip1 = np.abs(u) * Eg + (np.abs(ffn.silu(g)) + Eg) * Eu
+    worst = np.abs(ffn.swiglu(g + Eg, u) - h) - lip1
+    assert worst.max() > 0
+
+
+def test_ffn_swiglu_bound_covers_f32_evaluation():
+    # the rounding allowance 1e-6 |h| + 1e-6 covers h evaluated in f32 the way
+    # the epilogue does it (exp, add, divide, multiply), against float64
+    from oracle import ffn
+    rng = np.random.default_rng(902)
+    g = rng.normal(0, 6, 500_000).astype(np.float32)
+    u = rng.normal(0, 6, 500_000).astype(np.float32)
+    with np.errstate(over="ignore"):
+        h32 = (g / (np.float32(1) + np.exp(-g))) * u
+    h64 = ffn.swiglu(g.astype(np.float64), u.astype(np.float64))
+    assert (np.abs(h32.astype(np.float64) - h64) <= 1e-6 * np.abs(h64) + 1e-6).all()
+    assert (ffn.swiglu_bound(g, u, 0.0, 0.0) == 1e-6 * np.abs(h64) + 1e-6).all()
+
+
 # ---------------------------------------------------------------------------
 # q6_K x q8_1: oracle.q6k
 # ---------------------------------------------------------------------------
