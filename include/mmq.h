@@ -376,6 +376,13 @@ int mmq_q6K_gemm(mmq_q8_1_t aq, const uint8_t* bq6k_dev, float* C, int64_t M,
 int mmq_q6K_gemm_path(mmq_q8_1_t aq, const uint8_t* bq6k_dev, float* C, int64_t M,
                       int64_t N, int64_t K, int path, void* stream);
 
+/* The tcgen05 q6_K kernel's exact per-chunk dots from its own operands:
+ * S int32 [M][N][K/32], S_ijc = sum over the chunk's two 16-weight
+ * sub-blocks s of sc_js * S16_ijs (the products a * sc * q summed exactly;
+ * |S| <= 32 * 127 * 4096 < 2^24).  Shape rules and errors as mmq_q6K_gemm. */
+int mmq_q6K_scaled_block_dots(mmq_q8_1_t aq, const uint8_t* bq6k_dev, int32_t* S,
+                              int64_t M, int64_t N, int64_t K, void* stream);
+
 /* Kernels one mmq_q6K_gemm_path call enqueues for this shape: 1 or 2;
  * MMQ_ERR_ARG / MMQ_ERR_CUDA as mmq_q4K_gemm_launches. */
 int mmq_q6K_gemm_launches(int64_t M, int64_t N, int64_t K, int path);

@@ -35,7 +35,7 @@ MMQ_GGUF_F32, MMQ_GGUF_F16, MMQ_GGUF_Q4_K, MMQ_GGUF_Q6_K = 0, 1, 12, 14
 # Every symbol include/mmq.h declares.
 EXPORTS = (
     "mmq_q8_1_bytes", "mmq_q8_1_view", "mmq_quantize_q8_1", "mmq_q4K_bytes",
-    "mmq_pack_q4K", "mmq_q4K_gemm", "mmq_q8_1_tcop_bytes", "mmq_quantize_q8_1_tcop", "mmq_q4K_gemm_tcop", "mmq_q6K_gemm_path", "mmq_q6K_gemm_launches", "mmq_q4K_gemm_host_workspace", "mmq_q4K_gemm_host", "mmq_q4K_gemm_host_noalloc", "mmq_q4K_gemm_launches", "mmq_q4K_gemm_path", "mmq_q4K_gemm_q8_1", "mmq_q4K_block_dots", "mmq_q4K_scaled_block_dots",
+    "mmq_pack_q4K", "mmq_q4K_gemm", "mmq_q8_1_tcop_bytes", "mmq_quantize_q8_1_tcop", "mmq_q4K_gemm_tcop", "mmq_q6K_gemm_path", "mmq_q6K_gemm_launches", "mmq_q6K_scaled_block_dots", "mmq_q4K_gemm_host_workspace", "mmq_q4K_gemm_host", "mmq_q4K_gemm_host_noalloc", "mmq_q4K_gemm_launches", "mmq_q4K_gemm_path", "mmq_q4K_gemm_q8_1", "mmq_q4K_block_dots", "mmq_q4K_scaled_block_dots",
     "mmq_dequantize_q4K_f16", "mmq_convert_f32_f16", "mmq_gemm_f16",
     "mmq_q4K_gemm_swiglu_q8_1", "mmq_interleave_rows_q4K",
     "mmq_q6K_bytes", "mmq_pack_q6K", "mmq_q6K_dev_bytes", "mmq_repack_q6K", "mmq_q6K_gemm",
@@ -101,6 +101,7 @@ def load_library(path: str = LIB_PATH):
                 "mmq_q6K_gemm": ([Q, P, P, I, I, I, P], ctypes.c_int),
                 "mmq_q6K_gemm_path": ([Q, P, P, I, I, I, ctypes.c_int, P], ctypes.c_int),
                 "mmq_q6K_gemm_launches": ([I, I, I, ctypes.c_int], ctypes.c_int),
+                "mmq_q6K_scaled_block_dots": ([Q, P, P, I, I, I, P], ctypes.c_int),
                 "mmq_q6K_block_dots": ([Q, P, P, I, I, I, P], ctypes.c_int),
                 "mmq_gguf_open": ([ctypes.c_char_p, ctypes.POINTER(P)], ctypes.c_int),
                 "mmq_gguf_close": ([P], None),
@@ -440,6 +441,10 @@ def mmq_q6K_gemm_launches(M, N, K, path):
     return load_library().mmq_q6K_gemm_launches(M, N, K, path)
 
 
+def mmq_q6K_scaled_block_dots(aq, w, S, M, N, K, stream):
+    return load_library().mmq_q6K_scaled_block_dots(aq, w, S, M, N, K, stream)
+
+
 def mmq_q6K_block_dots(aq, w, S, M, N, K, stream):
     return load_library().mmq_q6K_block_dots(aq, w, S, M, N, K, stream)
 
@@ -485,6 +490,19 @@ def q6K_block_dots(aq, w_dev, N: int, out=None, stream=None):
     S = out if out is not None else torch.empty((M, N, K // 16), dtype=torch.int32, device=qs.device)
     _check(mmq_q6K_block_dots(q8_1_struct(qs, da, sa), ctypes.c_void_p(w_dev.data_ptr()),
                               ctypes.c_void_p(S.data_ptr()), M, N, K, _stream_ptr(stream)), "mmq_q6K_block_dots")
+    return S
+
+
+def q6K_scaled_block_dots(aq, w_dev, N: int, out=None, stream=None):
+    """The tcgen05 q6_K kernel's exact per-chunk dots S' [M][N][K/32] (int32):
+    per 32-k chunk the sum of sc * S16 over its two sub-blocks."""
+    import torch
+    qs, da, sa = aq
+    M, K = qs.shape
+    S = out if out is not None else torch.empty((M, N, K // 32), dtype=torch.int32, device=qs.device)
+    _check(mmq_q6K_scaled_block_dots(q8_1_struct(qs, da, sa), ctypes.c_void_p(w_dev.data_ptr()),
+                                     ctypes.c_void_p(S.data_ptr()), M, N, K, _stream_ptr(stream)),
+           "mmq_q6K_scaled_block_dots")
     return S
 
 

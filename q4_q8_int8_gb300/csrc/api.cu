@@ -404,7 +404,7 @@ int mmq_q6K_gemm_path(mmq_q8_1_t aq, const uint8_t* bq6k_dev, float* C, int64_t 
             if (!status) return MMQ_ERR_CUDA;
             const int inject = t_inject_timeout;
             t_inject_timeout = 0;
-            return from_cuda(mmq::launch_gemm_q6k_tc(aq, bq6k_dev, C, M, N, K, status, inject, s));
+            return from_cuda(mmq::launch_gemm_q6k_tc(aq, bq6k_dev, C, nullptr, M, N, K, status, inject, s));
         }
     }
 }
@@ -412,6 +412,17 @@ int mmq_q6K_gemm_path(mmq_q8_1_t aq, const uint8_t* bq6k_dev, float* C, int64_t 
 int mmq_q6K_gemm(mmq_q8_1_t aq, const uint8_t* bq6k_dev, float* C, int64_t M, int64_t N, int64_t K,
                  void* stream) {
     return mmq_q6K_gemm_path(aq, bq6k_dev, C, M, N, K, MMQ_PATH_AUTO, stream);
+}
+
+int mmq_q6K_scaled_block_dots(mmq_q8_1_t aq, const uint8_t* bq6k_dev, int32_t* S, int64_t M, int64_t N,
+                              int64_t K, void* stream) {
+    int rc = check_gemm_args(aq, bq6k_dev, S, M, N, K);
+    if (rc) return rc;
+    if ((rc = mmq::q6k_tc_check_resources())) return rc;
+    int* status = mmq::status_word_ptr();
+    if (!status) return MMQ_ERR_CUDA;
+    return from_cuda(mmq::launch_gemm_q6k_tc(aq, bq6k_dev, nullptr, S, M, N, K, status, 0,
+                                             static_cast<cudaStream_t>(stream)));
 }
 
 int mmq_q6K_gemm_launches(int64_t M, int64_t N, int64_t K, int path) {

@@ -132,9 +132,21 @@ __device__ __forceinline__ void q6_pairs(uint32_t qlw, uint32_t qhw, uint32_t ni
 
 __device__ __forceinline__ uint32_t h2u(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
 
+// 32 columns of one chunk's S' (exact integers held in f32) to S [M][N][nb].
+__device__ __forceinline__ void dump_s(int32_t* S, const uint32_t (&b)[32], int64_t gr, int gc0, int M, int N,
+                                       int nb, int kb) {
+    if (gr >= M) return;
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+        if (gc0 + j < N) S[(gr * N + gc0 + j) * int64_t(nb) + kb] = int32_t(__uint_as_float(b[j]));
+}
+
+// kDump: write each chunk's exact S' (int32 [M][N][K/32]) instead of C, from
+// the same operands and MMAs (one launch, split == 1).
+template <bool kDump>
 __global__ void __launch_bounds__(kThreads, 1)
-gemm_q6k_tc_kernel(const __grid_constant__ TmaMaps maps, float* __restrict__ C, int M, int N, int K, int split,
-                   int* status, int inject_timeout, int tile_lo, int num_tiles) {
+gemm_q6k_tc_kernel(const __grid_constant__ TmaMaps maps, float* __restrict__ C, int32_t* __restrict__ S, int M,
+                   int N, int K, int split, int* status, int inject_timeout, int tile_lo, int num_tiles) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~uintptr_t(1023));
@@ -411,7 +423,11 @@ gemm_q6k_tc_kernel(const __grid_constant__ TmaMaps maps, float* __restrict__ C, 
                     uint32_t b[32];
                     tmem_ld_32x32b_x32(ta, b);
                     tmem_wait_ld(b);
-                    half_fma<0>(asb, b, da2);
+                    if constexpr (kDump) {
+                        dump_s(S, b, int64_t(m0) + row, n0 + colhalf * 64, M, N, K / 32, sb * 8 + c);
+                    } else {
+                        half_fma<0>(asb, b, da2);
+                    }
                     tmem_ld_32x32b_x32(ta + 32, b);
                     tmem_wait_ld(b);
                     // the chunk's S' tile is in registers: hand the slot back
@@ -419,7 +435,11 @@ gemm_q6k_tc_kernel(const __grid_constant__ TmaMaps maps, float* __restrict__ C, 
                     __syncwarp();
                     if (lane == 0) mbar_arrive(bars.tm_empty(tr.slot));
                     tr.next();
-                    half_fma<1>(asb, b, da2);
+                    if constexpr (kDump) {
+                        dump_s(S, b, int64_t(m0) + row, n0 + colhalf * 64 + 32, M, N, K / 32, sb * 8 + c);
+                    } else {
+                        half_fma<1>(asb, b, da2);
+                    }
                 }
                 {
                     // acc += d * asb for this super-block
@@ -435,7 +455,7 @@ gemm_q6k_tc_kernel(const __grid_constant__ TmaMaps maps, float* __restrict__ C, 
                 if (lane == 0) mbar_arrive(bars.scl_empty(sr.slot));
                 sr.next();
             }
-            if (split == 1) store_tile(C, acc, M, N, m0, n0, row, colhalf);
+            if (!kDump && split == 1) store_tile(C, acc, M, N, m0, n0, row, colhalf);
         }
     epi_done:;
         if (split > 1) {
@@ -526,8 +546,8 @@ int q6k_tc_launch_count(int64_t M, int64_t N, int64_t K) {
     return p.tail_lo < p.tiles ? 2 : 1;
 }
 
-cudaError_t launch_gemm_q6k_tc(mmq_q8_1_t aq, const uint8_t* w, float* C, int64_t M, int64_t N, int64_t K,
-                               int* status, int inject_timeout, cudaStream_t s) {
+cudaError_t launch_gemm_q6k_tc(mmq_q8_1_t aq, const uint8_t* w, float* C, int32_t* S, int64_t M, int64_t N,
+                               int64_t K, int* status, int inject_timeout, cudaStream_t s) {
     TmaMaps maps;
     const uint64_t nb = uint64_t(K / 32), nsb = uint64_t(K / 256);
     if (!encode_2d(&maps.a, CU_TENSOR_MAP_DATA_TYPE_UINT8, aq.qs, uint64_t(K), uint64_t(M), uint64_t(K), 128, BM,
@@ -540,16 +560,16 @@ cudaError_t launch_gemm_q6k_tc(mmq_q8_1_t aq, const uint8_t* w, float* C, int64_
     int dev = 0, nsm = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
+    auto k = S ? gemm_q6k_tc_kernel<true> : gemm_q6k_tc_kernel<false>;
     {
         // setmaxnreg needs exactly kRegsLaunch registers per thread at launch
         cudaFuncAttributes fa;
-        cudaError_t e = cudaFuncGetAttributes(&fa, gemm_q6k_tc_kernel);
+        cudaError_t e = cudaFuncGetAttributes(&fa, k);
         if (e != cudaSuccess) return e;
         if (fa.numRegs != int(kRegsLaunch)) return cudaErrorInvalidConfiguration;
     }
     cudaError_t e;
-    if ((e = cudaFuncSetAttribute(gemm_q6k_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes)))
-        return e;
+    if ((e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes))) return e;
     auto launch = [&](int64_t lo, int64_t hi, int split, int inject) -> cudaError_t {
         const int64_t n = hi - lo;
         cudaLaunchAttribute attr[2];
@@ -560,12 +580,13 @@ cudaError_t launch_gemm_q6k_tc(mmq_q8_1_t aq, const uint8_t* w, float* C, int64_
         attr[cfg.numAttrs].val.clusterDim.y = 1;
         attr[cfg.numAttrs].val.clusterDim.z = 1;
         ++cfg.numAttrs;
-        const cudaError_t le = cudaLaunchKernelEx(&cfg, gemm_q6k_tc_kernel, maps, C, int(M), int(N), int(K), split,
-                                                  status, inject, int(lo), int(hi));
+        const cudaError_t le = cudaLaunchKernelEx(&cfg, k, maps, C, S, int(M), int(N), int(K), split, status, inject,
+                                                  int(lo), int(hi));
         return le != cudaSuccess ? le : cudaGetLastError();
     };
     const TcPlan p = tc_plan(M, N, K, nsm, true);
     if (p.tiles > (int64_t(1) << 30)) return cudaErrorInvalidValue;
+    if (S) return launch(0, p.tiles, 1, inject_timeout);   // the dump: every chunk written where it is formed
     if (p.tail_lo == p.tiles) return launch(0, p.tiles, p.first_split, inject_timeout);
     if ((e = launch(0, p.tail_lo, 1, inject_timeout)) != cudaSuccess) return e;
     return launch(p.tail_lo, p.tiles, p.tail_split, 0);

@@ -144,8 +144,10 @@ constexpr int64_t kQ6GemvMax = 16;
 // the q4_K kernel (tc_plan), one or two kernels per call.
 int q6k_tc_check_resources();   // MMQ_OK or MMQ_ERR_RESOURCE
 int q6k_tc_launch_count(int64_t M, int64_t N, int64_t K);
-cudaError_t launch_gemm_q6k_tc(mmq_q8_1_t aq, const uint8_t* w, float* C, int64_t M, int64_t N, int64_t K,
-                               int* status, int inject_timeout, cudaStream_t s);
+// S != nullptr: the exact per-chunk S' = sum a * sc * q (int32 [M][N][K/32])
+// instead of C, from the same operands and MMAs.
+cudaError_t launch_gemm_q6k_tc(mmq_q8_1_t aq, const uint8_t* w, float* C, int32_t* S, int64_t M, int64_t N,
+                               int64_t K, int* status, int inject_timeout, cudaStream_t s);
 constexpr int64_t kSmallMMax = 64;
 
 }  // namespace mmq

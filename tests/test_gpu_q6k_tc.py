@@ -53,6 +53,36 @@ def test_q6k_paths_within_tolerance(M, N, K):
         assert ok.all(), f"path {path}: {(~ok).sum()} of {ok.size} outside tolerance"
 
 
+@pytest.mark.parametrize("M,N,K", [(128, 256, 512), (77, 132, 768), (300, 388, 1280), (1, 4, 256),
+                                   (130, 260, 2816)])
+def test_q6k_tc_scaled_block_dots_bit_exact(M, N, K):
+    # the kernel's own per-chunk S' = sc_2c * S16_2c + sc_2c+1 * S16_2c+1,
+    # against the oracle's exact per-16 dots and the unpacked scales
+    x = synthetic.activations(M, K, 790 + M, 0.01)
+    blk = synthetic.q6K_weights(N, K, 795 + N)
+    mmq, w_dev, aq = _setup(blk, N, K, x)
+    S = mmq.q6K_scaled_block_dots(aq, w_dev, N).cpu().numpy()
+    assert mmq.status() == 0
+    q, _, _ = oracle.quantize_q8_1(x)
+    S16 = q6k.block_dots16(q, blk, N).astype(np.int64)                      # [M][N][K/16]
+    sc = q6k.unpack_q6K(blk, N, K)["sc"].astype(np.int64)                    # [N][K/16]
+    ref = (S16 * sc[None]).reshape(M, N, K // 32, 2).sum(axis=3)
+    assert (S.astype(np.int64) == ref).all()
+
+
+def test_q6k_tc_scaled_block_dots_extremes():
+    # |S'| = 32 * 127 * 4096 = 16,646,144 < 2^24 at sc = -128, q = -32, a = +-127
+    M, N, K = 128, 128, 512
+    x = np.full((M, K), 3.0, np.float32)
+    x[::2] *= -1.0
+    blk = q6k_layout.encode(np.full((N, K), -32), np.full((N, K // 16), -128), np.ones((N, K // 256)))
+    mmq, w_dev, aq = _setup(blk, N, K, x)
+    S = mmq.q6K_scaled_block_dots(aq, w_dev, N).cpu().numpy()
+    assert mmq.status() == 0
+    sign = np.where(np.arange(M) % 2 == 0, -1, 1)[:, None, None]
+    assert (S == sign * 16646144).all()
+
+
 @pytest.mark.parametrize("sc,q", [(-128, -32), (127, 31), (-127, 31), (-1, -32)])
 def test_q6k_tc_exact_at_the_product_extremes(sc, q):
     # x = 127 everywhere: da = 1 and a = 127; every weight sc * q with d = 1, so
