@@ -44,6 +44,28 @@ def test_fused_q8_1_output(M, N, K):
         assert np.array_equal(a.cpu().numpy(), b.cpu().numpy())
 
 
+@pytest.mark.parametrize("ks", [1, 2, 4])
+@pytest.mark.parametrize("M,N,K", [(1, 256, 11008), (4, 4096, 4096), (2, 288, 2816)])
+def test_fused_q8_1_output_every_split(ks, M, N, K):
+    # the dot-product kernel's q8_1 epilogue with each K split forced: the
+    # q8_1 bits of its own C, and C within tolerance
+    mmq = require_gpu()
+    x = synthetic.activations(M, K, 500 + M, 0.01)
+    blk = synthetic.q4K_weights(N, K, 510 + N)
+    aq = mmq.quantize_q8_1(to_dev(x))
+    mmq.force_gemv_split(ks)
+    try:
+        C, o = mmq.q4K_gemm_q8_1(aq, to_dev(blk.reshape(-1)), N)
+        assert mmq.status() == 0
+    finally:
+        mmq.force_gemv_split(0)
+    Ch = C.cpu().numpy()
+    _check_q8_of(Ch, o)
+    q, da, sa = oracle.quantize_q8_1(x)
+    C_ref, _, T = oracle.gemm(q, da, sa, blk, N)
+    assert oracle.within_tolerance(Ch, C_ref, T, RTOL, ATOL).all()
+
+
 def test_fused_q8_1_output_full_size():
     mmq = require_gpu()
     x, blk, N = synthetic.config_inputs("q_proj")

@@ -59,6 +59,27 @@ def test_swiglu_full(M, F, K):
     assert (qs == rq).all() and (da.view(np.uint32) == rda.view(np.uint32)).all() and (sa == rsa).all()
 
 
+@pytest.mark.parametrize("ks", [1, 2])
+@pytest.mark.parametrize("M,F,K", [(1, 128, 11008), (4, 2048, 4096), (3, 160, 2816)])
+def test_swiglu_dot_product_every_split(ks, M, F, K):
+    # the dot-product kernel's SwiGLU epilogue with each K split it takes
+    # (1 and 2) forced: h within the propagated bound, q8_1 bits of its own h
+    mmq = require_gpu()
+    mmq.force_gemv_split(ks)
+    try:
+        mmq, x, blk_gu, aq, w_gu, h, (qs, da, sa) = _run(M, F, K, 600 + M)
+    finally:
+        mmq.force_gemv_split(0)
+    h = h.cpu().numpy()
+    q, dq, sq = oracle.quantize_q8_1(x)
+    _, C64, T = oracle.gemm(q, dq, sq, blk_gu, 2 * F, want_c64=True)
+    g, u = C64[:, 0::2], C64[:, 1::2]
+    bound = ffn.swiglu_bound(g, u, RTOL * T[:, 0::2] + ATOL, RTOL * T[:, 1::2] + ATOL)
+    assert (np.abs(h.astype(np.float64) - ffn.swiglu(g, u)) <= bound).all()
+    rq, rda, rsa = oracle.quantize_q8_1(h)
+    assert (qs == rq).all() and (da.view(np.uint32) == rda.view(np.uint32)).all() and (sa == rsa).all()
+
+
 @pytest.mark.parametrize("M", [130, 1, 4, 16, 64])
 def test_swiglu_without_h_same_bits(M):
     mmq, x, blk_gu, aq, w_gu, h, o1 = _run(M, 256, 1024, 77, with_h=True)
