@@ -702,6 +702,27 @@ def run_mine(args, rank, world, local_rank):
         step(args.warmup + args.steps + i, evs[i])
     torch.cuda.synchronize(dev)
     step_ms = ev_t0.elapsed_time(ev_t1) / args.steps
+    # A third pass, outside the timed region: the same K steps' GEMMs alone,
+    # launched back to back as in the timed region (events only at the ends).
+    # Its time per call is the GEMM's share of an overlapped step; the step
+    # minus it is what the prepass adds to the step.
+    ev_g0, ev_g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev_g0.record(stream)
+    for i in range(args.steps):
+        r = (args.warmup + i) % R
+        w_, (qs_, da_, sa_), C_ = ws[r], aqs[r], Cs[r]
+        aq_ = mmq.q8_1_struct(qs_, da_, sa_)
+        if sb:
+            rc_ = mmq.mmq_q4K_gemm_tcop(ctypes.c_void_p(tcops[r].data_ptr()), ctypes.c_void_p(w_.data_ptr()),
+                                        ctypes.c_void_p(C_.data_ptr()), M, N, K, sp)
+        else:
+            rc_ = mmq.mmq_q4K_gemm_path(aq_, ctypes.c_void_p(w_.data_ptr()), ctypes.c_void_p(C_.data_ptr()),
+                                        M, N, K, path, sp)
+        if rc_:
+            raise RuntimeError(f"MMQ call failed: {rc_}")
+    ev_g1.record(stream)
+    torch.cuda.synchronize(dev)
+    gemm_loop_ms = ev_g0.elapsed_time(ev_g1) / args.steps
     # Soak: the same step loop for about --soak-seconds more, so that the
     # clock record holds many samples taken under load (the timed region of
     # a default run is only a few milliseconds).
@@ -723,7 +744,8 @@ def run_mine(args, rank, world, local_rank):
     g_all = np.array([e[1].elapsed_time(e[2]) for e in evs])
     g_ms = float(np.mean(g_all))
     g_dist = {"median": float(np.median(g_all)), "min": float(g_all.min()), "max": float(g_all.max())}
-    step_ms, split_step_ms, q_ms, g_ms = max_over_ranks([step_ms, split_step_ms, q_ms, g_ms], world, dev)
+    step_ms, split_step_ms, q_ms, g_ms, gemm_loop_ms = max_over_ranks(
+        [step_ms, split_step_ms, q_ms, g_ms, gemm_loop_ms], world, dev)
 
     # ---- end to end through the C ABI with pinned host buffers: mmq_q4K_gemm_host
     # (x in from host memory, C out to host memory, chunked so that the copies
@@ -914,7 +936,12 @@ def run_mine(args, rank, world, local_rank):
         "epilogue_alu": alu,
         "prepass": {"ms": q_ms, "gbs": (M * K * 5.25 + plane) / (q_ms * 1e-3) / 1e9,
                     "frac_of_hbm": (M * K * 5.25 + plane) / (q_ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
-                    "bytes": M * K * 5.25 + plane},
+                    "bytes": M * K * 5.25 + plane,
+                    "ms_added_to_step": step_ms - gemm_loop_ms,
+                    "gbs_added_to_step": (M * K * 5.25 + plane) / max((step_ms - gemm_loop_ms) * 1e-3, 1e-9) / 1e9,
+                    "what": "ms: between events around the kernel (split pass); ms_added_to_step: the timed "
+                            "step minus the same GEMMs launched back to back without prepasses (gemm_loop_ms)"},
+        "gemm_loop_ms": gemm_loop_ms,
         "roofline": roof,
         "cpu_baseline": cpu,
         "e2e": {"value": whole_job_tmacs(macs, world, e2e_ms), "unit": UNIT,
