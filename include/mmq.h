@@ -230,8 +230,9 @@ int mmq_q4K_gemm_tcop(const void* tcop, const uint8_t* bq4k, float* C, int64_t M
                       int64_t N, int64_t K, void* stream);
 
 /* Number of kernels mmq_q4K_gemm_path(…, path, …) enqueues for this shape
- * on the current device: 1, or 2 when the tcgen05 kernel splits off its
- * last partial round of tiles into a second, split-K launch.  For counting
+ * on the current device: 1, or 2 when the tcgen05 kernel or the 5-64 token
+ * kernel splits off its last partial round of tiles into a second, split-K
+ * launch.  For counting
  * launches (e.g. in a timed region); MMQ_ERR_ARG for a shape or path the
  * GEMM refuses, MMQ_ERR_DEVICE / MMQ_ERR_CUDA as the GEMM would. */
 int mmq_q4K_gemm_launches(int64_t M, int64_t N, int64_t K, int path);

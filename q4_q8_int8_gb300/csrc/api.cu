@@ -232,8 +232,8 @@ int mmq_q4K_gemm_launches(int64_t M, int64_t N, int64_t K, int path) {
     int rc = check_device();
     if (rc) return rc;
     if (path == MMQ_PATH_AUTO) path = auto_path(M, N);
-    if (path != MMQ_PATH_TC) return 1;
-    const int n = mmq::tc_gemm_launch_count(M, N, K);
+    if (path != MMQ_PATH_TC && path != MMQ_PATH_SMALL_M) return 1;
+    const int n = path == MMQ_PATH_TC ? mmq::tc_gemm_launch_count(M, N, K) : mmq::small_m_launch_count(M, N, K);
     return n < 0 ? MMQ_ERR_CUDA : n;
 }
 

@@ -39,6 +39,7 @@
 #include <atomic>
 #include <cstdint>
 #include <mutex>
+#include <type_traits>
 
 #include "mmq_internal.h"
 #include "sm103_ptx.cuh"
@@ -187,7 +188,7 @@ __host__ __device__ constexpr bool quant_out(int mode) { return mode == kQ8 || m
 template <int NF, int G, int D, int kOut>
 __global__ void __launch_bounds__(G * 128)
 gemm_small_kernel(const __grid_constant__ SmallMaps maps, float* __restrict__ C, mmq_q8_1_t out,
-                  int32_t* __restrict__ S, int M, int N, int K, int split, int* status) {
+                  int32_t* __restrict__ S, int M, int N, int K, int split, int tile0, int* status) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~uintptr_t(1023));
@@ -202,7 +203,7 @@ gemm_small_kernel(const __grid_constant__ SmallMaps maps, float* __restrict__ C,
     const int grp = warp >> 2, gt = threadIdx.x & 127;   // group, thread within the group
     const int g = lane >> 2, j = lane & 3;
     const int rank = int(blockIdx.x % unsigned(split));
-    const int n0 = int(blockIdx.x / unsigned(split)) * kRows;
+    const int n0 = (tile0 + int(blockIdx.x / unsigned(split))) * kRows;
     const int nsb = K / 256;
     const int sb_begin = (nsb * rank) / split, sb_end = (nsb * (rank + 1)) / split;
     const int nmine = sb_end - sb_begin;
@@ -849,15 +850,27 @@ bool encode(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t i
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// How a call's row tiles are launched: `tiles` of them in clusters of
+// `split` CTAs along K, and, when those fill whole rounds of resident CTAs
+// with a partial round left over, that remainder (`tail` tiles from tile
+// `tiles`) as a second launch with its own larger K split, so that it takes
+// a fraction of a round instead of a whole one.
+struct SmallPlan {
+    int64_t tiles = 0, tail = 0;
+    int split = 1, tail_split = 1;
+    int smem = 0, tail_smem = 0;
+};
+
 template <int NF, int G, int D, int kOut>
-cudaError_t launch_nf(const SmallMaps& maps, float* C, mmq_q8_1_t out, int32_t* S, int64_t M, int64_t N,
-                      int64_t K, int* status, cudaStream_t s) {
+cudaError_t plan_nf(int64_t N, int64_t K, SmallPlan& P) {
     int dev = 0, nsm = 0, optin = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
-    cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+        return cudaGetLastError();
     const int64_t row_tiles = (N + kRows - 1) / kRows;
     const int nsb = int(K / 256);
+    auto fits = [&](int sp) { return Layout::make(NF, G, D, sp).total + 1024 <= optin; };
     // Split K over a cluster so that every SM gets a CTA: about two per SM
     // for one token fragment, about one for more (each CTA converts the
     // tokens of its super-blocks, so more CTAs per weight row cost more
@@ -865,41 +878,90 @@ cudaError_t launch_nf(const SmallMaps& maps, float* C, mmq_q8_1_t out, int32_t* 
     // M = 16..64 at one), within the shared-memory budget of the landing area.
     const int64_t per_sm = NF == 1 ? 2 : 1;
     int split = 1;
-    while (split < kMaxSplit && row_tiles * split * 2 <= per_sm * int64_t(nsm) && split * 2 <= nsb &&
-           Layout::make(NF, G, D, split * 2).total + 1024 <= optin)
+    while (split < kMaxSplit && row_tiles * split * 2 <= per_sm * int64_t(nsm) && split * 2 <= nsb && fits(split * 2))
         split *= 2;
-    const Layout L = Layout::make(NF, G, D, split);
-    const int smem = L.total + 1024;   // + alignment slack
-    if (smem > optin) return cudaErrorInvalidConfiguration;
+    P = SmallPlan{};
+    P.tiles = row_tiles;
+    P.split = split;
+    P.smem = Layout::make(NF, G, D, split).total + 1024;   // + alignment slack
+    if (P.smem > optin) return cudaErrorInvalidConfiguration;
+    if (split == 1) {
+        int per = 0;
+        auto k = gemm_small_kernel<NF, G, D, kOut>;
+        if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, P.smem) != cudaSuccess ||
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, k, G * 128, size_t(P.smem)) != cudaSuccess)
+            return cudaGetLastError();
+        const int64_t resident = int64_t(per > 0 ? per : 1) * nsm;
+        const int64_t tail = row_tiles % resident;
+        if (row_tiles > resident && tail > 0) {
+            int ts = 1;
+            while (ts < kMaxSplit && tail * ts * 2 <= resident && ts * 2 <= nsb && fits(ts * 2)) ts *= 2;
+            if (ts > 1) {
+                P.tiles = row_tiles - tail;
+                P.tail = tail;
+                P.tail_split = ts;
+                P.tail_smem = Layout::make(NF, G, D, ts).total + 1024;
+            }
+        }
+    }
+    return cudaSuccess;
+}
+
+template <int NF, int G, int D, int kOut>
+cudaError_t launch_part(const SmallMaps& maps, float* C, mmq_q8_1_t out, int32_t* S, int64_t M, int64_t N,
+                        int64_t K, int* status, cudaStream_t s, int64_t tile0, int64_t tiles, int split, int smem) {
     // the quantizing epilogue stages its tile behind the groups' partials in stage memory
-    if (quant_out(kOut) && G * 128 * NF * 16 + 8 * NF * kRows * 4 > L.work_off) return cudaErrorInvalidConfiguration;
+    if (quant_out(kOut) && G * 128 * NF * 16 + 8 * NF * kRows * 4 > Layout::make(NF, G, D, split).work_off)
+        return cudaErrorInvalidConfiguration;
     auto k = gemm_small_kernel<NF, G, D, kOut>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     cudaLaunchAttribute attr[2];
-    cudaLaunchConfig_t cfg = mmq::launch_config(dim3(unsigned(row_tiles * split)), dim3(G * 128), size_t(smem), s,
-                                                attr);
+    cudaLaunchConfig_t cfg = mmq::launch_config(dim3(unsigned(tiles * split)), dim3(G * 128), size_t(smem), s, attr);
     attr[cfg.numAttrs].id = cudaLaunchAttributeClusterDimension;
     attr[cfg.numAttrs].val.clusterDim.x = unsigned(split);
     attr[cfg.numAttrs].val.clusterDim.y = 1;
     attr[cfg.numAttrs].val.clusterDim.z = 1;
     cfg.numAttrs += 1;
-    return cudaLaunchKernelEx(&cfg, k, maps, C, out, S, int(M), int(N), int(K), split, status);
+    return cudaLaunchKernelEx(&cfg, k, maps, C, out, S, int(M), int(N), int(K), split, int(tile0), status);
+}
+
+template <int NF, int G, int D, int kOut>
+cudaError_t launch_nf(const SmallMaps& maps, float* C, mmq_q8_1_t out, int32_t* S, int64_t M, int64_t N,
+                      int64_t K, int* status, cudaStream_t s) {
+    SmallPlan P;
+    cudaError_t e = plan_nf<NF, G, D, kOut>(N, K, P);
+    if (e != cudaSuccess) return e;
+    e = launch_part<NF, G, D, kOut>(maps, C, out, S, M, N, K, status, s, 0, P.tiles, P.split, P.smem);
+    if (e != cudaSuccess || P.tail == 0) return e;
+    return launch_part<NF, G, D, kOut>(maps, C, out, S, M, N, K, status, s, P.tiles, P.tail, P.tail_split,
+                                       P.tail_smem);
+}
+
+// The kernel instance per number of 8-token fragments: NF, warp groups G,
+// TMA stages per group D.
+template <typename Fn>
+cudaError_t dispatch_nf(int nf, Fn&& fn) {
+    using std::integral_constant;
+    switch (nf) {
+        case 1: return fn(integral_constant<int, 1>{}, integral_constant<int, 4>{}, integral_constant<int, 1>{});
+        case 2: return fn(integral_constant<int, 2>{}, integral_constant<int, 4>{}, integral_constant<int, 2>{});
+        case 3: return fn(integral_constant<int, 3>{}, integral_constant<int, 4>{}, integral_constant<int, 2>{});
+        case 4: return fn(integral_constant<int, 4>{}, integral_constant<int, 4>{}, integral_constant<int, 1>{});
+        case 5: return fn(integral_constant<int, 5>{}, integral_constant<int, 2>{}, integral_constant<int, 2>{});
+        case 6: return fn(integral_constant<int, 6>{}, integral_constant<int, 2>{}, integral_constant<int, 2>{});
+        case 7: return fn(integral_constant<int, 7>{}, integral_constant<int, 2>{}, integral_constant<int, 2>{});
+        default: return fn(integral_constant<int, 8>{}, integral_constant<int, 2>{}, integral_constant<int, 2>{});
+    }
 }
 
 template <int kOut>
 cudaError_t launch_nf_any(int nf, const SmallMaps& maps, float* C, mmq_q8_1_t out, int32_t* S, int64_t M,
                           int64_t N, int64_t K, int* status, cudaStream_t s) {
-    switch (nf) {
-        case 1: return launch_nf<1, 4, 1, kOut>(maps, C, out, S, M, N, K, status, s);
-        case 2: return launch_nf<2, 4, 2, kOut>(maps, C, out, S, M, N, K, status, s);
-        case 3: return launch_nf<3, 4, 2, kOut>(maps, C, out, S, M, N, K, status, s);
-        case 4: return launch_nf<4, 4, 1, kOut>(maps, C, out, S, M, N, K, status, s);
-        case 5: return launch_nf<5, 2, 2, kOut>(maps, C, out, S, M, N, K, status, s);
-        case 6: return launch_nf<6, 2, 2, kOut>(maps, C, out, S, M, N, K, status, s);
-        case 7: return launch_nf<7, 2, 2, kOut>(maps, C, out, S, M, N, K, status, s);
-        default: return launch_nf<8, 2, 2, kOut>(maps, C, out, S, M, N, K, status, s);
-    }
+    return dispatch_nf(nf, [&](auto F, auto G, auto D) {
+        return launch_nf<decltype(F)::value, decltype(G)::value, decltype(D)::value, kOut>(maps, C, out, S, M, N, K,
+                                                                                           status, s);
+    });
 }
 
 }  // namespace
@@ -945,6 +1007,16 @@ cudaError_t launch_gemm_small_m(mmq_q8_1_t aq, const uint8_t* w, float* C, int64
     if (mode == kSwiGLU) return launch_nf_any<kSwiGLU>(nf, maps, C, out, nullptr, M, N, K, status, s);
     if (mode == kDump) return launch_nf_any<kDump>(nf, maps, nullptr, none, S, M, N, K, status, s);
     return launch_nf_any<kF32>(nf, maps, C, out, nullptr, M, N, K, status, s);
+}
+
+int small_m_launch_count(int64_t M, int64_t N, int64_t K) {
+    if (M <= 4) return 1;
+    SmallPlan P;
+    const cudaError_t e = dispatch_nf(int((M + 7) / 8), [&](auto F, auto G, auto D) {
+        return plan_nf<decltype(F)::value, decltype(G)::value, decltype(D)::value, kF32>(N, K, P);
+    });
+    if (e != cudaSuccess) return -1;
+    return P.tail > 0 ? 2 : 1;
 }
 
 int set_force_gemv_split(int ks) {

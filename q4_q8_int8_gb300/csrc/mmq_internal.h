@@ -148,6 +148,7 @@ int q6k_tc_launch_count(int64_t M, int64_t N, int64_t K);
 // instead of C, from the same operands and MMAs.
 cudaError_t launch_gemm_q6k_tc(mmq_q8_1_t aq, const uint8_t* w, float* C, int32_t* S, int64_t M, int64_t N,
                                int64_t K, int* status, int inject_timeout, cudaStream_t s);
+int small_m_launch_count(int64_t M, int64_t N, int64_t K);   // kernels per call, -1 on a CUDA error
 constexpr int64_t kSmallMMax = 64;
 
 }  // namespace mmq

@@ -303,3 +303,31 @@ def test_exact_c_with_sub_block_scales(path_name, M, N, K):
     total = (S * sc[None, :, :]).sum(axis=2)
     assert np.abs(S * sc[None]).sum(axis=2).max() < 2 ** 24   # the exactness premise
     assert (C.astype(np.float64) == total * 2.0 ** -4).all()
+
+
+@pytest.mark.parametrize("M", [5, 16, 40, 64])
+@pytest.mark.parametrize("N", [11008, 9792])
+def test_small_m_partial_round_split(M, N):
+    # 5-64 tokens over more 64-row tiles than one round of CTAs holds: the
+    # partial last round runs as a second launch with K split over a cluster.
+    # C within tolerance everywhere, S bit-exact, the same bits on a rerun.
+    import torch
+    mmq = require_gpu()
+    K = 4096
+    x = synthetic.activations(M, K, 611 + M, 0.01)
+    blk = synthetic.q4K_weights(N, K, 621 + N)
+    C = _full_check(x, blk, N, mmq.MMQ_PATH_SMALL_M)
+    _, aq, w = _dev_inputs(x, blk)
+    C2 = mmq.q4K_gemm(aq, w, N, path=mmq.MMQ_PATH_SMALL_M).cpu().numpy()
+    assert mmq.status() == 0
+    assert np.array_equal(C.view(np.uint32), C2.view(np.uint32))
+    n = mmq.mmq_q4K_gemm_launches(M, N, K, mmq.MMQ_PATH_SMALL_M)
+    assert n in (1, 2)
+    assert mmq.mmq_q4K_gemm_launches(M, N, K, mmq.MMQ_PATH_AUTO) == n
+    if M == 16 and N == 11008 and torch.cuda.get_device_properties(0).multi_processor_count < 172:
+        assert n == 2   # 172 tiles of one CTA per SM: a partial second round
+    if M == 16:
+        q, _, _ = oracle.quantize_q8_1(x)
+        S = mmq.q4K_block_dots(aq, w, N, path=mmq.MMQ_PATH_SMALL_M).cpu().numpy()
+        assert mmq.status() == 0
+        assert (S == oracle.block_dots(q, blk, N)).all()
