@@ -26,6 +26,7 @@
 #include <cuda_fp16.h>
 
 #include "mmq_internal.h"
+#include "sm103_ptx.cuh"
 
 namespace {
 
@@ -338,6 +339,7 @@ gemv_q6k_kernel(mmq_q8_1_t aq, const uint8_t* __restrict__ w, float* __restrict_
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int slice = warp % KS, grp = warp / KS;
     const int row0 = (blockIdx.x * kGroups + grp) * kGvR;
+    mmq::ptx::griddep_launch_dependents();
     if (KS == 1 && row0 >= N) return;
     const int nsb = K / 256, nch = K / 32;
     float acc[MT][kGvR];
@@ -365,6 +367,9 @@ gemv_q6k_kernel(mmq_q8_1_t aq, const uint8_t* __restrict__ w, float* __restrict_
                 scw[r] = dw[r] = 0u;
             }
         }
+        // weights stream in while the previous kernel (programmatic dependent
+        // launch) finishes; activations and C only after it has
+        if (base == 32 * slice) mmq::ptx::griddep_wait();
         if (ci >= nch) continue;
         float ds[kGvR][2];   // d * sc of the chunk's two sub-blocks (exact in f32)
         uint32_t qw[kGvR][8];   // the chunk's 32 quants as int8, once for all tokens
@@ -449,8 +454,9 @@ template <int MT, int KS>
 cudaError_t launch_gemv_q6k_ks(mmq_q8_1_t aq, const uint8_t* w, float* C, int64_t M, int64_t N, int64_t K,
                                cudaStream_t s) {
     constexpr int rows = 4 / KS * kGvR;   // rows per CTA
-    gemv_q6k_kernel<MT, KS><<<unsigned((N + rows - 1) / rows), 128, 0, s>>>(aq, w, C, int(M), int(N), int(K));
-    return cudaGetLastError();
+    cudaLaunchAttribute attr[1];
+    const cudaLaunchConfig_t cfg = mmq::launch_config(dim3(unsigned((N + rows - 1) / rows)), dim3(128), 0, s, attr);
+    return cudaLaunchKernelEx(&cfg, gemv_q6k_kernel<MT, KS>, aq, w, C, int(M), int(N), int(K));
 }
 
 template <int MT>
