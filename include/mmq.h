@@ -445,10 +445,10 @@ const char* mmq_strerror(int code);
  * launched just before it on the same stream. */
 void mmq_set_programmatic_launch(int enable);
 
-/* Test hook: force the K split of the dot-product kernel (M <= 4) for
- * later calls on this host thread: ks = 1, 2 or 4 warps per row group
- * (the SwiGLU epilogue takes 1 or 2; a forced 4 makes its calls fail with
- * MMQ_ERR_CUDA), 0 restores the automatic choice.  Returns MMQ_ERR_ARG for
+/* Test hook: force the K split of the dot-product kernels (q4_K, M <= 4;
+ * q6_K, M <= 16) for later calls on this host thread: ks = 1, 2 or 4 warps
+ * per row group (the SwiGLU epilogue takes 1 or 2; a forced 4 makes its
+ * calls fail with MMQ_ERR_CUDA), 0 restores the automatic choice.  Returns MMQ_ERR_ARG for
  * any other value.  The split changes how the row's partial sums are
  * grouped, so f32 results may differ in the last bits between splits; the
  * integer dots and the tolerance do not. */

@@ -25,6 +25,8 @@
 // bits of 1.5 * 2^23, so one FADD recovers S as a float.
 #include <cuda_fp16.h>
 
+#include <atomic>
+
 #include "mmq_internal.h"
 #include "sm103_ptx.cuh"
 
@@ -459,13 +461,75 @@ cudaError_t launch_gemv_q6k_ks(mmq_q8_1_t aq, const uint8_t* w, float* C, int64_
     return cudaLaunchKernelEx(&cfg, gemv_q6k_kernel<MT, KS>, aq, w, C, int(M), int(N), int(K));
 }
 
+// CTAs of one kernel instance resident on the device at once (register
+// bound), found once per instance and device.
+constexpr int kMaxDevices = 64;
+template <int MT, int KS>
+int64_t gemv_q6k_resident() {
+    static std::atomic<int64_t> cached[kMaxDevices];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        cudaGetLastError();
+        dev = -1;
+    }
+    int64_t v = dev >= 0 ? cached[dev].load(std::memory_order_relaxed) : 0;
+    if (v == 0) {
+        int nsm = 0, per = 0;
+        if (dev < 0 || cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, gemv_q6k_kernel<MT, KS>, 128, 0) != cudaSuccess) {
+            cudaGetLastError();
+            nsm = nsm > 0 ? nsm : 1;
+            per = 1;
+        }
+        v = int64_t(per > 0 ? per : 1) * (nsm > 0 ? nsm : 1);
+        if (dev >= 0) cached[dev].store(v, std::memory_order_relaxed);
+    }
+    return v;
+}
+
+// The K split (KS warps per row group), from the resident CTAs of each
+// instance and a cost per launch:
+// * up to 4 tokens the kernel waits on memory: waves of CTAs x (dependent
+//   load rounds per warp + 1/2), as for the q4_K dot-product kernel;
+// * with 8 and 16 tokens it is compute-bound: waves x rounds, over splits 2
+//   and 4 (ties to 4; split 1 was slowest on every measured shape).
+// Measured at 16 tokens (graph replay, us, splits 1 / 2 / 4): 4096 x 4096
+// 32.1 / 24.2 / 23.8, 4096 -> 11008 57.7 / 38.4 / 52.4, 11008 -> 4096
+// 84.4 / 63.1 / 59.3; the rule picks the fastest of each.
 template <int MT>
 cudaError_t launch_gemv_q6k(mmq_q8_1_t aq, const uint8_t* w, float* C, int64_t M, int64_t N, int64_t K,
                             cudaStream_t s) {
-    const int64_t rounds = (K / 32 + 31) / 32;
-    if (rounds >= 4) return launch_gemv_q6k_ks<MT, 4>(aq, w, C, M, N, K, s);
-    if (rounds >= 2) return launch_gemv_q6k_ks<MT, 2>(aq, w, C, M, N, K, s);
-    return launch_gemv_q6k_ks<MT, 1>(aq, w, C, M, N, K, s);
+    const int64_t nch = K / 32;
+    switch (mmq::forced_gemv_split()) {   // test hook
+        case 1: return launch_gemv_q6k_ks<MT, 1>(aq, w, C, M, N, K, s);
+        case 2: return launch_gemv_q6k_ks<MT, 2>(aq, w, C, M, N, K, s);
+        case 4: return launch_gemv_q6k_ks<MT, 4>(aq, w, C, M, N, K, s);
+        default: break;
+    }
+    auto shape = [&](int k, int64_t resident, int64_t& waves, int64_t& rounds) {
+        const int64_t rows = 4 / k * kGvR;
+        const int64_t ctas = (N + rows - 1) / rows;
+        waves = (ctas + resident - 1) / resident;
+        rounds = (nch + 32 * k - 1) / (32 * k);
+    };
+    if constexpr (MT >= 8) {
+        int64_t w2, r2, w4, r4;
+        shape(2, gemv_q6k_resident<MT, 2>(), w2, r2);
+        shape(4, gemv_q6k_resident<MT, 4>(), w4, r4);
+        if (w4 * r4 <= w2 * r2) return launch_gemv_q6k_ks<MT, 4>(aq, w, C, M, N, K, s);
+        return launch_gemv_q6k_ks<MT, 2>(aq, w, C, M, N, K, s);
+    }
+    auto cost2 = [&](int k, int64_t resident) {   // twice the modelled cost
+        int64_t waves, rounds;
+        shape(k, resident, waves, rounds);
+        return waves * (2 * rounds + 1);
+    };
+    const int64_t c1 = cost2(1, gemv_q6k_resident<MT, 1>());
+    const int64_t c2 = cost2(2, gemv_q6k_resident<MT, 2>());
+    const int64_t c4 = cost2(4, gemv_q6k_resident<MT, 4>());
+    if (c1 <= c2 && c1 <= c4) return launch_gemv_q6k_ks<MT, 1>(aq, w, C, M, N, K, s);
+    if (c4 < c2) return launch_gemv_q6k_ks<MT, 4>(aq, w, C, M, N, K, s);
+    return launch_gemv_q6k_ks<MT, 2>(aq, w, C, M, N, K, s);
 }
 
 }  // namespace

@@ -1025,4 +1025,6 @@ int set_force_gemv_split(int ks) {
     return MMQ_OK;
 }
 
+int forced_gemv_split() { return t_force_ks; }
+
 }  // namespace mmq

@@ -104,6 +104,7 @@ constexpr int kSmallDump = 3;
 // Test hook of the dot-product kernel: force its K split (0, 1, 2, 4) for the
 // calling host thread; MMQ_ERR_ARG for other values.
 int set_force_gemv_split(int ks);
+int forced_gemv_split();   // this host thread's forced split, 0 for none
 // Host-buffer pipeline (host_pipeline.cu): rows per chunk, workspace bytes,
 // and the chunked copy-in / prepass + GEMM / copy-out, with `gemm` the GEMM
 // to run on each chunk's q8_1 planes (MMQ_* code).

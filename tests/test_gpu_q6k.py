@@ -136,3 +136,39 @@ def test_q6k_every_output_written_and_deterministic():
     assert torch.isfinite(C1).all()
     assert (buf[:1024] == 7.0).all() and (buf[-1024:] == 7.0).all()
     assert torch.equal(C1.view(torch.int32), C2.view(torch.int32))
+
+
+@pytest.mark.parametrize("ks", [1, 2, 4])
+@pytest.mark.parametrize("M,N,K", [(1, 260, 11008), (2, 132, 4096), (4, 68, 2816), (8, 260, 1280), (16, 132, 4096)])
+def test_q6k_dot_product_every_split(ks, M, N, K):
+    # each K split of the q6_K dot-product kernel (up to 16 tokens), forced,
+    # within tolerance of the oracle
+    x = synthetic.activations(M, K, 671 + M, 0.01)
+    blk = synthetic.q6K_weights(N, K, 681 + N)
+    mmq, w_dev = _dev(blk, N, K)
+    aq = mmq.quantize_q8_1(to_dev(x))
+    mmq.force_gemv_split(ks)
+    try:
+        C = mmq.q6K_gemm(aq, w_dev, N).cpu().numpy()
+        assert mmq.status() == 0
+    finally:
+        mmq.force_gemv_split(0)
+    q, da, _ = oracle.quantize_q8_1(x)
+    _, C64, T = q6k.gemm(q, da, blk, N)
+    ok = np.abs(C.astype(np.float64) - C64) <= RTOL * T + ATOL
+    assert ok.all(), f"{(~ok).sum()} of {ok.size} outside tolerance"
+
+
+@pytest.mark.parametrize("M,N,K", [(16, 11008, 4096), (8, 4096, 4096), (1, 4096, 4096)])
+def test_q6k_dot_product_chosen_split_sampled(M, N, K):
+    # the automatic split on decode shapes where the choice differs from the
+    # widest split (16 tokens on 4096 -> 11008 takes 2), sampled
+    x = synthetic.activations(M, K, 691 + M, 0.01)
+    blk = synthetic.q6K_weights(N, K, 695 + N)
+    mmq, w_dev = _dev(blk, N, K)
+    C = mmq.q6K_gemm(mmq.quantize_q8_1(to_dev(x)), w_dev, N).cpu().numpy()
+    assert mmq.status() == 0
+    q, da, _ = oracle.quantize_q8_1(x)
+    rows, cols = sample_points(M, N, 3000, 13)
+    _, C64, T = q6k.gemm(q, da, blk, N, rows=rows, cols=cols)
+    assert (np.abs(C[rows, cols].astype(np.float64) - C64) <= RTOL * T + ATOL).all()
