@@ -331,3 +331,18 @@ def test_small_m_partial_round_split(M, N):
         S = mmq.q4K_block_dots(aq, w, N, path=mmq.MMQ_PATH_SMALL_M).cpu().numpy()
         assert mmq.status() == 0
         assert (S == oracle.block_dots(q, blk, N)).all()
+
+
+@pytest.mark.parametrize("name", ["gate_up", "down"])
+def test_ffn_every_element(name):
+    # the FFN workloads at 2048 tokens, every output against the oracle
+    # (gate/up: 22.5 M outputs; down: K = 11008)
+    mmq = require_gpu()
+    x, blk, N = synthetic.config_inputs(name)
+    _, aq, w = _dev_inputs(x, blk)
+    C = mmq.q4K_gemm(aq, w, N).cpu().numpy()
+    assert mmq.status() == 0
+    q, da, sa = oracle.quantize_q8_1(x)
+    C_ref, _, T = oracle.gemm(q, da, sa, blk, N)
+    ok = oracle.within_tolerance(C, C_ref, T, RTOL, ATOL)
+    assert ok.all(), f"{(~ok).sum()} of {ok.size} outputs outside tolerance"
