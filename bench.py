@@ -497,7 +497,8 @@ def run_sweep_q6k(mmq, dev, peaks):
     import torch
     from q4_q8_int8_gb300 import synthetic
     res = {}
-    for label, M, K, N in (("q6k_M1", 1, 4096, 4096), ("q6k_M128", 128, 4096, 4096),
+    for label, M, K, N in (("q6k_M1", 1, 4096, 4096), ("q6k_M1_11008x4096", 1, 11008, 4096),
+                           ("q6k_M16_4096x11008", 16, 4096, 11008), ("q6k_M128", 128, 4096, 4096),
                            ("q6k_q_proj", 2048, 4096, 4096), ("q6k_down", 2048, 11008, 4096)):
         wbytes = 210.0 / 256.0 * N * K
         set_bytes = wbytes + 1.25 * M * K + 4 * M * N
