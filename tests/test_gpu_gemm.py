@@ -346,3 +346,14 @@ def test_ffn_every_element(name):
     C_ref, _, T = oracle.gemm(q, da, sa, blk, N)
     ok = oracle.within_tolerance(C, C_ref, T, RTOL, ATOL)
     assert ok.all(), f"{(~ok).sum()} of {ok.size} outputs outside tolerance"
+
+
+@pytest.mark.parametrize("M", [4, 5, 64, 65])
+@pytest.mark.parametrize("N,K", [(1100, 1280), (4100, 256)])
+def test_auto_path_boundaries(M, N, K):
+    # the automatic choice on both sides of each switch (dot product | mma.sync
+    # at 4/5 tokens, mma.sync | tcgen05 at 64/65), every output, ragged N
+    mmq = require_gpu()
+    x = synthetic.activations(M, K, 731 + M, 0.01)
+    blk = synthetic.q4K_weights(N, K, 741 + N)
+    _full_check(x, blk, N, mmq.MMQ_PATH_AUTO)
