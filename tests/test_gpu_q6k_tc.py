@@ -132,13 +132,15 @@ def test_q6k_tc_full_size_sampled(name):
     assert ok.all(), f"{(~ok).sum()} sampled outputs outside tolerance"
 
 
-def test_q6k_tc_q_proj_every_element():
-    # every output at q-proj against the oracle's brute-force dequantized dot
-    # (float64 BLAS over the same a = da * q and w = d * sc * q; pinned to the
-    # blockwise form in the oracle tests), with T = |a| . |w|^T
-    M, K, N = synthetic.SHAPES["q_proj"]
-    x = synthetic.activations(M, K, 731, 0.01)
-    blk = synthetic.q6K_weights(N, K, 741)
+@pytest.mark.parametrize("name", ["q_proj", "gate_up", "down"])
+def test_q6k_tc_every_element(name):
+    # every output of the 2048-token workloads against the oracle's
+    # brute-force dequantized dot (float64 BLAS over the same a = da * q and
+    # w = d * sc * q; pinned to the blockwise form in the oracle tests), with
+    # T = |a| . |w|^T
+    M, K, N = synthetic.SHAPES[name]
+    x = synthetic.activations(M, K, 731 + K + N, 0.01)
+    blk = synthetic.q6K_weights(N, K, 741 + N)
     mmq, w_dev, aq = _setup(blk, N, K, x)
     C = mmq.q6K_gemm(aq, w_dev, N, path=mmq.MMQ_PATH_TC).cpu().numpy()
     assert mmq.status() == 0
