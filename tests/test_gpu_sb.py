@@ -187,10 +187,11 @@ def test_full_size_sampled(name):
     assert np.isfinite(C).all()
 
 
-def test_q_proj_every_element():
-    # every output of the headline workload through the operand plane
+@pytest.mark.parametrize("name", ["q_proj", "gate_up", "down"])
+def test_every_element(name):
+    # every output of the 2048-token workloads through the operand plane
     mmq = require_gpu()
-    x, blk, N = synthetic.config_inputs("q_proj")
+    x, blk, N = synthetic.config_inputs(name)
     M, K = x.shape
     _, tcop = mmq.quantize_q8_1_tcop(to_dev(x))
     C = mmq.q4K_gemm_tcop(tcop, to_dev(blk.reshape(-1)), M, N, K).cpu().numpy()
